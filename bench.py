@@ -1,0 +1,478 @@
+#!/usr/bin/env python
+"""WTConv layer benchmark on GB300: fwd + bwd throughput (Gelem/s) and roofline fractions.
+
+One step = one pass of the whole layer over one batch:
+    fold scales (Eq. 8) -> forward -> backward-data -> backward-weight (+ Eq. 9 unfold)
+all through the C ABI of libwtconv, inputs resident in HBM. The default workload is the
+largest single-GPU one: N=16, C=256, H=W=256, k=5, L=5, bf16 I/O (X and dY are 537 MB
+each, larger than the 126 MB L2, so consecutive steps cannot hit in L2).
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (weak scaling,
+no collective on the data path); rank 0 prints one JSON line with the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "WTConv fwd+bwd Gelem/s and achieved HBM GB/s as % of GB300 peak (1 GPU)"
+NUM_SMS = 152
+FP32_LANES_PER_SM = 128
+SM_MAX_MHZ = 2070.0
+HBM_FALLBACK_GBS = 6800.0
+PROFILES = os.path.join(ROOT, "profiles")
+CSRC = os.path.join(ROOT, "depthwise_receptive_field_gb300", "csrc")
+
+
+# ----------------------------------------------------------------------------------
+# helpers
+# ----------------------------------------------------------------------------------
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": HBM_FALLBACK_GBS, "source": "fallback"}
+
+
+def fp32_peak_tflops(mhz: float = SM_MAX_MHZ) -> float:
+    """FP32 FMA peak from unit counts: 152 SMs x 128 FP32 lanes x 2 FLOP x SM clock."""
+    return NUM_SMS * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+
+
+def source_sha256() -> str:
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(CSRC, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def committed_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
+    kernel sources (its source hash matches); else None."""
+    path = os.path.join(PROFILES, f"traffic_{kernel}_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+    if kv.get("source_sha256") != source_sha256():
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm_sorted = sorted(sm)
+        return {"sm_mhz": sm_sorted[len(sm_sorted) // 2], "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a host float over all ranks (identity when world == 1)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def workload_config(wl) -> dict:
+    return {
+        "workload": f"{wl.name}: N={wl.n} C={wl.c} H={wl.h} W={wl.w} k={wl.k} L={wl.levels}, "
+                    f"{wl.dtype} I/O, fp32 accumulate",
+        "n": wl.n, "c": wl.c, "h": wl.h, "w": wl.w, "k": wl.k, "levels": wl.levels,
+        "io_dtype": wl.dtype,
+        "step": "fold + forward + backward_data + backward_weight (C ABI)",
+        "l2": "no flush: X and dY are each larger than L2, read once per pass",
+    }
+
+
+# ----------------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# ----------------------------------------------------------------------------------
+
+def oracle_sample(wl, images: int, channels: int):
+    """A bounded sample of the workload: the first `images` batch entries of the first
+    `channels` channels, same recipe and seed (inputs drawn at full size, then sliced)."""
+    from depthwise_receptive_field_gb300.inputs import make_inputs
+    inp = make_inputs(wl, n=images)
+    sl = slice(0, channels)
+    return {"x": inp["x"][:, sl], "dy": inp["dy"][:, sl], "w0": inp["w0"][sl],
+            "b0": inp["b0"][sl], "s0": inp["s0"][sl], "wl": inp["wl"][:, sl],
+            "sl": inp["sl"][:, sl]}
+
+
+def time_oracle_step(s: dict, levels: int) -> float:
+    import oracle
+    t0 = time.perf_counter()
+    oracle.forward(s["x"], s["w0"], s["b0"], s["s0"], s["wl"], s["sl"], levels)
+    oracle.backward(s["x"], s["dy"], s["w0"], s["b0"], s["s0"], s["wl"], s["sl"], levels)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wl) -> dict:
+    import oracle
+    oracle.build()
+    cores = oracle.num_threads()
+    images = max(1, min(wl.n, 4))
+    s = oracle_sample(wl, images, wl.c)
+    elems = s["x"].numel()
+    dt = time_oracle_step(s, wl.levels)
+    return {"value": elems / dt / 1e9, "unit": "Gelem/s", "cores": cores, "kind": "oracle",
+            "sample": f"{images} of {wl.n} images x all {wl.c} channels ({elems} elements), "
+                      f"one fwd+bwd pass in {dt:.2f} s, float64, OpenMP over planes/channels"}
+
+
+def run_reference(args, wl):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    cores = oracle.num_threads()
+    s = oracle_sample(wl, 1, wl.c)
+    elems = s["x"].numel()
+    for _ in range(args.warmup):
+        time_oracle_step(s, wl.levels)
+    total = 0.0
+    for _ in range(args.steps):
+        total += time_oracle_step(s, wl.levels)
+    value = elems * args.steps / total / 1e9
+    sample = (f"1 of {wl.n} images x all {wl.c} channels ({elems} elements) per step, "
+              "float64 plain loops, OpenMP")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "Gelem/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(wl),
+        "cpu_baseline": {"value": value, "unit": "Gelem/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "Gelem/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------------
+# the CUDA path
+# ----------------------------------------------------------------------------------
+
+def run_ours(args, wl):
+    import torch
+
+    from depthwise_receptive_field_gb300 import binding as B
+    from depthwise_receptive_field_gb300 import iomodel, layer
+    from depthwise_receptive_field_gb300.inputs import make_inputs
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    B.load_library()
+
+    inp = make_inputs(wl)
+    p = layer.Params.from_inputs(inp, dev)
+    x = inp["x"].to(dev)
+    dy = inp["dy"].to(dev)
+    desc = B.desc_like(x, p.k, wl.levels)
+    ws = layer.Workspace(dev)
+    _, nbd, nbw = B.wtconv_workspace_size(desc)
+    buf, bufn = ws.get(max(nbd, nbw))
+    f = layer.fold(p, desc)
+    y = torch.empty_like(x)
+    g = {"dx": torch.empty_like(dy), "dw0": torch.empty_like(p.w0),
+         "db0": torch.empty_like(p.s0), "ds0": torch.empty_like(p.s0),
+         "dwl": torch.empty_like(p.wl), "dsl": torch.empty_like(p.sl)}
+    stream = torch.cuda.current_stream(dev)
+    lv = wl.levels > 0
+
+    launches = {"n": 0}
+
+    def step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
+        B.wtconv_fold_scales(desc, p.w0, p.b0, p.s0, p.wl if lv else None,
+                             p.sl if lv else None, f.w0f, f.b0f, f.wlf if lv else None, stream)
+        launches["n"] += B.wtconv_last_launch_count()
+        mark(1)
+        B.wtconv_forward(desc, x, f.w0f, f.b0f, f.wlf if lv else None, y, buf, bufn, stream)
+        launches["n"] += B.wtconv_last_launch_count()
+        mark(2)
+        B.wtconv_backward_data(desc, dy, f.w0f, f.wlf if lv else None, g["dx"], buf, bufn,
+                               stream)
+        launches["n"] += B.wtconv_last_launch_count()
+        mark(3)
+        B.wtconv_backward_weight(desc, x, dy, p.w0, p.b0, p.s0, p.wl if lv else None,
+                                 p.sl if lv else None, g["dw0"], g["db0"], g["ds0"],
+                                 g["dwl"] if lv else None, g["dsl"] if lv else None, buf,
+                                 bufn, stream)
+        launches["n"] += B.wtconv_last_launch_count()
+        mark(4)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    launches["n"] = 0
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(total_ms, world, dev)
+
+    seg = {"fold": 0.0, "forward": 0.0, "backward_data": 0.0, "backward_weight": 0.0}
+    for ev in evs:
+        seg["fold"] += ev[0].elapsed_time(ev[1])
+        seg["forward"] += ev[1].elapsed_time(ev[2])
+        seg["backward_data"] += ev[2].elapsed_time(ev[3])
+        seg["backward_weight"] += ev[3].elapsed_time(ev[4])
+    seg_ms = {k: v / args.steps for k, v in seg.items()}
+
+    elems = wl.elements
+    value = world * elems * args.steps / (total_ms * 1e-3) / 1e9
+    peaks = measured_peaks()
+    alg = iomodel.algorithmic(wl.k, wl.levels, 2 if wl.dtype == "bf16" else 4)
+    # dominant kernel: the plane kernel shared by forward and backward-data, or dW
+    fwd_kernel_ms = (seg_ms["forward"] + seg_ms["backward_data"]) / 2
+    dw_ms = seg_ms["backward_weight"]
+    if 2 * fwd_kernel_ms >= dw_ms:
+        dom, dom_ms, dom_alg = "wt_fwd_plane_kernel", fwd_kernel_ms, alg["forward"]
+    else:
+        dom, dom_ms, dom_alg = "wt_dw_plane_kernel", dw_ms, alg["backward_weight"]
+    tflops = elems * dom_alg["flops"] / (dom_ms * 1e-3) / 1e12
+    peak_tf = fp32_peak_tflops()
+    traffic = committed_traffic(dom, wl.name)
+    step_bytes = elems * sum(a["bytes"] for a in alg.values())
+    hbm_gbs = step_bytes * args.steps / (total_ms * 1e-3) / 1e9
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "Gelem/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(wl),
+        "roofline": {
+            "bound": "alu", "kernel": dom, "achieved": tflops, "peak": peak_tf,
+            "unit": "TFLOP/s", "frac": tflops / peak_tf, "traffic": traffic,
+            "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x 2070 MHz",
+            "algorithmic_flops_per_element": dom_alg["flops"],
+        },
+        "hbm": {
+            "achieved_gbs": hbm_gbs, "peak_gbs": peaks["hbm_gbs"],
+            "frac": hbm_gbs / peaks["hbm_gbs"], "peak_source": peaks["source"],
+            "algorithmic_bytes_per_step": step_bytes,
+        },
+        "segments_ms": seg_ms,
+        "clocks": clk,
+        "gpu_launches": launches["n"],
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, wl, inp, p, f, desc, buf, bufn, stream, world, dev)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, wl, inp, p, f, desc, buf, bufn, stream, world, dev) -> dict:
+    """Same step through the public API, with the step's inputs copied from pinned host
+    memory and its results copied back inside the timed region."""
+    import torch
+
+    from depthwise_receptive_field_gb300 import binding as B
+
+    lv = wl.levels > 0
+    xh = inp["x"].pin_memory()
+    dyh = inp["dy"].pin_memory()
+    x = torch.empty_like(xh, device=dev)
+    dy = torch.empty_like(dyh, device=dev)
+    y = torch.empty_like(x)
+    dx = torch.empty_like(dy)
+    yh = torch.empty_like(xh).pin_memory()
+    dxh = torch.empty_like(dyh).pin_memory()
+    grads = {"dw0": torch.empty_like(p.w0), "db0": torch.empty_like(p.s0),
+             "ds0": torch.empty_like(p.s0), "dwl": torch.empty_like(p.wl),
+             "dsl": torch.empty_like(p.sl)}
+    gh = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in grads.items()}
+    h2d = xh.numel() * xh.element_size() + dyh.numel() * dyh.element_size()
+    d2h = (yh.numel() * yh.element_size() + dxh.numel() * dxh.element_size() +
+           sum(v.numel() * v.element_size() for v in gh.values()))
+
+    def step():
+        x.copy_(xh, non_blocking=True)
+        dy.copy_(dyh, non_blocking=True)
+        B.wtconv_fold_scales(desc, p.w0, p.b0, p.s0, p.wl if lv else None,
+                             p.sl if lv else None, f.w0f, f.b0f, f.wlf if lv else None, stream)
+        B.wtconv_forward(desc, x, f.w0f, f.b0f, f.wlf if lv else None, y, buf, bufn, stream)
+        B.wtconv_backward(desc, x, dy, f.w0f, f.wlf if lv else None, p.w0, p.b0, p.s0,
+                          p.wl if lv else None, p.sl if lv else None, dx, grads["dw0"],
+                          grads["db0"], grads["ds0"], grads["dwl"] if lv else None,
+                          grads["dsl"] if lv else None, buf, bufn, stream)
+        yh.copy_(y, non_blocking=True)
+        dxh.copy_(dx, non_blocking=True)
+        for k in grads:
+            gh[k].copy_(grads[k], non_blocking=True)
+
+    steps = max(1, min(args.steps, 10))
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), world, dev)
+    return {"value": world * wl.elements * steps / (ms * 1e-3) / 1e9, "unit": "Gelem/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": ms / steps}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c5_large_bf16")
+    ap.add_argument("--levels", type=int, default=None,
+                    help="override the workload's L (e.g. the 128x128 level sweep)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+
+    from depthwise_receptive_field_gb300.inputs import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    if args.levels is not None:
+        wl = wl.with_levels(args.levels)
+    if not wl.backward:
+        raise SystemExit(f"{wl.name} is forward-only; the benchmarked step needs dY")
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

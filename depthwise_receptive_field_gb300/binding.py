@@ -1,0 +1,177 @@
+"""ctypes binding of libwtconv's C ABI (include/wtconv.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does no arithmetic of
+its own. Tensor arguments may be torch tensors (their ``data_ptr()`` is passed), raw
+integer device pointers, or None for optional arguments. ``stream`` may be a
+``torch.cuda.Stream``, an integer handle, or None for torch's current stream.
+
+The library is built from source on first use if it is missing or stale; if it cannot be
+built or loaded, every call raises: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+from . import build as _build
+
+WT_OK, WT_ERR_INVALID_ARG, WT_ERR_UNSUPPORTED, WT_ERR_WORKSPACE, WT_ERR_CUDA = range(5)
+WT_F32, WT_BF16 = 0, 1
+
+HEADER = os.path.join(_build.INCLUDE, "wtconv.h")
+
+
+class wt_desc(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int), ("c", ctypes.c_int), ("h", ctypes.c_int),
+                ("w", ctypes.c_int), ("k", ctypes.c_int), ("levels", ctypes.c_int),
+                ("io", ctypes.c_int)]
+
+    def __repr__(self):
+        return (f"wt_desc(n={self.n}, c={self.c}, h={self.h}, w={self.w}, k={self.k}, "
+                f"levels={self.levels}, io={'bf16' if self.io == WT_BF16 else 'f32'})")
+
+
+class WTConvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+_LOCK = threading.Lock()
+_LIB = None
+_vp = ctypes.c_void_p
+_DESC_P = ctypes.POINTER(wt_desc)
+
+_SIGNATURES = {
+    "wtconv_workspace_size": [_DESC_P, ctypes.POINTER(ctypes.c_size_t),
+                              ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)],
+    "wtconv_fold_scales": [_DESC_P] + [_vp] * 9,
+    "wtconv_forward": [_DESC_P, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp],
+    "wtconv_backward_data": [_DESC_P, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp],
+    "wtconv_backward_weight": [_DESC_P] + [_vp] * 14 + [ctypes.c_size_t, _vp],
+    "wtconv_backward": [_DESC_P] + [_vp] * 17 + [ctypes.c_size_t, _vp],
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(rebuild_if_stale: bool = True):
+    """Load (building first if needed) libwtconv.so and declare its signatures."""
+    global _LIB
+    with _LOCK:
+        if _LIB is None:
+            if rebuild_if_stale and _build.stale():
+                _build.build()
+            if not os.path.exists(_build.LIB):
+                raise RuntimeError(f"libwtconv.so not found at {_build.LIB}; run build() first")
+            lib = ctypes.CDLL(_build.LIB)
+            for name, argtypes in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = argtypes
+                fn.restype = ctypes.c_int
+            lib.wtconv_status_string.argtypes = [ctypes.c_int]
+            lib.wtconv_status_string.restype = ctypes.c_char_p
+            lib.wtconv_last_launch_count.argtypes = []
+            lib.wtconv_last_launch_count.restype = ctypes.c_int
+            _LIB = lib
+    return _LIB
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/wtconv.h declares."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:wt_status|const char\*|int)\s+(wtconv_\w+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != WT_OK:
+        raise WTConvError(status, where)
+
+
+def status_string(status: int) -> str:
+    return load_library().wtconv_status_string(int(status)).decode()
+
+
+def make_desc(n, c, h, w, k, levels, io) -> wt_desc:
+    if not isinstance(io, int):
+        import torch
+        io = WT_BF16 if io == torch.bfloat16 else WT_F32
+    return wt_desc(int(n), int(c), int(h), int(w), int(k), int(levels), int(io))
+
+
+def desc_like(x, k: int, levels: int) -> wt_desc:
+    n, c, h, w = x.shape
+    return make_desc(n, c, h, w, k, levels, x.dtype)
+
+
+def wtconv_workspace_size(desc: wt_desc):
+    """Returns (fwd, bwd_data, bwd_weight) workspace bytes."""
+    a, b, c = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load_library().wtconv_workspace_size(ctypes.byref(desc), ctypes.byref(a),
+                                                ctypes.byref(b), ctypes.byref(c)),
+           "wtconv_workspace_size")
+    return a.value, b.value, c.value
+
+
+def wtconv_fold_scales(desc, w0, b0, s0, wl, sl, w0f, b0f, wlf, stream=None):
+    _check(load_library().wtconv_fold_scales(
+        ctypes.byref(desc), _ptr(w0), _ptr(b0), _ptr(s0), _ptr(wl), _ptr(sl), _ptr(w0f),
+        _ptr(b0f), _ptr(wlf), _stream(stream)), "wtconv_fold_scales")
+
+
+def wtconv_forward(desc, x, w0f, b0f, wlf, y, ws=None, ws_bytes=0, stream=None):
+    _check(load_library().wtconv_forward(
+        ctypes.byref(desc), _ptr(x), _ptr(w0f), _ptr(b0f), _ptr(wlf), _ptr(y), _ptr(ws),
+        int(ws_bytes), _stream(stream)), "wtconv_forward")
+
+
+def wtconv_backward_data(desc, dy, w0f, wlf, dx, ws=None, ws_bytes=0, stream=None):
+    _check(load_library().wtconv_backward_data(
+        ctypes.byref(desc), _ptr(dy), _ptr(w0f), _ptr(wlf), _ptr(dx), _ptr(ws), int(ws_bytes),
+        _stream(stream)), "wtconv_backward_data")
+
+
+def wtconv_backward_weight(desc, x, dy, w0, b0, s0, wl, sl, dw0, db0, ds0, dwl, dsl, ws,
+                           ws_bytes, stream=None):
+    _check(load_library().wtconv_backward_weight(
+        ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(w0), _ptr(b0), _ptr(s0), _ptr(wl),
+        _ptr(sl), _ptr(dw0), _ptr(db0), _ptr(ds0), _ptr(dwl), _ptr(dsl), _ptr(ws),
+        int(ws_bytes), _stream(stream)), "wtconv_backward_weight")
+
+
+def wtconv_backward(desc, x, dy, w0f, wlf, w0, b0, s0, wl, sl, dx, dw0, db0, ds0, dwl, dsl,
+                    ws, ws_bytes, stream=None):
+    _check(load_library().wtconv_backward(
+        ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(w0f), _ptr(wlf), _ptr(w0), _ptr(b0),
+        _ptr(s0), _ptr(wl), _ptr(sl), _ptr(dx), _ptr(dw0), _ptr(db0), _ptr(ds0), _ptr(dwl),
+        _ptr(dsl), _ptr(ws), int(ws_bytes), _stream(stream)), "wtconv_backward")
+
+
+def wtconv_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def wtconv_last_launch_count() -> int:
+    return int(load_library().wtconv_last_launch_count())

@@ -1,0 +1,36 @@
+// Host-side declarations shared by the translation units of libwtconv (not part of the
+// public C ABI; that lives in include/wtconv.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "../../include/wtconv.h"
+
+namespace wt {
+
+// sm_103a: 227 KB of shared memory per block (opt-in), 152 SMs.
+constexpr size_t kMaxSmemPerBlock = 227 * 1024;
+constexpr int kNumSMs = 152;
+
+// forward (flip = 0) and backward-data (flip = 1, no bias): one launch
+wt_status launch_forward(const wt_desc& d, const void* x, const float* w0f, const float* b0f,
+                         const float* wlf, void* y, int flip, cudaStream_t stream,
+                         int* launches);
+size_t forward_smem_bytes(const wt_desc& d);
+
+// backward-weight: plane kernel + reduce/unfold kernel
+wt_status launch_backward_weight(const wt_desc& d, const void* x, const void* dy,
+                                 const float* w0, const float* b0, const float* s0,
+                                 const float* wl, const float* sl, float* dw0, float* db0,
+                                 float* ds0, float* dwl, float* dsl, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream, int* launches);
+size_t backward_weight_ws_bytes(const wt_desc& d);
+size_t backward_weight_smem_bytes(const wt_desc& d);
+
+// scale folding (Eq. 8): one launch
+wt_status launch_fold(const wt_desc& d, const float* w0, const float* b0, const float* s0,
+                      const float* wl, const float* sl, float* w0f, float* b0f, float* wlf,
+                      cudaStream_t stream, int* launches);
+
+}  // namespace wt

@@ -1,0 +1,110 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the C ABI and the
+CPU oracle on the same seeded inputs, and measure their disagreement."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from depthwise_receptive_field_gb300 import layer
+from depthwise_receptive_field_gb300.inputs import Workload, make_inputs
+
+# Norm-wise max relative error gates (|gpu - oracle|_max / |oracle|_max): 1e-5 for fp32
+# I/O; 2e-2 for bf16 I/O with fp32 accumulation (outputs are rounded to bf16, 2^-9 rel).
+TOL = {"f32": 1e-5, "bf16": 2e-2}
+# Parameter gradients are always fp32 sums of products of the (exact) inputs.
+TOL_PARAM = {"f32": 1e-5, "bf16": 1e-4}
+
+
+def rel_err(got, ref) -> float:
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    scale = np.abs(ref).max()
+    if scale == 0:
+        return float(np.abs(got).max())
+    return float(np.abs(got - ref).max() / scale)
+
+
+def to64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def gpu_run(inp: dict, levels: int, backward: bool, fused: bool = True) -> dict:
+    """Run fold + forward (+ backward) on cuda:0 through the C ABI."""
+    dev = torch.device("cuda", 0)
+    p = layer.Params.from_inputs(inp, dev)
+    x = inp["x"].to(dev)
+    ws = layer.Workspace(dev)
+    desc = layer.B.desc_like(x, p.k, levels)
+    f = layer.fold(p, desc)
+    out = {"y": layer.forward(x, p, f, ws)}
+    if backward:
+        dy = inp["dy"].to(dev)
+        if fused:
+            g = layer.backward(x, dy, p, f, ws)
+        else:
+            g = layer.backward_weight(x, dy, p, ws)
+            g["dx"] = layer.backward_data(dy, p, f, ws)
+        out.update(g)
+    torch.cuda.synchronize()
+    return {k: to64(v) for k, v in out.items()}
+
+
+def oracle_run(inp: dict, levels: int, backward: bool, n_idx=None, c_idx=None) -> dict:
+    """Oracle on the whole input, or on the sub-batch of batch indices n_idx and channels
+    c_idx (the layer is independent across planes; parameter gradients of a channel sum
+    over the batch, so n_idx must then be the whole batch)."""
+    x = inp["x"]
+    dy = inp["dy"]
+    w0, b0, s0, wl, sl = inp["w0"], inp["b0"], inp["s0"], inp["wl"], inp["sl"]
+    if c_idx is not None:
+        ci = torch.as_tensor(c_idx)
+        x = x[:, ci]
+        dy = dy[:, ci] if dy is not None else None
+        w0, b0, s0 = w0[ci], b0[ci], s0[ci]
+        wl, sl = wl[:, ci], sl[:, ci]
+    if n_idx is not None:
+        ni = torch.as_tensor(n_idx)
+        x = x[ni]
+        dy = dy[ni] if dy is not None else None
+    out = {"y": oracle.forward(x, w0, b0, s0, wl, sl, levels)}
+    if backward:
+        g = oracle.backward(x, dy, w0, b0, s0, wl, sl, levels)
+        out.update(g)
+    return out
+
+
+def compare(gpu: dict, ref: dict, dtype: str, levels: int, c_idx=None, n_idx=None) -> dict:
+    """Per-tensor relative errors (gpu sliced to the oracle's sub-batch when sampled)."""
+    errs = {}
+    for name, r in ref.items():
+        g = gpu[name]
+        if name in ("y", "dx"):
+            if c_idx is not None:
+                g = g[:, list(c_idx)]
+            if n_idx is not None:
+                g = g[list(n_idx)]
+        elif c_idx is not None:
+            if name in ("dw0", "db0", "ds0"):
+                g = g[list(c_idx)]
+            else:
+                g = g[:, list(c_idx)]
+        if name in ("dwl", "dsl") and levels == 0:
+            continue
+        errs[name] = rel_err(g, r)
+    return errs
+
+
+def assert_within(errs: dict, dtype: str, what: str = ""):
+    for name, e in errs.items():
+        tol = TOL[dtype] if name in ("y", "dx") else TOL_PARAM[dtype]
+        assert e <= tol, f"{what} {name}: rel err {e:.3e} > {tol:.1e} (all: {errs})"
+
+
+def run_and_compare(wl: Workload, *, bias_and_scale=False, sample_channels=None, fused=True):
+    inp = make_inputs(wl, bias_and_scale=bias_and_scale)
+    gpu = gpu_run(inp, wl.levels, wl.backward, fused=fused)
+    ref = oracle_run(inp, wl.levels, wl.backward, c_idx=sample_channels)
+    errs = compare(gpu, ref, wl.dtype, wl.levels, c_idx=sample_channels)
+    return errs, gpu

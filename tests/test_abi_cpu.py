@@ -1,0 +1,91 @@
+"""The C-ABI library builds, loads without a GPU, exports every declared symbol, and its
+host-side validation and workspace sizing behave as include/wtconv.h documents. No CUDA
+kernel is launched here: every call below returns before reaching the device."""
+import ctypes
+
+import pytest
+
+from depthwise_receptive_field_gb300 import binding as B
+from depthwise_receptive_field_gb300.inputs import WORKLOADS
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return B.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = B.declared_functions()
+    assert len(names) >= 8, names
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_header_declares_the_method_entry_points():
+    names = set(B.declared_functions())
+    for required in ("wtconv_forward", "wtconv_backward_data", "wtconv_backward_weight",
+                     "wtconv_fold_scales", "wtconv_workspace_size", "wtconv_status_string"):
+        assert required in names
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert B.status_string(s).startswith("WT_")
+    assert "unknown" in B.status_string(99)
+
+
+BAD = [
+    dict(k=4),              # even kernel
+    dict(k=0),
+    dict(levels=-1),
+    dict(levels=13),
+    dict(h=30, levels=2),   # 30 % 4 != 0
+    dict(w=12, levels=3),   # 12 % 8 != 0
+    dict(n=0),
+    dict(c=0),
+    dict(io=7),
+]
+
+
+@pytest.mark.parametrize("override", BAD)
+def test_invalid_descriptors_rejected(lib, override):
+    base = dict(n=2, c=3, h=32, w=32, k=5, levels=2, io=B.WT_F32)
+    base.update(override)
+    d = B.wt_desc(**base)
+    a = ctypes.c_size_t()
+    st = lib.wtconv_workspace_size(ctypes.byref(d), ctypes.byref(a), None, None)
+    assert st == B.WT_ERR_INVALID_ARG
+    # the compute entry points validate the same way before touching the device
+    st = lib.wtconv_forward(ctypes.byref(d), 16, 16, None, 16, 16, None, 0, None)
+    assert st == B.WT_ERR_INVALID_ARG
+
+
+def test_unbuilt_kernel_size_is_unsupported(lib):
+    d = B.wt_desc(1, 1, 32, 32, 9, 1, B.WT_F32)
+    assert lib.wtconv_workspace_size(ctypes.byref(d), None, None, None) == B.WT_ERR_UNSUPPORTED
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    d = B.wt_desc(1, 2, 16, 16, 5, 1, B.WT_F32)
+    assert lib.wtconv_forward(ctypes.byref(d), None, 16, None, 16, 16, None, 0, None) == 1
+    assert lib.wtconv_forward(ctypes.byref(d), 8, 16, None, 16, 16, None, 0, None) == 1
+    assert lib.wtconv_backward_data(ctypes.byref(d), 16, 16, 16, 24, None, 0, None) == 1
+    assert lib.wtconv_fold_scales(ctypes.byref(d), 16, None, 16, None, 16, 16, None, 16,
+                                  None) == 1
+    # backward_weight: too small a workspace is reported before any launch
+    args = [16] * 14
+    st = lib.wtconv_backward_weight(ctypes.byref(d), *args, 0, None)
+    assert st in (B.WT_ERR_WORKSPACE, B.WT_ERR_INVALID_ARG)
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_workspace_sizes_for_workloads(lib, name):
+    wl = WORKLOADS[name]
+    d = B.make_desc(wl.n, wl.c, wl.h, wl.w, wl.k, wl.levels,
+                    B.WT_BF16 if wl.dtype == "bf16" else B.WT_F32)
+    fwd, bwd_d, bwd_w = B.wtconv_workspace_size(d)
+    assert fwd == 0 and bwd_d == 0
+    kk = wl.k * wl.k
+    per_partial = (kk + 1 + 4 * kk * wl.levels) * 4
+    assert bwd_w > 0 and bwd_w % per_partial == 0
+    assert bwd_w // per_partial >= wl.c  # at least one partial vector per channel

@@ -1,0 +1,112 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle, element by element,
+on the seeded synthetic workloads and on edge shapes. All tests need a GB300."""
+import numpy as np
+import pytest
+import torch
+
+from depthwise_receptive_field_gb300 import binding as B
+from depthwise_receptive_field_gb300 import layer
+from depthwise_receptive_field_gb300.inputs import WORKLOADS, make_inputs, shape_workload
+from parity_util import assert_within, gpu_run, run_and_compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    B.load_library()
+
+
+def test_c1_small_forward():
+    wl = WORKLOADS["c1_small_fwd"]
+    errs, _ = run_and_compare(wl)
+    assert_within(errs, wl.dtype, wl.name)
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_c2_fp32_train(fused):
+    wl = WORKLOADS["c2_fp32_train"]
+    errs, _ = run_and_compare(wl, fused=fused)
+    assert_within(errs, wl.dtype, wl.name)
+
+
+def test_c2_with_bias_and_base_scale():
+    wl = WORKLOADS["c2_fp32_train"]
+    errs, _ = run_and_compare(wl, bias_and_scale=True)
+    assert_within(errs, wl.dtype, wl.name)
+
+
+def test_c3_stage1_bf16_full():
+    wl = WORKLOADS["c3_stage1_bf16"]
+    errs, _ = run_and_compare(wl)
+    assert_within(errs, wl.dtype, wl.name)
+
+
+@pytest.mark.parametrize("levels", [0, 1, 2, 3, 4])
+def test_c4_level_sweep_sampled(levels):
+    """Full 32x128x128x128 bf16 shape, checked on three channels (all batch entries)."""
+    wl = WORKLOADS["c4_sweep_bf16"].with_levels(levels)
+    errs, _ = run_and_compare(wl, sample_channels=[0, 77, 127])
+    assert_within(errs, wl.dtype, wl.name)
+
+
+def test_c5_large_sampled():
+    """Full 16x256x256x256 bf16 L=5 shape (the benchmarked one), three channels checked."""
+    wl = WORKLOADS["c5_large_bf16"]
+    errs, _ = run_and_compare(wl, sample_channels=[0, 131, 255])
+    assert_within(errs, wl.dtype, wl.name)
+
+
+EDGE = [  # n, c, h, w, k, L, dtype
+    (1, 1, 8, 8, 3, 3, "f32"),        # deepest level 1x1
+    (2, 3, 48, 40, 5, 3, "f32"),      # ragged deep grids (6x5 at L=3)
+    (1, 2, 7, 9, 5, 0, "f32"),        # odd plane, plain depthwise
+    (1, 2, 6, 10, 3, 1, "f32"),       # H, W = 2 mod 4
+    (2, 2, 136, 72, 5, 3, "bf16"),    # several 64x64 tiles with a ragged tail
+    (1, 1, 64, 64, 7, 6, "f32"),      # k = 7 down to a 1x1 level
+    (1, 3, 32, 32, 1, 2, "f32"),      # k = 1
+    (1, 1, 256, 256, 5, 5, "f32"),    # largest fp32 plane of the workloads
+    (3, 5, 20, 12, 5, 2, "bf16"),     # odd channel count, small planes
+    (2, 4, 96, 160, 3, 4, "bf16"),    # wide plane, k = 3
+]
+
+
+@pytest.mark.parametrize("n,c,h,w,k,L,dtype", EDGE)
+def test_edge_shapes(n, c, h, w, k, L, dtype):
+    wl = shape_workload(n, c, h, w, k, L, dtype, seed=1000 + h + w + k + L)
+    errs, _ = run_and_compare(wl, bias_and_scale=True)
+    assert_within(errs, wl.dtype, wl.name)
+
+
+def test_backward_is_deterministic():
+    wl = WORKLOADS["c3_stage1_bf16"]
+    inp = make_inputs(wl)
+    a = gpu_run(inp, wl.levels, True)
+    b = gpu_run(inp, wl.levels, True)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_workspace_errors():
+    wl = WORKLOADS["c2_fp32_train"]
+    inp = make_inputs(wl)
+    dev = torch.device("cuda", 0)
+    p = layer.Params.from_inputs(inp, dev)
+    x = inp["x"].to(dev)
+    dy = inp["dy"].to(dev)
+    desc = B.desc_like(x, p.k, wl.levels)
+    _, _, nb = B.wtconv_workspace_size(desc)
+    assert nb > 0
+    small = torch.empty(nb - 16, dtype=torch.uint8, device=dev)
+    g = {k: torch.empty_like(v) for k, v in
+         {"dw0": p.w0, "db0": p.s0, "ds0": p.s0, "dwl": p.wl, "dsl": p.sl}.items()}
+    with pytest.raises(B.WTConvError) as ei:
+        B.wtconv_backward_weight(desc, x, dy, p.w0, p.b0, p.s0, p.wl, p.sl, g["dw0"], g["db0"],
+                                 g["ds0"], g["dwl"], g["dsl"], small, small.numel())
+    assert ei.value.status == B.WT_ERR_WORKSPACE
+    # misaligned input pointer
+    with pytest.raises(B.WTConvError) as ei:
+        B.wtconv_forward(desc, x.data_ptr() + 4, p.w0, None, p.wl, torch.empty_like(x))
+    assert ei.value.status == B.WT_ERR_INVALID_ARG
