@@ -50,8 +50,8 @@ _SIGNATURES = {
     "wtconv_fold_scales": [_DESC_P] + [_vp] * 9,
     "wtconv_forward": [_DESC_P, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp],
     "wtconv_backward_data": [_DESC_P, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp],
-    "wtconv_backward_weight": [_DESC_P] + [_vp] * 14 + [ctypes.c_size_t, _vp],
-    "wtconv_backward": [_DESC_P] + [_vp] * 17 + [ctypes.c_size_t, _vp],
+    "wtconv_backward_weight": [_DESC_P] + [_vp] * 13 + [ctypes.c_size_t, _vp],
+    "wtconv_backward": [_DESC_P] + [_vp] * 16 + [ctypes.c_size_t, _vp],
 }
 
 

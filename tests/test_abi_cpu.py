@@ -73,7 +73,7 @@ def test_null_and_misaligned_pointers_rejected(lib):
     assert lib.wtconv_fold_scales(ctypes.byref(d), 16, None, 16, None, 16, 16, None, 16,
                                   None) == 1
     # backward_weight: too small a workspace is reported before any launch
-    args = [16] * 14
+    args = [16] * 13
     st = lib.wtconv_backward_weight(ctypes.byref(d), *args, 0, None)
     assert st in (B.WT_ERR_WORKSPACE, B.WT_ERR_INVALID_ARG)
 
@@ -89,3 +89,14 @@ def test_workspace_sizes_for_workloads(lib, name):
     per_partial = (kk + 1 + 4 * kk * wl.levels) * 4
     assert bwd_w > 0 and bwd_w % per_partial == 0
     assert bwd_w // per_partial >= wl.c  # at least one partial vector per channel
+
+
+def test_binding_arity_matches_header():
+    """Each ctypes signature has exactly as many parameters as the header declares."""
+    import re
+    text = open(B.HEADER).read()
+    for name, argtypes in B._SIGNATURES.items():
+        m = re.search(rf"\b{name}\s*\(([^;]*?)\)\s*;", text, flags=re.S)
+        assert m, name
+        params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
+        assert len(params) == len(argtypes), (name, len(params), len(argtypes))
