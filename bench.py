@@ -185,8 +185,8 @@ def workload_config(wl) -> dict:
 # ----------------------------------------------------------------------------------
 
 def oracle_sample(wl, images: int, channels: int):
-    """A bounded sample of the workload: the first `images` batch entries of the first
-    `channels` channels, same recipe and seed (inputs drawn at full size, then sliced)."""
+    """A bounded sample of the workload: `images` batch entries of its first `channels`
+    channels, drawn with the workload's recipe and seed at the smaller batch size."""
     from depthwise_receptive_field_gb300.inputs import make_inputs
     inp = make_inputs(wl, n=images)
     sl = slice(0, channels)
