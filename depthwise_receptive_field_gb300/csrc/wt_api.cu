@@ -81,10 +81,12 @@ wt_status wtconv_workspace_size(const wt_desc* desc, size_t* fwd, size_t* bwd_da
                                 size_t* bwd_weight) {
     wt_status st = check_desc(desc);
     if (st != WT_OK) return st;
-    if (forward_smem_bytes(*desc) > kMaxSmemPerBlock) return WT_ERR_UNSUPPORTED;
+    size_t fsmem = 0, fws = 0;
+    if (!forward_sizes(*desc, &fsmem, &fws)) return WT_ERR_UNSUPPORTED;
+    if (fsmem > kMaxSmemPerBlock) return WT_ERR_UNSUPPORTED;
     if (backward_weight_smem_bytes(*desc) > kMaxSmemPerBlock) return WT_ERR_UNSUPPORTED;
-    if (fwd) *fwd = 0;
-    if (bwd_data) *bwd_data = 0;
+    if (fwd) *fwd = fws;
+    if (bwd_data) *bwd_data = fws;
     if (bwd_weight) *bwd_weight = backward_weight_ws_bytes(*desc);
     return WT_OK;
 }
@@ -109,16 +111,15 @@ wt_status wtconv_fold_scales(const wt_desc* desc, const float* w0, const float* 
 wt_status wtconv_forward(const wt_desc* desc, const void* x, const float* w0f,
                          const float* b0f, const float* wlf, void* y, void* ws,
                          size_t ws_bytes, wt_stream_t stream) {
-    (void)ws;
-    (void)ws_bytes;
     wt_status st = check_desc(desc);
     if (st != WT_OK) return st;
     if (check_io(x) || check_io(y) || check_param(w0f)) return WT_ERR_INVALID_ARG;
+    if (ws && !aligned(ws, 256)) return WT_ERR_INVALID_ARG;
     if (b0f && !aligned(b0f, 4)) return WT_ERR_INVALID_ARG;
     if (desc->levels > 0 && check_param(wlf)) return WT_ERR_INVALID_ARG;
     int launches = 0;
-    st = launch_forward(*desc, x, w0f, b0f, wlf, y, 0, reinterpret_cast<cudaStream_t>(stream),
-                        &launches);
+    st = launch_forward(*desc, x, w0f, b0f, wlf, y, 0, ws, ws_bytes,
+                        reinterpret_cast<cudaStream_t>(stream), &launches);
     if (st == WT_OK) g_last_launches = launches;
     return st;
 }
@@ -126,14 +127,13 @@ wt_status wtconv_forward(const wt_desc* desc, const void* x, const float* w0f,
 wt_status wtconv_backward_data(const wt_desc* desc, const void* dy, const float* w0f,
                                const float* wlf, void* dx, void* ws, size_t ws_bytes,
                                wt_stream_t stream) {
-    (void)ws;
-    (void)ws_bytes;
     wt_status st = check_desc(desc);
     if (st != WT_OK) return st;
     if (check_io(dy) || check_io(dx) || check_param(w0f)) return WT_ERR_INVALID_ARG;
+    if (ws && !aligned(ws, 256)) return WT_ERR_INVALID_ARG;
     if (desc->levels > 0 && check_param(wlf)) return WT_ERR_INVALID_ARG;
     int launches = 0;
-    st = launch_forward(*desc, dy, w0f, nullptr, wlf, dx, 1,
+    st = launch_forward(*desc, dy, w0f, nullptr, wlf, dx, 1, ws, ws_bytes,
                         reinterpret_cast<cudaStream_t>(stream), &launches);
     if (st == WT_OK) g_last_launches = launches;
     return st;
@@ -153,7 +153,7 @@ wt_status wtconv_backward_weight(const wt_desc* desc, const void* x, const void*
     if (desc->levels > 0 &&
         (check_param(wl) || check_param(sl) || check_param(dwl) || check_param(dsl)))
         return WT_ERR_INVALID_ARG;
-    if (ws && !aligned(ws, 16)) return WT_ERR_INVALID_ARG;
+    if (ws && !aligned(ws, 256)) return WT_ERR_INVALID_ARG;
     if (ws_bytes < backward_weight_ws_bytes(*desc) || ws == nullptr) return WT_ERR_WORKSPACE;
     int launches = 0;
     st = launch_backward_weight(*desc, x, dy, w0, b0, s0, wl, sl, dw0, db0, ds0, dwl, dsl, ws,
@@ -176,11 +176,11 @@ wt_status wtconv_backward(const wt_desc* desc, const void* x, const void* dy,
     if (desc->levels > 0 && (check_param(wlf) || check_param(wl) || check_param(sl) ||
                              check_param(dwl) || check_param(dsl)))
         return WT_ERR_INVALID_ARG;
-    if (ws && !aligned(ws, 16)) return WT_ERR_INVALID_ARG;
+    if (ws && !aligned(ws, 256)) return WT_ERR_INVALID_ARG;
     if (ws_bytes < backward_weight_ws_bytes(*desc) || ws == nullptr) return WT_ERR_WORKSPACE;
     int launches = 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    st = launch_forward(*desc, dy, w0f, nullptr, wlf, dx, 1, s, &launches);
+    st = launch_forward(*desc, dy, w0f, nullptr, wlf, dx, 1, ws, ws_bytes, s, &launches);
     if (st != WT_OK) return st;
     st = launch_backward_weight(*desc, x, dy, w0, b0, s0, wl, sl, dw0, db0, ds0, dwl, dsl, ws,
                                 ws_bytes, s, &launches);

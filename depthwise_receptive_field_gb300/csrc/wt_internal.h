@@ -13,11 +13,12 @@ namespace wt {
 constexpr size_t kMaxSmemPerBlock = 227 * 1024;
 constexpr int kNumSMs = 152;
 
-// forward (flip = 0) and backward-data (flip = 1, no bias): one launch
+// forward (flip = 0) and backward-data (flip = 1, no bias): one persistent launch; the
+// workspace holds one deep-level scratch slot per CTA (none when L < 2)
 wt_status launch_forward(const wt_desc& d, const void* x, const float* w0f, const float* b0f,
-                         const float* wlf, void* y, int flip, cudaStream_t stream,
-                         int* launches);
-size_t forward_smem_bytes(const wt_desc& d);
+                         const float* wlf, void* y, int flip, void* ws, size_t ws_bytes,
+                         cudaStream_t stream, int* launches);
+bool forward_sizes(const wt_desc& d, size_t* smem, size_t* ws);
 
 // backward-weight: plane kernel + reduce/unfold kernel
 wt_status launch_backward_weight(const wt_desc& d, const void* x, const void* dy,

@@ -1,0 +1,228 @@
+// Tile geometry and streaming register-blocked k x k stencils shared by the forward /
+// backward-data kernel and the backward-weight kernel (sm_103a).
+//
+// A full-resolution tile is 64x64 pixels staged with a 2R-pixel halo (R = (k-1)/2), so
+// that its 32x32 level-1 Haar coefficients (§4.1 Eq. 5 of "Fast and Memory-Efficient
+// Wavelet Convolutions via I/O-Aware Reformulation") can be formed with an R-coefficient
+// halo. Every k x k filter (or its weight-gradient correlation) streams one window row at
+// a time through registers with the k*k taps in registers and independent accumulators
+// innermost. Shared-memory rows are read as 16-byte vectors at consecutive addresses
+// across the lanes of a warp (no bank conflicts).
+#pragma once
+
+#include "wt_common.cuh"
+
+namespace wt {
+
+constexpr int kTile = 64;       // full-resolution tile side, pixels
+constexpr int kCT = kTile / 2;  // coefficient tile side; also the deep-level output tile
+
+template <int K>
+struct FG {
+    static constexpr int R = (K - 1) / 2;
+    static constexpr int KK = K * K;
+    static constexpr int KKP = (KK + 3) & ~3;              // padded kernel stride (16 B)
+    static constexpr int PAD = (4 - (R % 4)) % 4;          // aligns 8x4 windows to 16 B
+    static constexpr int XROWS = kTile + 4 * R;
+    static constexpr int XCOLS = kTile + 4 * R;
+    static constexpr int BWR = 8 + 2 * R;                  // window rows of an 8x4 block
+    static constexpr int BNC = (4 + 2 * R + 3) / 4;        // float4 per window row (4-wide)
+    static constexpr int XPITCH_A = PAD + XCOLS;
+    static constexpr int XPITCH_B = PAD + (kTile - 4) + R + 4 * BNC;
+    static constexpr int XPITCH = ((XPITCH_A > XPITCH_B ? XPITCH_A : XPITCH_B) + 3) & ~3;
+    static constexpr int BT = kCT + 2 * R;                 // coefficient tile side with halo
+    static constexpr int CNC = (4 + 2 * R + 3) / 4;        // float4 per window row (4x4 block)
+    static constexpr int BPITCH_B = (kCT - 4) + 4 * CNC;
+    static constexpr int BPITCH = ((BT > BPITCH_B ? BT : BPITCH_B) + 3) & ~3;
+    static constexpr int BAND = BT * BPITCH;               // floats per haloed band tile
+    static constexpr int ZAND = kCT * kCT;                 // floats per un-haloed band tile
+    static constexpr int STAGE_STORE = (2 * R + PAD) % 4;  // alignment of staged 4-groups
+};
+
+template <int N>
+__device__ __forceinline__ void load_row(const float* p, float (&v)[4 * N]) {
+#pragma unroll
+    for (int m = 0; m < N; ++m) {
+        const float4 t = *reinterpret_cast<const float4*>(p + 4 * m);
+        v[4 * m] = t.x;
+        v[4 * m + 1] = t.y;
+        v[4 * m + 2] = t.z;
+        v[4 * m + 3] = t.w;
+    }
+}
+
+// acc[o][q] = sum_{u,v} w[u][v] win[o+u][q+v] for a 4x4 output block (acc overwritten).
+template <int K>
+__device__ __forceinline__ void conv4x4(const float* win, int pitch, const float* wsm,
+                                        float (&acc)[4][4]) {
+    constexpr int KK = FG<K>::KK, R = FG<K>::R, CNC = FG<K>::CNC;
+    float w[KK];
+#pragma unroll
+    for (int q = 0; q < KK; ++q) w[q] = wsm[q];
+#pragma unroll
+    for (int o = 0; o < 4; ++o)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[o][q] = 0.f;
+#pragma unroll
+    for (int r = 0; r < 4 + 2 * R; ++r) {
+        float v[4 * CNC];
+        load_row<CNC>(win + r * pitch, v);
+#pragma unroll
+        for (int o = 0; o < 4; ++o) {
+            const int u = r - o;
+            if (u < 0 || u >= K) continue;
+#pragma unroll
+            for (int vv = 0; vv < K; ++vv)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[o][q] = fmaf(w[u * K + vv], v[q + vv], acc[o][q]);
+        }
+    }
+}
+
+// acc[o][q] += sum_{u,v} w[u][v] win[o+u][q+v] for an 8-row x 4-col output block.
+template <int K>
+__device__ __forceinline__ void conv8x4(const float* win, int pitch, const float* wsm,
+                                        float (&acc)[8][4]) {
+    constexpr int KK = FG<K>::KK, BWR = FG<K>::BWR, BNC = FG<K>::BNC;
+    float w[KK];
+#pragma unroll
+    for (int q = 0; q < KK; ++q) w[q] = wsm[q];
+#pragma unroll
+    for (int r = 0; r < BWR; ++r) {
+        float v[4 * BNC];
+        load_row<BNC>(win + r * pitch, v);
+#pragma unroll
+        for (int o = 0; o < 8; ++o) {
+            const int u = r - o;
+            if (u < 0 || u >= K) continue;
+#pragma unroll
+            for (int vv = 0; vv < K; ++vv)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[o][q] = fmaf(w[u * K + vv], v[q + vv], acc[o][q]);
+        }
+    }
+}
+
+// Weight-gradient correlation: acc[u*K+v] += sum_{o,q} g[o][q] win[o+u][q+v] over a block
+// of ROWS x 4 gradient values (ROWS = 4 or 8); acc may be longer than K*K (extra entries
+// are left alone).
+template <int K, int ROWS, int NA>
+__device__ __forceinline__ void corr_rows(const float* win, int pitch, const float (&g)[ROWS][4],
+                                          float (&acc)[NA]) {
+    static_assert(NA >= K * K, "accumulator too short");
+    constexpr int R = FG<K>::R, NC = (4 + 2 * R + 3) / 4;
+#pragma unroll
+    for (int r = 0; r < ROWS + 2 * R; ++r) {
+        float v[4 * NC];
+        load_row<NC>(win + r * pitch, v);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int o = 0; o < ROWS; ++o) {
+                const int u = r - o;
+                if (u < 0 || u >= K) continue;
+#pragma unroll
+                for (int vv = 0; vv < K; ++vv)
+                    acc[u * K + vv] = fmaf(g[o][q], v[q + vv], acc[u * K + vv]);
+            }
+    }
+}
+
+// Stage pixels [y0-2R, y0+64+2R) x [x0-2R, x0+64+2R) of a plane into xs (pitch XPITCH,
+// column c stored at c + PAD), zero outside the plane. vec: W % 4 == 0 (aligned rows).
+template <int K, typename T>
+__device__ __forceinline__ void stage_tile(const T* xp, int H, int W, int vec, float* xs,
+                                           int y0, int x0) {
+    constexpr int R = FG<K>::R, PAD = FG<K>::PAD, XP = FG<K>::XPITCH;
+    constexpr int ROWS = FG<K>::XROWS, COLS = FG<K>::XCOLS;
+    const int c_lo = x0 - 2 * R;
+    if (vec) {
+        const int g_lo = c_lo >= 0 ? (c_lo & ~3) : -((-c_lo + 3) & ~3);
+        const int ng = (x0 + kTile + 2 * R - g_lo + 3) >> 2;
+        for (int idx = threadIdx.x; idx < ROWS * ng; idx += blockDim.x) {
+            const int r = idx / ng, g = idx - r * ng;
+            const int gy = y0 - 2 * R + r, gx = g_lo + 4 * g;
+            float4 v = f4_zero();
+            if (gy >= 0 && gy < H && gx >= 0 && gx < W) v = IO<T>::ld4(xp + (size_t)gy * W + gx);
+            const int cc = gx - c_lo;
+            float* dst = xs + r * XP + PAD + cc;
+            if (cc >= 0 && cc + 3 < COLS) {
+                if constexpr (FG<K>::STAGE_STORE == 0) {
+                    *reinterpret_cast<float4*>(dst) = v;
+                } else if constexpr (FG<K>::STAGE_STORE == 2) {
+                    reinterpret_cast<float2*>(dst)[0] = make_float2(v.x, v.y);
+                    reinterpret_cast<float2*>(dst)[1] = make_float2(v.z, v.w);
+                } else {
+                    dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
+                }
+            } else {
+                const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (cc + q >= 0 && cc + q < COLS) dst[q] = e[q];
+            }
+        }
+    } else {
+        for (int idx = threadIdx.x; idx < ROWS * COLS; idx += blockDim.x) {
+            const int r = idx / COLS, cc = idx - r * COLS;
+            const int gy = y0 - 2 * R + r, gx = c_lo + cc;
+            float v = 0.f;
+            if (gy >= 0 && gy < H && gx >= 0 && gx < W) v = IO<T>::ld(xp + (size_t)gy * W + gx);
+            xs[r * XP + PAD + cc] = v;
+        }
+    }
+}
+
+// Level-1 unnormalized subbands of the staged tile with an R-coefficient halo,
+// band-major [4][BT][BPITCH] (cell (ci, cj) <-> coefficient (y0/2 - R + ci, x0/2 - R + cj)).
+template <int K>
+__device__ __forceinline__ void bands_from_tile(const float* xs, float* bs) {
+    constexpr int PAD = FG<K>::PAD, XP = FG<K>::XPITCH, BT = FG<K>::BT;
+    constexpr int BP = FG<K>::BPITCH, BAND = FG<K>::BAND;
+    for (int idx = threadIdx.x; idx < BT * BT; idx += blockDim.x) {
+        const int ci = idx / BT, cj = idx - ci * BT;
+        const float* p = xs + (2 * ci) * XP + PAD + 2 * cj;
+        float a, b, c, d;
+        if constexpr ((PAD & 1) == 0) {
+            const float2 t0 = *reinterpret_cast<const float2*>(p);
+            const float2 t1 = *reinterpret_cast<const float2*>(p + XP);
+            a = t0.x; b = t0.y; c = t1.x; d = t1.y;
+        } else {
+            a = p[0]; b = p[1]; c = p[XP]; d = p[XP + 1];
+        }
+        const float4 u = haar_u(a, b, c, d);
+        float* q = bs + ci * BP + cj;
+        q[0] = u.x;
+        q[BAND] = u.y;
+        q[2 * BAND] = u.z;
+        q[3 * BAND] = u.w;
+    }
+}
+
+// Level-l (l >= 2) carrier 2x2 block feeding subband cell (gi, gj): from X itself when
+// l == 2 (its 4x4 pixel block, through the level-1 carrier), else from the carrier
+// X^(l-1) of width Wp in shared memory. Values are Eq. 5's normalized low-pass carrier.
+template <typename T>
+__device__ __forceinline__ void carrier_block(int l, const T* xp, int W, const float* carp,
+                                              int Wp, int gi, int gj, float& ca, float& cb,
+                                              float& cc, float& cd) {
+    if (l == 2) {
+        const T* p = xp + (size_t)(4 * gi) * W + 4 * gj;
+        const float4 r0 = IO<T>::ld4(p);
+        const float4 r1 = IO<T>::ld4(p + W);
+        const float4 r2 = IO<T>::ld4(p + 2 * (size_t)W);
+        const float4 r3 = IO<T>::ld4(p + 3 * (size_t)W);
+        ca = 0.5f * (r0.x + r0.y + r1.x + r1.y);
+        cb = 0.5f * (r0.z + r0.w + r1.z + r1.w);
+        cc = 0.5f * (r2.x + r2.y + r3.x + r3.y);
+        cd = 0.5f * (r2.z + r2.w + r3.z + r3.w);
+    } else {
+        const float* q = carp + (size_t)(2 * gi) * Wp + 2 * gj;
+        ca = q[0];
+        cb = q[1];
+        cc = q[Wp];
+        cd = q[Wp + 1];
+    }
+}
+
+}  // namespace wt
