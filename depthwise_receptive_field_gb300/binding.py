@@ -52,6 +52,7 @@ _SIGNATURES = {
     "wtconv_backward_data": [_DESC_P, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp],
     "wtconv_backward_weight": [_DESC_P] + [_vp] * 13 + [ctypes.c_size_t, _vp],
     "wtconv_backward": [_DESC_P] + [_vp] * 16 + [ctypes.c_size_t, _vp],
+    "wtconv_backward_weight_noalloc": [_DESC_P] + [_vp] * 12 + [_vp],
 }
 
 
@@ -167,6 +168,15 @@ def wtconv_backward(desc, x, dy, w0f, wlf, w0, b0, s0, wl, sl, dx, dw0, db0, ds0
         ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(w0f), _ptr(wlf), _ptr(w0), _ptr(b0),
         _ptr(s0), _ptr(wl), _ptr(sl), _ptr(dx), _ptr(dw0), _ptr(db0), _ptr(ds0), _ptr(dwl),
         _ptr(dsl), _ptr(ws), int(ws_bytes), _stream(stream)), "wtconv_backward")
+
+
+def wtconv_backward_weight_noalloc(desc, x, dy, w0, b0, s0, wl, sl, dw0, db0, ds0, dwl, dsl,
+                                   stream=None):
+    """Backward-weight with the library's built-in 4 MiB scratch (no workspace)."""
+    _check(load_library().wtconv_backward_weight_noalloc(
+        ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(w0), _ptr(b0), _ptr(s0), _ptr(wl),
+        _ptr(sl), _ptr(dw0), _ptr(db0), _ptr(ds0), _ptr(dwl), _ptr(dsl), _stream(stream)),
+        "wtconv_backward_weight_noalloc")
 
 
 def wtconv_status_string(status: int) -> str:

@@ -27,6 +27,15 @@ wt_status launch_backward_weight(const wt_desc& d, const void* x, const void* dy
                                  float* ds0, float* dwl, float* dsl, void* ws, size_t ws_bytes,
                                  cudaStream_t stream, int* launches);
 size_t backward_weight_ws_bytes(const wt_desc& d);
+// pieces of the backward-weight path: the per-plane partial kernel alone (partials
+// [C][d.n][KP] to `part`) and the reduce + unfold kernel alone over [C][groups][KP]
+wt_status launch_dw_partials(const wt_desc& d, const void* x, const void* dy, float* part,
+                             cudaStream_t stream, int* launches);
+wt_status launch_dw_reduce(const wt_desc& d, const float* part, int groups, const float* w0,
+                           const float* b0, const float* s0, const float* wl, const float* sl,
+                           float* dw0, float* db0, float* ds0, float* dwl, float* dsl,
+                           cudaStream_t stream, int* launches);
+size_t dw_partial_floats(const wt_desc& d);
 size_t backward_weight_smem_bytes(const wt_desc& d);
 
 // scale folding (Eq. 8): one launch

@@ -1,0 +1,134 @@
+// Backward-weight entry point that allocates nothing and takes no workspace.
+//
+// Some callers cannot give this library a workspace: a runtime that owns all device
+// memory through its own pool and forbids raw cudaMalloc calls, or a latency-critical
+// path that must not call cudaMalloc because it may synchronize the whole device. For
+// them, wtconv_backward_weight_noalloc keeps its scratch in a fixed array compiled into
+// the library (kNoAllocScratchBytes, 4 MiB). Every GPU that loads the library holds that
+// array until the process exits.
+//
+// The scratch holds the per-channel running totals [C][KP] followed by the per-plane
+// partial vectors of one chunk of images [C][nc][KP] (KP = k*k + 1 + 4 k*k L). The batch
+// is processed in chunks of nc images, as many as fit; each chunk runs the ordinary
+// per-plane partial kernel, then a small kernel folds the chunk into the totals (the
+// first chunk overwrites them, so nothing needs clearing beforehand), and finally the
+// ordinary reduce + unfold kernel turns the totals into gradients.
+//
+// Every call shares the one array and leaves its last contents behind: two calls whose
+// kernels overlap on the GPU (different streams, or different host threads on the same
+// device) race on it. The first call on each device looks up the array's device address
+// with cudaGetSymbolAddress (host code cannot use the symbol itself: it names a host-side
+// stand-in); make that first call before any stream capture.
+#include <mutex>
+
+#include "wt_internal.h"
+
+namespace wt {
+
+namespace {
+
+constexpr size_t kNoAllocScratchFloats = size_t(1) << 20;
+constexpr size_t kNoAllocScratchBytes = kNoAllocScratchFloats * sizeof(float);  // 4 MiB
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+
+std::mutex g_setup_mu;
+float* g_scratch_dev_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up once per device).
+wt_status scratch_on_current_device(float** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return WT_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return WT_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    if (g_scratch_dev_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+            return WT_ERR_CUDA;
+        g_scratch_dev_ptr[dev] = static_cast<float*>(p);
+    }
+    *out = g_scratch_dev_ptr[dev];
+    return WT_OK;
+}
+
+// totals[c][e] = (first ? 0 : totals[c][e]) + sum_{j < nc} part[c][j][e], fixed order.
+__global__ void wt_dw_accumulate_kernel(const float* part, int C, int nc, int KP, float* totals,
+                                        int first) {
+    const size_t n_tot = (size_t)C * KP;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n_tot;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const size_t c = i / KP, e = i - c * KP;
+        float s = first ? 0.f : totals[i];
+        for (int j = 0; j < nc; ++j) s += part[(c * nc + j) * KP + e];
+        totals[i] = s;
+    }
+}
+
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+}  // namespace
+
+}  // namespace wt
+
+using namespace wt;
+
+extern "C" wt_status wtconv_backward_weight_noalloc(const wt_desc* desc, const void* x,
+                                                    const void* dy, const float* w0,
+                                                    const float* b0, const float* s0,
+                                                    const float* wl, const float* sl,
+                                                    float* dw0, float* db0, float* ds0,
+                                                    float* dwl, float* dsl,
+                                                    wt_stream_t stream) {
+    size_t fws = 0, bws = 0;
+    wt_status st = wtconv_workspace_size(desc, &fws, nullptr, &bws);  // validates desc
+    if (st != WT_OK) return st;
+    if (x == nullptr || dy == nullptr || (reinterpret_cast<uintptr_t>(x) & 15u) ||
+        (reinterpret_cast<uintptr_t>(dy) & 15u))
+        return WT_ERR_INVALID_ARG;
+    if (!w0 || !s0 || !dw0 || !ds0 || !aligned4(w0) || !aligned4(s0) || !aligned4(dw0) ||
+        !aligned4(ds0) || (b0 && !aligned4(b0)) || (db0 && !aligned4(db0)))
+        return WT_ERR_INVALID_ARG;
+    if (desc->levels > 0 && (!wl || !sl || !dwl || !dsl || !aligned4(wl) || !aligned4(sl) ||
+                             !aligned4(dwl) || !aligned4(dsl)))
+        return WT_ERR_INVALID_ARG;
+
+    // sizes: totals [C][KP], then one chunk of partial vectors [C][nc][KP]
+    const size_t KP = dw_partial_floats(*desc);
+    const size_t per_image = (size_t)desc->c * KP;
+    const size_t totals_floats = (per_image + 63) & ~size_t(63);
+    if (totals_floats + per_image > kNoAllocScratchFloats) return WT_ERR_WORKSPACE;
+    size_t nc_max = (kNoAllocScratchFloats - totals_floats) / per_image;
+    if (nc_max > (size_t)desc->n) nc_max = (size_t)desc->n;
+
+    float* scratch = nullptr;
+    st = scratch_on_current_device(&scratch);
+    if (st != WT_OK) return st;
+    float* totals = scratch;
+    float* part = scratch + totals_floats;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    const size_t esize = desc->io == WT_BF16 ? 2 : 4;
+    const size_t image_bytes = (size_t)desc->c * desc->h * desc->w * esize;
+    int launches = 0;
+    for (int n0 = 0; n0 < desc->n; n0 += (int)nc_max) {
+        const int nc = (desc->n - n0) < (int)nc_max ? (desc->n - n0) : (int)nc_max;
+        wt_desc sub = *desc;
+        sub.n = nc;
+        const char* xb = static_cast<const char*>(x) + (size_t)n0 * image_bytes;
+        const char* gb = static_cast<const char*>(dy) + (size_t)n0 * image_bytes;
+        st = launch_dw_partials(sub, xb, gb, part, s, &launches);
+        if (st != WT_OK) return st;
+        const size_t n_tot = per_image;
+        const unsigned blocks = (unsigned)((n_tot + 255) / 256 < 1024 ? (n_tot + 255) / 256 : 1024);
+        wt_dw_accumulate_kernel<<<blocks, 256, 0, s>>>(part, desc->c, nc, (int)KP, totals,
+                                                      n0 == 0 ? 1 : 0);
+        if (cudaGetLastError() != cudaSuccess) return WT_ERR_CUDA;
+        ++launches;
+    }
+    st = launch_dw_reduce(*desc, totals, 1, w0, b0, s0, wl, sl, dw0, db0, ds0, dwl, dsl, s,
+                          &launches);
+    (void)fws;
+    (void)bws;
+    return st;
+}

@@ -363,7 +363,68 @@ wt_status launch_dw_k(const wt_desc& d, const void* x, const void* dy, const flo
     return WT_OK;
 }
 
+template <int K, typename T>
+wt_status launch_dw_partials_k(const wt_desc& d, const void* x, const void* dy, float* part,
+                               cudaStream_t stream, int* launches) {
+    DwArgs a;
+    size_t smem = 0;
+    dw_layout<K>(d, a, smem);
+    if (smem > kMaxSmemPerBlock) return WT_ERR_UNSUPPORTED;
+    a.x = x;
+    a.dy = dy;
+    a.part = part;
+    a.N = d.n;
+    a.C = d.c;
+    a.H = d.h;
+    a.W = d.w;
+    a.L = d.levels;
+    a.vec = (d.w % 4 == 0) ? 1 : 0;
+    auto kern = wt_dw_plane_kernel<K, T>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return WT_ERR_CUDA;
+    kern<<<dim3((unsigned)d.c, (unsigned)d.n), kDT, smem, stream>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return WT_ERR_CUDA;
+    ++*launches;
+    return WT_OK;
+}
+
 }  // namespace
+
+wt_status launch_dw_partials(const wt_desc& d, const void* x, const void* dy, float* part,
+                             cudaStream_t stream, int* launches) {
+    const bool bf = d.io == WT_BF16;
+    switch (d.k) {
+#define WT_CASE(KV)                                                                          \
+    case KV:                                                                                 \
+        return bf ? launch_dw_partials_k<KV, __nv_bfloat16>(d, x, dy, part, stream, launches) \
+                  : launch_dw_partials_k<KV, float>(d, x, dy, part, stream, launches);
+        WT_CASE(1)
+        WT_CASE(3)
+        WT_CASE(5)
+        WT_CASE(7)
+#undef WT_CASE
+        default:
+            return WT_ERR_UNSUPPORTED;
+    }
+}
+
+wt_status launch_dw_reduce(const wt_desc& d, const float* part, int groups, const float* w0,
+                           const float* b0, const float* s0, const float* wl, const float* sl,
+                           float* dw0, float* db0, float* ds0, float* dwl, float* dsl,
+                           cudaStream_t stream, int* launches) {
+    const int KP = (int)dw_partial_floats(d);
+    wt_dw_reduce_kernel<<<(unsigned)d.c, 128, (size_t)KP * sizeof(float), stream>>>(
+        part, d.c, groups, KP, d.k, d.levels, w0, b0, s0, wl, sl, dw0, db0, ds0, dwl, dsl);
+    if (cudaGetLastError() != cudaSuccess) return WT_ERR_CUDA;
+    ++*launches;
+    return WT_OK;
+}
+
+size_t dw_partial_floats(const wt_desc& d) {
+    const int KK = d.k * d.k;
+    return (size_t)KK + 1 + 4 * (size_t)KK * d.levels;
+}
 
 size_t backward_weight_ws_bytes(const wt_desc& d) {
     const int KK = d.k * d.k;

@@ -129,6 +129,33 @@ wt_status wtconv_backward(const wt_desc* desc, const void* x, const void* dy,
                           void* dx, float* dw0, float* db0, float* ds0, float* dwl,
                           float* dsl, void* ws, size_t ws_bytes, wt_stream_t stream);
 
+/*
+ * wtconv_backward_weight without a workspace (the paper has no counterpart: this entry
+ * point exists for callers of this library that cannot provide device memory).
+ * Same arguments, results and determinism as wtconv_backward_weight, minus ws/ws_bytes.
+ *
+ * Who needs it: callers that cannot hand the library a workspace, e.g. a runtime that
+ * owns all device memory through its own pool and forbids raw cudaMalloc, or a
+ * latency-critical path that must not call cudaMalloc because it may synchronize the
+ * whole device. The scratch lives in a fixed 4 MiB array compiled into the library
+ * (held by every GPU that loads the library until the process exits); this call makes
+ * no cudaMalloc/cudaFree and calls no allocating library routine.
+ *
+ * Limit: the per-channel totals plus one image's partial vectors must fit in 4 MiB:
+ * 2 * C * (k*k + 1 + 4*k*k*L) * 4 bytes <= 4 MiB (e.g. C <= 996 at k = 5, L = 5);
+ * larger shapes return WT_ERR_WORKSPACE. The batch is processed in chunks of images.
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Concurrency: all calls share the one array and leave its contents behind; calls whose
+ * kernels overlap on the GPU (other streams or host threads on the same device) race.
+ */
+wt_status wtconv_backward_weight_noalloc(const wt_desc* desc, const void* x, const void* dy,
+                                         const float* w0, const float* b0, const float* s0,
+                                         const float* wl, const float* sl, float* dw0,
+                                         float* db0, float* ds0, float* dwl, float* dsl,
+                                         wt_stream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* wtconv_status_string(wt_status status);
 
