@@ -1,58 +1,84 @@
 // WTConv forward and backward-data kernel for sm_103a.
 //
 // Method: "Fast and Memory-Efficient Wavelet Convolutions via I/O-Aware Reformulation"
-// (Aflalo et al.). A persistent CTA walks (n, c) planes and evaluates the whole layer on
-// each with one read of X and one write of Y in HBM:
+// (Aflalo et al.). A persistent CTA (256 threads) walks (n, c) planes and evaluates the
+// whole layer on each with one read of X and one write of Y in HBM:
 //
 //   deep phase (L >= 2) -- levels l = 2..L run at their own resolution: 32x32 output
-//     tiles of the level's Haar subbands (§4.1 Eq. 5, recomputed on chip from the
-//     low-pass carrier X^(l-1); level 2 reads X itself in 4x4 pixel blocks) are staged in
-//     shared memory with an R-coefficient halo, the four folded k x k filters (§4.3 Eq. 8)
-//     are applied, and the filtered subbands Z^(l) go to this CTA's private scratch slot
-//     (a few tens of KB per CTA: L2-resident, never a full-tensor HBM round trip).
-//   full-resolution phase -- 64x64-pixel tiles of X (halo 2R) are staged once; the four
-//     level-1 subbands of the tile are formed in shared memory; each subband is filtered
-//     by a streaming register-blocked k x k pass (4x4 outputs per thread), and a final pass
-//     computes the base k x k convolution (8x4 pixels per thread) and adds, in the same
-//     store, the closed-form bit-indexed synthesis of §4.2 Prop. 2 / Eq. 7 over all levels
-//     (level 1 from the tile, levels >= 2 from the scratch slot).
-//
-// Every k x k filter is a streaming stencil: one window row at a time in registers,
-// k*k weights in registers, independent accumulators innermost. Shared-memory accesses
-// are 16-byte vectors at consecutive addresses across lanes (no bank conflicts).
+//     tiles of the level's Haar subbands (§4.1 Eq. 5, recomputed on chip from the low-pass
+//     carrier X^(l-1); level 2 reads X itself in 4x4 pixel blocks) are staged in shared
+//     memory with an R-coefficient halo and filtered by the four folded k x k kernels
+//     (§4.3 Eq. 8). The filtered subbands Z^(l) go to this CTA's scratch slot (tens of KB,
+//     L2-resident). A last pass sums Eq. 7's terms of levels 2..L at level-1 resolution
+//     (§4.2 Prop. 2: coefficient address by coordinate shifts, signs by coordinate bits)
+//     and writes that sum in place of Z^(2).
+//   full-resolution phase -- 64x64-pixel tiles: a TMA load brings the tile of X with a
+//     2R halo (zero outside the plane) into shared memory while the previous tile is being
+//     computed; one pass widens it to fp32 and forms the four level-1 subbands; four
+//     streaming 4x4-block passes filter the subbands; a last pass computes the base k x k
+//     convolution and stores, in the same write, base + level-1 synthesis (Eq. 7's l = 1
+//     term) + the deep sum (TMA-loaded per tile).
 //
 // Backward-data is the same operator on dY with every kernel rotated by 180 degrees and
 // no bias (§2.2 Eq. 1: the adjoint of analysis is synthesis; the adjoint of
 // cross-correlation is correlation with the rotated kernel); `flip` selects it.
+#include <mutex>
+
 #include "wt_internal.h"
 #include "wt_tile.cuh"
+#include "wt_tma.cuh"
 
 namespace wt {
 
-constexpr int kFT = 128;        // threads per CTA
+constexpr int kFT = 256;  // threads per CTA
+
 struct FwdArgs {
+    CUtensorMap tmx;  // X: dims {W, H, planes}, box {XBW, XBH, 1}
+    CUtensorMap tmd;  // deep sum: dims {4*W2, H2, slots}, box {64, 16, 1}
     const void* x;
     void* y;
     const float* w0f;
     const float* b0f;
     const float* wlf;
-    float* zd;             // deep scratch, one slot of zd_slot floats per CTA
+    float* zd;         // scratch: one slot of zd_slot floats per CTA
+    int* err;          // first word of the workspace: set on a stuck TMA wait
     long long zd_slot;
-    long long zd_off[kMaxLevels + 1];  // offset of Z^(l) inside a slot, band-major [4][Hl][Wl]
+    long long zd_off[kMaxLevels + 1];  // Z^(l) in a slot, interleaved [Hl][Wl][4]
     long long planes;
     int C, H, W, L;
-    int flip, vec;
-    int o_w, o_x, o_b, o_z;            // shared-memory regions (floats)
-    int o_car[kMaxLevels + 1];         // carriers X^(l), l = 2..L-1
+    int flip, vec, use_tma;
+    int o_bar, o_raw, o_dblk, o_w, o_b, o_x, o_z;  // shared-memory regions (floats)
+    int o_car[kMaxLevels + 1];                    // carriers X^(l), l = 2..L-1
 };
 
-// ---------------------------------------------------------------------------------
-// phases
-// ---------------------------------------------------------------------------------
+// TMA box of the staged X tile: columns from x0 - XOFF (16-byte aligned start), XBW wide.
+template <int K, typename T>
+struct XBox {
+    static constexpr int R = FG<K>::R;
+    static constexpr int A = 16 / (int)sizeof(T);             // elements per 16 bytes
+    static constexpr int XOFF = ((2 * R + A - 1) / A) * A;
+    static constexpr int XBW = ((kTile + 2 * R + XOFF + A - 1) / A) * A;
+    static constexpr int XBH = kTile + 4 * R;
+    static constexpr int C0 = XOFF - 2 * R;                   // raw column of tile column 0
+    static constexpr int BYTES = XBW * XBH * (int)sizeof(T);
+};
+constexpr int kDBytes = 16 * 64 * 4;  // deep-sum box: 16 level-2 rows x 16 positions x 4
+
+template <typename T>
+__device__ __forceinline__ float2 ld2_smem(const T* p);
+template <>
+__device__ __forceinline__ float2 ld2_smem<float>(const float* p) {
+    return *reinterpret_cast<const float2*>(p);
+}
+template <>
+__device__ __forceinline__ float2 ld2_smem<__nv_bfloat16>(const __nv_bfloat16* p) {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
 
 // Folded weights of channel c into shared memory: base kernel, then level l band b at
-// slot 1 + 4(l-1) + b, each scaled by 2^-(l+1) (1/2 turns the unnormalized subbands back
-// into Eq. 5's, 2^-l is Eq. 7's level weight) and rotated when `flip`.
+// slot 1 + 4(l-1) + b, scaled by 2^-(l+1) (1/2 turns unnormalized subbands into Eq. 5's,
+// 2^-l is Eq. 7's level weight) and rotated by 180 degrees when `flip`.
 template <int K>
 __device__ __forceinline__ void load_weights(const FwdArgs& a, int c, float* wsm) {
     constexpr int KK = FG<K>::KK, KKP = FG<K>::KKP;
@@ -72,9 +98,8 @@ __device__ __forceinline__ void load_weights(const FwdArgs& a, int c, float* wsm
     }
 }
 
-// Deep phase stage for level l: subbands of the 32x32 output tile at (ti0, tj0) with an
-// R halo (zero outside the level grid), band-major; carrier X^(l) for the tile's own
-// positions when l < L.
+// Deep stage for level l: subbands of the 32x32 output tile at (ti0, tj0) with an R halo
+// (zero outside the level grid), band-major; carrier X^(l) for the tile's own positions.
 template <int K, typename T>
 __device__ __forceinline__ void deep_stage(const FwdArgs& a, const T* xp, float* sm, int l,
                                            int ti0, int tj0) {
@@ -102,26 +127,91 @@ __device__ __forceinline__ void deep_stage(const FwdArgs& a, const T* xp, float*
     }
 }
 
+// Widen the TMA-staged raw tile to the fp32 tile (column c at c + PAD) and, when `bands`,
+// form the level-1 unnormalized subbands with an R halo (band-major).
 template <int K, typename T>
-__global__ void __launch_bounds__(kFT, 4) wt_fwd_plane_kernel(const FwdArgs a) {
+__device__ __forceinline__ void convert_raw(const T* raw, float* xs, float* bs, bool bands) {
+    constexpr int PAD = FG<K>::PAD, XP = FG<K>::XPITCH, BT = FG<K>::BT;
+    constexpr int BP = FG<K>::BPITCH, BAND = FG<K>::BAND;
+    constexpr int RW = XBox<K, T>::XBW, C0 = XBox<K, T>::C0;
+    for (int idx = threadIdx.x; idx < BT * BT; idx += blockDim.x) {
+        const int ci = idx / BT, cj = idx - ci * BT;
+        const T* r0 = raw + (2 * ci) * RW + C0 + 2 * cj;
+        const float2 p0 = ld2_smem<T>(r0);
+        const float2 p1 = ld2_smem<T>(r0 + RW);
+        float* d0 = xs + (2 * ci) * XP + PAD + 2 * cj;
+        if constexpr ((PAD & 1) == 0) {
+            *reinterpret_cast<float2*>(d0) = p0;
+            *reinterpret_cast<float2*>(d0 + XP) = p1;
+        } else {
+            d0[0] = p0.x; d0[1] = p0.y; d0[XP] = p1.x; d0[XP + 1] = p1.y;
+        }
+        if (bands) {
+            const float4 u = haar_u(p0.x, p0.y, p1.x, p1.y);
+            float* q = bs + ci * BP + cj;
+            q[0] = u.x;
+            q[BAND] = u.y;
+            q[2 * BAND] = u.z;
+            q[3 * BAND] = u.w;
+        }
+    }
+}
+
+template <int K, typename T>
+__global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_constant__ FwdArgs a) {
     constexpr int R = FG<K>::R, KKP = FG<K>::KKP, PAD = FG<K>::PAD;
     constexpr int XP = FG<K>::XPITCH, BP = FG<K>::BPITCH, BAND = FG<K>::BAND;
-    extern __shared__ float4 smem_f4[];
+    extern __shared__ __align__(128) float4 smem_f4[];
     float* sm = reinterpret_cast<float*>(smem_f4);
+    uint64_t* bar_x = reinterpret_cast<uint64_t*>(sm + a.o_bar);
+    uint64_t* bar_d = bar_x + 1;
+    T* raw = reinterpret_cast<T*>(sm + a.o_raw);
+    float* dblk = sm + a.o_dblk;
     float* wsm = sm + a.o_w;
     float* xs = sm + a.o_x;
     float* bs = sm + a.o_b;
     float* zs = sm + a.o_z;
     float* zslot = a.zd + (size_t)blockIdx.x * a.zd_slot;
     const size_t plane_elems = (size_t)a.H * a.W;
+    const int tid = threadIdx.x;
+    const bool leader = tid == 0;
+    const int tiles_x = (a.W + kTile - 1) / kTile;
+    const int ntiles = tiles_x * ((a.H + kTile - 1) / kTile);
+
+    if (a.use_tma && leader) {
+        mbar_init(bar_x, 1);
+        mbar_init(bar_d, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    uint32_t ph_x = 0, ph_d = 0;
+    bool failed = false;
 
     for (long long plane = blockIdx.x; plane < a.planes; plane += gridDim.x) {
         const int c = (int)(plane % a.C);
         const T* xp = reinterpret_cast<const T*>(a.x) + plane * plane_elems;
         T* yp = reinterpret_cast<T*>(a.y) + plane * plane_elems;
-        __syncthreads();  // previous plane is done with shared memory and weights
+        __syncthreads();  // the previous plane is done with shared memory
         load_weights<K>(a, c, wsm);
         const float bias = (a.b0f != nullptr) ? __ldg(a.b0f + c) : 0.f;
+        if (leader) {
+            const long long nxt = plane + gridDim.x;
+            if (a.use_tma && nxt < a.planes) {
+                // next plane of this CTA: bring it into L2 while this one is computed
+                const char* np =
+                    reinterpret_cast<const char*>(a.x) + (size_t)nxt * plane_elems * sizeof(T);
+                const size_t bytes = plane_elems * sizeof(T);
+                for (size_t o = 0; o < bytes; o += (1u << 20)) {
+                    const size_t nb = (bytes - o) < (1u << 20) ? (bytes - o) : (1u << 20);
+                    prefetch_l2_bulk(np + o, (uint32_t)nb);
+                }
+            }
+            if (a.use_tma) {  // first tile of this plane
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar_x, XBox<K, T>::BYTES);
+                tma_load_3d(raw, &a.tmx, -XBox<K, T>::XOFF, -2 * R, (int)plane, bar_x);
+            }
+        }
         __syncthreads();
 
         // ---- deep phase: Z^(l), l = 2..L, into the scratch slot ----
@@ -132,132 +222,172 @@ __global__ void __launch_bounds__(kFT, 4) wt_fwd_plane_kernel(const FwdArgs a) {
                 for (int tj0 = 0; tj0 < Wl; tj0 += kCT) {
                     deep_stage<K, T>(a, xp, sm, l, ti0, tj0);
                     __syncthreads();
-                    for (int it = threadIdx.x; it < 4 * 64; it += blockDim.x) {
-                        const int b = it >> 6, bi = (it >> 3) & 7, bj = it & 7;
+                    {
+                        const int b = tid >> 6, bi = (tid >> 3) & 7, bj = tid & 7;
                         const int gi0 = ti0 + 4 * bi, gj0 = tj0 + 4 * bj;
-                        if (gi0 >= Hl || gj0 >= Wl) continue;
-                        float acc[4][4];
-                        conv4x4<K>(bs + b * BAND + (4 * bi) * BP + 4 * bj, BP,
-                                   wsm + (1 + 4 * (l - 1) + b) * KKP, acc);
-                        float* zb = zl + (size_t)b * Hl * Wl;
+                        if (gi0 < Hl && gj0 < Wl) {
+                            float acc[4][4];
+                            conv4x4<K>(bs + b * BAND + (4 * bi) * BP + 4 * bj, BP,
+                                       wsm + (1 + 4 * (l - 1) + b) * KKP, acc);
 #pragma unroll
-                        for (int o = 0; o < 4; ++o) {
-                            if (gi0 + o >= Hl) continue;
+                            for (int o = 0; o < 4; ++o) {
+                                if (gi0 + o >= Hl) continue;
 #pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                if (gj0 + q < Wl) zb[(size_t)(gi0 + o) * Wl + gj0 + q] = acc[o][q];
+                                for (int q = 0; q < 4; ++q)
+                                    if (gj0 + q < Wl)
+                                        zl[((size_t)(gi0 + o) * Wl + gj0 + q) * 4 + b] = acc[o][q];
+                            }
                         }
                     }
                     __syncthreads();
                 }
             }
         }
+        if (a.L >= 2) {
+            // Eq. 7 terms of levels 2..L, summed at level-1 resolution, written over Z^(2):
+            // position (i2, j2) of level 2 holds the sums of level-1 positions
+            // (2i2 + a, 2j2 + b) as (a, b) = (0,0), (0,1), (1,0), (1,1).
+            const int H2 = a.H >> 2, W2 = a.W >> 2;
+            float4* z2 = reinterpret_cast<float4*>(zslot);
+            for (int p = tid; p < H2 * W2; p += blockDim.x) {
+                const int i2 = p / W2, j2 = p - i2 * W2;
+                float v = 0.f;
+                for (int l = 3; l <= a.L; ++l) {
+                    const int sh = l - 2, Wl = a.W >> l;
+                    const float4 zl = reinterpret_cast<const float4*>(zslot + a.zd_off[l])
+                        [(size_t)(i2 >> sh) * Wl + (j2 >> sh)];
+                    v += synth_rt(zl, (i2 >> (l - 3)) & 1, (j2 >> (l - 3)) & 1);
+                }
+                const float4 z = z2[p];
+                z2[p] = make_float4(synth<0, 0>(z) + v, synth<0, 1>(z) + v, synth<1, 0>(z) + v,
+                                    synth<1, 1>(z) + v);
+            }
+            fence_proxy_async_global();
+            __syncthreads();
+        }
 
         // ---- full-resolution phase ----
-        const int by = threadIdx.x >> 4, bx = threadIdx.x & 15;  // 8x4-pixel base block
-        for (int y0 = 0; y0 < a.H; y0 += kTile) {
-            for (int x0 = 0; x0 < a.W; x0 += kTile) {
+        const int by = tid >> 4, bx = tid & 15;  // 4x4-pixel block of this thread
+        for (int t = 0; t < ntiles; ++t) {
+            const int ty = t / tiles_x, tx = t - ty * tiles_x;
+            const int y0 = ty * kTile, x0 = tx * kTile;
+            if (a.L >= 2) {
+                if (a.use_tma) {
+                    if (leader) {
+                        fence_proxy_async_smem();
+                        mbar_arrive_expect_tx(bar_d, kDBytes);
+                        tma_load_3d(dblk, &a.tmd, x0, y0 >> 2, (int)blockIdx.x, bar_d);
+                    }
+                } else {
+                    // plain copy of the 16x16 level-2 block of deep sums (zero outside)
+                    const int H2 = a.H >> 2, W2 = a.W >> 2;
+                    const float4* z2 = reinterpret_cast<const float4*>(zslot);
+                    const int i0 = y0 >> 2, j0 = x0 >> 2;
+                    const int i = tid >> 4, j = tid & 15;
+                    float4 v = f4_zero();
+                    if (i0 + i < H2 && j0 + j < W2) v = z2[(size_t)(i0 + i) * W2 + j0 + j];
+                    reinterpret_cast<float4*>(dblk)[tid] = v;
+                }
+            }
+            if (a.use_tma) {
+                const bool ok = mbar_wait_bounded(bar_x, ph_x);
+                ph_x ^= 1;
+                if (__syncthreads_or(!ok)) {
+                    failed = true;
+                    break;
+                }
+                convert_raw<K, T>(raw, xs, bs, a.L >= 1);
+                __syncthreads();
+                if (leader && t + 1 < ntiles) {  // prefetch the next tile of this plane
+                    const int ny = (t + 1) / tiles_x, nx = (t + 1) - ny * tiles_x;
+                    fence_proxy_async_smem();
+                    mbar_arrive_expect_tx(bar_x, XBox<K, T>::BYTES);
+                    tma_load_3d(raw, &a.tmx, nx * kTile - XBox<K, T>::XOFF, ny * kTile - 2 * R,
+                                (int)plane, bar_x);
+                }
+            } else {
                 stage_tile<K, T>(xp, a.H, a.W, a.vec, xs, y0, x0);
                 __syncthreads();
                 if (a.L >= 1) {
                     bands_from_tile<K>(xs, bs);
                     __syncthreads();
-                    // level-1 filters: 4 bands x 64 blocks of 4x4 coefficients
-                    for (int it = threadIdx.x; it < 4 * 64; it += blockDim.x) {
-                        const int b = it >> 6, bi = (it >> 3) & 7, bj = it & 7;
-                        if (y0 / 2 + 4 * bi >= (a.H + 1) / 2 || x0 / 2 + 4 * bj >= (a.W + 1) / 2)
-                            continue;
-                        float acc[4][4];
-                        conv4x4<K>(bs + b * BAND + (4 * bi) * BP + 4 * bj, BP,
-                                   wsm + (1 + b) * KKP, acc);
-#pragma unroll
-                        for (int o = 0; o < 4; ++o)
-                            *reinterpret_cast<float4*>(zs + b * (kCT * kCT) + (4 * bi + o) * kCT + 4 * bj) =
-                                make_float4(acc[o][0], acc[o][1], acc[o][2], acc[o][3]);
-                    }
-                    __syncthreads();
                 }
-                const int gy = y0 + 8 * by, gx = x0 + 4 * bx;
-                if (gy < a.H && gx < a.W) {
-                    float acc[8][4];
+            }
+            if (a.L >= 1) {
+                // level-1 filters: 4 bands x 64 blocks of 4x4 coefficients, one per thread
+                const int b = tid >> 6, bi = (tid >> 3) & 7, bj = tid & 7;
+                if (y0 / 2 + 4 * bi < a.H / 2 && x0 / 2 + 4 * bj < a.W / 2) {
+                    float acc[4][4];
+                    conv4x4<K>(bs + b * BAND + (4 * bi) * BP + 4 * bj, BP, wsm + (1 + b) * KKP,
+                               acc);
 #pragma unroll
-                    for (int o = 0; o < 8; ++o)
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) acc[o][q] = bias;
-                    conv8x4<K>(xs + (8 * by + R) * XP + 4 * bx + R + PAD, XP, wsm, acc);
-                    if (a.L >= 1) {
-                        // Eq. 7: level 1 from the z tile, levels >= 2 from the scratch slot
-                        float d[4][2];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) d[i][0] = d[i][1] = 0.f;
-                        const int gci0 = gy >> 1, gcj0 = gx >> 1;  // gci0 % 4 == 0, gcj0 even
-                        for (int l = 2; l <= a.L; ++l) {
-                            const int Hl = a.H >> l, Wl = a.W >> l;
-                            const float* zl = zslot + a.zd_off[l];
-                            const size_t bst = (size_t)Hl * Wl;
-                            const int sh = l - 1;
-                            const int jl = gcj0 >> sh;
-                            const int sx = (gcj0 >> (l - 2)) & 1;  // l >= 3: same for both columns
-#pragma unroll
-                            for (int half = 0; half < 2; ++half) {
-                                // l == 2: rows gci0/2 and gci0/2 + 1; l >= 3: one row
-                                if (l >= 3 && half == 1) break;
-                                const int il = (gci0 >> sh) + half;
-                                if (il >= Hl) break;  // rows past H (H = 4 mod 8) are not stored
-                                const float* zp = zl + (size_t)il * Wl + jl;
-                                const float4 z = make_float4(zp[0], zp[bst], zp[2 * bst], zp[3 * bst]);
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    if (l == 2 && (i >> 1) != half) continue;
-                                    const int syb = (l == 2) ? (i & 1)
-                                                  : (l == 3) ? ((i >> 1) & 1)
-                                                             : ((gci0 >> (l - 2)) & 1);
-#pragma unroll
-                                    for (int j = 0; j < 2; ++j) {
-                                        const int sxb = (l == 2) ? j : sx;
-                                        d[i][j] += synth_rt(z, syb, sxb);
-                                    }
-                                }
-                            }
-                        }
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            float z1[2][4];
-                            const float* zr = zs + (4 * by + i) * kCT + 2 * bx;
-#pragma unroll
-                            for (int b = 0; b < 4; ++b) {
-                                const float2 t = *reinterpret_cast<const float2*>(zr + b * (kCT * kCT));
-                                z1[0][b] = t.x;
-                                z1[1][b] = t.y;
-                            }
-#pragma unroll
-                            for (int j = 0; j < 2; ++j) {
-                                const float4 z = make_float4(z1[j][0], z1[j][1], z1[j][2], z1[j][3]);
-                                acc[2 * i][2 * j] += synth<0, 0>(z) + d[i][j];
-                                acc[2 * i][2 * j + 1] += synth<0, 1>(z) + d[i][j];
-                                acc[2 * i + 1][2 * j] += synth<1, 0>(z) + d[i][j];
-                                acc[2 * i + 1][2 * j + 1] += synth<1, 1>(z) + d[i][j];
-                            }
-                        }
-                    }
-                    if (a.vec && gy + 8 <= a.H && gx + 4 <= a.W) {
-#pragma unroll
-                        for (int o = 0; o < 8; ++o)
-                            IO<T>::st4(yp + (size_t)(gy + o) * a.W + gx,
-                                       make_float4(acc[o][0], acc[o][1], acc[o][2], acc[o][3]));
-                    } else {
-#pragma unroll
-                        for (int o = 0; o < 8; ++o)
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                if (gy + o < a.H && gx + q < a.W)
-                                    IO<T>::st(yp + (size_t)(gy + o) * a.W + gx + q, acc[o][q]);
-                    }
+                    for (int o = 0; o < 4; ++o)
+                        *reinterpret_cast<float4*>(zs + b * (kCT * kCT) + (4 * bi + o) * kCT +
+                                                   4 * bj) =
+                            make_float4(acc[o][0], acc[o][1], acc[o][2], acc[o][3]);
                 }
                 __syncthreads();
             }
+            if (a.L >= 2 && a.use_tma) {
+                const bool ok = mbar_wait_bounded(bar_d, ph_d);
+                ph_d ^= 1;
+                if (__syncthreads_or(!ok)) {
+                    failed = true;
+                    break;
+                }
+            }
+            const int gy = y0 + 4 * by, gx = x0 + 4 * bx;
+            if (gy < a.H && gx < a.W) {
+                float acc[4][4];
+                conv4x4<K>(xs + (4 * by + R) * XP + 4 * bx + R + PAD, XP, wsm, acc);
+#pragma unroll
+                for (int o = 0; o < 4; ++o)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[o][q] += bias;
+                if (a.L >= 1) {
+                    float4 d = f4_zero();
+                    if (a.L >= 2) d = reinterpret_cast<const float4*>(dblk)[tid];
+                    const float dv[2][2] = {{d.x, d.y}, {d.z, d.w}};
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        float z1[2][4];
+                        const float* zr = zs + (2 * by + i) * kCT + 2 * bx;
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            const float2 tz =
+                                *reinterpret_cast<const float2*>(zr + b * (kCT * kCT));
+                            z1[0][b] = tz.x;
+                            z1[1][b] = tz.y;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const float4 z = make_float4(z1[j][0], z1[j][1], z1[j][2], z1[j][3]);
+                            acc[2 * i][2 * j] += synth<0, 0>(z) + dv[i][j];
+                            acc[2 * i][2 * j + 1] += synth<0, 1>(z) + dv[i][j];
+                            acc[2 * i + 1][2 * j] += synth<1, 0>(z) + dv[i][j];
+                            acc[2 * i + 1][2 * j + 1] += synth<1, 1>(z) + dv[i][j];
+                        }
+                    }
+                }
+                if (a.vec && gy + 4 <= a.H && gx + 4 <= a.W) {
+#pragma unroll
+                    for (int o = 0; o < 4; ++o)
+                        IO<T>::st4(yp + (size_t)(gy + o) * a.W + gx,
+                                   make_float4(acc[o][0], acc[o][1], acc[o][2], acc[o][3]));
+                } else {
+#pragma unroll
+                    for (int o = 0; o < 4; ++o)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (gy + o < a.H && gx + q < a.W)
+                                IO<T>::st(yp + (size_t)(gy + o) * a.W + gx + q, acc[o][q]);
+                }
+            }
+            __syncthreads();
         }
+        if (failed) break;
     }
+    if (failed && leader && a.err != nullptr) atomicExch(a.err, kErrTmaTimeout);
 }
 
 // ---------------------------------------------------------------------------------
@@ -267,6 +397,44 @@ __global__ void __launch_bounds__(kFT, 4) wt_fwd_plane_kernel(const FwdArgs a) {
 namespace {
 
 int round4(int v) { return (v + 3) & ~3; }
+int round32(int v) { return (v + 31) & ~31; }
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 3-D tiled tensor map: dims {d0, d1, d2}, byte strides {s1, s2}, box {b0, b1, 1};
+// reads outside the tensor return zeros.
+bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base,
+               unsigned long long d0, unsigned long long d1, unsigned long long d2,
+               unsigned long long s1_bytes, unsigned long long s2_bytes, unsigned b0,
+               unsigned b1) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {s1_bytes, s2_bytes};
+    const cuuint32_t box[3] = {b0, b1, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 struct FwdPlan {
     FwdArgs a;
@@ -275,19 +443,27 @@ struct FwdPlan {
     size_t ws_bytes = 0;
 };
 
-template <int K>
+constexpr size_t kErrWordBytes = 256;  // the workspace starts with the error word
+
+template <int K, typename T>
 FwdPlan fwd_plan(const wt_desc& d) {
     FwdPlan p;
     FwdArgs& a = p.a;
     const int L = d.levels;
     int off = 0;
+    a.o_bar = off;
+    off += 32;  // two mbarriers, padded to 128 bytes
+    a.o_raw = off;
+    off += round32((XBox<K, T>::BYTES + 3) / 4);
+    a.o_dblk = off;
+    off += (L >= 2) ? kDBytes / 4 : 0;
     a.o_w = off;
     off += FG<K>::KKP * (1 + 4 * L);
-    off = round4(off);
-    // the F-phase buffers; the deep carriers alias the X and z tiles
+    off = round32(off);
     a.o_b = off;
     off += 4 * FG<K>::BAND;
-    const int alias0 = off;
+    off = round4(off);
+    const int alias0 = off;  // the deep carriers alias the X and z tiles
     a.o_x = off;
     off += FG<K>::XROWS * FG<K>::XPITCH;
     a.o_z = off;
@@ -300,22 +476,22 @@ FwdPlan fwd_plan(const wt_desc& d) {
     }
     const int total = off > cp ? off : cp;
     p.smem = (size_t)total * sizeof(float);
-    // deep scratch slot: Z^(l) band-major for l = 2..L
     long long zo = 0;
     for (int l = 0; l <= kMaxLevels; ++l) a.zd_off[l] = 0;
     for (int l = 2; l <= L; ++l) {
         a.zd_off[l] = zo;
         zo += 4LL * (d.h >> l) * (d.w >> l);
     }
-    a.zd_slot = (zo + 63) & ~63LL;  // 256-byte aligned slots
+    a.zd_slot = (zo + 63) & ~63LL;  // 256-byte slots
     const long long planes = (long long)d.n * d.c;
     int occ = (int)((228 * 1024) / (p.smem + 1024));
-    if (occ > 4) occ = 4;
+    if (occ > 2) occ = 2;
     if (occ < 1) occ = 1;
     long long grid = (long long)kNumSMs * occ;
     if (grid > planes) grid = planes;
     p.grid = (int)grid;
-    p.ws_bytes = (L >= 2) ? (size_t)grid * (size_t)a.zd_slot * sizeof(float) : 0;
+    p.ws_bytes =
+        kErrWordBytes + ((L >= 2) ? (size_t)grid * (size_t)a.zd_slot * sizeof(float) : 0);
     return p;
 }
 
@@ -323,16 +499,17 @@ template <int K, typename T>
 wt_status launch_fwd_k(const wt_desc& d, const void* x, const float* w0f, const float* b0f,
                        const float* wlf, void* y, int flip, void* ws, size_t ws_bytes,
                        cudaStream_t stream, int* launches) {
-    FwdPlan p = fwd_plan<K>(d);
+    FwdPlan p = fwd_plan<K, T>(d);
     if (p.smem > kMaxSmemPerBlock) return WT_ERR_UNSUPPORTED;
-    if (p.ws_bytes > 0 && (ws == nullptr || ws_bytes < p.ws_bytes)) return WT_ERR_WORKSPACE;
+    if (ws == nullptr || ws_bytes < p.ws_bytes) return WT_ERR_WORKSPACE;
     FwdArgs& a = p.a;
     a.x = x;
     a.y = y;
     a.w0f = w0f;
     a.b0f = flip ? nullptr : b0f;
     a.wlf = wlf;
-    a.zd = reinterpret_cast<float*>(ws);
+    a.err = reinterpret_cast<int*>(ws);
+    a.zd = reinterpret_cast<float*>(static_cast<char*>(ws) + kErrWordBytes);
     a.planes = (long long)d.n * d.c;
     a.C = d.c;
     a.H = d.h;
@@ -340,6 +517,25 @@ wt_status launch_fwd_k(const wt_desc& d, const void* x, const float* w0f, const 
     a.L = d.levels;
     a.flip = flip;
     a.vec = (d.w % 4 == 0) ? 1 : 0;
+    // TMA needs 16-byte row strides; otherwise the tile is staged with plain loads
+    const size_t esize = sizeof(T);
+    const CUtensorMapDataType dt =
+        sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    a.use_tma = 0;
+    if (((size_t)d.w * esize) % 16 == 0) {
+        bool ok = encode_3d(&a.tmx, dt, x, d.w, d.h, (unsigned long long)d.n * d.c,
+                            (unsigned long long)d.w * esize,
+                            (unsigned long long)d.w * d.h * esize, XBox<K, T>::XBW,
+                            XBox<K, T>::XBH);
+        if (ok && d.levels >= 2) {
+            const unsigned long long w2 = d.w >> 2, h2 = d.h >> 2;
+            ok = encode_3d(&a.tmd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.zd, 4 * w2, h2,
+                           (unsigned long long)p.grid, 16 * w2, (unsigned long long)a.zd_slot * 4,
+                           64, 16);
+        }
+        a.use_tma = ok ? 1 : 0;
+    }
+    if (cudaMemsetAsync(a.err, 0, sizeof(int), stream) != cudaSuccess) return WT_ERR_CUDA;
     auto kern = wt_fwd_plane_kernel<K, T>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) !=
         cudaSuccess)
@@ -352,7 +548,7 @@ wt_status launch_fwd_k(const wt_desc& d, const void* x, const float* w0f, const 
 
 template <int K>
 bool fwd_sizes(const wt_desc& d, size_t* smem, size_t* ws) {
-    FwdPlan p = fwd_plan<K>(d);
+    FwdPlan p = (d.io == WT_BF16) ? fwd_plan<K, __nv_bfloat16>(d) : fwd_plan<K, float>(d);
     *smem = p.smem;
     *ws = p.ws_bytes;
     return true;

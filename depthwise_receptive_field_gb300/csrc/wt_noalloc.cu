@@ -31,6 +31,7 @@ constexpr size_t kNoAllocScratchFloats = size_t(1) << 20;
 constexpr size_t kNoAllocScratchBytes = kNoAllocScratchFloats * sizeof(float);  // 4 MiB
 constexpr int kMaxDevices = 64;
 
+static_assert(kNoAllocScratchBytes == (size_t(4) << 20), "the documented size is 4 MiB");
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
 
 std::mutex g_setup_mu;

@@ -85,13 +85,14 @@ def test_workspace_sizes_for_workloads(lib, name):
                     B.WT_BF16 if wl.dtype == "bf16" else B.WT_F32)
     fwd, bwd_d, bwd_w = B.wtconv_workspace_size(d)
     # forward / backward-data: one deep-level scratch slot (Z^(l), l >= 2) per resident CTA
+    # (the workspace starts with a 256-byte status word)
     assert fwd == bwd_d
     if wl.levels < 2:
-        assert fwd == 0
+        assert fwd == 256
     else:
         slot = sum(4 * (wl.h >> l) * (wl.w >> l) for l in range(2, wl.levels + 1)) * 4
-        assert fwd >= slot and fwd % 256 == 0
-        assert fwd <= 4 * 152 * ((slot + 255) // 256 * 256)  # at most 4 CTAs per SM
+        assert fwd >= 256 + slot and fwd % 256 == 0
+        assert fwd <= 256 + 2 * 152 * ((slot + 255) // 256 * 256)  # at most 2 CTAs per SM
     # backward-weight: one partial vector [dW0 | db | dW^(l)] per (channel, image)
     kk = wl.k * wl.k
     per_partial = (kk + 1 + 4 * kk * wl.levels) * 4
