@@ -108,3 +108,39 @@ __device__ __forceinline__ float synth_rt(const float4& z, int by, int bx) {
 __device__ __forceinline__ int split_col(int c, int half) { return (c >> 1) + (c & 1) * half; }
 
 }  // namespace wt
+
+namespace wt {
+
+// ---------------------------------------------------------------------------------
+// Packed fp32 pairs (sm_100+ f32x2 arithmetic): two independent lanes of work per
+// instruction, halving the issue slots of the FMA-bound loops.
+// ---------------------------------------------------------------------------------
+typedef unsigned long long f2x;
+
+__device__ __forceinline__ f2x pk2(float lo, float hi) {
+    f2x r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 upk2(f2x v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ f2x fma2(f2x a, f2x b, f2x c) {
+    f2x d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f2x add2(f2x a, f2x b) {
+    f2x d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2x sub2(f2x a, f2x b) {
+    f2x d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+}  // namespace wt

@@ -76,34 +76,38 @@ __device__ __forceinline__ float2 ld2_smem<__nv_bfloat16>(const __nv_bfloat16* p
     return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
-// Folded weights of channel c into shared memory: base kernel, then level l band b at
-// slot 1 + 4(l-1) + b, scaled by 2^-(l+1) (1/2 turns unnormalized subbands into Eq. 5's,
-// 2^-l is Eq. 7's level weight) and rotated by 180 degrees when `flip`.
+// Folded weights of channel c into shared memory as packed pairs: slot 0 holds the base
+// taps duplicated (w, w); slot 1 + 2(l-1) + p holds level l's band pair p as
+// (w_{2p}, w_{2p+1}), each scaled by 2^-(l+1) (1/2 turns unnormalized subbands into
+// Eq. 5's, 2^-l is Eq. 7's level weight). Taps are rotated by 180 degrees when `flip`.
 template <int K>
 __device__ __forceinline__ void load_weights(const FwdArgs& a, int c, float* wsm) {
-    constexpr int KK = FG<K>::KK, KKP = FG<K>::KKP;
-    const int nk = 1 + 4 * a.L;
+    constexpr int KK = FG<K>::KK, WS = PG<K>::WS;
+    const int nk = 1 + 4 * a.L;  // base + 4 bands per level
     for (int e = threadIdx.x; e < nk * KK; e += blockDim.x) {
         const int s = e / KK, uv = e - s * KK;
         const int src = a.flip ? (KK - 1 - uv) : uv;
-        float v;
         if (s == 0) {
-            v = __ldg(a.w0f + (size_t)c * KK + src);
+            const float v = __ldg(a.w0f + (size_t)c * KK + src);
+            wsm[2 * uv] = v;
+            wsm[2 * uv + 1] = v;
         } else {
             const int l = 1 + (s - 1) / 4, b = (s - 1) & 3;
-            v = ldexpf(1.0f, -(l + 1)) *
-                __ldg(a.wlf + (((size_t)(l - 1) * a.C + c) * 4 + b) * KK + src);
+            const float v = ldexpf(1.0f, -(l + 1)) *
+                            __ldg(a.wlf + (((size_t)(l - 1) * a.C + c) * 4 + b) * KK + src);
+            wsm[(1 + 2 * (l - 1) + (b >> 1)) * WS + 2 * uv + (b & 1)] = v;
         }
-        wsm[s * KKP + uv] = v;
     }
 }
 
 // Deep stage for level l: subbands of the 32x32 output tile at (ti0, tj0) with an R halo
-// (zero outside the level grid), band-major; carrier X^(l) for the tile's own positions.
+// (zero outside the level grid) into the two band-pair tiles; carrier X^(l) for the
+// tile's own positions when l < L.
 template <int K, typename T>
 __device__ __forceinline__ void deep_stage(const FwdArgs& a, const T* xp, float* sm, int l,
                                            int ti0, int tj0) {
-    constexpr int R = FG<K>::R, BT = FG<K>::BT, BP = FG<K>::BPITCH, BAND = FG<K>::BAND;
+    constexpr int R = FG<K>::R, BT = FG<K>::BT;
+    constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, PHALF = PG<K>::PHALF;
     const int Hl = a.H >> l, Wl = a.W >> l, Wp = a.W >> (l - 1);
     float* bs = sm + a.o_b;
     const float* carp = (l >= 3) ? sm + a.o_car[l - 1] : nullptr;
@@ -119,48 +123,66 @@ __device__ __forceinline__ void deep_stage(const FwdArgs& a, const T* xp, float*
             if (carl && si >= R && si < R + kCT && sj >= R && sj < R + kCT)
                 carl[(size_t)gi * Wl + gj] = 0.5f * u.x;
         }
-        float* q = bs + si * BP + sj;
-        q[0] = u.x;
-        q[BAND] = u.y;
-        q[2 * BAND] = u.z;
-        q[3 * BAND] = u.w;
+        float* q = bs + si * PROW + 4 * pchunk(sj >> 1, PHALF) + 2 * (sj & 1);
+        *reinterpret_cast<float2*>(q) = make_float2(u.x, u.y);
+        *reinterpret_cast<float2*>(q + PTILE) = make_float2(u.z, u.w);
     }
 }
 
 // Widen the TMA-staged raw tile to the fp32 tile (column c at c + PAD) and, when `bands`,
-// form the level-1 unnormalized subbands with an R halo (band-major).
+// form the level-1 unnormalized subbands with an R halo in the two band-pair tiles.
+// One item = two horizontally adjacent cells (a 2x4 pixel block).
 template <int K, typename T>
 __device__ __forceinline__ void convert_raw(const T* raw, float* xs, float* bs, bool bands) {
     constexpr int PAD = FG<K>::PAD, XP = FG<K>::XPITCH, BT = FG<K>::BT;
-    constexpr int BP = FG<K>::BPITCH, BAND = FG<K>::BAND;
+    constexpr int NCR = PG<K>::NCR, PROW = PG<K>::PROW, PTILE = PG<K>::PTILE;
+    constexpr int PHALF = PG<K>::PHALF;
     constexpr int RW = XBox<K, T>::XBW, C0 = XBox<K, T>::C0;
-    for (int idx = threadIdx.x; idx < BT * BT; idx += blockDim.x) {
-        const int ci = idx / BT, cj = idx - ci * BT;
-        const T* r0 = raw + (2 * ci) * RW + C0 + 2 * cj;
-        const float2 p0 = ld2_smem<T>(r0);
-        const float2 p1 = ld2_smem<T>(r0 + RW);
-        float* d0 = xs + (2 * ci) * XP + PAD + 2 * cj;
+    for (int idx = threadIdx.x; idx < BT * NCR; idx += blockDim.x) {
+        const int ci = idx / NCR, m = idx - ci * NCR;
+        const T* r0 = raw + (2 * ci) * RW + C0 + 4 * m;
+        const float2 a0 = ld2_smem<T>(r0), a1 = ld2_smem<T>(r0 + 2);
+        const float2 b0 = ld2_smem<T>(r0 + RW), b1 = ld2_smem<T>(r0 + RW + 2);
+        float* d0 = xs + (2 * ci) * XP + PAD + 4 * m;
         if constexpr ((PAD & 1) == 0) {
-            *reinterpret_cast<float2*>(d0) = p0;
-            *reinterpret_cast<float2*>(d0 + XP) = p1;
+            reinterpret_cast<float2*>(d0)[0] = a0;
+            reinterpret_cast<float2*>(d0)[1] = a1;
+            reinterpret_cast<float2*>(d0 + XP)[0] = b0;
+            reinterpret_cast<float2*>(d0 + XP)[1] = b1;
         } else {
-            d0[0] = p0.x; d0[1] = p0.y; d0[XP] = p1.x; d0[XP + 1] = p1.y;
+            d0[0] = a0.x; d0[1] = a0.y; d0[2] = a1.x; d0[3] = a1.y;
+            d0[XP] = b0.x; d0[XP + 1] = b0.y; d0[XP + 2] = b1.x; d0[XP + 3] = b1.y;
         }
         if (bands) {
-            const float4 u = haar_u(p0.x, p0.y, p1.x, p1.y);
-            float* q = bs + ci * BP + cj;
-            q[0] = u.x;
-            q[BAND] = u.y;
-            q[2 * BAND] = u.z;
-            q[3 * BAND] = u.w;
+            const float4 u = haar_u(a0.x, a0.y, b0.x, b0.y);
+            const float4 v = haar_u(a1.x, a1.y, b1.x, b1.y);
+            float* q = bs + ci * PROW + 4 * pchunk(m, PHALF);
+            *reinterpret_cast<float4*>(q) = make_float4(u.x, u.y, v.x, v.y);
+            *reinterpret_cast<float4*>(q + PTILE) = make_float4(u.z, u.w, v.z, v.w);
         }
+    }
+}
+
+// Non-TMA path: level-1 band-pair tiles from the staged fp32 tile.
+template <int K>
+__device__ __forceinline__ void pair_bands_from_tile(const float* xs, float* bs) {
+    constexpr int PAD = FG<K>::PAD, XP = FG<K>::XPITCH, BT = FG<K>::BT;
+    constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, PHALF = PG<K>::PHALF;
+    for (int idx = threadIdx.x; idx < BT * BT; idx += blockDim.x) {
+        const int ci = idx / BT, cj = idx - ci * BT;
+        const float* p = xs + (2 * ci) * XP + PAD + 2 * cj;
+        const float4 u = haar_u(p[0], p[1], p[XP], p[XP + 1]);
+        float* q = bs + ci * PROW + 4 * pchunk(cj >> 1, PHALF) + 2 * (cj & 1);
+        *reinterpret_cast<float2*>(q) = make_float2(u.x, u.y);
+        *reinterpret_cast<float2*>(q + PTILE) = make_float2(u.z, u.w);
     }
 }
 
 template <int K, typename T>
 __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_constant__ FwdArgs a) {
-    constexpr int R = FG<K>::R, KKP = FG<K>::KKP, PAD = FG<K>::PAD;
-    constexpr int XP = FG<K>::XPITCH, BP = FG<K>::BPITCH, BAND = FG<K>::BAND;
+    constexpr int R = FG<K>::R, PAD = FG<K>::PAD, XP = FG<K>::XPITCH;
+    constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, WS = PG<K>::WS;
+    constexpr int ZROW = PG<K>::ZROW, ZTILE = PG<K>::ZTILE;
     extern __shared__ __align__(128) float4 smem_f4[];
     float* sm = reinterpret_cast<float*>(smem_f4);
     uint64_t* bar_x = reinterpret_cast<uint64_t*>(sm + a.o_bar);
@@ -223,19 +245,22 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                     deep_stage<K, T>(a, xp, sm, l, ti0, tj0);
                     __syncthreads();
                     {
-                        const int b = tid >> 6, bi = (tid >> 3) & 7, bj = tid & 7;
-                        const int gi0 = ti0 + 4 * bi, gj0 = tj0 + 4 * bj;
+                        // band pair pp = tid / 128, 2x4 output block (bi, bj)
+                        const int pp = tid >> 7, bi = (tid >> 3) & 15, bj = tid & 7;
+                        const int gi0 = ti0 + 2 * bi, gj0 = tj0 + 4 * bj;
                         if (gi0 < Hl && gj0 < Wl) {
-                            float acc[4][4];
-                            conv4x4<K>(bs + b * BAND + (4 * bi) * BP + 4 * bj, BP,
-                                       wsm + (1 + 4 * (l - 1) + b) * KKP, acc);
+                            f2x acc[2][4];
+                            conv_pair_2x4<K>(bs + pp * PTILE + (2 * bi) * PROW, bj,
+                                             wsm + (1 + 2 * (l - 1) + pp) * WS, acc);
 #pragma unroll
-                            for (int o = 0; o < 4; ++o) {
+                            for (int o = 0; o < 2; ++o) {
                                 if (gi0 + o >= Hl) continue;
 #pragma unroll
                                 for (int q = 0; q < 4; ++q)
                                     if (gj0 + q < Wl)
-                                        zl[((size_t)(gi0 + o) * Wl + gj0 + q) * 4 + b] = acc[o][q];
+                                        *reinterpret_cast<float2*>(
+                                            zl + ((size_t)(gi0 + o) * Wl + gj0 + q) * 4 + 2 * pp) =
+                                            upk2(acc[o][q]);
                             }
                         }
                     }
@@ -309,22 +334,25 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                 stage_tile<K, T>(xp, a.H, a.W, a.vec, xs, y0, x0);
                 __syncthreads();
                 if (a.L >= 1) {
-                    bands_from_tile<K>(xs, bs);
+                    pair_bands_from_tile<K>(xs, bs);
                     __syncthreads();
                 }
             }
             if (a.L >= 1) {
-                // level-1 filters: 4 bands x 64 blocks of 4x4 coefficients, one per thread
-                const int b = tid >> 6, bi = (tid >> 3) & 7, bj = tid & 7;
-                if (y0 / 2 + 4 * bi < a.H / 2 && x0 / 2 + 4 * bj < a.W / 2) {
-                    float acc[4][4];
-                    conv4x4<K>(bs + b * BAND + (4 * bi) * BP + 4 * bj, BP, wsm + (1 + b) * KKP,
-                               acc);
+                // level-1 filters: 2 band pairs x 128 blocks of 2x4 coefficients, one per thread
+                const int pp = tid >> 7, bi = (tid >> 3) & 15, bj = tid & 7;
+                if (y0 / 2 + 2 * bi < a.H / 2 && x0 / 2 + 4 * bj < a.W / 2) {
+                    f2x acc[2][4];
+                    conv_pair_2x4<K>(bs + pp * PTILE + (2 * bi) * PROW, bj, wsm + (1 + pp) * WS,
+                                     acc);
 #pragma unroll
-                    for (int o = 0; o < 4; ++o)
-                        *reinterpret_cast<float4*>(zs + b * (kCT * kCT) + (4 * bi + o) * kCT +
-                                                   4 * bj) =
-                            make_float4(acc[o][0], acc[o][1], acc[o][2], acc[o][3]);
+                    for (int o = 0; o < 2; ++o) {
+                        float* zr = zs + pp * ZTILE + (2 * bi + o) * ZROW + 8 * bj;
+                        const float2 q0 = upk2(acc[o][0]), q1 = upk2(acc[o][1]);
+                        const float2 q2 = upk2(acc[o][2]), q3 = upk2(acc[o][3]);
+                        reinterpret_cast<float4*>(zr)[0] = make_float4(q0.x, q0.y, q1.x, q1.y);
+                        reinterpret_cast<float4*>(zr)[1] = make_float4(q2.x, q2.y, q3.x, q3.y);
+                    }
                 }
                 __syncthreads();
             }
@@ -338,36 +366,44 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
             }
             const int gy = y0 + 4 * by, gx = x0 + 4 * bx;
             if (gy < a.H && gx < a.W) {
-                float acc[4][4];
-                conv4x4<K>(xs + (4 * by + R) * XP + 4 * bx + R + PAD, XP, wsm, acc);
+                f2x acc2[4][2];
+                const f2x bias2 = pk2(bias, bias);
 #pragma unroll
-                for (int o = 0; o < 4; ++o)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) acc[o][q] += bias;
+                for (int o = 0; o < 4; ++o) acc2[o][0] = acc2[o][1] = bias2;
+                conv_base_4x4<K>(xs + (4 * by + R) * XP + 4 * bx + R + PAD, XP, wsm, acc2);
                 if (a.L >= 1) {
                     float4 d = f4_zero();
                     if (a.L >= 2) d = reinterpret_cast<const float4*>(dblk)[tid];
                     const float dv[2][2] = {{d.x, d.y}, {d.z, d.w}};
 #pragma unroll
                     for (int i = 0; i < 2; ++i) {
-                        float z1[2][4];
-                        const float* zr = zs + (2 * by + i) * kCT + 2 * bx;
-#pragma unroll
-                        for (int b = 0; b < 4; ++b) {
-                            const float2 tz =
-                                *reinterpret_cast<const float2*>(zr + b * (kCT * kCT));
-                            z1[0][b] = tz.x;
-                            z1[1][b] = tz.y;
-                        }
-#pragma unroll
-                        for (int j = 0; j < 2; ++j) {
-                            const float4 z = make_float4(z1[j][0], z1[j][1], z1[j][2], z1[j][3]);
-                            acc[2 * i][2 * j] += synth<0, 0>(z) + dv[i][j];
-                            acc[2 * i][2 * j + 1] += synth<0, 1>(z) + dv[i][j];
-                            acc[2 * i + 1][2 * j] += synth<1, 0>(z) + dv[i][j];
-                            acc[2 * i + 1][2 * j + 1] += synth<1, 1>(z) + dv[i][j];
-                        }
+                        // (LL, LH) and (HL, HH) of coefficients (2by+i, 2bx) and (2by+i, 2bx+1)
+                        const float4 za = *reinterpret_cast<const float4*>(
+                            zs + (2 * by + i) * ZROW + 4 * bx);
+                        const float4 zb = *reinterpret_cast<const float4*>(
+                            zs + ZTILE + (2 * by + i) * ZROW + 4 * bx);
+                        const f2x s0 = add2(pk2(za.x, za.y), pk2(zb.x, zb.y));  // LL+HL, LH+HH
+                        const f2x m0 = sub2(pk2(za.x, za.y), pk2(zb.x, zb.y));  // LL-HL, LH-HH
+                        const f2x s1 = add2(pk2(za.z, za.w), pk2(zb.z, zb.w));
+                        const f2x m1 = sub2(pk2(za.z, za.w), pk2(zb.z, zb.w));
+                        const float2 S0 = upk2(s0), M0 = upk2(m0), S1 = upk2(s1), M1 = upk2(m1);
+                        // Eq. 12/13 signs: (ry, rx) = (0,0): S.x+S.y, (0,1): M.x+M.y,
+                        // (1,0): S.x-S.y, (1,1): M.x-M.y
+                        acc2[2 * i][0] = add2(acc2[2 * i][0],
+                                              pk2(S0.x + S0.y + dv[i][0], M0.x + M0.y + dv[i][0]));
+                        acc2[2 * i][1] = add2(acc2[2 * i][1],
+                                              pk2(S1.x + S1.y + dv[i][1], M1.x + M1.y + dv[i][1]));
+                        acc2[2 * i + 1][0] = add2(acc2[2 * i + 1][0],
+                                                  pk2(S0.x - S0.y + dv[i][0], M0.x - M0.y + dv[i][0]));
+                        acc2[2 * i + 1][1] = add2(acc2[2 * i + 1][1],
+                                                  pk2(S1.x - S1.y + dv[i][1], M1.x - M1.y + dv[i][1]));
                     }
+                }
+                float acc[4][4];
+#pragma unroll
+                for (int o = 0; o < 4; ++o) {
+                    const float2 lo = upk2(acc2[o][0]), hi = upk2(acc2[o][1]);
+                    acc[o][0] = lo.x; acc[o][1] = lo.y; acc[o][2] = hi.x; acc[o][3] = hi.y;
                 }
                 if (a.vec && gy + 4 <= a.H && gx + 4 <= a.W) {
 #pragma unroll
@@ -458,16 +494,16 @@ FwdPlan fwd_plan(const wt_desc& d) {
     a.o_dblk = off;
     off += (L >= 2) ? kDBytes / 4 : 0;
     a.o_w = off;
-    off += FG<K>::KKP * (1 + 4 * L);
+    off += PG<K>::WS * (1 + 2 * L);
     off = round32(off);
     a.o_b = off;
-    off += 4 * FG<K>::BAND;
+    off += 2 * PG<K>::PTILE;
     off = round4(off);
     const int alias0 = off;  // the deep carriers alias the X and z tiles
     a.o_x = off;
     off += FG<K>::XROWS * FG<K>::XPITCH;
     a.o_z = off;
-    off += 4 * FG<K>::ZAND;
+    off += 2 * PG<K>::ZTILE;
     int cp = alias0;
     for (int l = 0; l <= kMaxLevels; ++l) a.o_car[l] = 0;
     for (int l = 2; l < L; ++l) {

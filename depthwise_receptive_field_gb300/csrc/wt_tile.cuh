@@ -128,6 +128,118 @@ __device__ __forceinline__ void corr_rows(const float* win, int pitch, const flo
     }
 }
 
+// ---------------------------------------------------------------------------------
+// Band-pair tiles for packed (f32x2) filtering: the four subbands are stored as two
+// tiles of interleaved pairs, (LL, LH) and (HL, HH), so that one packed FMA applies the
+// two bands' own taps to their own coefficients. A row holds BT cells (2 floats each);
+// 16-byte chunks of 2 cells are laid out even chunks first, then odd chunks, so that the
+// lanes of a warp, which own 4-cell-wide blocks, read consecutive 16-byte words.
+// ---------------------------------------------------------------------------------
+template <int K>
+struct PG {
+    static constexpr int R = FG<K>::R, BT = FG<K>::BT, KK = FG<K>::KK;
+    static constexpr int NCR = BT / 2;                 // chunks per row
+    static constexpr int PHALF = (NCR + 1) / 2;        // start of the odd chunks
+    static constexpr int PROW = 8 * PHALF;             // floats per row
+    static constexpr int PTILE = BT * PROW;            // floats per pair tile
+    static constexpr int NCH = 2 + R;                  // chunks per window row (2x4 block)
+    static constexpr int WS = (2 * KK + 3) & ~3;       // floats per weight-pair slot
+    static constexpr int ZROW = 2 * kCT;               // floats per row of a filtered pair tile
+    static constexpr int ZTILE = kCT * ZROW;
+};
+
+__device__ __forceinline__ int pchunk(int c, int half) { return (c >> 1) + (c & 1) * half; }
+
+// Packed k x k filter of a 2x4 block of one band pair: acc[o][q] = sum_{u,v} w[u][v] (.)
+// cell[o+u][q+v], two bands at once. `rows` = pair tile + (first window row) * PROW;
+// the block's window starts at cell 4*bj. wsl = KK taps as (w_b0, w_b1) pairs.
+template <int K>
+__device__ __forceinline__ void conv_pair_2x4(const float* rows, int bj, const float* wsl,
+                                              f2x (&acc)[2][4]) {
+    constexpr int R = PG<K>::R, KK = PG<K>::KK, NCH = PG<K>::NCH, PROW = PG<K>::PROW;
+    constexpr int PHALF = PG<K>::PHALF;
+    f2x w[KK];
+#pragma unroll
+    for (int q = 0; q + 1 < KK; q += 2) {
+        const float4 t = *reinterpret_cast<const float4*>(wsl + 2 * q);
+        w[q] = pk2(t.x, t.y);
+        w[q + 1] = pk2(t.z, t.w);
+    }
+    if constexpr (KK & 1) {
+        const float2 t = *reinterpret_cast<const float2*>(wsl + 2 * (KK - 1));
+        w[KK - 1] = pk2(t.x, t.y);
+    }
+#pragma unroll
+    for (int o = 0; o < 2; ++o)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[o][q] = 0ull;
+#pragma unroll
+    for (int r = 0; r < 2 + 2 * R; ++r) {
+        const float* rp = rows + r * PROW;
+        f2x v[2 * NCH];
+#pragma unroll
+        for (int m = 0; m < NCH; ++m) {
+            const float4 t = *reinterpret_cast<const float4*>(
+                rp + 4 * (bj + (m >> 1) + (m & 1) * PHALF));
+            v[2 * m] = pk2(t.x, t.y);
+            v[2 * m + 1] = pk2(t.z, t.w);
+        }
+#pragma unroll
+        for (int o = 0; o < 2; ++o) {
+            const int u = r - o;
+            if (u < 0 || u >= K) continue;
+#pragma unroll
+            for (int vv = 0; vv < K; ++vv)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[o][q] = fma2(w[u * K + vv], v[q + vv], acc[o][q]);
+        }
+    }
+}
+
+// Packed base k x k filter of a 4x4 pixel block from the fp32 tile, accumulating onto
+// acc[o][p] = (pixel (o, 2p), pixel (o, 2p+1)). The odd-offset input pairs are formed in
+// registers. wdup = KK taps as (w, w) pairs.
+template <int K>
+__device__ __forceinline__ void conv_base_4x4(const float* win, int pitch, const float* wdup,
+                                              f2x (&acc)[4][2]) {
+    constexpr int R = FG<K>::R, KK = FG<K>::KK, CNC = FG<K>::CNC;
+    constexpr int NV = 4 * CNC;
+    f2x w[KK];
+#pragma unroll
+    for (int q = 0; q + 1 < KK; q += 2) {
+        const float4 t = *reinterpret_cast<const float4*>(wdup + 2 * q);
+        w[q] = pk2(t.x, t.y);
+        w[q + 1] = pk2(t.z, t.w);
+    }
+    if constexpr (KK & 1) {
+        const float2 t = *reinterpret_cast<const float2*>(wdup + 2 * (KK - 1));
+        w[KK - 1] = pk2(t.x, t.y);
+    }
+#pragma unroll
+    for (int r = 0; r < 4 + 2 * R; ++r) {
+        float v[NV];
+        load_row<CNC>(win + r * pitch, v);
+        f2x A[NV / 2], B[NV / 2 - 1];
+#pragma unroll
+        for (int m = 0; m < NV / 2; ++m) A[m] = pk2(v[2 * m], v[2 * m + 1]);
+#pragma unroll
+        for (int m = 0; m < NV / 2 - 1; ++m) B[m] = pk2(v[2 * m + 1], v[2 * m + 2]);
+#pragma unroll
+        for (int o = 0; o < 4; ++o) {
+            const int u = r - o;
+            if (u < 0 || u >= K) continue;
+#pragma unroll
+            for (int vv = 0; vv < K; ++vv)
+#pragma unroll
+                for (int pp = 0; pp < 2; ++pp) {
+                    const int idx = 2 * pp + vv;
+                    const f2x in = (idx & 1) ? B[(idx - 1) >> 1] : A[idx >> 1];
+                    acc[o][pp] = fma2(w[u * K + vv], in, acc[o][pp]);
+                }
+        }
+    }
+}
+
 // Stage pixels [y0-2R, y0+64+2R) x [x0-2R, x0+64+2R) of a plane into xs (pitch XPITCH,
 // column c stored at c + PAD), zero outside the plane. vec: W % 4 == 0 (aligned rows).
 template <int K, typename T>
