@@ -40,15 +40,15 @@ struct FwdArgs {
     const float* w0f;
     const float* b0f;
     const float* wlf;
-    float* zd;         // scratch: one slot of zd_slot floats per CTA
+    float* zd;         // scratch: one slot of zd_slot floats per CTA (the deep sums)
     int* err;          // first word of the workspace: set on a stuck TMA wait
     long long zd_slot;
-    long long zd_off[kMaxLevels + 1];  // Z^(l) in a slot, interleaved [Hl][Wl][4]
     long long planes;
     int C, H, W, L;
     int flip, vec, use_tma;
     int o_bar, o_raw, o_dblk, o_w, o_b, o_x, o_z;  // shared-memory regions (floats)
     int o_car[kMaxLevels + 1];                    // carriers X^(l), l = 2..L-1
+    int o_zl[kMaxLevels + 1];                     // Z^(l), l = 3..L, interleaved [Hl][Wl][4]
 };
 
 // TMA box of the staged X tile: columns from x0 - XOFF (16-byte aligned start), XBW wide.
@@ -101,18 +101,22 @@ __device__ __forceinline__ void load_weights(const FwdArgs& a, int c, float* wsm
 }
 
 // Deep stage for level l: subbands of the 32x32 output tile at (ti0, tj0) with an R halo
-// (zero outside the level grid) into the two band-pair tiles; carrier X^(l) for the
-// tile's own positions when l < L.
+// (zero outside the level grid) into the two band-pair tiles. Level 2 reads the 4x4
+// pixel blocks of X (L2-resident), deeper levels the carrier X^(l-1) in shared memory.
+// The trip count is a compile-time constant so that the loads of all cells issue early.
 template <int K, typename T>
 __device__ __forceinline__ void deep_stage(const FwdArgs& a, const T* xp, float* sm, int l,
                                            int ti0, int tj0) {
     constexpr int R = FG<K>::R, BT = FG<K>::BT;
     constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, PHALF = PG<K>::PHALF;
+    constexpr int NIT = (BT * BT + kFT - 1) / kFT;
     const int Hl = a.H >> l, Wl = a.W >> l, Wp = a.W >> (l - 1);
     float* bs = sm + a.o_b;
     const float* carp = (l >= 3) ? sm + a.o_car[l - 1] : nullptr;
-    float* carl = (l < a.L) ? sm + a.o_car[l] : nullptr;
-    for (int idx = threadIdx.x; idx < BT * BT; idx += blockDim.x) {
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+        const int idx = threadIdx.x + it * kFT;
+        if (idx >= BT * BT) break;
         const int si = idx / BT, sj = idx - si * BT;
         const int gi = ti0 - R + si, gj = tj0 - R + sj;
         float4 u = f4_zero();
@@ -120,12 +124,44 @@ __device__ __forceinline__ void deep_stage(const FwdArgs& a, const T* xp, float*
             float ca, cb, cc, cd;
             carrier_block<T>(l, xp, a.W, carp, Wp, gi, gj, ca, cb, cc, cd);
             u = haar_u(ca, cb, cc, cd);
-            if (carl && si >= R && si < R + kCT && sj >= R && sj < R + kCT)
-                carl[(size_t)gi * Wl + gj] = 0.5f * u.x;
         }
         float* q = bs + si * PROW + 4 * pchunk(sj >> 1, PHALF) + 2 * (sj & 1);
         *reinterpret_cast<float2*>(q) = make_float2(u.x, u.y);
         *reinterpret_cast<float2*>(q + PTILE) = make_float2(u.z, u.w);
+    }
+}
+
+// Low-pass carriers for the deep levels: X^(2) from the 4x4 pixel blocks of X (through
+// the level-1 carrier, Eq. 5's LL twice), then X^(l) from X^(l-1) for l = 3..L-1.
+template <typename T>
+__device__ __forceinline__ void deep_carriers(const FwdArgs& a, const T* xp, float* sm) {
+    {
+        const int H2 = a.H >> 2, W2 = a.W >> 2, n = H2 * W2;
+        float* c2 = sm + a.o_car[2];
+        for (int base = threadIdx.x; base < n; base += 4 * kFT) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int p = base + u * kFT;
+                if (p < n) {
+                    const int i2 = p / W2, j2 = p - i2 * W2;
+                    float ca, cb, cc, cd;
+                    carrier_block<T>(2, xp, a.W, nullptr, 0, i2, j2, ca, cb, cc, cd);
+                    c2[p] = 0.5f * (ca + cb + cc + cd);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    for (int l = 3; l < a.L; ++l) {
+        const int Hl = a.H >> l, Wl = a.W >> l, Wp = a.W >> (l - 1);
+        const float* cp = sm + a.o_car[l - 1];
+        float* cl = sm + a.o_car[l];
+        for (int p = threadIdx.x; p < Hl * Wl; p += kFT) {
+            const int i = p / Wl, j = p - i * Wl;
+            const float* q = cp + (size_t)(2 * i) * Wp + 2 * j;
+            cl[p] = 0.5f * (q[0] + q[1] + q[Wp] + q[Wp + 1]);
+        }
+        __syncthreads();
     }
 }
 
@@ -236,56 +272,78 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
         }
         __syncthreads();
 
-        // ---- deep phase: Z^(l), l = 2..L, into the scratch slot ----
-        for (int l = 2; l <= a.L; ++l) {
-            const int Hl = a.H >> l, Wl = a.W >> l;
-            float* zl = zslot + a.zd_off[l];
-            for (int ti0 = 0; ti0 < Hl; ti0 += kCT) {
-                for (int tj0 = 0; tj0 < Wl; tj0 += kCT) {
-                    deep_stage<K, T>(a, xp, sm, l, ti0, tj0);
-                    __syncthreads();
-                    {
-                        // band pair pp = tid / 128, 2x4 output block (bi, bj)
-                        const int pp = tid >> 7, bi = (tid >> 3) & 15, bj = tid & 7;
-                        const int gi0 = ti0 + 2 * bi, gj0 = tj0 + 4 * bj;
-                        if (gi0 < Hl && gj0 < Wl) {
-                            f2x acc[2][4];
-                            conv_pair_2x4<K>(bs + pp * PTILE + (2 * bi) * PROW, bj,
-                                             wsm + (1 + 2 * (l - 1) + pp) * WS, acc);
+        // ---- deep phase (L >= 2) ----
+        // carriers top-down; levels L..3 filtered into shared memory; level 2 last, its
+        // filtered subbands combined at once with the deeper levels into Eq. 7's sum over
+        // levels 2..L at level-1 resolution, written to the scratch slot: level-2 position
+        // (i2, j2) holds the sums for level-1 positions (2i2 + a, 2j2 + b) as
+        // (a, b) = (0,0), (0,1), (1,0), (1,1).
+        if (a.L >= 2) {
+            if (a.L >= 3) deep_carriers<T>(a, xp, sm);
+            for (int l = a.L; l >= 2; --l) {
+                const int Hl = a.H >> l, Wl = a.W >> l;
+                for (int ti0 = 0; ti0 < Hl; ti0 += kCT) {
+                    for (int tj0 = 0; tj0 < Wl; tj0 += kCT) {
+                        deep_stage<K, T>(a, xp, sm, l, ti0, tj0);
+                        __syncthreads();
+                        {
+                            // band pair pp = tid / 128, 2x4 output block (bi, bj)
+                            const int pp = tid >> 7, bi = (tid >> 3) & 15, bj = tid & 7;
+                            const int gi0 = ti0 + 2 * bi, gj0 = tj0 + 4 * bj;
+                            if (gi0 < Hl && gj0 < Wl) {
+                                f2x acc[2][4];
+                                conv_pair_2x4<K>(bs + pp * PTILE + (2 * bi) * PROW, bj,
+                                                 wsm + (1 + 2 * (l - 1) + pp) * WS, acc);
+                                if (l >= 3) {
+                                    float* zl = sm + a.o_zl[l];
 #pragma unroll
-                            for (int o = 0; o < 2; ++o) {
-                                if (gi0 + o >= Hl) continue;
+                                    for (int o = 0; o < 2; ++o) {
+                                        if (gi0 + o >= Hl) continue;
 #pragma unroll
-                                for (int q = 0; q < 4; ++q)
-                                    if (gj0 + q < Wl)
-                                        *reinterpret_cast<float2*>(
-                                            zl + ((size_t)(gi0 + o) * Wl + gj0 + q) * 4 + 2 * pp) =
-                                            upk2(acc[o][q]);
+                                        for (int q = 0; q < 4; ++q)
+                                            if (gj0 + q < Wl)
+                                                *reinterpret_cast<float2*>(
+                                                    zl + ((gi0 + o) * Wl + gj0 + q) * 4 + 2 * pp) =
+                                                    upk2(acc[o][q]);
+                                    }
+                                } else {
+#pragma unroll
+                                    for (int o = 0; o < 2; ++o) {
+                                        float* zr = zs + pp * ZTILE + (2 * bi + o) * ZROW + 8 * bj;
+                                        const float2 q0 = upk2(acc[o][0]), q1 = upk2(acc[o][1]);
+                                        const float2 q2 = upk2(acc[o][2]), q3 = upk2(acc[o][3]);
+                                        reinterpret_cast<float4*>(zr)[0] = make_float4(q0.x, q0.y, q1.x, q1.y);
+                                        reinterpret_cast<float4*>(zr)[1] = make_float4(q2.x, q2.y, q3.x, q3.y);
+                                    }
+                                }
+                            }
+                        }
+                        __syncthreads();
+                        if (l == 2) {
+                            // deep sums of this level-2 tile's positions
+                            float4* dsum = reinterpret_cast<float4*>(zslot);
+#pragma unroll
+                            for (int k = 0; k < (kCT * kCT) / kFT; ++k) {
+                                const int p = tid + k * kFT, ti = p >> 5, tj = p & 31;
+                                const int i2 = ti0 + ti, j2 = tj0 + tj;
+                                if (i2 >= Hl || j2 >= Wl) continue;
+                                const float2 za = *reinterpret_cast<const float2*>(zs + ti * ZROW + 2 * tj);
+                                const float2 zb = *reinterpret_cast<const float2*>(zs + ZTILE + ti * ZROW + 2 * tj);
+                                const float4 z = make_float4(za.x, za.y, zb.x, zb.y);
+                                float v = 0.f;
+                                for (int m = 3; m <= a.L; ++m) {
+                                    const int sh = m - 2, Wm = a.W >> m;
+                                    const float4 zm = reinterpret_cast<const float4*>(sm + a.o_zl[m])
+                                        [(i2 >> sh) * Wm + (j2 >> sh)];
+                                    v += synth_rt(zm, (i2 >> (m - 3)) & 1, (j2 >> (m - 3)) & 1);
+                                }
+                                dsum[(size_t)i2 * Wl + j2] =
+                                    make_float4(synth<0, 0>(z) + v, synth<0, 1>(z) + v,
+                                                synth<1, 0>(z) + v, synth<1, 1>(z) + v);
                             }
                         }
                     }
-                    __syncthreads();
                 }
-            }
-        }
-        if (a.L >= 2) {
-            // Eq. 7 terms of levels 2..L, summed at level-1 resolution, written over Z^(2):
-            // position (i2, j2) of level 2 holds the sums of level-1 positions
-            // (2i2 + a, 2j2 + b) as (a, b) = (0,0), (0,1), (1,0), (1,1).
-            const int H2 = a.H >> 2, W2 = a.W >> 2;
-            float4* z2 = reinterpret_cast<float4*>(zslot);
-            for (int p = tid; p < H2 * W2; p += blockDim.x) {
-                const int i2 = p / W2, j2 = p - i2 * W2;
-                float v = 0.f;
-                for (int l = 3; l <= a.L; ++l) {
-                    const int sh = l - 2, Wl = a.W >> l;
-                    const float4 zl = reinterpret_cast<const float4*>(zslot + a.zd_off[l])
-                        [(size_t)(i2 >> sh) * Wl + (j2 >> sh)];
-                    v += synth_rt(zl, (i2 >> (l - 3)) & 1, (j2 >> (l - 3)) & 1);
-                }
-                const float4 z = z2[p];
-                z2[p] = make_float4(synth<0, 0>(z) + v, synth<0, 1>(z) + v, synth<1, 0>(z) + v,
-                                    synth<1, 1>(z) + v);
             }
             fence_proxy_async_global();
             __syncthreads();
@@ -499,26 +557,26 @@ FwdPlan fwd_plan(const wt_desc& d) {
     a.o_b = off;
     off += 2 * PG<K>::PTILE;
     off = round4(off);
-    const int alias0 = off;  // the deep carriers alias the X and z tiles
-    a.o_x = off;
-    off += FG<K>::XROWS * FG<K>::XPITCH;
     a.o_z = off;
     off += 2 * PG<K>::ZTILE;
+    // the full-resolution X tile and the deep-phase carriers + Z^(l >= 3) share a region
+    const int alias0 = off;
+    a.o_x = off;
+    const int xend = off + FG<K>::XROWS * FG<K>::XPITCH;
     int cp = alias0;
-    for (int l = 0; l <= kMaxLevels; ++l) a.o_car[l] = 0;
+    for (int l = 0; l <= kMaxLevels; ++l) a.o_car[l] = a.o_zl[l] = 0;
     for (int l = 2; l < L; ++l) {
         a.o_car[l] = cp;
         cp += round4((d.h >> l) * (d.w >> l));
     }
-    const int total = off > cp ? off : cp;
-    p.smem = (size_t)total * sizeof(float);
-    long long zo = 0;
-    for (int l = 0; l <= kMaxLevels; ++l) a.zd_off[l] = 0;
-    for (int l = 2; l <= L; ++l) {
-        a.zd_off[l] = zo;
-        zo += 4LL * (d.h >> l) * (d.w >> l);
+    for (int l = 3; l <= L; ++l) {
+        a.o_zl[l] = cp;
+        cp += 4 * (d.h >> l) * (d.w >> l);
     }
-    a.zd_slot = (zo + 63) & ~63LL;  // 256-byte slots
+    const int total = xend > cp ? xend : cp;
+    p.smem = (size_t)total * sizeof(float);
+    // deep-sum slot: [H/4][W/4][4] fp32
+    a.zd_slot = (L >= 2) ? ((4LL * (d.h >> 2) * (d.w >> 2) + 63) & ~63LL) : 0;
     const long long planes = (long long)d.n * d.c;
     int occ = (int)((228 * 1024) / (p.smem + 1024));
     if (occ > 2) occ = 2;

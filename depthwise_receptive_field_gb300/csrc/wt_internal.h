@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 
-#include "../../include/wtconv.h"
+#include "wtconv.h"
 
 namespace wt {
 
