@@ -51,30 +51,7 @@ struct FwdArgs {
     int o_zl[kMaxLevels + 1];                     // Z^(l), l = 3..L, interleaved [Hl][Wl][4]
 };
 
-// TMA box of the staged X tile: columns from x0 - XOFF (16-byte aligned start), XBW wide.
-template <int K, typename T>
-struct XBox {
-    static constexpr int R = FG<K>::R;
-    static constexpr int A = 16 / (int)sizeof(T);             // elements per 16 bytes
-    static constexpr int XOFF = ((2 * R + A - 1) / A) * A;
-    static constexpr int XBW = ((kTile + 2 * R + XOFF + A - 1) / A) * A;
-    static constexpr int XBH = kTile + 4 * R;
-    static constexpr int C0 = XOFF - 2 * R;                   // raw column of tile column 0
-    static constexpr int BYTES = XBW * XBH * (int)sizeof(T);
-};
 constexpr int kDBytes = 16 * 64 * 4;  // deep-sum box: 16 level-2 rows x 16 positions x 4
-
-template <typename T>
-__device__ __forceinline__ float2 ld2_smem(const T* p);
-template <>
-__device__ __forceinline__ float2 ld2_smem<float>(const float* p) {
-    return *reinterpret_cast<const float2*>(p);
-}
-template <>
-__device__ __forceinline__ float2 ld2_smem<__nv_bfloat16>(const __nv_bfloat16* p) {
-    const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
-    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
-}
 
 // Folded weights of channel c into shared memory as packed pairs: slot 0 holds the base
 // taps duplicated (w, w); slot 1 + 2(l-1) + p holds level l's band pair p as
@@ -162,55 +139,6 @@ __device__ __forceinline__ void deep_carriers(const FwdArgs& a, const T* xp, flo
             cl[p] = 0.5f * (q[0] + q[1] + q[Wp] + q[Wp + 1]);
         }
         __syncthreads();
-    }
-}
-
-// Widen the TMA-staged raw tile to the fp32 tile (column c at c + PAD) and, when `bands`,
-// form the level-1 unnormalized subbands with an R halo in the two band-pair tiles.
-// One item = two horizontally adjacent cells (a 2x4 pixel block).
-template <int K, typename T>
-__device__ __forceinline__ void convert_raw(const T* raw, float* xs, float* bs, bool bands) {
-    constexpr int PAD = FG<K>::PAD, XP = FG<K>::XPITCH, BT = FG<K>::BT;
-    constexpr int NCR = PG<K>::NCR, PROW = PG<K>::PROW, PTILE = PG<K>::PTILE;
-    constexpr int PHALF = PG<K>::PHALF;
-    constexpr int RW = XBox<K, T>::XBW, C0 = XBox<K, T>::C0;
-    for (int idx = threadIdx.x; idx < BT * NCR; idx += blockDim.x) {
-        const int ci = idx / NCR, m = idx - ci * NCR;
-        const T* r0 = raw + (2 * ci) * RW + C0 + 4 * m;
-        const float2 a0 = ld2_smem<T>(r0), a1 = ld2_smem<T>(r0 + 2);
-        const float2 b0 = ld2_smem<T>(r0 + RW), b1 = ld2_smem<T>(r0 + RW + 2);
-        float* d0 = xs + (2 * ci) * XP + PAD + 4 * m;
-        if constexpr ((PAD & 1) == 0) {
-            reinterpret_cast<float2*>(d0)[0] = a0;
-            reinterpret_cast<float2*>(d0)[1] = a1;
-            reinterpret_cast<float2*>(d0 + XP)[0] = b0;
-            reinterpret_cast<float2*>(d0 + XP)[1] = b1;
-        } else {
-            d0[0] = a0.x; d0[1] = a0.y; d0[2] = a1.x; d0[3] = a1.y;
-            d0[XP] = b0.x; d0[XP + 1] = b0.y; d0[XP + 2] = b1.x; d0[XP + 3] = b1.y;
-        }
-        if (bands) {
-            const float4 u = haar_u(a0.x, a0.y, b0.x, b0.y);
-            const float4 v = haar_u(a1.x, a1.y, b1.x, b1.y);
-            float* q = bs + ci * PROW + 4 * pchunk(m, PHALF);
-            *reinterpret_cast<float4*>(q) = make_float4(u.x, u.y, v.x, v.y);
-            *reinterpret_cast<float4*>(q + PTILE) = make_float4(u.z, u.w, v.z, v.w);
-        }
-    }
-}
-
-// Non-TMA path: level-1 band-pair tiles from the staged fp32 tile.
-template <int K>
-__device__ __forceinline__ void pair_bands_from_tile(const float* xs, float* bs) {
-    constexpr int PAD = FG<K>::PAD, XP = FG<K>::XPITCH, BT = FG<K>::BT;
-    constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, PHALF = PG<K>::PHALF;
-    for (int idx = threadIdx.x; idx < BT * BT; idx += blockDim.x) {
-        const int ci = idx / BT, cj = idx - ci * BT;
-        const float* p = xs + (2 * ci) * XP + PAD + 2 * cj;
-        const float4 u = haar_u(p[0], p[1], p[XP], p[XP + 1]);
-        float* q = bs + ci * PROW + 4 * pchunk(cj >> 1, PHALF) + 2 * (cj & 1);
-        *reinterpret_cast<float2*>(q) = make_float2(u.x, u.y);
-        *reinterpret_cast<float2*>(q + PTILE) = make_float2(u.z, u.w);
     }
 }
 
@@ -488,11 +416,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
 // Host side
 // ---------------------------------------------------------------------------------
 
-namespace {
-
-int round4(int v) { return (v + 3) & ~3; }
-int round32(int v) { return (v + 31) & ~31; }
-
+// Tensor-map encoding through the driver entry point (no libcuda link needed).
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -529,6 +453,12 @@ bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+
+namespace {
+
+int round4(int v) { return (v + 3) & ~3; }
+int round32(int v) { return (v + 31) & ~31; }
 
 struct FwdPlan {
     FwdArgs a;

@@ -2,6 +2,7 @@
 // public C ABI; that lives in include/wtconv.h).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 
@@ -37,6 +38,12 @@ wt_status launch_dw_reduce(const wt_desc& d, const float* part, int groups, cons
                            cudaStream_t stream, int* launches);
 size_t dw_partial_floats(const wt_desc& d);
 size_t backward_weight_smem_bytes(const wt_desc& d);
+
+// 3-D tiled TMA tensor map: dims {d0, d1, d2}, byte strides {s1, s2}, box {b0, b1, 1};
+// reads outside the tensor return zeros. False when the driver cannot encode it.
+bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, unsigned long long d0,
+               unsigned long long d1, unsigned long long d2, unsigned long long s1_bytes,
+               unsigned long long s2_bytes, unsigned b0, unsigned b1);
 
 // scale folding (Eq. 8): one launch
 wt_status launch_fold(const wt_desc& d, const float* w0, const float* b0, const float* s0,

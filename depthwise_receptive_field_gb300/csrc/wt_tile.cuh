@@ -240,6 +240,144 @@ __device__ __forceinline__ void conv_base_4x4(const float* win, int pitch, const
     }
 }
 
+// Packed weight-gradient correlation of a ROWS x 4 block of one band pair:
+// acc[u*K+v] += sum_{o,q} g[o][q] (.) cell[o+u][q+v], two bands at once. `rows` = pair
+// tile + (first window row) * PROW; the window starts at cell 4*bj.
+template <int K, int ROWS>
+__device__ __forceinline__ void corr_pair(const float* rows, int bj, const f2x (&g)[ROWS][4],
+                                          f2x (&acc)[K * K]) {
+    constexpr int R = PG<K>::R, NCH = PG<K>::NCH, PROW = PG<K>::PROW, PHALF = PG<K>::PHALF;
+#pragma unroll
+    for (int r = 0; r < ROWS + 2 * R; ++r) {
+        const float* rp = rows + r * PROW;
+        f2x v[2 * NCH];
+#pragma unroll
+        for (int m = 0; m < NCH; ++m) {
+            const float4 t = *reinterpret_cast<const float4*>(
+                rp + 4 * (bj + (m >> 1) + (m & 1) * PHALF));
+            v[2 * m] = pk2(t.x, t.y);
+            v[2 * m + 1] = pk2(t.z, t.w);
+        }
+#pragma unroll
+        for (int o = 0; o < ROWS; ++o) {
+            const int u = r - o;
+            if (u < 0 || u >= K) continue;
+#pragma unroll
+            for (int vv = 0; vv < K; ++vv)
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    acc[u * K + vv] = fma2(g[o][q], v[q + vv], acc[u * K + vv]);
+        }
+    }
+}
+
+// Packed base weight-gradient correlation of a 4x4 pixel block: with g[o][p] =
+// (dY[o][2p], dY[o][2p+1]), acc[u*K+v] accumulates the even- and odd-column partial sums
+// of sum_{o,q} dY[o][q] X[o+u][q+v] (add the two halves at the end).
+template <int K>
+__device__ __forceinline__ void corr_base_4x4(const float* win, int pitch, const f2x (&g)[4][2],
+                                              f2x (&acc)[K * K]) {
+    constexpr int R = FG<K>::R, CNC = FG<K>::CNC;
+    constexpr int NV = 4 * CNC;
+#pragma unroll
+    for (int r = 0; r < 4 + 2 * R; ++r) {
+        float v[NV];
+        load_row<CNC>(win + r * pitch, v);
+        f2x A[NV / 2], B[NV / 2 - 1];
+#pragma unroll
+        for (int m = 0; m < NV / 2; ++m) A[m] = pk2(v[2 * m], v[2 * m + 1]);
+#pragma unroll
+        for (int m = 0; m < NV / 2 - 1; ++m) B[m] = pk2(v[2 * m + 1], v[2 * m + 2]);
+#pragma unroll
+        for (int o = 0; o < 4; ++o) {
+            const int u = r - o;
+            if (u < 0 || u >= K) continue;
+#pragma unroll
+            for (int vv = 0; vv < K; ++vv)
+#pragma unroll
+                for (int pp = 0; pp < 2; ++pp) {
+                    const int idx = 2 * pp + vv;
+                    const f2x in = (idx & 1) ? B[(idx - 1) >> 1] : A[idx >> 1];
+                    acc[u * K + vv] = fma2(g[o][pp], in, acc[u * K + vv]);
+                }
+        }
+    }
+}
+
+// TMA box of a staged tile with a 2R halo: columns from x0 - XOFF (16-byte aligned
+// start), XBW wide; rows from y0 - 2R, XBH high.
+template <int K, typename T>
+struct XBox {
+    static constexpr int R = FG<K>::R;
+    static constexpr int A = 16 / (int)sizeof(T);             // elements per 16 bytes
+    static constexpr int XOFF = ((2 * R + A - 1) / A) * A;
+    static constexpr int XBW = ((kTile + 2 * R + XOFF + A - 1) / A) * A;
+    static constexpr int XBH = kTile + 4 * R;
+    static constexpr int C0 = XOFF - 2 * R;                   // raw column of tile column 0
+    static constexpr int BYTES = XBW * XBH * (int)sizeof(T);
+};
+
+template <typename T>
+__device__ __forceinline__ float2 ld2_smem(const T* p);
+template <>
+__device__ __forceinline__ float2 ld2_smem<float>(const float* p) {
+    return *reinterpret_cast<const float2*>(p);
+}
+template <>
+__device__ __forceinline__ float2 ld2_smem<__nv_bfloat16>(const __nv_bfloat16* p) {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
+// Widen the TMA-staged raw tile to the fp32 tile (column c at c + PAD) and, when `bands`,
+// form the level-1 unnormalized subbands with an R halo in the two band-pair tiles.
+// One item = two horizontally adjacent cells (a 2x4 pixel block).
+template <int K, typename T>
+__device__ __forceinline__ void convert_raw(const T* raw, float* xs, float* bs, bool bands) {
+    constexpr int PAD = FG<K>::PAD, XP = FG<K>::XPITCH, BT = FG<K>::BT;
+    constexpr int NCR = PG<K>::NCR, PROW = PG<K>::PROW, PTILE = PG<K>::PTILE;
+    constexpr int PHALF = PG<K>::PHALF;
+    constexpr int RW = XBox<K, T>::XBW, C0 = XBox<K, T>::C0;
+    for (int idx = threadIdx.x; idx < BT * NCR; idx += blockDim.x) {
+        const int ci = idx / NCR, m = idx - ci * NCR;
+        const T* r0 = raw + (2 * ci) * RW + C0 + 4 * m;
+        const float2 a0 = ld2_smem<T>(r0), a1 = ld2_smem<T>(r0 + 2);
+        const float2 b0 = ld2_smem<T>(r0 + RW), b1 = ld2_smem<T>(r0 + RW + 2);
+        float* d0 = xs + (2 * ci) * XP + PAD + 4 * m;
+        if constexpr ((PAD & 1) == 0) {
+            reinterpret_cast<float2*>(d0)[0] = a0;
+            reinterpret_cast<float2*>(d0)[1] = a1;
+            reinterpret_cast<float2*>(d0 + XP)[0] = b0;
+            reinterpret_cast<float2*>(d0 + XP)[1] = b1;
+        } else {
+            d0[0] = a0.x; d0[1] = a0.y; d0[2] = a1.x; d0[3] = a1.y;
+            d0[XP] = b0.x; d0[XP + 1] = b0.y; d0[XP + 2] = b1.x; d0[XP + 3] = b1.y;
+        }
+        if (bands) {
+            const float4 u = haar_u(a0.x, a0.y, b0.x, b0.y);
+            const float4 v = haar_u(a1.x, a1.y, b1.x, b1.y);
+            float* q = bs + ci * PROW + 4 * pchunk(m, PHALF);
+            *reinterpret_cast<float4*>(q) = make_float4(u.x, u.y, v.x, v.y);
+            *reinterpret_cast<float4*>(q + PTILE) = make_float4(u.z, u.w, v.z, v.w);
+        }
+    }
+}
+
+// Non-TMA path: level-1 band-pair tiles from the staged fp32 tile.
+template <int K>
+__device__ __forceinline__ void pair_bands_from_tile(const float* xs, float* bs) {
+    constexpr int PAD = FG<K>::PAD, XP = FG<K>::XPITCH, BT = FG<K>::BT;
+    constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, PHALF = PG<K>::PHALF;
+    for (int idx = threadIdx.x; idx < BT * BT; idx += blockDim.x) {
+        const int ci = idx / BT, cj = idx - ci * BT;
+        const float* p = xs + (2 * ci) * XP + PAD + 2 * cj;
+        const float4 u = haar_u(p[0], p[1], p[XP], p[XP + 1]);
+        float* q = bs + ci * PROW + 4 * pchunk(cj >> 1, PHALF) + 2 * (cj & 1);
+        *reinterpret_cast<float2*>(q) = make_float2(u.x, u.y);
+        *reinterpret_cast<float2*>(q + PTILE) = make_float2(u.z, u.w);
+    }
+}
+
 // Stage pixels [y0-2R, y0+64+2R) x [x0-2R, x0+64+2R) of a plane into xs (pitch XPITCH,
 // column c stored at c + PAD), zero outside the plane. vec: W % 4 == 0 (aligned rows).
 template <int K, typename T>

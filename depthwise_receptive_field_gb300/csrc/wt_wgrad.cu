@@ -22,29 +22,39 @@
 // No atomics anywhere: results are bitwise reproducible.
 #include "wt_internal.h"
 #include "wt_tile.cuh"
+#include "wt_tma.cuh"
 
 namespace wt {
 
-constexpr int kDT = 128;  // threads per CTA
+constexpr int kDT = 256;  // threads per CTA
 
 struct DwArgs {
+    CUtensorMap tmx;  // X: dims {W, H, planes}, box {XBW, XBH, 1} (2R halo)
+    CUtensorMap tmg;  // dY: dims {W, H, planes}, box {64, 64, 1}
     const void* x;
     const void* dy;
     float* part;  // [C][N][KP]
+    int* err;     // set when a TMA wait times out (may be null)
     int N, C, H, W, L;
-    int vec;
+    int vec, use_tma;
     int KP;
-    int o_acc, o_red, o_xb, o_gb, o_x;  // shared-memory regions (floats)
+    int o_bar, o_rawx, o_rawg, o_acc, o_red, o_xb, o_gb, o_x, o_g;  // shared memory (floats)
     int o_carx[kMaxLevels + 1], o_cary[kMaxLevels + 1];
 };
 
-// Deep stage for level l: X subbands with an R halo into xb (band-major, BPITCH) and the
-// dY subbands of the tile's own 32x32 cells into gb ([4][32][32]); carriers for l < L.
+// dY subband-pair tiles (no halo): 32 rows x 32 cells, 16-byte chunks split even/odd.
+constexpr int kGHalf = 8;             // chunks per half row
+constexpr int kGRow = 8 * kGHalf;     // floats per row
+constexpr int kGTile = kCT * kGRow;   // floats per pair tile
+
+// Deep stage for level l: X subbands with an R halo into the X pair tiles, dY subbands of
+// the tile's own cells into the dY pair tiles; carriers X^(l), dY^(l) for l < L.
 template <int K, typename T>
 __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const T* xp, const T* gp,
                                               float* sm, int l, int ti0, int tj0) {
-    constexpr int R = FG<K>::R, BT = FG<K>::BT, BP = FG<K>::BPITCH, BAND = FG<K>::BAND;
-    constexpr int ZAND = FG<K>::ZAND;
+    constexpr int R = FG<K>::R, BT = FG<K>::BT;
+    constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, PHALF = PG<K>::PHALF;
+    constexpr int NIT = (BT * BT + kDT - 1) / kDT;
     const int Hl = a.H >> l, Wl = a.W >> l, Wp = a.W >> (l - 1);
     float* xb = sm + a.o_xb;
     float* gb = sm + a.o_gb;
@@ -52,7 +62,10 @@ __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const T* xp, cons
     const float* cpy = (l >= 3) ? sm + a.o_cary[l - 1] : nullptr;
     float* clx = (l < a.L) ? sm + a.o_carx[l] : nullptr;
     float* cly = (l < a.L) ? sm + a.o_cary[l] : nullptr;
-    for (int idx = threadIdx.x; idx < BT * BT; idx += blockDim.x) {
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+        const int idx = threadIdx.x + it * kDT;
+        if (idx >= BT * BT) break;
         const int si = idx / BT, sj = idx - si * BT;
         const int gi = ti0 - R + si, gj = tj0 - R + sj;
         const bool inner = si >= R && si < R + kCT && sj >= R && sj < R + kCT;
@@ -62,194 +75,285 @@ __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const T* xp, cons
             carrier_block<T>(l, xp, a.W, cpx, Wp, gi, gj, ca, cb, cc, cd);
             ux = haar_u(ca, cb, cc, cd);
             if (inner) {
-                if (clx) clx[(size_t)gi * Wl + gj] = 0.5f * ux.x;
+                if (clx) clx[gi * Wl + gj] = 0.5f * ux.x;
                 carrier_block<T>(l, gp, a.W, cpy, Wp, gi, gj, ca, cb, cc, cd);
                 ug = haar_u(ca, cb, cc, cd);
-                if (cly) cly[(size_t)gi * Wl + gj] = 0.5f * ug.x;
+                if (cly) cly[gi * Wl + gj] = 0.5f * ug.x;
             }
         }
-        float* q = xb + si * BP + sj;
-        q[0] = ux.x;
-        q[BAND] = ux.y;
-        q[2 * BAND] = ux.z;
-        q[3 * BAND] = ux.w;
+        float* q = xb + si * PROW + 4 * pchunk(sj >> 1, PHALF) + 2 * (sj & 1);
+        *reinterpret_cast<float2*>(q) = make_float2(ux.x, ux.y);
+        *reinterpret_cast<float2*>(q + PTILE) = make_float2(ux.z, ux.w);
         if (inner) {
-            float* r = gb + (si - R) * kCT + (sj - R);
-            r[0] = ug.x;
-            r[ZAND] = ug.y;
-            r[2 * ZAND] = ug.z;
-            r[3 * ZAND] = ug.w;
+            const int ci = si - R, cj = sj - R;
+            float* r = gb + ci * kGRow + 4 * pchunk(cj >> 1, kGHalf) + 2 * (cj & 1);
+            *reinterpret_cast<float2*>(r) = make_float2(ug.x, ug.y);
+            *reinterpret_cast<float2*>(r + kGTile) = make_float2(ug.z, ug.w);
         }
     }
 }
 
-// Sum v[] over all 32 lanes (xor butterfly); every lane ends with the totals.
+// Widen the TMA-staged raw dY tile (64x64) to the fp32 dY tile and, when `bands`, form
+// its level-1 unnormalized subbands in the dY pair tiles. One item = 2x4 pixels.
+template <typename T>
+__device__ __forceinline__ void convert_raw_dy(const T* raw, float* gs, float* gb, bool bands) {
+    for (int idx = threadIdx.x; idx < kCT * (kCT / 2); idx += blockDim.x) {
+        const int ci = idx >> 4, m = idx & 15;
+        const T* r0 = raw + (2 * ci) * kTile + 4 * m;
+        const float2 a0 = ld2_smem<T>(r0), a1 = ld2_smem<T>(r0 + 2);
+        const float2 b0 = ld2_smem<T>(r0 + kTile), b1 = ld2_smem<T>(r0 + kTile + 2);
+        float* d0 = gs + (2 * ci) * kTile + 4 * m;
+        *reinterpret_cast<float4*>(d0) = make_float4(a0.x, a0.y, a1.x, a1.y);
+        *reinterpret_cast<float4*>(d0 + kTile) = make_float4(b0.x, b0.y, b1.x, b1.y);
+        if (bands) {
+            const float4 u = haar_u(a0.x, a0.y, b0.x, b0.y);
+            const float4 v = haar_u(a1.x, a1.y, b1.x, b1.y);
+            float* q = gb + ci * kGRow + 4 * pchunk(m, kGHalf);
+            *reinterpret_cast<float4*>(q) = make_float4(u.x, u.y, v.x, v.y);
+            *reinterpret_cast<float4*>(q + kGTile) = make_float4(u.z, u.w, v.z, v.w);
+        }
+    }
+}
+
+// Non-TMA staging of the dY tile (fp32 tile + pair tiles), zero outside the plane.
+template <typename T>
+__device__ __forceinline__ void stage_dy_plain(const T* gp, int H, int W, float* gs, float* gb,
+                                               bool bands, int y0, int x0) {
+    for (int idx = threadIdx.x; idx < kCT * kCT; idx += blockDim.x) {
+        const int ci = idx / kCT, cj = idx - ci * kCT;
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int gy = y0 + 2 * ci + (e >> 1), gx = x0 + 2 * cj + (e & 1);
+            v[e] = (gy < H && gx < W) ? IO<T>::ld(gp + (size_t)gy * W + gx) : 0.f;
+        }
+        float* d0 = gs + (2 * ci) * kTile + 2 * cj;
+        d0[0] = v[0]; d0[1] = v[1]; d0[kTile] = v[2]; d0[kTile + 1] = v[3];
+        if (bands) {
+            const float4 u = haar_u(v[0], v[1], v[2], v[3]);
+            float* q = gb + ci * kGRow + 4 * pchunk(cj >> 1, kGHalf) + 2 * (cj & 1);
+            *reinterpret_cast<float2*>(q) = make_float2(u.x, u.y);
+            *reinterpret_cast<float2*>(q + kGTile) = make_float2(u.z, u.w);
+        }
+    }
+}
+
+// Sum NV values over the lanes of a warp (xor butterfly; every lane gets the totals).
 template <int NV>
-__device__ __forceinline__ void warp_sum(float (&v)[NV], int lanes) {
+__device__ __forceinline__ void warp_sum(float (&v)[NV]) {
 #pragma unroll
     for (int e = 0; e < NV; ++e) {
         float s = v[e];
-        for (int m = 1; m < lanes; m <<= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
         v[e] = s;
     }
 }
 
 template <int K, typename T>
-__global__ void __launch_bounds__(kDT, 3) wt_dw_plane_kernel(const DwArgs a) {
-    constexpr int R = FG<K>::R, KK = FG<K>::KK, PAD = FG<K>::PAD;
-    constexpr int XP = FG<K>::XPITCH, BP = FG<K>::BPITCH, BAND = FG<K>::BAND;
-    constexpr int ZAND = FG<K>::ZAND;
-    extern __shared__ float4 smem_f4[];
+__global__ void __launch_bounds__(kDT, 2) wt_dw_plane_kernel(const __grid_constant__ DwArgs a) {
+    constexpr int R = FG<K>::R, KK = FG<K>::KK, PAD = FG<K>::PAD, XP = FG<K>::XPITCH;
+    constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE;
+    extern __shared__ __align__(128) float4 smem_f4[];
     float* sm = reinterpret_cast<float*>(smem_f4);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + a.o_bar);
+    T* rawx = reinterpret_cast<T*>(sm + a.o_rawx);
+    T* rawg = reinterpret_cast<T*>(sm + a.o_rawg);
     float* acc_sm = sm + a.o_acc;
-    float* red = sm + a.o_red;
+    float* red = sm + a.o_red;  // [8 warps][64]
     float* xb = sm + a.o_xb;
     float* gb = sm + a.o_gb;
     float* xs = sm + a.o_x;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float* gs = sm + a.o_g;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool leader = tid == 0;
 
     const int c = blockIdx.x, n = blockIdx.y;
-    const size_t plane = (size_t)n * a.C + c;
+    const long long plane = (long long)n * a.C + c;
     const size_t plane_elems = (size_t)a.H * a.W;
     const T* xp = reinterpret_cast<const T*>(a.x) + plane * plane_elems;
     const T* gp = reinterpret_cast<const T*>(a.dy) + plane * plane_elems;
-    for (int e = threadIdx.x; e < a.KP; e += blockDim.x) acc_sm[e] = 0.f;
-    __syncthreads();
+    const int tiles_x = (a.W + kTile - 1) / kTile;
+    const int ntiles = tiles_x * ((a.H + kTile - 1) / kTile);
+    constexpr int BYTES = XBox<K, T>::BYTES + kTile * kTile * (int)sizeof(T);
 
-    // ---- deep levels: warp w correlates band w ----
+    for (int e = tid; e < a.KP; e += kDT) acc_sm[e] = 0.f;
+    if (a.use_tma && leader) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (a.use_tma && leader) {  // first tile, in flight during the deep levels
+        mbar_arrive_expect_tx(bar, BYTES);
+        tma_load_3d(rawx, &a.tmx, -XBox<K, T>::XOFF, -2 * R, (int)plane, bar);
+        tma_load_3d(rawg, &a.tmg, 0, 0, (int)plane, bar);
+    }
+    uint32_t ph = 0;
+
+    // ---- deep levels l = 2..L: band pair pp = tid / 128, 2x4 block per thread ----
     for (int l = 2; l <= a.L; ++l) {
         const int Hl = a.H >> l, Wl = a.W >> l;
-        float accd[KK];
+        const int pp = tid >> 7, bi = (tid >> 3) & 15, bj = tid & 7;
+        f2x accd[KK];
 #pragma unroll
-        for (int q = 0; q < KK; ++q) accd[q] = 0.f;
+        for (int q = 0; q < KK; ++q) accd[q] = 0ull;
         for (int ti0 = 0; ti0 < Hl; ti0 += kCT) {
             for (int tj0 = 0; tj0 < Wl; tj0 += kCT) {
                 dw_deep_stage<K, T>(a, xp, gp, sm, l, ti0, tj0);
                 __syncthreads();
+                if (ti0 + 2 * bi < Hl && tj0 + 4 * bj < Wl) {
+                    f2x g[2][4];
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int blk = lane + 32 * k, bi = blk >> 3, bj = blk & 7;
-                    if (ti0 + 4 * bi >= Hl || tj0 + 4 * bj >= Wl) continue;
-                    float g[4][4];
-                    const float* gr = gb + warp * ZAND + (4 * bi) * kCT + 4 * bj;
-#pragma unroll
-                    for (int o = 0; o < 4; ++o) {
-                        const float4 t = *reinterpret_cast<const float4*>(gr + o * kCT);
-                        g[o][0] = t.x; g[o][1] = t.y; g[o][2] = t.z; g[o][3] = t.w;
+                    for (int o = 0; o < 2; ++o) {
+                        const float* gr = gb + pp * kGTile + (2 * bi + o) * kGRow;
+                        const float4 t0 = *reinterpret_cast<const float4*>(gr + 4 * bj);
+                        const float4 t1 = *reinterpret_cast<const float4*>(gr + 4 * (kGHalf + bj));
+                        g[o][0] = pk2(t0.x, t0.y);
+                        g[o][1] = pk2(t0.z, t0.w);
+                        g[o][2] = pk2(t1.x, t1.y);
+                        g[o][3] = pk2(t1.z, t1.w);
                     }
-                    corr_rows<K, 4>(xb + warp * BAND + (4 * bi) * BP + 4 * bj, BP, g, accd);
+                    corr_pair<K, 2>(xb + pp * PTILE + (2 * bi) * PROW, bj, g, accd);
                 }
                 __syncthreads();
             }
         }
-        warp_sum<KK>(accd, 32);
-        float* dst = acc_sm + KK + 1 + (l - 1) * 4 * KK + warp * KK;
+        // flush: warps 4pp..4pp+3 hold band pair pp; fixed-order sum into acc_sm
+        float v[2 * KK];
 #pragma unroll
-        for (int e = 0; e < KK; ++e)
-            if (lane == (e & 31)) dst[e] += accd[e];
+        for (int q = 0; q < KK; ++q) {
+            const float2 t = upk2(accd[q]);
+            v[2 * q] = t.x;
+            v[2 * q + 1] = t.y;
+        }
+        warp_sum<2 * KK>(v);
+        if (lane == 0) {
+#pragma unroll
+            for (int e = 0; e < 2 * KK; ++e) red[warp * 128 + e] = v[e];
+        }
+        __syncthreads();
+        for (int e = tid; e < 4 * KK; e += kDT) {
+            const int p2 = e / (2 * KK), k = e - p2 * 2 * KK;  // k = 2*tap + band-in-pair
+            float s = 0.f;
+            for (int w = 0; w < 4; ++w) s += red[(4 * p2 + w) * 128 + k];
+            acc_sm[KK + 1 + (l - 1) * 4 * KK + (2 * p2 + (k & 1)) * KK + (k >> 1)] += s;
+        }
+        __syncthreads();
     }
 
-    // ---- level 1 and the base path ----
-    const bool base_role = (a.L == 0) || (warp < 2);
-    float acc[KK + 1];  // taps (+ bias sum for the base role)
+    // ---- full resolution: warps 0-3 base path, warps 4-7 level-1 band pairs ----
+    const bool base_role = (a.L == 0) || (tid < 128);
+    f2x acc[KK];
 #pragma unroll
-    for (int q = 0; q <= KK; ++q) acc[q] = 0.f;
-    for (int y0 = 0; y0 < a.H; y0 += kTile) {
-        for (int x0 = 0; x0 < a.W; x0 += kTile) {
-            stage_tile<K, T>(xp, a.H, a.W, a.vec, xs, y0, x0);
-            if (a.L >= 1) {
-                // dY subbands of the tile's 32x32 coefficients (no halo needed)
-                for (int idx = threadIdx.x; idx < kCT * kCT; idx += blockDim.x) {
-                    const int ci = idx / kCT, cj = idx - ci * kCT;
-                    const int gy = y0 + 2 * ci, gx = x0 + 2 * cj;
-                    float4 u = f4_zero();
-                    if (gy < a.H && gx < a.W) {
-                        const float2 r0 = IO<T>::ld2(gp + (size_t)gy * a.W + gx);
-                        const float2 r1 = IO<T>::ld2(gp + (size_t)(gy + 1) * a.W + gx);
-                        u = haar_u(r0.x, r0.y, r1.x, r1.y);
-                    }
-                    float* r = gb + ci * kCT + cj;
-                    r[0] = u.x;
-                    r[ZAND] = u.y;
-                    r[2 * ZAND] = u.z;
-                    r[3 * ZAND] = u.w;
-                }
+    for (int q = 0; q < KK; ++q) acc[q] = 0ull;
+    float dbs = 0.f;
+    bool failed = false;
+    for (int t = 0; t < ntiles; ++t) {
+        const int ty = t / tiles_x, tx = t - ty * tiles_x;
+        const int y0 = ty * kTile, x0 = tx * kTile;
+        if (a.use_tma) {
+            const bool ok = mbar_wait_bounded(bar, ph);
+            ph ^= 1;
+            if (__syncthreads_or(!ok)) {
+                failed = true;
+                break;
             }
+            convert_raw<K, T>(rawx, xs, xb, a.L >= 1);
+            convert_raw_dy<T>(rawg, gs, gb, a.L >= 1);
+            __syncthreads();
+            if (leader && t + 1 < ntiles) {
+                const int ny = (t + 1) / tiles_x, nx = (t + 1) - ny * tiles_x;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar, BYTES);
+                tma_load_3d(rawx, &a.tmx, nx * kTile - XBox<K, T>::XOFF, ny * kTile - 2 * R,
+                            (int)plane, bar);
+                tma_load_3d(rawg, &a.tmg, nx * kTile, ny * kTile, (int)plane, bar);
+            }
+        } else {
+            stage_tile<K, T>(xp, a.H, a.W, a.vec, xs, y0, x0);
+            stage_dy_plain<T>(gp, a.H, a.W, gs, gb, a.L >= 1, y0, x0);
             __syncthreads();
             if (a.L >= 1) {
-                bands_from_tile<K>(xs, xb);
+                pair_bands_from_tile<K>(xs, xb);
                 __syncthreads();
             }
-            if (base_role) {
-                const int nb = (a.L == 0) ? 1 : 2;
-                for (int k = 0; k < nb; ++k) {
-                    const int blk = (a.L == 0) ? threadIdx.x : threadIdx.x + 64 * k;
-                    const int by = blk >> 4, bx = blk & 15;
-                    const int gy = y0 + 8 * by, gx = x0 + 4 * bx;
-                    if (gy >= a.H || gx >= a.W) continue;
-                    float g[8][4];
-#pragma unroll
-                    for (int o = 0; o < 8; ++o) {
-                        if (a.vec && gy + o < a.H) {
-                            const float4 t = IO<T>::ld4(gp + (size_t)(gy + o) * a.W + gx);
-                            g[o][0] = t.x; g[o][1] = t.y; g[o][2] = t.z; g[o][3] = t.w;
-                        } else {
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                g[o][q] = (gy + o < a.H && gx + q < a.W)
-                                              ? IO<T>::ld(gp + (size_t)(gy + o) * a.W + gx + q)
-                                              : 0.f;
-                        }
-                        acc[KK] += (g[o][0] + g[o][1]) + (g[o][2] + g[o][3]);
-                    }
-                    corr_rows<K, 8>(xs + (8 * by + R) * XP + 4 * bx + R + PAD, XP, g, acc);
-                }
-            } else {
-                const int b = (threadIdx.x - 64) >> 4, j = (threadIdx.x - 64) & 15;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int blk = j + 16 * k, bi = blk >> 3, bj = blk & 7;
-                    if (y0 / 2 + 4 * bi >= a.H / 2 || x0 / 2 + 4 * bj >= a.W / 2) continue;
-                    float g[4][4];
-                    const float* gr = gb + b * ZAND + (4 * bi) * kCT + 4 * bj;
-#pragma unroll
-                    for (int o = 0; o < 4; ++o) {
-                        const float4 t = *reinterpret_cast<const float4*>(gr + o * kCT);
-                        g[o][0] = t.x; g[o][1] = t.y; g[o][2] = t.z; g[o][3] = t.w;
-                    }
-                    corr_rows<K, 4>(xb + b * BAND + (4 * bi) * BP + 4 * bj, BP, g, acc);
-                }
-            }
-            __syncthreads();
         }
+        if (base_role) {
+            const int nb = (a.L == 0) ? 1 : 2;
+            for (int k = 0; k < nb; ++k) {
+                const int blk = tid + kDT / 2 * k;  // L == 0: tid covers all 256 blocks
+                const int by = blk >> 4, bx = blk & 15;
+                if (y0 + 4 * by >= a.H || x0 + 4 * bx >= a.W) continue;
+                f2x g[4][2];
+#pragma unroll
+                for (int o = 0; o < 4; ++o) {
+                    const float4 tv = *reinterpret_cast<const float4*>(gs + (4 * by + o) * kTile + 4 * bx);
+                    g[o][0] = pk2(tv.x, tv.y);
+                    g[o][1] = pk2(tv.z, tv.w);
+                    dbs += (tv.x + tv.y) + (tv.z + tv.w);
+                }
+                corr_base_4x4<K>(xs + (4 * by + R) * XP + 4 * bx + R + PAD, XP, g, acc);
+            }
+        } else {
+            const int t2 = tid - 128, pp = t2 >> 6, bi = (t2 >> 3) & 7, bj = t2 & 7;
+            if (y0 / 2 + 4 * bi < a.H / 2 && x0 / 2 + 4 * bj < a.W / 2) {
+                f2x g[4][4];
+#pragma unroll
+                for (int o = 0; o < 4; ++o) {
+                    const float* gr = gb + pp * kGTile + (4 * bi + o) * kGRow;
+                    const float4 t0 = *reinterpret_cast<const float4*>(gr + 4 * bj);
+                    const float4 t1 = *reinterpret_cast<const float4*>(gr + 4 * (kGHalf + bj));
+                    g[o][0] = pk2(t0.x, t0.y);
+                    g[o][1] = pk2(t0.z, t0.w);
+                    g[o][2] = pk2(t1.x, t1.y);
+                    g[o][3] = pk2(t1.z, t1.w);
+                }
+                corr_pair<K, 4>(xb + pp * PTILE + (4 * bi) * PROW, bj, g, acc);
+            }
+        }
+        __syncthreads();
+    }
+    if (failed) {
+        if (leader && a.err != nullptr) atomicExch(a.err, kErrTmaTimeout);
+        return;
     }
 
     // ---- flush: fixed-order reductions into acc_sm, then the partial vector ----
-    if (base_role) {
-        warp_sum<KK + 1>(acc, 32);
+    {
+        float v[2 * KK + 1];
+#pragma unroll
+        for (int q = 0; q < KK; ++q) {
+            const float2 tv = upk2(acc[q]);
+            v[2 * q] = tv.x;
+            v[2 * q + 1] = tv.y;
+        }
+        v[2 * KK] = dbs;
+        warp_sum<2 * KK + 1>(v);
         if (lane == 0) {
 #pragma unroll
-            for (int e = 0; e <= KK; ++e) red[warp * (KK + 1) + e] = acc[e];
-        }
-    } else {
-        warp_sum<KK + 1>(acc, 16);  // lanes 0-15 and 16-31 hold one band each
-        const int b = (threadIdx.x - 64) >> 4;
-        float* dst = acc_sm + KK + 1 + b * KK;
-        if ((lane & 15) == 0) {
-#pragma unroll
-            for (int e = 0; e < KK; ++e) dst[e] += acc[e];
+            for (int e = 0; e <= 2 * KK; ++e) red[warp * 128 + e] = v[e];
         }
     }
     __syncthreads();
-    const int nbase = (a.L == 0) ? 4 : 2;
-    for (int e = threadIdx.x; e <= KK; e += blockDim.x) {
+    const int nbase = (a.L == 0) ? 8 : 4;
+    for (int e = tid; e <= KK; e += kDT) {
+        // base taps: even + odd column halves of each base warp; e == KK: the bias sum
         float s = 0.f;
-        for (int w = 0; w < nbase; ++w) s += red[w * (KK + 1) + e];
+        for (int w = 0; w < nbase; ++w)
+            s += (e < KK) ? (red[w * 128 + 2 * e] + red[w * 128 + 2 * e + 1]) : red[w * 128 + 2 * KK];
         acc_sm[e] += s;
+    }
+    if (a.L >= 1) {
+        for (int e = tid; e < 4 * KK; e += kDT) {
+            // band pair pp lives in warps 4 + 2pp and 5 + 2pp
+            const int p2 = e / (2 * KK), k = e - p2 * 2 * KK;
+            const float s = red[(4 + 2 * p2) * 128 + k] + red[(5 + 2 * p2) * 128 + k];
+            acc_sm[KK + 1 + (2 * p2 + (k & 1)) * KK + (k >> 1)] += s;
+        }
     }
     __syncthreads();
     float* out = a.part + ((size_t)c * a.N + n) * a.KP;
-    for (int e = threadIdx.x; e < a.KP; e += blockDim.x) out[e] = acc_sm[e];
+    for (int e = tid; e < a.KP; e += kDT) out[e] = acc_sm[e];
 }
 
 // Per channel: fixed-order sum of the N partial vectors, then §4.3 Eq. 9.
@@ -298,24 +402,38 @@ __global__ void wt_dw_reduce_kernel(const float* part, int C, int G, int KP, int
 namespace {
 
 int round4(int v) { return (v + 3) & ~3; }
+int round32(int v) { return (v + 31) & ~31; }
 
-template <int K>
+constexpr size_t kDwErrBytes = 256;  // the workspace starts with a status word
+
+template <int K, typename T>
 void dw_layout(const wt_desc& d, DwArgs& a, size_t& smem_bytes) {
     constexpr int KK = FG<K>::KK;
     const int L = d.levels;
     a.KP = KK + 1 + 4 * KK * L;
     int off = 0;
+    a.o_bar = off;
+    off += 32;
+    a.o_rawx = off;
+    off += round32((XBox<K, T>::BYTES + 3) / 4);
+    a.o_rawg = off;
+    off += round32(kTile * kTile * (int)sizeof(T) / 4);
     a.o_acc = off;
-    off += round4(a.KP);
+    off += round32(a.KP);
     a.o_red = off;
-    off += round4(4 * (KK + 1));
+    off += 8 * 128;
     a.o_xb = off;
-    off += 4 * FG<K>::BAND;
+    off += 2 * PG<K>::PTILE;
+    off = round4(off);
     a.o_gb = off;
-    off += 4 * FG<K>::ZAND;
-    a.o_x = off;
+    off += 2 * kGTile;
+    // the fp32 X and dY tiles share their region with the deep-level carriers
     const int alias0 = off;
+    a.o_x = off;
     off += FG<K>::XROWS * FG<K>::XPITCH;
+    off = round4(off);
+    a.o_g = off;
+    off += kTile * kTile;
     int cp = alias0;
     for (int l = 0; l <= kMaxLevels; ++l) a.o_carx[l] = a.o_cary[l] = 0;
     for (int l = 2; l < L; ++l) {
@@ -329,26 +447,41 @@ void dw_layout(const wt_desc& d, DwArgs& a, size_t& smem_bytes) {
     smem_bytes = (size_t)total * sizeof(float);
 }
 
+// Fill the kernel arguments (layout, pointers, tensor maps) for one launch.
 template <int K, typename T>
-wt_status launch_dw_k(const wt_desc& d, const void* x, const void* dy, const float* w0,
-                      const float* b0, const float* s0, const float* wl, const float* sl,
-                      float* dw0, float* db0, float* ds0, float* dwl, float* dsl, void* ws,
-                      size_t ws_bytes, cudaStream_t stream, int* launches) {
-    DwArgs a;
-    size_t smem = 0;
-    dw_layout<K>(d, a, smem);
-    if (smem > kMaxSmemPerBlock) return WT_ERR_UNSUPPORTED;
-    const size_t need = (size_t)d.c * d.n * a.KP * sizeof(float);
-    if (ws == nullptr || ws_bytes < need) return WT_ERR_WORKSPACE;
+bool dw_prepare(const wt_desc& d, const void* x, const void* dy, float* part, int* err,
+                DwArgs& a, size_t& smem) {
+    dw_layout<K, T>(d, a, smem);
+    if (smem > kMaxSmemPerBlock) return false;
     a.x = x;
     a.dy = dy;
-    a.part = reinterpret_cast<float*>(ws);
+    a.part = part;
+    a.err = err;
     a.N = d.n;
     a.C = d.c;
     a.H = d.h;
     a.W = d.w;
     a.L = d.levels;
     a.vec = (d.w % 4 == 0) ? 1 : 0;
+    a.use_tma = 0;
+    const size_t esize = sizeof(T);
+    if (((size_t)d.w * esize) % 16 == 0) {
+        const CUtensorMapDataType dt =
+            sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+        const unsigned long long planes = (unsigned long long)d.n * d.c;
+        const unsigned long long s1 = (unsigned long long)d.w * esize;
+        const unsigned long long s2 = (unsigned long long)d.w * d.h * esize;
+        const bool ok =
+            encode_3d(&a.tmx, dt, x, d.w, d.h, planes, s1, s2, XBox<K, T>::XBW, XBox<K, T>::XBH) &&
+            encode_3d(&a.tmg, dt, dy, d.w, d.h, planes, s1, s2, kTile, kTile);
+        a.use_tma = ok ? 1 : 0;
+    }
+    return true;
+}
+
+template <int K, typename T>
+wt_status launch_dw_plane(const DwArgs& a, size_t smem, const wt_desc& d, cudaStream_t stream,
+                          int* launches) {
     auto kern = wt_dw_plane_kernel<K, T>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
@@ -356,8 +489,27 @@ wt_status launch_dw_k(const wt_desc& d, const void* x, const void* dy, const flo
     kern<<<dim3((unsigned)d.c, (unsigned)d.n), kDT, smem, stream>>>(a);
     if (cudaGetLastError() != cudaSuccess) return WT_ERR_CUDA;
     ++*launches;
+    return WT_OK;
+}
+
+template <int K, typename T>
+wt_status launch_dw_k(const wt_desc& d, const void* x, const void* dy, const float* w0,
+                      const float* b0, const float* s0, const float* wl, const float* sl,
+                      float* dw0, float* db0, float* ds0, float* dwl, float* dsl, void* ws,
+                      size_t ws_bytes, cudaStream_t stream, int* launches) {
+    const int KP = FG<K>::KK + 1 + 4 * FG<K>::KK * d.levels;
+    const size_t need = kDwErrBytes + (size_t)d.c * d.n * KP * sizeof(float);
+    if (ws == nullptr || ws_bytes < need) return WT_ERR_WORKSPACE;
+    int* err = reinterpret_cast<int*>(ws);
+    float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + kDwErrBytes);
+    DwArgs a;
+    size_t smem = 0;
+    if (!dw_prepare<K, T>(d, x, dy, part, err, a, smem)) return WT_ERR_UNSUPPORTED;
+    if (cudaMemsetAsync(err, 0, sizeof(int), stream) != cudaSuccess) return WT_ERR_CUDA;
+    wt_status st = launch_dw_plane<K, T>(a, smem, d, stream, launches);
+    if (st != WT_OK) return st;
     wt_dw_reduce_kernel<<<(unsigned)d.c, 128, (size_t)a.KP * sizeof(float), stream>>>(
-        a.part, d.c, d.n, a.KP, K, d.levels, w0, b0, s0, wl, sl, dw0, db0, ds0, dwl, dsl);
+        part, d.c, d.n, a.KP, K, d.levels, w0, b0, s0, wl, sl, dw0, db0, ds0, dwl, dsl);
     if (cudaGetLastError() != cudaSuccess) return WT_ERR_CUDA;
     ++*launches;
     return WT_OK;
@@ -368,25 +520,8 @@ wt_status launch_dw_partials_k(const wt_desc& d, const void* x, const void* dy, 
                                cudaStream_t stream, int* launches) {
     DwArgs a;
     size_t smem = 0;
-    dw_layout<K>(d, a, smem);
-    if (smem > kMaxSmemPerBlock) return WT_ERR_UNSUPPORTED;
-    a.x = x;
-    a.dy = dy;
-    a.part = part;
-    a.N = d.n;
-    a.C = d.c;
-    a.H = d.h;
-    a.W = d.w;
-    a.L = d.levels;
-    a.vec = (d.w % 4 == 0) ? 1 : 0;
-    auto kern = wt_dw_plane_kernel<K, T>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-        return WT_ERR_CUDA;
-    kern<<<dim3((unsigned)d.c, (unsigned)d.n), kDT, smem, stream>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return WT_ERR_CUDA;
-    ++*launches;
-    return WT_OK;
+    if (!dw_prepare<K, T>(d, x, dy, part, nullptr, a, smem)) return WT_ERR_UNSUPPORTED;
+    return launch_dw_plane<K, T>(a, smem, d, stream, launches);
 }
 
 }  // namespace
@@ -395,8 +530,8 @@ wt_status launch_dw_partials(const wt_desc& d, const void* x, const void* dy, fl
                              cudaStream_t stream, int* launches) {
     const bool bf = d.io == WT_BF16;
     switch (d.k) {
-#define WT_CASE(KV)                                                                          \
-    case KV:                                                                                 \
+#define WT_CASE(KV)                                                                           \
+    case KV:                                                                                  \
         return bf ? launch_dw_partials_k<KV, __nv_bfloat16>(d, x, dy, part, stream, launches) \
                   : launch_dw_partials_k<KV, float>(d, x, dy, part, stream, launches);
         WT_CASE(1)
@@ -427,19 +562,18 @@ size_t dw_partial_floats(const wt_desc& d) {
 }
 
 size_t backward_weight_ws_bytes(const wt_desc& d) {
-    const int KK = d.k * d.k;
-    const size_t KP = (size_t)KK + 1 + 4 * (size_t)KK * d.levels;
-    return (size_t)d.c * d.n * KP * sizeof(float);
+    return kDwErrBytes + (size_t)d.c * d.n * dw_partial_floats(d) * sizeof(float);
 }
 
 size_t backward_weight_smem_bytes(const wt_desc& d) {
     DwArgs a;
     size_t smem = 0;
+    const bool bf = d.io == WT_BF16;
     switch (d.k) {
-        case 1: dw_layout<1>(d, a, smem); break;
-        case 3: dw_layout<3>(d, a, smem); break;
-        case 5: dw_layout<5>(d, a, smem); break;
-        case 7: dw_layout<7>(d, a, smem); break;
+        case 1: bf ? dw_layout<1, __nv_bfloat16>(d, a, smem) : dw_layout<1, float>(d, a, smem); break;
+        case 3: bf ? dw_layout<3, __nv_bfloat16>(d, a, smem) : dw_layout<3, float>(d, a, smem); break;
+        case 5: bf ? dw_layout<5, __nv_bfloat16>(d, a, smem) : dw_layout<5, float>(d, a, smem); break;
+        case 7: bf ? dw_layout<7, __nv_bfloat16>(d, a, smem) : dw_layout<7, float>(d, a, smem); break;
         default: return 0;
     }
     return smem;

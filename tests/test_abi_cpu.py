@@ -93,7 +93,8 @@ def test_workspace_sizes_for_workloads(lib, name):
         slot = sum(4 * (wl.h >> l) * (wl.w >> l) for l in range(2, wl.levels + 1)) * 4
         assert fwd >= 256 + slot and fwd % 256 == 0
         assert fwd <= 256 + 2 * 152 * ((slot + 255) // 256 * 256)  # at most 2 CTAs per SM
-    # backward-weight: one partial vector [dW0 | db | dW^(l)] per (channel, image)
+    # backward-weight: a 256-byte status word, then one partial vector
+    # [dW0 | db | dW^(l)] per (channel, image)
     kk = wl.k * wl.k
     per_partial = (kk + 1 + 4 * kk * wl.levels) * 4
-    assert bwd_w == wl.c * wl.n * per_partial
+    assert bwd_w == 256 + wl.c * wl.n * per_partial
