@@ -138,20 +138,49 @@ __device__ __forceinline__ void stage_dy_plain(const T* gp, int H, int W, float*
     }
 }
 
-// Sum NV values over the lanes of a warp (xor butterfly; every lane gets the totals).
-template <int NV>
-__device__ __forceinline__ void warp_sum(float (&v)[NV]) {
+// Recursive-halving warp reduction of 32 values: lane l ends with the warp total of
+// entry l in v[0]. 31 shuffles per lane instead of 160 for an all-to-all butterfly.
+__device__ __forceinline__ void warp_reduce32(float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int e = 0; e < NV; ++e) {
-        float s = v[e];
+    for (int s = 0; s < 5; ++s) {
+        const int mask = 16 >> s;
+        const int half = 16 >> s;
+        const bool upper = (lane & mask) != 0;
 #pragma unroll
-        for (int m = 1; m < 32; m <<= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
-        v[e] = s;
+        for (int i = 0; i < half; ++i) {
+            const float keep = upper ? v[i + half] : v[i];
+            const float send = upper ? v[i] : v[i + half];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+        }
+    }
+}
+
+// Warp totals of NV values (pairs of packed accumulators, then an optional extra
+// scalar) into red[e], e < NV, 32 entries at a time.
+template <int NQ, int NV>
+__device__ __forceinline__ void warp_totals_to(const f2x (&acc)[NQ], float extra, float* red) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int c0 = 0; c0 < NV; c0 += 32) {
+        float t[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int e = c0 + j;
+            if (e < 2 * NQ) {
+                const float2 p = upk2(acc[e >> 1]);
+                t[j] = (e & 1) ? p.y : p.x;
+            } else {
+                t[j] = (e == 2 * NQ && e < NV) ? extra : 0.f;
+            }
+        }
+        warp_reduce32(t);
+        if (c0 + lane < NV) red[c0 + lane] = t[0];
     }
 }
 
 template <int K, typename T>
-__global__ void __launch_bounds__(kDT, 2) wt_dw_plane_kernel(const __grid_constant__ DwArgs a) {
+__global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(const __grid_constant__ DwArgs a) {
     constexpr int R = FG<K>::R, KK = FG<K>::KK, PAD = FG<K>::PAD, XP = FG<K>::XPITCH;
     constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE;
     extern __shared__ __align__(128) float4 smem_f4[];
@@ -219,18 +248,7 @@ __global__ void __launch_bounds__(kDT, 2) wt_dw_plane_kernel(const __grid_consta
             }
         }
         // flush: warps 4pp..4pp+3 hold band pair pp; fixed-order sum into acc_sm
-        float v[2 * KK];
-#pragma unroll
-        for (int q = 0; q < KK; ++q) {
-            const float2 t = upk2(accd[q]);
-            v[2 * q] = t.x;
-            v[2 * q + 1] = t.y;
-        }
-        warp_sum<2 * KK>(v);
-        if (lane == 0) {
-#pragma unroll
-            for (int e = 0; e < 2 * KK; ++e) red[warp * 128 + e] = v[e];
-        }
+        warp_totals_to<KK, 2 * KK>(accd, 0.f, red + warp * 128);
         __syncthreads();
         for (int e = tid; e < 4 * KK; e += kDT) {
             const int p2 = e / (2 * KK), k = e - p2 * 2 * KK;  // k = 2*tap + band-in-pair
@@ -319,21 +337,7 @@ __global__ void __launch_bounds__(kDT, 2) wt_dw_plane_kernel(const __grid_consta
     }
 
     // ---- flush: fixed-order reductions into acc_sm, then the partial vector ----
-    {
-        float v[2 * KK + 1];
-#pragma unroll
-        for (int q = 0; q < KK; ++q) {
-            const float2 tv = upk2(acc[q]);
-            v[2 * q] = tv.x;
-            v[2 * q + 1] = tv.y;
-        }
-        v[2 * KK] = dbs;
-        warp_sum<2 * KK + 1>(v);
-        if (lane == 0) {
-#pragma unroll
-            for (int e = 0; e <= 2 * KK; ++e) red[warp * 128 + e] = v[e];
-        }
-    }
+    warp_totals_to<KK, 2 * KK + 1>(acc, dbs, red + warp * 128);
     __syncthreads();
     const int nbase = (a.L == 0) ? 8 : 4;
     for (int e = tid; e <= KK; e += kDT) {
