@@ -4,14 +4,15 @@
 // (Aflalo et al.). A persistent CTA (256 threads) walks (n, c) planes and evaluates the
 // whole layer on each with one read of X and one write of Y in HBM:
 //
-//   deep phase (L >= 2) -- levels l = 2..L run at their own resolution: 32x32 output
-//     tiles of the level's Haar subbands (§4.1 Eq. 5, recomputed on chip from the low-pass
-//     carrier X^(l-1); level 2 reads X itself in 4x4 pixel blocks) are staged in shared
-//     memory with an R-coefficient halo and filtered by the four folded k x k kernels
-//     (§4.3 Eq. 8). The filtered subbands Z^(l) go to this CTA's scratch slot (tens of KB,
-//     L2-resident). A last pass sums Eq. 7's terms of levels 2..L at level-1 resolution
-//     (§4.2 Prop. 2: coefficient address by coordinate shifts, signs by coordinate bits)
-//     and writes that sum in place of Z^(2).
+//   deep phase (L >= 2) -- a first sweep streams X through shared memory in TMA boxes
+//     (several in flight) and turns every 4x4 pixel block into the four subbands of level
+//     2 (§4.1 Eq. 5 twice: the level-1 carrier X^(1), then its Haar transform), stored in
+//     the CTA's scratch slot, and into the carrier X^(2) in shared memory. Levels l = 3..L
+//     then run from the carriers at their own resolution, and level 2 from the stored
+//     subbands: 32x32 output tiles of the subbands are staged with an R-coefficient halo
+//     and filtered by the four folded k x k kernels (§4.3 Eq. 8). A last pass sums Eq. 7's
+//     terms of levels 2..L at level-1 resolution (§4.2 Prop. 2: coefficient address by
+//     coordinate shifts, signs by coordinate bits) into the scratch slot.
 //   full-resolution phase -- 64x64-pixel tiles: a TMA load brings the tile of X with a
 //     2R halo (zero outside the plane) into shared memory while the previous tile is being
 //     computed; one pass widens it to fp32 and forms the four level-1 subbands; four
@@ -35,17 +36,19 @@ constexpr int kFT = 256;  // threads per CTA
 struct FwdArgs {
     CUtensorMap tmx;  // X: dims {W, H, planes}, box {XBW, XBH, 1}
     CUtensorMap tmd;  // deep sum: dims {4*W2, H2, slots}, box {64, 16, 1}
+    CUtensorMap tms;  // X for the level-2 sweep: dims {W, H, planes}, box {64, SweepBox::BH, 1}
     const void* x;
     void* y;
-    const float* w0f;
     const float* b0f;
-    const float* wlf;
-    float* zd;         // scratch: one slot of zd_slot floats per CTA (the deep sums)
+    const float* wimg;  // per channel, the shared-memory image of its folded weights
+    float* zd;         // scratch: per CTA the deep sums, then the level-2 subbands
     int* err;          // first word of the workspace: set on a stuck TMA wait
-    long long zd_slot;
+    long long zd_slot;  // floats of each of the two arrays of a CTA's slot
+    long long slot;     // floats between consecutive CTAs' slots (2 * zd_slot)
     long long planes;
     int C, H, W, L;
-    int flip, vec, use_tma;
+    int img;  // floats of one channel's weight image (a multiple of 4)
+    int vec, use_tma;
     int o_bar, o_raw, o_dblk, o_w, o_b, o_x, o_z;  // shared-memory regions (floats)
     int o_car[kMaxLevels + 1];                    // carriers X^(l), l = 2..L-1
     int o_zl[kMaxLevels + 1];                     // Z^(l), l = 3..L, interleaved [Hl][Wl][4]
@@ -53,82 +56,128 @@ struct FwdArgs {
 
 constexpr int kDBytes = 16 * 64 * 4;  // deep-sum box: 16 level-2 rows x 16 positions x 4
 
-// Folded weights of channel c into shared memory as packed pairs: slot 0 holds the base
-// taps duplicated (w, w); slot 1 + 2(l-1) + p holds level l's band pair p as
-// (w_{2p}, w_{2p+1}), each scaled by 2^-(l+1) (1/2 turns unnormalized subbands into
-// Eq. 5's, 2^-l is Eq. 7's level weight). Taps are rotated by 180 degrees when `flip`.
+// Shared-memory image of each channel's folded weights, built once per call: slot 0 holds
+// the base taps duplicated (w, w); slot 1 + 2(l-1) + p holds level l's band pair p as
+// (w_{2p}, w_{2p+1}), each scaled by 2^-(l+1) (1/2 turns unnormalized subbands into Eq. 5's,
+// 2^-l is Eq. 7's level weight). Taps are rotated by 180 degrees when `flip` (backward-data).
+// The plane kernel brings a channel's image into shared memory with one bulk copy.
 template <int K>
-__device__ __forceinline__ void load_weights(const FwdArgs& a, int c, float* wsm) {
+__global__ void wt_fwd_weight_image_kernel(const float* w0f, const float* wlf, int C, int L,
+                                           int flip, float* img) {
     constexpr int KK = FG<K>::KK, WS = PG<K>::WS;
-    const int nk = 1 + 4 * a.L;  // base + 4 bands per level
-    for (int e = threadIdx.x; e < nk * KK; e += blockDim.x) {
-        const int s = e / KK, uv = e - s * KK;
-        const int src = a.flip ? (KK - 1 - uv) : uv;
-        if (s == 0) {
-            const float v = __ldg(a.w0f + (size_t)c * KK + src);
-            wsm[2 * uv] = v;
-            wsm[2 * uv + 1] = v;
-        } else {
-            const int l = 1 + (s - 1) / 4, b = (s - 1) & 3;
-            const float v = ldexpf(1.0f, -(l + 1)) *
-                            __ldg(a.wlf + (((size_t)(l - 1) * a.C + c) * 4 + b) * KK + src);
-            wsm[(1 + 2 * (l - 1) + (b >> 1)) * WS + 2 * uv + (b & 1)] = v;
+    const int per_c = WS * (1 + 2 * L);
+    const long long n = (long long)C * per_c;
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < n;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int c = (int)(e / per_c), o = (int)(e - (long long)c * per_c);
+        const int slot = o / WS, r = o - slot * WS;
+        float v = 0.f;
+        if (r < 2 * KK) {
+            const int uv = r >> 1, h = r & 1;
+            const int src = flip ? (KK - 1 - uv) : uv;
+            if (slot == 0) {
+                v = w0f[(size_t)c * KK + src];
+            } else {
+                const int l = 1 + (slot - 1) / 2, band = 2 * ((slot - 1) & 1) + h;
+                v = ldexpf(1.0f, -(l + 1)) * wlf[(((size_t)(l - 1) * C + c) * 4 + band) * KK + src];
+            }
         }
+        img[e] = v;
     }
 }
 
-// Deep stage for level l: subbands of the 32x32 output tile at (ti0, tj0) with an R halo
-// (zero outside the level grid) into the two band-pair tiles. Level 2 reads the 4x4
-// pixel blocks of X (L2-resident), deeper levels the carrier X^(l-1) in shared memory.
-// The trip count is a compile-time constant so that the loads of all cells issue early.
-template <int K, typename T>
-__device__ __forceinline__ void deep_stage(const FwdArgs& a, const T* xp, float* sm, int l,
-                                           int ti0, int tj0) {
-    constexpr int R = FG<K>::R, BT = FG<K>::BT;
-    constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, PHALF = PG<K>::PHALF;
-    constexpr int NIT = (BT * BT + kFT - 1) / kFT;
-    const int Hl = a.H >> l, Wl = a.W >> l, Wp = a.W >> (l - 1);
-    float* bs = sm + a.o_b;
-    const float* carp = (l >= 3) ? sm + a.o_car[l - 1] : nullptr;
-#pragma unroll
-    for (int it = 0; it < NIT; ++it) {
-        const int idx = threadIdx.x + it * kFT;
-        if (idx >= BT * BT) break;
-        const int si = idx / BT, sj = idx - si * BT;
-        const int gi = ti0 - R + si, gj = tj0 - R + sj;
-        float4 u = f4_zero();
-        if (gi >= 0 && gi < Hl && gj >= 0 && gj < Wl) {
-            float ca, cb, cc, cd;
-            carrier_block<T>(l, xp, a.W, carp, Wp, gi, gj, ca, cb, cc, cd);
-            u = haar_u(ca, cb, cc, cd);
-        }
-        float* q = bs + si * PROW + 4 * pchunk(sj >> 1, PHALF) + 2 * (sj & 1);
-        *reinterpret_cast<float2*>(q) = make_float2(u.x, u.y);
-        *reinterpret_cast<float2*>(q + PTILE) = make_float2(u.z, u.w);
-    }
-}
-
-// Low-pass carriers for the deep levels: X^(2) from the 4x4 pixel blocks of X (through
-// the level-1 carrier, Eq. 5's LL twice), then X^(l) from X^(l-1) for l = 3..L-1.
+// Box of the level-2 sweep: 64 columns x BH rows of X, 8 KB in either dtype; NBUF boxes
+// are in flight (they occupy the band-pair and filtered-subband tiles, idle at that time).
 template <typename T>
-__device__ __forceinline__ void deep_carriers(const FwdArgs& a, const T* xp, float* sm) {
-    {
-        const int H2 = a.H >> 2, W2 = a.W >> 2, n = H2 * W2;
-        float* c2 = sm + a.o_car[2];
-        for (int base = threadIdx.x; base < n; base += 4 * kFT) {
+struct SweepBox {
+    static constexpr int BW = 64;
+    static constexpr int BH = sizeof(T) == 2 ? 64 : 32;
+    static constexpr int BYTES = BW * BH * (int)sizeof(T);
+    static constexpr int NBUF = 4;
+    static_assert((BW / 4) * (BH / 4) <= 256, "one level-2 position per thread");
+};
+
+__device__ __forceinline__ int sweep_boxes(int H, int W, int bw, int bh) {
+    return ((W + bw - 1) / bw) * ((H + bh - 1) / bh);
+}
+
+// Level-2 subbands (unnormalized) and carrier of the 4x4 pixel block r0..r3 (Eq. 5 applied
+// to the pixels gives X^(1) = LL; applied again to the 2x2 block of X^(1) it gives level 2).
+__device__ __forceinline__ float4 level2_block(const float4& r0, const float4& r1,
+                                               const float4& r2, const float4& r3) {
+    const float ca = 0.5f * (r0.x + r0.y + r1.x + r1.y);
+    const float cb = 0.5f * (r0.z + r0.w + r1.z + r1.w);
+    const float cc = 0.5f * (r2.x + r2.y + r3.x + r3.y);
+    const float cd = 0.5f * (r2.z + r2.w + r3.z + r3.w);
+    return haar_u(ca, cb, cc, cd);
+}
+
+// Level-2 sweep: the unnormalized subbands of every level-2 position go to u2
+// [H/4][W/4][4] (LL, LH, HL, HH) and, when L >= 3, the carrier X^(2) = LL / 2 to shared
+// memory. TMA path: the first NBUF boxes were issued at the start of the plane; box t + NBUF
+// reuses box t's buffer once every thread is past it. Returns false if a TMA wait timed
+// out (the vote makes the result uniform over the CTA).
+template <typename T>
+__device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, float* sm, float* u2,
+                                             uint64_t* bar_s, uint32_t& ph_s, long long plane) {
+    constexpr int BW = SweepBox<T>::BW, BH = SweepBox<T>::BH, NB = SweepBox<T>::NBUF;
+    constexpr int PR = BH / 4;  // rows of level-2 positions per box
+    const int H2 = a.H >> 2, W2 = a.W >> 2;
+    float* c2 = sm + a.o_car[2];
+    float4* u2v = reinterpret_cast<float4*>(u2);
+    const int tid = threadIdx.x;
+    if (a.use_tma) {
+        T* buf = reinterpret_cast<T*>(sm + a.o_b);
+        const int bxn = (a.W + BW - 1) / BW;
+        const int nbox = sweep_boxes(a.H, a.W, BW, BH);
+        constexpr int PC = BW / 4;  // level-2 positions per box row
+        const int pi = tid / PC, pj = tid % PC;
+        for (int t = 0; t < nbox; ++t) {
+            const int b = t % NB;
+            const bool ok = mbar_wait_bounded(bar_s + b, (ph_s >> b) & 1u);
+            ph_s ^= 1u << b;
+            if (__syncthreads_or(!ok)) return false;
+            if (tid == 0 && t >= 1 && t - 1 + NB < nbox) {
+                // every thread is past box t - 1: refill its buffer with box t - 1 + NB
+                const int nt = t - 1 + NB, nb = (t - 1) % NB;
+                const int ny = nt / bxn, nx = nt - ny * bxn;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar_s + nb, SweepBox<T>::BYTES);
+                tma_load_3d(buf + nb * (BW * BH), &a.tms, nx * BW, ny * BH, (int)plane, bar_s + nb);
+            }
+            const int by = t / bxn, bx = t - by * bxn;
+            const int i2 = by * PR + pi, j2 = bx * PC + pj;
+            if (pi < PR && i2 < H2 && j2 < W2) {
+                const T* q = buf + b * (BW * BH) + (4 * pi) * BW + 4 * pj;
+                const float4 u = level2_block(ld4_smem<T>(q), ld4_smem<T>(q + BW),
+                                              ld4_smem<T>(q + 2 * BW), ld4_smem<T>(q + 3 * BW));
+                __stcg(u2v + (size_t)i2 * W2 + j2, u);
+                if (a.L >= 3) c2[i2 * W2 + j2] = 0.5f * u.x;
+            }
+        }
+    } else {
+        const int n = H2 * W2;
+        for (int base = tid; base < n; base += 4 * kFT) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int p = base + u * kFT;
+            for (int k = 0; k < 4; ++k) {
+                const int p = base + k * kFT;
                 if (p < n) {
                     const int i2 = p / W2, j2 = p - i2 * W2;
-                    float ca, cb, cc, cd;
-                    carrier_block<T>(2, xp, a.W, nullptr, 0, i2, j2, ca, cb, cc, cd);
-                    c2[p] = 0.5f * (ca + cb + cc + cd);
+                    const T* q = xp + (size_t)(4 * i2) * a.W + 4 * j2;
+                    const float4 u = level2_block(IO<T>::ld4(q), IO<T>::ld4(q + a.W),
+                                                  IO<T>::ld4(q + 2 * (size_t)a.W),
+                                                  IO<T>::ld4(q + 3 * (size_t)a.W));
+                    __stcg(u2v + p, u);
+                    if (a.L >= 3) c2[p] = 0.5f * u.x;
                 }
             }
         }
     }
-    __syncthreads();
+    return true;
+}
+
+// Carriers X^(l) = LL of X^(l-1) (normalized, Eq. 5) for l = 3..L-1, in shared memory.
+__device__ __forceinline__ void deep_carriers(const FwdArgs& a, float* sm) {
     for (int l = 3; l < a.L; ++l) {
         const int Hl = a.H >> l, Wl = a.W >> l, Wp = a.W >> (l - 1);
         const float* cp = sm + a.o_car[l - 1];
@@ -142,6 +191,41 @@ __device__ __forceinline__ void deep_carriers(const FwdArgs& a, const T* xp, flo
     }
 }
 
+// Deep stage for level l: subbands of the 32x32 output tile at (ti0, tj0) with an R halo
+// (zero outside the level grid) into the two band-pair tiles. Level 2 reads its subbands
+// from the sweep's output (L2-resident), deeper levels transform the carrier X^(l-1) in
+// shared memory. The trip count is a compile-time constant so that all loads issue early.
+template <int K>
+__device__ __forceinline__ void deep_stage(const FwdArgs& a, const float* u2, float* sm, int l,
+                                           int ti0, int tj0) {
+    constexpr int R = FG<K>::R, BT = FG<K>::BT;
+    constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, PHALF = PG<K>::PHALF;
+    constexpr int NIT = (BT * BT + kFT - 1) / kFT;
+    const int Hl = a.H >> l, Wl = a.W >> l, Wp = a.W >> (l - 1);
+    float* bs = sm + a.o_b;
+    const float* carp = (l >= 3) ? sm + a.o_car[l - 1] : nullptr;
+    const float4* u2v = reinterpret_cast<const float4*>(u2);
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+        const int idx = threadIdx.x + it * kFT;
+        if (idx >= BT * BT) break;
+        const int si = idx / BT, sj = idx - si * BT;
+        const int gi = ti0 - R + si, gj = tj0 - R + sj;
+        float4 u = f4_zero();
+        if (gi >= 0 && gi < Hl && gj >= 0 && gj < Wl) {
+            if (l == 2) {
+                u = __ldcg(u2v + (size_t)gi * Wl + gj);
+            } else {
+                const float* q = carp + (size_t)(2 * gi) * Wp + 2 * gj;
+                u = haar_u(q[0], q[1], q[Wp], q[Wp + 1]);
+            }
+        }
+        float* q = bs + si * PROW + 4 * pchunk(sj >> 1, PHALF) + 2 * (sj & 1);
+        *reinterpret_cast<float2*>(q) = make_float2(u.x, u.y);
+        *reinterpret_cast<float2*>(q + PTILE) = make_float2(u.z, u.w);
+    }
+}
+
 template <int K, typename T>
 __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_constant__ FwdArgs a) {
     constexpr int R = FG<K>::R, PAD = FG<K>::PAD, XP = FG<K>::XPITCH;
@@ -149,15 +233,19 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
     constexpr int ZROW = PG<K>::ZROW, ZTILE = PG<K>::ZTILE;
     extern __shared__ __align__(128) float4 smem_f4[];
     float* sm = reinterpret_cast<float*>(smem_f4);
+    // mbarriers: X tile, deep-sum blocks (2 buffers), weights, level-2 sweep boxes
     uint64_t* bar_x = reinterpret_cast<uint64_t*>(sm + a.o_bar);
     uint64_t* bar_d = bar_x + 1;
+    uint64_t* bar_w = bar_x + 3;
+    uint64_t* bar_s = bar_x + 4;
     T* raw = reinterpret_cast<T*>(sm + a.o_raw);
-    float* dblk = sm + a.o_dblk;
+    float* dblk = sm + a.o_dblk;  // two buffers of kDBytes
     float* wsm = sm + a.o_w;
     float* xs = sm + a.o_x;
     float* bs = sm + a.o_b;
     float* zs = sm + a.o_z;
-    float* zslot = a.zd + (size_t)blockIdx.x * a.zd_slot;
+    float* zslot = a.zd + (size_t)blockIdx.x * a.slot;  // deep sums [H/4][W/4][4]
+    float* u2 = zslot + a.zd_slot;                          // level-2 subbands, same shape
     const size_t plane_elems = (size_t)a.H * a.W;
     const int tid = threadIdx.x;
     const bool leader = tid == 0;
@@ -167,35 +255,51 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
     if (a.use_tma && leader) {
         mbar_init(bar_x, 1);
         mbar_init(bar_d, 1);
+        mbar_init(bar_d + 1, 1);
+        mbar_init(bar_w, 1);
+        for (int b = 0; b < SweepBox<T>::NBUF; ++b) mbar_init(bar_s + b, 1);
         fence_mbar_init();
     }
     __syncthreads();
-    uint32_t ph_x = 0, ph_d = 0;
+    uint32_t ph_x = 0, ph_d = 0, ph_w = 0, ph_s = 0;
     bool failed = false;
+    // weights of the current plane are in shared memory (uniform over the CTA)
+    auto weights_ready = [&]() -> bool {
+        bool ok = true;
+        if (a.use_tma) {
+            ok = mbar_wait_bounded(bar_w, ph_w);
+            ph_w ^= 1;
+        }
+        return !__syncthreads_or(!ok);
+    };
 
     for (long long plane = blockIdx.x; plane < a.planes; plane += gridDim.x) {
         const int c = (int)(plane % a.C);
         const T* xp = reinterpret_cast<const T*>(a.x) + plane * plane_elems;
         T* yp = reinterpret_cast<T*>(a.y) + plane * plane_elems;
         __syncthreads();  // the previous plane is done with shared memory
-        load_weights<K>(a, c, wsm);
         const float bias = (a.b0f != nullptr) ? __ldg(a.b0f + c) : 0.f;
+        const float* wimg = a.wimg + (size_t)c * a.img;
+        if (!a.use_tma)
+            for (int e = tid; e < a.img; e += kFT) wsm[e] = __ldg(wimg + e);
         if (leader) {
-            const long long nxt = plane + gridDim.x;
-            if (a.use_tma && nxt < a.planes) {
-                // next plane of this CTA: bring it into L2 while this one is computed
-                const char* np =
-                    reinterpret_cast<const char*>(a.x) + (size_t)nxt * plane_elems * sizeof(T);
-                const size_t bytes = plane_elems * sizeof(T);
-                for (size_t o = 0; o < bytes; o += (1u << 20)) {
-                    const size_t nb = (bytes - o) < (1u << 20) ? (bytes - o) : (1u << 20);
-                    prefetch_l2_bulk(np + o, (uint32_t)nb);
-                }
-            }
-            if (a.use_tma) {  // first tile of this plane
+            if (a.use_tma) {  // this channel's weights and the first tile of this plane
                 fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar_w, (uint32_t)a.img * 4u);
+                bulk_load(wsm, wimg, (uint32_t)a.img * 4u, bar_w);
                 mbar_arrive_expect_tx(bar_x, XBox<K, T>::BYTES);
                 tma_load_3d(raw, &a.tmx, -XBox<K, T>::XOFF, -2 * R, (int)plane, bar_x);
+            }
+            if (a.use_tma && a.L >= 2) {  // first boxes of the level-2 sweep
+                constexpr int BW = SweepBox<T>::BW, BH = SweepBox<T>::BH;
+                const int bxn = (a.W + BW - 1) / BW, nbox = sweep_boxes(a.H, a.W, BW, BH);
+                T* buf = reinterpret_cast<T*>(sm + a.o_b);
+                for (int t = 0; t < SweepBox<T>::NBUF && t < nbox; ++t) {
+                    const int ny = t / bxn, nx = t - ny * bxn;
+                    mbar_arrive_expect_tx(bar_s + t, SweepBox<T>::BYTES);
+                    tma_load_3d(buf + t * (BW * BH), &a.tms, nx * BW, ny * BH, (int)plane,
+                                bar_s + t);
+                }
             }
         }
         __syncthreads();
@@ -207,12 +311,16 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
         // (i2, j2) holds the sums for level-1 positions (2i2 + a, 2j2 + b) as
         // (a, b) = (0,0), (0,1), (1,0), (1,1).
         if (a.L >= 2) {
-            if (a.L >= 3) deep_carriers<T>(a, xp, sm);
+            if (!level2_sweep<T>(a, xp, sm, u2, bar_s, ph_s, plane) || !weights_ready()) {
+                failed = true;
+                break;
+            }
+            deep_carriers(a, sm);
             for (int l = a.L; l >= 2; --l) {
                 const int Hl = a.H >> l, Wl = a.W >> l;
                 for (int ti0 = 0; ti0 < Hl; ti0 += kCT) {
                     for (int tj0 = 0; tj0 < Wl; tj0 += kCT) {
-                        deep_stage<K, T>(a, xp, sm, l, ti0, tj0);
+                        deep_stage<K>(a, u2, sm, l, ti0, tj0);
                         __syncthreads();
                         {
                             // band pair pp = tid / 128, 2x4 output block (bi, bj)
@@ -278,18 +386,22 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
         }
 
         // ---- full-resolution phase ----
+        if (a.L < 2 && !weights_ready()) {
+            failed = true;
+            break;
+        }
+        if (a.L >= 2 && a.use_tma && leader) {  // deep sums of the first tile
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar_d, kDBytes);
+            tma_load_3d(dblk, &a.tmd, 0, 0, (int)blockIdx.x, bar_d);
+        }
         const int by = tid >> 4, bx = tid & 15;  // 4x4-pixel block of this thread
         for (int t = 0; t < ntiles; ++t) {
             const int ty = t / tiles_x, tx = t - ty * tiles_x;
             const int y0 = ty * kTile, x0 = tx * kTile;
+            float* dcur = dblk + (t & 1) * (kDBytes / 4);
             if (a.L >= 2) {
-                if (a.use_tma) {
-                    if (leader) {
-                        fence_proxy_async_smem();
-                        mbar_arrive_expect_tx(bar_d, kDBytes);
-                        tma_load_3d(dblk, &a.tmd, x0, y0 >> 2, (int)blockIdx.x, bar_d);
-                    }
-                } else {
+                if (!a.use_tma) {
                     // plain copy of the 16x16 level-2 block of deep sums (zero outside)
                     const int H2 = a.H >> 2, W2 = a.W >> 2;
                     const float4* z2 = reinterpret_cast<const float4*>(zslot);
@@ -297,7 +409,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                     const int i = tid >> 4, j = tid & 15;
                     float4 v = f4_zero();
                     if (i0 + i < H2 && j0 + j < W2) v = z2[(size_t)(i0 + i) * W2 + j0 + j];
-                    reinterpret_cast<float4*>(dblk)[tid] = v;
+                    reinterpret_cast<float4*>(dcur)[tid] = v;
                 }
             }
             if (a.use_tma) {
@@ -309,12 +421,18 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                 }
                 convert_raw<K, T>(raw, xs, bs, a.L >= 1);
                 __syncthreads();
-                if (leader && t + 1 < ntiles) {  // prefetch the next tile of this plane
+                if (leader && t + 1 < ntiles) {  // next tile: X and its deep sums
                     const int ny = (t + 1) / tiles_x, nx = (t + 1) - ny * tiles_x;
                     fence_proxy_async_smem();
                     mbar_arrive_expect_tx(bar_x, XBox<K, T>::BYTES);
                     tma_load_3d(raw, &a.tmx, nx * kTile - XBox<K, T>::XOFF, ny * kTile - 2 * R,
                                 (int)plane, bar_x);
+                    if (a.L >= 2) {
+                        const int nb = (t + 1) & 1;
+                        mbar_arrive_expect_tx(bar_d + nb, kDBytes);
+                        tma_load_3d(dblk + nb * (kDBytes / 4), &a.tmd, nx * kTile,
+                                    (ny * kTile) >> 2, (int)blockIdx.x, bar_d + nb);
+                    }
                 }
             } else {
                 stage_tile<K, T>(xp, a.H, a.W, a.vec, xs, y0, x0);
@@ -343,8 +461,9 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                 __syncthreads();
             }
             if (a.L >= 2 && a.use_tma) {
-                const bool ok = mbar_wait_bounded(bar_d, ph_d);
-                ph_d ^= 1;
+                const int b = t & 1;
+                const bool ok = mbar_wait_bounded(bar_d + b, (ph_d >> b) & 1u);
+                ph_d ^= 1u << b;
                 if (__syncthreads_or(!ok)) {
                     failed = true;
                     break;
@@ -359,7 +478,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                 conv_base_4x4<K>(xs + (4 * by + R) * XP + 4 * bx + R + PAD, XP, wsm, acc2);
                 if (a.L >= 1) {
                     float4 d = f4_zero();
-                    if (a.L >= 2) d = reinterpret_cast<const float4*>(dblk)[tid];
+                    if (a.L >= 2) d = reinterpret_cast<const float4*>(dcur)[tid];
                     const float dv[2][2] = {{d.x, d.y}, {d.z, d.w}};
 #pragma unroll
                     for (int i = 0; i < 2; ++i) {
@@ -460,8 +579,11 @@ namespace {
 int round4(int v) { return (v + 3) & ~3; }
 int round32(int v) { return (v + 31) & ~31; }
 
+size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
+
 struct FwdPlan {
     FwdArgs a;
+    size_t img_bytes = 0;
     size_t smem = 0;
     int grid = 0;
     size_t ws_bytes = 0;
@@ -476,23 +598,27 @@ FwdPlan fwd_plan(const wt_desc& d) {
     const int L = d.levels;
     int off = 0;
     a.o_bar = off;
-    off += 32;  // two mbarriers, padded to 128 bytes
+    off += 32;  // eight mbarriers, padded to 128 bytes
     a.o_raw = off;
     off += round32((XBox<K, T>::BYTES + 3) / 4);
-    a.o_dblk = off;
-    off += (L >= 2) ? kDBytes / 4 : 0;
     a.o_w = off;
-    off += PG<K>::WS * (1 + 2 * L);
+    a.img = PG<K>::WS * (1 + 2 * L);
+    off += a.img;
     off = round32(off);
     a.o_b = off;
     off += 2 * PG<K>::PTILE;
     off = round4(off);
     a.o_z = off;
     off += 2 * PG<K>::ZTILE;
-    // the full-resolution X tile and the deep-phase carriers + Z^(l >= 3) share a region
-    const int alias0 = off;
-    a.o_x = off;
-    const int xend = off + FG<K>::XROWS * FG<K>::XPITCH;
+    // the level-2 sweep's boxes reuse the band-pair and filtered-subband tiles
+    const int sweep_end = a.o_b + SweepBox<T>::NBUF * SweepBox<T>::BYTES / 4;
+    if (off < sweep_end) off = round32(sweep_end);
+    // the full-resolution phase's X tile + deep-sum blocks and the deep phase's carriers +
+    // Z^(l >= 3) share a region
+    const int alias0 = round32(off);
+    a.o_x = alias0;
+    a.o_dblk = round32(alias0 + FG<K>::XROWS * FG<K>::XPITCH);
+    const int xend = a.o_dblk + ((L >= 2) ? 2 * kDBytes / 4 : 0);
     int cp = alias0;
     for (int l = 0; l <= kMaxLevels; ++l) a.o_car[l] = a.o_zl[l] = 0;
     for (int l = 2; l < L; ++l) {
@@ -505,8 +631,9 @@ FwdPlan fwd_plan(const wt_desc& d) {
     }
     const int total = xend > cp ? xend : cp;
     p.smem = (size_t)total * sizeof(float);
-    // deep-sum slot: [H/4][W/4][4] fp32
+    // per CTA: deep sums and level-2 subbands, each [H/4][W/4][4] fp32
     a.zd_slot = (L >= 2) ? ((4LL * (d.h >> 2) * (d.w >> 2) + 63) & ~63LL) : 0;
+    a.slot = 2 * a.zd_slot;
     const long long planes = (long long)d.n * d.c;
     int occ = (int)((228 * 1024) / (p.smem + 1024));
     if (occ > 2) occ = 2;
@@ -514,8 +641,9 @@ FwdPlan fwd_plan(const wt_desc& d) {
     long long grid = (long long)kNumSMs * occ;
     if (grid > planes) grid = planes;
     p.grid = (int)grid;
-    p.ws_bytes =
-        kErrWordBytes + ((L >= 2) ? (size_t)grid * (size_t)a.zd_slot * sizeof(float) : 0);
+    p.img_bytes = round256((size_t)d.c * a.img * sizeof(float));
+    p.ws_bytes = kErrWordBytes + p.img_bytes +
+                 ((L >= 2) ? (size_t)grid * (size_t)a.slot * sizeof(float) : 0);
     return p;
 }
 
@@ -529,17 +657,16 @@ wt_status launch_fwd_k(const wt_desc& d, const void* x, const float* w0f, const 
     FwdArgs& a = p.a;
     a.x = x;
     a.y = y;
-    a.w0f = w0f;
     a.b0f = flip ? nullptr : b0f;
-    a.wlf = wlf;
     a.err = reinterpret_cast<int*>(ws);
-    a.zd = reinterpret_cast<float*>(static_cast<char*>(ws) + kErrWordBytes);
+    float* wimg = reinterpret_cast<float*>(static_cast<char*>(ws) + kErrWordBytes);
+    a.wimg = wimg;
+    a.zd = reinterpret_cast<float*>(static_cast<char*>(ws) + kErrWordBytes + p.img_bytes);
     a.planes = (long long)d.n * d.c;
     a.C = d.c;
     a.H = d.h;
     a.W = d.w;
     a.L = d.levels;
-    a.flip = flip;
     a.vec = (d.w % 4 == 0) ? 1 : 0;
     // TMA needs 16-byte row strides; otherwise the tile is staged with plain loads
     const size_t esize = sizeof(T);
@@ -554,12 +681,25 @@ wt_status launch_fwd_k(const wt_desc& d, const void* x, const float* w0f, const 
         if (ok && d.levels >= 2) {
             const unsigned long long w2 = d.w >> 2, h2 = d.h >> 2;
             ok = encode_3d(&a.tmd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.zd, 4 * w2, h2,
-                           (unsigned long long)p.grid, 16 * w2, (unsigned long long)a.zd_slot * 4,
+                           (unsigned long long)p.grid, 16 * w2, (unsigned long long)a.slot * 4,
                            64, 16);
+            if (ok)
+                ok = encode_3d(&a.tms, dt, x, d.w, d.h, (unsigned long long)d.n * d.c,
+                               (unsigned long long)d.w * esize,
+                               (unsigned long long)d.w * d.h * esize, SweepBox<T>::BW,
+                               SweepBox<T>::BH);
         }
         a.use_tma = ok ? 1 : 0;
     }
     if (cudaMemsetAsync(a.err, 0, sizeof(int), stream) != cudaSuccess) return WT_ERR_CUDA;
+    {
+        const long long n = (long long)d.c * a.img;
+        const int blocks = (int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
+        wt_fwd_weight_image_kernel<K><<<blocks, 256, 0, stream>>>(w0f, wlf, d.c, d.levels, flip,
+                                                                  wimg);
+        if (cudaGetLastError() != cudaSuccess) return WT_ERR_CUDA;
+        ++*launches;
+    }
     auto kern = wt_fwd_plane_kernel<K, T>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) !=
         cudaSuccess)

@@ -329,6 +329,21 @@ __device__ __forceinline__ float2 ld2_smem<__nv_bfloat16>(const __nv_bfloat16* p
     return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
+// Four consecutive elements from shared memory, widened (8-byte aligned for bfloat16,
+// 16-byte aligned for fp32).
+template <typename T>
+__device__ __forceinline__ float4 ld4_smem(const T* p);
+template <>
+__device__ __forceinline__ float4 ld4_smem<float>(const float* p) {
+    return *reinterpret_cast<const float4*>(p);
+}
+template <>
+__device__ __forceinline__ float4 ld4_smem<__nv_bfloat16>(const __nv_bfloat16* p) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+
 // Widen the TMA-staged raw tile to the fp32 tile (column c at c + PAD) and, when `bands`,
 // form the level-1 unnormalized subbands with an R halo in the two band-pair tiles.
 // One item = two horizontally adjacent cells (a 2x4 pixel block).

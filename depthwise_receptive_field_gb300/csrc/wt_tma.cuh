@@ -1,4 +1,4 @@
-// Tensor Memory Accelerator (TMA) loads, mbarriers and L2 bulk prefetch for sm_103a, as
+// Tensor Memory Accelerator (TMA) loads, bulk copies and mbarriers for sm_103a, as
 // inline PTX. Every wait on an mbarrier is bounded (about one second of %globaltimer);
 // a caller that sees a timeout records an error code and leaves the kernel.
 #pragma once
@@ -81,9 +81,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
-// Ask L2 to fetch [p, p + bytes) (16-byte aligned, multiple of 16 bytes).
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+// Bulk copy of `bytes` contiguous bytes from global to shared memory, completing on `bar`
+// (both addresses 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
 }
 
 }  // namespace wt

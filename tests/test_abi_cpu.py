@@ -84,15 +84,20 @@ def test_workspace_sizes_for_workloads(lib, name):
     d = B.make_desc(wl.n, wl.c, wl.h, wl.w, wl.k, wl.levels,
                     B.WT_BF16 if wl.dtype == "bf16" else B.WT_F32)
     fwd, bwd_d, bwd_w = B.wtconv_workspace_size(d)
-    # forward / backward-data: one deep-level scratch slot (Z^(l), l >= 2) per resident CTA
-    # (the workspace starts with a 256-byte status word)
+    # forward / backward-data: a 256-byte status word, the per-channel shared-memory images of
+    # the folded weights (base + 2 band pairs per level, each round4(2 k^2) floats), then per
+    # resident CTA one scratch slot holding the deep sums and the level-2 subbands, each
+    # [H/4][W/4][4] fp32
     assert fwd == bwd_d
+    ws_pair = (2 * wl.k * wl.k + 3) // 4 * 4
+    img = (wl.c * ws_pair * (1 + 2 * wl.levels) * 4 + 255) // 256 * 256
     if wl.levels < 2:
-        assert fwd == 256
+        assert fwd == 256 + img
     else:
-        slot = sum(4 * (wl.h >> l) * (wl.w >> l) for l in range(2, wl.levels + 1)) * 4
-        assert fwd >= 256 + slot and fwd % 256 == 0
-        assert fwd <= 256 + 2 * 152 * ((slot + 255) // 256 * 256)  # at most 2 CTAs per SM
+        half = (4 * (wl.h >> 2) * (wl.w >> 2) + 63) // 64 * 64 * 4
+        slot = 2 * half
+        assert fwd >= 256 + img + slot and (fwd - 256 - img) % slot == 0
+        assert fwd <= 256 + img + 2 * 152 * slot  # at most 2 CTAs per SM
     # backward-weight: a 256-byte status word, then one partial vector
     # [dW0 | db | dW^(l)] per (channel, image)
     kk = wl.k * wl.k
