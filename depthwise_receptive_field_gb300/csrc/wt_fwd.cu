@@ -413,14 +413,14 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                 }
             }
             if (a.use_tma) {
+                // a timed-out wait converts stale data; the vote after the pass ends the kernel
                 const bool ok = mbar_wait_bounded(bar_x, ph_x);
                 ph_x ^= 1;
+                convert_raw<K, T>(raw, xs, bs, a.L >= 1);
                 if (__syncthreads_or(!ok)) {
                     failed = true;
                     break;
                 }
-                convert_raw<K, T>(raw, xs, bs, a.L >= 1);
-                __syncthreads();
                 if (leader && t + 1 < ntiles) {  // next tile: X and its deep sums
                     const int ny = (t + 1) / tiles_x, nx = (t + 1) - ny * tiles_x;
                     fence_proxy_async_smem();
@@ -460,15 +460,10 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                 }
                 __syncthreads();
             }
-            if (a.L >= 2 && a.use_tma) {
-                const int b = t & 1;
-                const bool ok = mbar_wait_bounded(bar_d + b, (ph_d >> b) & 1u);
-                ph_d ^= 1u << b;
-                if (__syncthreads_or(!ok)) {
-                    failed = true;
-                    break;
-                }
-            }
+            // the deep sums are waited for just before their use; the wait is voted on at the
+            // end of the tile
+            const int db = t & 1;
+            bool ok_d = true;
             const int gy = y0 + 4 * by, gx = x0 + 4 * bx;
             if (gy < a.H && gx < a.W) {
                 f2x acc2[4][2];
@@ -478,7 +473,10 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                 conv_base_4x4<K>(xs + (4 * by + R) * XP + 4 * bx + R + PAD, XP, wsm, acc2);
                 if (a.L >= 1) {
                     float4 d = f4_zero();
-                    if (a.L >= 2) d = reinterpret_cast<const float4*>(dcur)[tid];
+                    if (a.L >= 2) {
+                        if (a.use_tma) ok_d = mbar_wait_bounded(bar_d + db, (ph_d >> db) & 1u);
+                        d = reinterpret_cast<const float4*>(dcur)[tid];
+                    }
                     const float dv[2][2] = {{d.x, d.y}, {d.z, d.w}};
 #pragma unroll
                     for (int i = 0; i < 2; ++i) {
@@ -524,7 +522,11 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                                 IO<T>::st(yp + (size_t)(gy + o) * a.W + gx + q, acc[o][q]);
                 }
             }
-            __syncthreads();
+            if (a.L >= 2 && a.use_tma) ph_d ^= 1u << db;
+            if (__syncthreads_or(!ok_d)) {
+                failed = true;
+                break;
+            }
         }
         if (failed) break;
     }
