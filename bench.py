@@ -30,6 +30,7 @@ METRIC = "WTConv fwd+bwd Gelem/s and achieved HBM GB/s as % of GB300 peak (1 GPU
 NUM_SMS = 152
 FP32_LANES_PER_SM = 128
 SM_MAX_MHZ = 2070.0
+NOMINAL_HBM_GBS = 7900.0
 HBM_FALLBACK_GBS = 6800.0
 PROFILES = os.path.join(ROOT, "profiles")
 CSRC = os.path.join(ROOT, "depthwise_receptive_field_gb300", "csrc")
@@ -381,6 +382,8 @@ def run_ours(args, wl):
         "hbm": {
             "achieved_gbs": hbm_gbs, "peak_gbs": peaks["hbm_gbs"],
             "frac": hbm_gbs / peaks["hbm_gbs"], "peak_source": peaks["source"],
+            "nominal_gbs": NOMINAL_HBM_GBS, "frac_of_nominal": hbm_gbs / NOMINAL_HBM_GBS,
+            "nominal_source": "nominal HBM3e bandwidth of one GB300 GPU (7.9 TB/s)",
             "algorithmic_bytes_per_step": step_bytes,
         },
         "segments_ms": seg_ms,
@@ -388,6 +391,8 @@ def run_ours(args, wl):
         "gpu_launches": launches["n"],
     }
 
+    if wl.levels > 0 and not args.no_depthwise:
+        result["depthwise_context"] = run_depthwise_context(args, wl, p, x, dy, g, stream, dev)
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, wl, inp, p, f, desc, buf, bufn, stream, world, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -397,6 +402,129 @@ def run_ours(args, wl):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+    return 0
+
+
+def run_depthwise_context(args, wl, p, x, dy, g, stream, dev) -> dict:
+    """The same-shape plain depthwise k x k conv (this layer at L = 0: base conv + bias and
+    scale, no wavelet levels), forward + backward-data + backward-weight through the same
+    C ABI, timed like the main step. Context for what the wavelet levels cost on top."""
+    import torch
+
+    from depthwise_receptive_field_gb300 import binding as B
+    from depthwise_receptive_field_gb300 import iomodel, layer
+
+    desc0 = B.desc_like(x, p.k, 0)
+    _, nbd, nbw = B.wtconv_workspace_size(desc0)
+    ws0 = layer.Workspace(dev)
+    buf0, bufn0 = ws0.get(max(nbd, nbw))
+    w0f = torch.empty_like(p.w0)
+    b0f = torch.empty_like(p.s0)
+    y0 = torch.empty_like(x)
+    steps = max(5, min(args.steps, 50))
+
+    def step():
+        B.wtconv_fold_scales(desc0, p.w0, p.b0, p.s0, None, None, w0f, b0f, None, stream)
+        B.wtconv_forward(desc0, x, w0f, b0f, None, y0, buf0, bufn0, stream)
+        B.wtconv_backward_data(desc0, dy, w0f, None, g["dx"], buf0, bufn0, stream)
+        B.wtconv_backward_weight(desc0, x, dy, p.w0, p.b0, p.s0, None, None, g["dw0"],
+                                 g["db0"], g["ds0"], None, None, buf0, bufn0, stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    alg = iomodel.algorithmic(wl.k, 0, 2 if wl.dtype == "bf16" else 4)
+    flops = wl.elements * sum(a["flops"] for a in alg.values())
+    return {"op": f"plain depthwise {wl.k}x{wl.k} conv, same shape (this library at L=0)",
+            "value": wl.elements / (ms * 1e-3) / 1e9, "unit": "Gelem/s", "ms_per_step": ms,
+            "steps": steps, "alu_tflops": flops / (ms * 1e-3) / 1e12}
+
+
+def run_ablation(args) -> int:
+    """The cumulative ablation of the reformulations (forward pass, fp32): the reference's
+    materializing stage chain, + fused analysis, + collapsed synthesis, + folded scales (the
+    pages' fused plan), and this library's single-pass forward, on the 8 x 128 x 128 x 128,
+    k = 5 shape of the pages' traffic table, for L = 1..5 (or --levels). One JSON line per
+    (L, variant): device time per forward (L2 flushed before every timed call), Gelem/s,
+    speedup over the reference, and the modeled HBM traffic of the variant.
+    With --nvtx, one extra call per (L, variant) runs inside an NVTX push/pop range named
+    "wt_measured" (for a counter capture restricted to those calls; each line's "launches"
+    says how many kernels of the capture belong to it, in the printed order)."""
+    import torch
+
+    from depthwise_receptive_field_gb300 import binding as B
+    from depthwise_receptive_field_gb300 import iomodel, layer
+    from depthwise_receptive_field_gb300.inputs import ABLATION_SHAPE, make_inputs, shape_workload
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    B.load_library()
+    n, c, h, w, k = ABLATION_SHAPE
+    levels = [args.levels] if args.levels is not None else [1, 2, 3, 4, 5]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 256 MB > L2
+    stream = torch.cuda.current_stream(dev)
+    names = dict(B.VARIANT_NAMES)
+    names[-1] = "single_pass"
+    for L in levels:
+        wl = shape_workload(n, c, h, w, k, L, "f32", seed=7, backward=False)
+        inp = make_inputs(wl, bias_and_scale=True)
+        p = layer.Params.from_inputs(inp, dev)
+        x = inp["x"].to(dev)
+        y = torch.empty_like(x)
+        ws = layer.Workspace(dev)
+        desc = B.desc_like(x, k, L)
+
+        def call(v):
+            if v < 0:  # scale fold + the single-pass forward
+                layer.forward(x, p, layer.fold(p, desc), ws, y)
+            else:
+                layer.forward_variant(x, p, v, ws, y)
+
+        times, launches = {}, {}
+        for v in (0, 1, 2, 3, -1):
+            for _ in range(max(3, args.warmup)):
+                call(v)
+            launches[v] = B.wtconv_last_launch_count() + (1 if v < 0 else 0)  # + the fold
+            tot = 0.0
+            for _ in range(args.steps):
+                flush.fill_(1)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                call(v)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                tot += e0.elapsed_time(e1)
+            times[v] = tot / args.steps
+            if args.nvtx:
+                flush.fill_(1)
+                torch.cuda.synchronize()
+                torch.cuda.nvtx.range_push("wt_measured")
+                call(v)
+                torch.cuda.nvtx.range_pop()
+                torch.cuda.synchronize()
+        for v in (0, 1, 2, 3, -1):
+            q = iomodel.q_variant(v, L) if v >= 0 else 2.0
+            ms = times[v]
+            print(json.dumps({
+                "ablation": names[v], "levels": L, "shape": [n, c, h, w], "k": k,
+                "dtype": "f32", "ms": ms, "gelem_s": wl.elements / (ms * 1e-3) / 1e9,
+                "speedup_vs_reference": times[0] / ms,
+                "model_traffic_per_element": q,
+                "model_gbs": q * wl.elements * 4 / (ms * 1e-3) / 1e9,
+                "steps": args.steps, "l2": "flushed (256 MB write) before every timed call",
+                "launches": launches[v],
+            }), flush=True)
     return 0
 
 
@@ -492,7 +620,15 @@ def main(argv=None):
                     help="override the workload's L (e.g. the 128x128 level sweep)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ablation", action="store_true",
+                    help="time the staged ablation pipelines instead of the training step")
+    ap.add_argument("--nvtx", action="store_true",
+                    help="with --ablation: one extra call per variant inside an NVTX range")
+    ap.add_argument("--no-depthwise", action="store_true",
+                    help="skip the same-shape plain depthwise conv context line")
     args = ap.parse_args(argv)
+    if args.ablation:
+        return run_ablation(args)
 
     from depthwise_receptive_field_gb300.inputs import WORKLOADS
     wl = WORKLOADS[args.workload]

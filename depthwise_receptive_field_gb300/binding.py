@@ -1,4 +1,5 @@
-"""ctypes binding of libwtconv's C ABI (include/wtconv.h): argument marshalling only.
+"""ctypes binding of libwtconv's C ABI (include/wtconv.h and include/wtconv_ablation.h):
+argument marshalling only.
 
 Every function here has the name of the C entry point it calls and does no arithmetic of
 its own. Tensor arguments may be torch tensors (their ``data_ptr()`` is passed), raw
@@ -19,8 +20,14 @@ from . import build as _build
 
 WT_OK, WT_ERR_INVALID_ARG, WT_ERR_UNSUPPORTED, WT_ERR_WORKSPACE, WT_ERR_CUDA = range(5)
 WT_F32, WT_BF16 = 0, 1
+(WT_VARIANT_REFERENCE, WT_VARIANT_FUSED_ANALYSIS, WT_VARIANT_COLLAPSED_SYNTHESIS,
+ WT_VARIANT_FOLDED) = range(4)
+VARIANT_NAMES = {WT_VARIANT_REFERENCE: "reference", WT_VARIANT_FUSED_ANALYSIS: "fused_analysis",
+                 WT_VARIANT_COLLAPSED_SYNTHESIS: "collapsed_synthesis",
+                 WT_VARIANT_FOLDED: "folded"}
 
 HEADER = os.path.join(_build.INCLUDE, "wtconv.h")
+HEADERS = [HEADER, os.path.join(_build.INCLUDE, "wtconv_ablation.h")]
 
 
 class wt_desc(ctypes.Structure):
@@ -53,6 +60,8 @@ _SIGNATURES = {
     "wtconv_backward_weight": [_DESC_P] + [_vp] * 13 + [ctypes.c_size_t, _vp],
     "wtconv_backward": [_DESC_P] + [_vp] * 16 + [ctypes.c_size_t, _vp],
     "wtconv_backward_weight_noalloc": [_DESC_P] + [_vp] * 12 + [_vp],
+    "wtconv_variant_workspace_size": [_DESC_P, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)],
+    "wtconv_forward_variant": [_DESC_P, ctypes.c_int] + [_vp] * 8 + [ctypes.c_size_t, _vp],
 }
 
 
@@ -83,10 +92,13 @@ def load_library(rebuild_if_stale: bool = True):
 
 
 def declared_functions() -> list[str]:
-    """Names of the functions include/wtconv.h declares."""
-    text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:wt_status|const char\*|int)\s+(wtconv_\w+)\s*\(",
-                                 text, flags=re.M)))
+    """Names of the functions the public headers (include/*.h) declare."""
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        names.update(re.findall(r"^\s*(?:wt_status|const char\*|int)\s+(wtconv_\w+)\s*\(",
+                                text, flags=re.M))
+    return sorted(names)
 
 
 def _ptr(t):
@@ -177,6 +189,21 @@ def wtconv_backward_weight_noalloc(desc, x, dy, w0, b0, s0, wl, sl, dw0, db0, ds
         ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(w0), _ptr(b0), _ptr(s0), _ptr(wl),
         _ptr(sl), _ptr(dw0), _ptr(db0), _ptr(ds0), _ptr(dwl), _ptr(dsl), _stream(stream)),
         "wtconv_backward_weight_noalloc")
+
+
+def wtconv_variant_workspace_size(desc: wt_desc, variant: int) -> int:
+    """Workspace bytes of wtconv_forward_variant for (desc, variant)."""
+    n = ctypes.c_size_t()
+    _check(load_library().wtconv_variant_workspace_size(ctypes.byref(desc), int(variant),
+                                                        ctypes.byref(n)),
+           "wtconv_variant_workspace_size")
+    return n.value
+
+
+def wtconv_forward_variant(desc, variant, x, w0, b0, s0, wl, sl, y, ws, ws_bytes, stream=None):
+    _check(load_library().wtconv_forward_variant(
+        ctypes.byref(desc), int(variant), _ptr(x), _ptr(w0), _ptr(b0), _ptr(s0), _ptr(wl),
+        _ptr(sl), _ptr(y), _ptr(ws), int(ws_bytes), _stream(stream)), "wtconv_forward_variant")
 
 
 def wtconv_status_string(status: int) -> str:

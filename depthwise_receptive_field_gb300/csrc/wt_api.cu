@@ -39,6 +39,8 @@ wt_status check_param(const void* p) {
 
 }  // namespace
 
+void set_last_launch_count(int launches) { g_last_launches = launches; }
+
 // §4.3 Eq. 8: one thread per folded weight (plus the bias fold).
 __global__ void wt_fold_kernel(int C, int KK, int L, const float* w0, const float* b0,
                                const float* s0, const float* wl, const float* sl, float* w0f,

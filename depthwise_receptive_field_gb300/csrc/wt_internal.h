@@ -45,6 +45,9 @@ bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, unsigne
                unsigned long long d1, unsigned long long d2, unsigned long long s1_bytes,
                unsigned long long s2_bytes, unsigned b0, unsigned b1);
 
+// number of kernel launches of the calling thread's last successful entry-point call
+void set_last_launch_count(int launches);
+
 // scale folding (Eq. 8): one launch
 wt_status launch_fold(const wt_desc& d, const float* w0, const float* b0, const float* s0,
                       const float* wl, const float* sl, float* w0f, float* b0f, float* wlf,

@@ -83,6 +83,11 @@ def make_inputs(wl: Workload, *, bias_and_scale: bool = False, n: int | None = N
     return {"x": x, "dy": dy, "w0": w0, "b0": b0, "s0": s0, "wl": wlv, "sl": sl}
 
 
+# Shape of the pages' measured-traffic table (App. B, Table 11): B = 8, C = 128, H = W = 128,
+# k = 5, fp32; used by the ablation of the reformulations (L = 1..5).
+ABLATION_SHAPE = (8, 128, 128, 128, 5)
+
+
 def shape_workload(n, c, h, w, k, levels, dtype="f32", seed=0, backward=True) -> Workload:
     """An ad-hoc workload for edge-case tests (same recipe, any shape)."""
     return Workload(f"shape_{n}x{c}x{h}x{w}_k{k}_L{levels}_{dtype}", n, c, h, w, k, levels,

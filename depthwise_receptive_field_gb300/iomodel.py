@@ -31,6 +31,35 @@ def q_fused(levels: int) -> float:
     return 4.0 + 13.0 / 3.0 * (1.0 - 4.0 ** (-levels)) - 4.0 ** (-levels)
 
 
+def q_variant(variant: int, levels: int) -> float:
+    """Elements per input element that each staged pipeline of include/wtconv_ablation.h
+    moves through HBM in one forward pass, counted stage by stage as in §3.1 and §4.4
+    (each stage reads its inputs once and writes its outputs once; weights negligible).
+
+    S = sum_l N_l / N, d = N_L / (4N) = 4^-L (the deepest level's low-pass band):
+      0 reference            7 + (6 + 19/4) S - d   (Eq. 2, except that the deepest level's
+                             low-pass add has no coarser level to add: it reads one operand)
+      1 fused analysis       7 + (9/4 + 19/4) S - 2d (per level: read the carrier, write Z and,
+                             except at the deepest level, the raw low-pass carrier)
+      2 collapsed synthesis  8 + (9/4 + 1) S - d    (one synthesis pass reads every Z^(l) and
+                             writes the level sum; base conv, scale and add stay separate)
+      3 folded               4 + 13/4 S - d         (Eq. 10: the pages' fused plan)
+    """
+    if levels == 0:  # base conv, scale, and the final add with nothing to add (2N each)
+        return 2.0 if variant == 3 else 6.0
+    S = level_fraction(levels)
+    d = 4.0 ** (-levels)
+    if variant == 0:
+        return 7.0 + (6.0 + 19.0 / 4.0) * S - d
+    if variant == 1:
+        return 7.0 + 7.0 * S - 2.0 * d
+    if variant == 2:
+        return 8.0 + 13.0 / 4.0 * S - d
+    if variant == 3:
+        return 4.0 + 13.0 / 4.0 * S - d
+    raise ValueError(variant)
+
+
 def mac_ref(k: int, levels: int) -> float:
     """Eq. 3: multiply-accumulates per input element of the reference implementation."""
     return k * k + (k * k + 8) * level_fraction(levels)

@@ -85,6 +85,19 @@ def forward(x: torch.Tensor, p: Params, f: Folded | None = None, ws: Workspace |
     return y
 
 
+def forward_variant(x: torch.Tensor, p: Params, variant: int, ws: Workspace | None = None,
+                    y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The forward computed by one of the staged ablation pipelines (fp32 only): the
+    reference's materializing stages or one of its cumulative reformulations."""
+    desc = B.desc_like(x, p.k, p.levels)
+    y = torch.empty_like(x) if y is None else y
+    nb = B.wtconv_variant_workspace_size(desc, variant)
+    buf, size = (ws or Workspace(x.device)).get(nb)
+    B.wtconv_forward_variant(desc, variant, x, p.w0, p.b0, p.s0, p.wl if p.levels else None,
+                             p.sl if p.levels else None, y, buf, size, stream)
+    return y
+
+
 def backward_data(dy: torch.Tensor, p: Params, f: Folded | None = None,
                   ws: Workspace | None = None, dx: torch.Tensor | None = None,
                   stream=None) -> torch.Tensor:

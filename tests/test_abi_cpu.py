@@ -103,3 +103,47 @@ def test_workspace_sizes_for_workloads(lib, name):
     kk = wl.k * wl.k
     per_partial = (kk + 1 + 4 * kk * wl.levels) * 4
     assert bwd_w == 256 + wl.c * wl.n * per_partial
+
+
+def _header_prototypes():
+    """(name, parameter count) of every function the public headers declare."""
+    import re
+    protos = {}
+    for h in B.HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"(?:wt_status|const char\*|int)\s+(wtconv_\w+)\s*\(([^;]*?)\)\s*;",
+                             text, flags=re.S):
+            args = m.group(2).strip()
+            protos[m.group(1)] = 0 if args in ("", "void") else args.count(",") + 1
+    return protos
+
+
+def test_binding_arity_matches_header():
+    protos = _header_prototypes()
+    assert set(protos) == set(B.declared_functions())
+    for name, argtypes in B._SIGNATURES.items():
+        assert name in protos, name
+        assert len(argtypes) == protos[name], (name, len(argtypes), protos[name])
+
+
+def test_variant_validation(lib):
+    d = B.make_desc(2, 3, 64, 64, 5, 2, B.WT_F32)
+    sizes = [B.wtconv_variant_workspace_size(d, v) for v in range(4)]
+    assert all(s > 0 and s % 256 == 0 for s in sizes)
+    # the reference materializes the most: every stage output of every level
+    assert sizes[B.WT_VARIANT_REFERENCE] == max(sizes)
+    for bad in (-1, 4):
+        with pytest.raises(B.WTConvError) as e:
+            B.wtconv_variant_workspace_size(d, bad)
+        assert e.value.status == B.WT_ERR_INVALID_ARG
+    with pytest.raises(B.WTConvError) as e:
+        B.wtconv_variant_workspace_size(B.make_desc(2, 3, 64, 64, 5, 2, B.WT_BF16), 0)
+    assert e.value.status == B.WT_ERR_UNSUPPORTED
+    with pytest.raises(B.WTConvError) as e:
+        B.wtconv_variant_workspace_size(B.make_desc(2, 3, 60, 64, 5, 3, B.WT_F32), 0)
+    assert e.value.status == B.WT_ERR_INVALID_ARG
+    # null input pointer: rejected before any launch
+    with pytest.raises(B.WTConvError) as e:
+        B.wtconv_forward_variant(d, 0, None, 16, None, 16, 16, 16, 16, 256, sizes[0], stream=0)
+    assert e.value.status == B.WT_ERR_INVALID_ARG

@@ -414,3 +414,18 @@ def test_traffic_model_reproduces_table1():
 def test_mac_model_reproduces_section1():
     for k, L, macs in _golden("mac_counts_sec1.txt"):
         assert iomodel.mac_ref(int(k), int(L)) == pytest.approx(macs, abs=0.05)
+
+
+def test_variant_traffic_models_against_the_pages():
+    """The staged pipelines' traffic counts reduce to the pages' own formulas: the folded
+    variant is Eq. 10 exactly, the reference is Eq. 2 less the one operand the deepest
+    level's low-pass add does not read, and every reformulation lowers the count."""
+    for L in range(1, 8):
+        assert iomodel.q_variant(3, L) == pytest.approx(iomodel.q_fused(L), abs=1e-12)
+        assert iomodel.q_variant(0, L) == pytest.approx(iomodel.q_ref(L) - 4.0 ** (-L),
+                                                        abs=1e-12)
+        qs = [iomodel.q_variant(v, L) for v in range(4)]
+        assert qs == sorted(qs, reverse=True) and len(set(qs)) == 4
+    # Table 1 values at L = 1 (17.75N reference, 7.00N fused)
+    assert iomodel.q_variant(3, 1) == pytest.approx(7.0)
+    assert iomodel.q_variant(0, 1) + 0.25 == pytest.approx(17.75)
