@@ -470,6 +470,8 @@ def run_ablation(args) -> int:
     torch.cuda.set_device(dev)
     B.load_library()
     n, c, h, w, k = ABLATION_SHAPE
+    if args.ablation_n is not None:
+        n = args.ablation_n
     levels = [args.levels] if args.levels is not None else [1, 2, 3, 4, 5]
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 256 MB > L2
     stream = torch.cuda.current_stream(dev)
@@ -622,6 +624,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ablation", action="store_true",
                     help="time the staged ablation pipelines instead of the training step")
+    ap.add_argument("--ablation-n", type=int, default=None,
+                    help="with --ablation: batch size (default 8, the pages' traffic table)")
     ap.add_argument("--nvtx", action="store_true",
                     help="with --ablation: one extra call per variant inside an NVTX range")
     ap.add_argument("--no-depthwise", action="store_true",
