@@ -353,7 +353,7 @@ def run_ours(args, wl):
     elems = wl.elements
     value = world * elems * args.steps / (total_ms * 1e-3) / 1e9
     peaks = measured_peaks()
-    alg = iomodel.algorithmic(wl.k, wl.levels, 2 if wl.dtype == "bf16" else 4)
+    alg = iomodel.algorithmic(wl.k, wl.levels, 4 if wl.dtype == "f32" else 2)
     # dominant kernel: the plane kernel shared by forward and backward-data, or dW
     fwd_kernel_ms = (seg_ms["forward"] + seg_ms["backward_data"]) / 2
     dw_ms = seg_ms["backward_weight"]
@@ -441,7 +441,7 @@ def run_depthwise_context(args, wl, p, x, dy, g, stream, dev) -> dict:
     t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / steps
-    alg = iomodel.algorithmic(wl.k, 0, 2 if wl.dtype == "bf16" else 4)
+    alg = iomodel.algorithmic(wl.k, 0, 4 if wl.dtype == "f32" else 2)
     flops = wl.elements * sum(a["flops"] for a in alg.values())
     return {"op": f"plain depthwise {wl.k}x{wl.k} conv, same shape (this library at L=0)",
             "value": wl.elements / (ms * 1e-3) / 1e9, "unit": "Gelem/s", "ms_per_step": ms,
@@ -620,6 +620,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="c5_large_bf16")
     ap.add_argument("--levels", type=int, default=None,
                     help="override the workload's L (e.g. the 128x128 level sweep)")
+    ap.add_argument("--io", choices=["f32", "bf16", "f16"], default=None,
+                    help="override the workload's I/O dtype (the pages also measure fp16)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ablation", action="store_true",
@@ -638,6 +640,8 @@ def main(argv=None):
     wl = WORKLOADS[args.workload]
     if args.levels is not None:
         wl = wl.with_levels(args.levels)
+    if args.io is not None and args.io != wl.dtype:
+        wl = wl.with_dtype(args.io)
     if not wl.backward:
         raise SystemExit(f"{wl.name} is forward-only; the benchmarked step needs dY")
     if args.impl == "reference":

@@ -19,7 +19,7 @@ import threading
 from . import build as _build
 
 WT_OK, WT_ERR_INVALID_ARG, WT_ERR_UNSUPPORTED, WT_ERR_WORKSPACE, WT_ERR_CUDA = range(5)
-WT_F32, WT_BF16 = 0, 1
+WT_F32, WT_BF16, WT_F16 = 0, 1, 2
 (WT_VARIANT_REFERENCE, WT_VARIANT_FUSED_ANALYSIS, WT_VARIANT_COLLAPSED_SYNTHESIS,
  WT_VARIANT_FOLDED) = range(4)
 VARIANT_NAMES = {WT_VARIANT_REFERENCE: "reference", WT_VARIANT_FUSED_ANALYSIS: "fused_analysis",
@@ -37,7 +37,7 @@ class wt_desc(ctypes.Structure):
 
     def __repr__(self):
         return (f"wt_desc(n={self.n}, c={self.c}, h={self.h}, w={self.w}, k={self.k}, "
-                f"levels={self.levels}, io={'bf16' if self.io == WT_BF16 else 'f32'})")
+                f"levels={self.levels}, io={['f32', 'bf16', 'f16'][self.io]})")
 
 
 class WTConvError(RuntimeError):
@@ -130,7 +130,7 @@ def status_string(status: int) -> str:
 def make_desc(n, c, h, w, k, levels, io) -> wt_desc:
     if not isinstance(io, int):
         import torch
-        io = WT_BF16 if io == torch.bfloat16 else WT_F32
+        io = {torch.bfloat16: WT_BF16, torch.float16: WT_F16}.get(io, WT_F32)
     return wt_desc(int(n), int(c), int(h), int(w), int(k), int(levels), int(io))
 
 

@@ -17,7 +17,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 wt_status check_desc(const wt_desc* d) {
     if (d == nullptr) return WT_ERR_INVALID_ARG;
     if (d->n < 1 || d->c < 1 || d->h < 1 || d->w < 1) return WT_ERR_INVALID_ARG;
-    if (d->io != WT_F32 && d->io != WT_BF16) return WT_ERR_INVALID_ARG;
+    if (d->io != WT_F32 && d->io != WT_BF16 && d->io != WT_F16) return WT_ERR_INVALID_ARG;
     if (d->k < 1 || (d->k % 2) == 0) return WT_ERR_INVALID_ARG;
     if (d->levels < 0 || d->levels > kMaxLevels) return WT_ERR_INVALID_ARG;
     const int m = 1 << d->levels;

@@ -12,6 +12,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -62,6 +63,30 @@ struct IO<__nv_bfloat16> {
     static __device__ __forceinline__ void st4(__nv_bfloat16* p, float4 v) {
         __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
         __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t*>(&lo);
+        u.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(p) = u;
+    }
+};
+
+template <>
+struct IO<__half> {
+    static __device__ __forceinline__ float ld(const __half* p) { return __half2float(*p); }
+    static __device__ __forceinline__ float2 ld2(const __half* p) {
+        const unsigned int u = __ldg(reinterpret_cast<const unsigned int*>(p));
+        return __half22float2(*reinterpret_cast<const __half2*>(&u));
+    }
+    static __device__ __forceinline__ float4 ld4(const __half* p) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    }
+    static __device__ __forceinline__ void st(__half* p, float v) { *p = __float2half_rn(v); }
+    static __device__ __forceinline__ void st4(__half* p, float4 v) {
+        __half2 lo = __floats2half2_rn(v.x, v.y);
+        __half2 hi = __floats2half2_rn(v.z, v.w);
         uint2 u;
         u.x = *reinterpret_cast<uint32_t*>(&lo);
         u.y = *reinterpret_cast<uint32_t*>(&hi);

@@ -672,8 +672,7 @@ wt_status launch_fwd_k(const wt_desc& d, const void* x, const float* w0f, const 
     a.vec = (d.w % 4 == 0) ? 1 : 0;
     // TMA needs 16-byte row strides; otherwise the tile is staged with plain loads
     const size_t esize = sizeof(T);
-    const CUtensorMapDataType dt =
-        sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const CUtensorMapDataType dt = tma_dtype<T>();
     a.use_tma = 0;
     if (((size_t)d.w * esize) % 16 == 0) {
         bool ok = encode_3d(&a.tmx, dt, x, d.w, d.h, (unsigned long long)d.n * d.c,
@@ -714,7 +713,7 @@ wt_status launch_fwd_k(const wt_desc& d, const void* x, const float* w0f, const 
 
 template <int K>
 bool fwd_sizes(const wt_desc& d, size_t* smem, size_t* ws) {
-    FwdPlan p = (d.io == WT_BF16) ? fwd_plan<K, __nv_bfloat16>(d) : fwd_plan<K, float>(d);
+    FwdPlan p = with_io_type(d.io, [&](auto t) { return fwd_plan<K, decltype(t)>(d); });
     *smem = p.smem;
     *ws = p.ws_bytes;
     return true;
@@ -725,14 +724,13 @@ bool fwd_sizes(const wt_desc& d, size_t* smem, size_t* ws) {
 wt_status launch_forward(const wt_desc& d, const void* x, const float* w0f, const float* b0f,
                          const float* wlf, void* y, int flip, void* ws, size_t ws_bytes,
                          cudaStream_t stream, int* launches) {
-    const bool bf = d.io == WT_BF16;
     switch (d.k) {
 #define WT_CASE(KV)                                                                          \
     case KV:                                                                                 \
-        return bf ? launch_fwd_k<KV, __nv_bfloat16>(d, x, w0f, b0f, wlf, y, flip, ws,        \
-                                                    ws_bytes, stream, launches)              \
-                  : launch_fwd_k<KV, float>(d, x, w0f, b0f, wlf, y, flip, ws, ws_bytes,      \
-                                            stream, launches);
+        return with_io_type(d.io, [&](auto t) {                                              \
+            return launch_fwd_k<KV, decltype(t)>(d, x, w0f, b0f, wlf, y, flip, ws, ws_bytes, \
+                                                 stream, launches);                          \
+        });
         WT_CASE(1)
         WT_CASE(3)
         WT_CASE(5)

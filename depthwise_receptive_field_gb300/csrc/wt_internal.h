@@ -4,11 +4,36 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stddef.h>
 
 #include "wtconv.h"
 
 namespace wt {
+
+// TMA element type of an I/O dtype.
+template <typename T>
+inline CUtensorMapDataType tma_dtype();
+template <>
+inline CUtensorMapDataType tma_dtype<float>() { return CU_TENSOR_MAP_DATA_TYPE_FLOAT32; }
+template <>
+inline CUtensorMapDataType tma_dtype<__nv_bfloat16>() { return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; }
+template <>
+inline CUtensorMapDataType tma_dtype<__half>() { return CU_TENSOR_MAP_DATA_TYPE_FLOAT16; }
+
+// Calls f(T{}) with T the element type of the I/O dtype (float, bfloat16 or half).
+template <typename F>
+auto with_io_type(wt_dtype io, F&& f) {
+    switch (io) {
+        case WT_BF16: return f(__nv_bfloat16{});
+        case WT_F16: return f(__half{});
+        default: return f(float{});
+    }
+}
+
+// Bytes per element of an I/O dtype.
+inline size_t io_bytes(wt_dtype io) { return io == WT_F32 ? 4 : 2; }
 
 // sm_103a: 227 KB of shared memory per block (opt-in), 152 SMs.
 constexpr size_t kMaxSmemPerBlock = 227 * 1024;

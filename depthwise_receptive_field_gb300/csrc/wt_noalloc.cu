@@ -109,7 +109,7 @@ extern "C" wt_status wtconv_backward_weight_noalloc(const wt_desc* desc, const v
     float* part = scratch + totals_floats;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-    const size_t esize = desc->io == WT_BF16 ? 2 : 4;
+    const size_t esize = io_bytes(desc->io);
     const size_t image_bytes = (size_t)desc->c * desc->h * desc->w * esize;
     int launches = 0;
     for (int n0 = 0; n0 < desc->n; n0 += (int)nc_max) {

@@ -344,6 +344,18 @@ __device__ __forceinline__ float4 ld4_smem<__nv_bfloat16>(const __nv_bfloat16* p
                        __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
 }
 
+template <>
+__device__ __forceinline__ float2 ld2_smem<__half>(const __half* p) {
+    return __half22float2(*reinterpret_cast<const __half2*>(p));
+}
+template <>
+__device__ __forceinline__ float4 ld4_smem<__half>(const __half* p) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
 // Widen the TMA-staged raw tile to the fp32 tile (column c at c + PAD) and, when `bands`,
 // form the level-1 unnormalized subbands with an R halo in the two band-pair tiles.
 // One item = two horizontally adjacent cells (a 2x4 pixel block).

@@ -470,8 +470,7 @@ bool dw_prepare(const wt_desc& d, const void* x, const void* dy, float* part, in
     a.use_tma = 0;
     const size_t esize = sizeof(T);
     if (((size_t)d.w * esize) % 16 == 0) {
-        const CUtensorMapDataType dt =
-            sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+        const CUtensorMapDataType dt = tma_dtype<T>();
         const unsigned long long planes = (unsigned long long)d.n * d.c;
         const unsigned long long s1 = (unsigned long long)d.w * esize;
         const unsigned long long s2 = (unsigned long long)d.w * d.h * esize;
@@ -532,12 +531,12 @@ wt_status launch_dw_partials_k(const wt_desc& d, const void* x, const void* dy, 
 
 wt_status launch_dw_partials(const wt_desc& d, const void* x, const void* dy, float* part,
                              cudaStream_t stream, int* launches) {
-    const bool bf = d.io == WT_BF16;
     switch (d.k) {
 #define WT_CASE(KV)                                                                           \
     case KV:                                                                                  \
-        return bf ? launch_dw_partials_k<KV, __nv_bfloat16>(d, x, dy, part, stream, launches) \
-                  : launch_dw_partials_k<KV, float>(d, x, dy, part, stream, launches);
+        return with_io_type(d.io, [&](auto t) {                                               \
+            return launch_dw_partials_k<KV, decltype(t)>(d, x, dy, part, stream, launches);   \
+        });
         WT_CASE(1)
         WT_CASE(3)
         WT_CASE(5)
@@ -572,12 +571,16 @@ size_t backward_weight_ws_bytes(const wt_desc& d) {
 size_t backward_weight_smem_bytes(const wt_desc& d) {
     DwArgs a;
     size_t smem = 0;
-    const bool bf = d.io == WT_BF16;
     switch (d.k) {
-        case 1: bf ? dw_layout<1, __nv_bfloat16>(d, a, smem) : dw_layout<1, float>(d, a, smem); break;
-        case 3: bf ? dw_layout<3, __nv_bfloat16>(d, a, smem) : dw_layout<3, float>(d, a, smem); break;
-        case 5: bf ? dw_layout<5, __nv_bfloat16>(d, a, smem) : dw_layout<5, float>(d, a, smem); break;
-        case 7: bf ? dw_layout<7, __nv_bfloat16>(d, a, smem) : dw_layout<7, float>(d, a, smem); break;
+#define WT_CASE(KV)                                                                          \
+    case KV:                                                                                 \
+        with_io_type(d.io, [&](auto t) { dw_layout<KV, decltype(t)>(d, a, smem); return 0; }); \
+        break;
+        WT_CASE(1)
+        WT_CASE(3)
+        WT_CASE(5)
+        WT_CASE(7)
+#undef WT_CASE
         default: return 0;
     }
     return smem;
@@ -588,15 +591,13 @@ wt_status launch_backward_weight(const wt_desc& d, const void* x, const void* dy
                                  const float* wl, const float* sl, float* dw0, float* db0,
                                  float* ds0, float* dwl, float* dsl, void* ws, size_t ws_bytes,
                                  cudaStream_t stream, int* launches) {
-    const bool bf = d.io == WT_BF16;
     switch (d.k) {
 #define WT_CASE(KV)                                                                          \
     case KV:                                                                                 \
-        return bf ? launch_dw_k<KV, __nv_bfloat16>(d, x, dy, w0, b0, s0, wl, sl, dw0, db0,   \
-                                                   ds0, dwl, dsl, ws, ws_bytes, stream,      \
-                                                   launches)                                 \
-                  : launch_dw_k<KV, float>(d, x, dy, w0, b0, s0, wl, sl, dw0, db0, ds0, dwl, \
-                                           dsl, ws, ws_bytes, stream, launches);
+        return with_io_type(d.io, [&](auto t) {                                              \
+            return launch_dw_k<KV, decltype(t)>(d, x, dy, w0, b0, s0, wl, sl, dw0, db0, ds0, \
+                                                dwl, dsl, ws, ws_bytes, stream, launches);   \
+        });
         WT_CASE(1)
         WT_CASE(3)
         WT_CASE(5)

@@ -13,8 +13,8 @@ Recipe (the paper's layer sweep uses synthetic tensors only):
     s^(1..L) ~ U(0.05, 0.2) [L, C, 4]
     base scale s^(0) = 1, bias b = 0, unless ``bias_and_scale`` asks for
     s^(0) ~ U(0.5, 1.5) and b ~ N(0, 0.04), drawn after everything above.
-  X and dY are drawn in float32 and rounded to bfloat16 (round to nearest even) when
-  the workload's I/O dtype is bf16; parameters stay float32.
+  X and dY are drawn in float32 and rounded to bfloat16 or float16 (round to nearest
+  even) when the workload's I/O dtype is bf16 or f16; parameters stay float32.
 """
 from __future__ import annotations
 
@@ -32,7 +32,7 @@ class Workload:
     w: int
     k: int
     levels: int
-    dtype: str  # "f32" or "bf16": the I/O dtype; accumulation is always fp32
+    dtype: str  # "f32", "bf16" or "f16": the I/O dtype; accumulation is always fp32
     seed: int
     backward: bool
 
@@ -42,7 +42,10 @@ class Workload:
 
     @property
     def torch_dtype(self):
-        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+        return {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[self.dtype]
+
+    def with_dtype(self, dtype: str) -> "Workload":
+        return replace(self, dtype=dtype, name=f"{self.name}-{dtype}")
 
     def with_levels(self, levels: int) -> "Workload":
         return replace(self, levels=levels, name=f"{self.name.split('-L')[0]}-L{levels}")
@@ -77,9 +80,9 @@ def make_inputs(wl: Workload, *, bias_and_scale: bool = False, n: int | None = N
     else:
         s0 = torch.ones((wl.c,), dtype=torch.float32)
         b0 = torch.zeros((wl.c,), dtype=torch.float32)
-    if wl.dtype == "bf16":
-        x = x.to(torch.bfloat16)
-        dy = dy.to(torch.bfloat16) if dy is not None else None
+    if wl.dtype in ("bf16", "f16"):
+        x = x.to(wl.torch_dtype)
+        dy = dy.to(wl.torch_dtype) if dy is not None else None
     return {"x": x, "dy": dy, "w0": w0, "b0": b0, "s0": s0, "wl": wlv, "sl": sl}
 
 

@@ -54,7 +54,7 @@ typedef enum {
     WT_ERR_CUDA = 4         /* a CUDA launch or runtime call failed */
 } wt_status;
 
-typedef enum { WT_F32 = 0, WT_BF16 = 1 } wt_dtype;
+typedef enum { WT_F32 = 0, WT_BF16 = 1, WT_F16 = 2 } wt_dtype;
 
 typedef struct {
     int n, c, h, w; /* input shape [N][C][H][W] */

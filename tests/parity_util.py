@@ -10,10 +10,11 @@ from depthwise_receptive_field_gb300 import layer
 from depthwise_receptive_field_gb300.inputs import Workload, make_inputs
 
 # Norm-wise max relative error gates (|gpu - oracle|_max / |oracle|_max): 1e-5 for fp32
-# I/O; 2e-2 for bf16 I/O with fp32 accumulation (outputs are rounded to bf16, 2^-9 rel).
-TOL = {"f32": 1e-5, "bf16": 2e-2}
+# I/O; 2e-2 for bf16 I/O with fp32 accumulation (outputs are rounded to bf16, 2^-9 rel);
+# 2e-3 for fp16 I/O (outputs rounded to fp16, 2^-11 rel, with a 4x margin).
+TOL = {"f32": 1e-5, "bf16": 2e-2, "f16": 2e-3}
 # Parameter gradients are always fp32 sums of products of the (exact) inputs.
-TOL_PARAM = {"f32": 1e-5, "bf16": 1e-4}
+TOL_PARAM = {"f32": 1e-5, "bf16": 1e-4, "f16": 1e-4}
 
 
 def rel_err(got, ref) -> float:

@@ -73,10 +73,25 @@ EDGE = [  # n, c, h, w, k, L, dtype
 ]
 
 
-@pytest.mark.parametrize("n,c,h,w,k,L,dtype", EDGE)
+F16 = [  # fp16 I/O (the pages' half-precision measurements): TMA path and plain path
+    (2, 4, 64, 64, 5, 2, "f16"),      # TMA (W * 2 bytes a multiple of 16)
+    (2, 3, 40, 36, 5, 2, "f16"),      # W * 2 not a multiple of 16: plain staging
+    (1, 2, 128, 96, 7, 4, "f16"),     # k = 7, deep levels
+    (2, 2, 56, 56, 3, 3, "f16"),      # stage-1 plane, k = 3
+]
+
+
+@pytest.mark.parametrize("n,c,h,w,k,L,dtype", EDGE + F16)
 def test_edge_shapes(n, c, h, w, k, L, dtype):
     wl = shape_workload(n, c, h, w, k, L, dtype, seed=1000 + h + w + k + L)
     errs, _ = run_and_compare(wl, bias_and_scale=True)
+    assert_within(errs, wl.dtype, wl.name)
+
+
+def test_c3_stage1_f16_sampled():
+    """The stage-1 shape with fp16 I/O, four channels checked (all batch entries)."""
+    wl = WORKLOADS["c3_stage1_bf16"].with_dtype("f16")
+    errs, _ = run_and_compare(wl, sample_channels=[0, 31, 64, 95])
     assert_within(errs, wl.dtype, wl.name)
 
 
