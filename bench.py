@@ -530,6 +530,73 @@ def run_ablation(args) -> int:
     return 0
 
 
+def run_memory(args, wl) -> int:
+    """Peak device memory of one training step (fold + forward + backward-data +
+    backward-weight through the C ABI), from a clean allocator state: the input X, the
+    incoming gradient dY, parameters, outputs, gradients and workspace. Reported for the
+    wavelet layer, for the same-shape plain depthwise conv (L = 0), and, for fp32 I/O, for
+    the forward of the reference's materializing stage chain (its intermediates are what a
+    framework keeps for the backward pass, so this is a lower bound on its training peak).
+    Units: bytes and multiples of the input tensor's size (the analogue of the pages'
+    Tables 4, 5 and 9)."""
+    import torch
+
+    from depthwise_receptive_field_gb300 import binding as B
+    from depthwise_receptive_field_gb300 import layer
+    from depthwise_receptive_field_gb300.inputs import make_inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    B.load_library()
+    inp = make_inputs(wl)
+    x_bytes = wl.elements * (4 if wl.dtype == "f32" else 2)
+
+    def measure(levels: int, staged_reference: bool = False) -> int:
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        torch.cuda.reset_peak_memory_stats(dev)
+        base = torch.cuda.memory_allocated(dev)
+        p = layer.Params.from_inputs(inp, dev)
+        if levels == 0:
+            p = layer.Params(p.w0, p.b0, p.s0, p.wl[:0], p.sl[:0])
+        x = inp["x"].to(dev)
+        if staged_reference:
+            y = layer.forward_variant(x, p, B.WT_VARIANT_REFERENCE)
+        else:
+            dy = inp["dy"].to(dev)
+            ws = layer.Workspace(dev)
+            f = layer.fold(p, B.desc_like(x, p.k, levels))
+            y = layer.forward(x, p, f, ws)
+            g = layer.backward(x, dy, p, f, ws)
+            del g, dy, ws, f
+        torch.cuda.synchronize()
+        peak = torch.cuda.max_memory_allocated(dev) - base
+        del y, x, p
+        return peak
+
+    out = {"memory": True, "workload": workload_config(wl)["workload"],
+           "input_bytes": x_bytes}
+    peak = measure(wl.levels)
+    dw = measure(0)
+    out["wtconv_step_peak_bytes"] = peak
+    out["wtconv_step_peak_x_input"] = peak / x_bytes
+    out["depthwise_step_peak_bytes"] = dw
+    out["depthwise_step_peak_x_input"] = dw / x_bytes
+    out["wtconv_over_depthwise"] = peak / dw
+    if wl.dtype == "f32" and wl.levels > 0:
+        ref = measure(wl.levels, staged_reference=True)
+        out["reference_forward_peak_bytes"] = ref
+        out["reference_forward_peak_x_input"] = ref / x_bytes
+        out["wtconv_step_over_reference_forward"] = peak / ref
+    else:
+        out["reference_forward_peak_bytes"] = None
+        out["reference_note"] = "the staged reference pipeline is fp32-only"
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def run_e2e(args, wl, inp, p, f, desc, buf, bufn, stream, world, dev) -> dict:
     """Same step through the public API, with every step's inputs copied from pinned host
     memory and its results (Y, dX and all parameter gradients) copied back, inside the
@@ -626,6 +693,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ablation", action="store_true",
                     help="time the staged ablation pipelines instead of the training step")
+    ap.add_argument("--memory", action="store_true",
+                    help="report the peak device memory of one training step instead")
     ap.add_argument("--ablation-n", type=int, default=None,
                     help="with --ablation: batch size (default 8, the pages' traffic table)")
     ap.add_argument("--nvtx", action="store_true",
@@ -644,6 +713,8 @@ def main(argv=None):
         wl = wl.with_dtype(args.io)
     if not wl.backward:
         raise SystemExit(f"{wl.name} is forward-only; the benchmarked step needs dY")
+    if args.memory:
+        return run_memory(args, wl)
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)

@@ -8,14 +8,17 @@
 // and the base-path gradients are dW~^(0)[u][v] = sum dY[y][x] X[y+u-R][x+v-R],
 // db~ = sum dY. Only X and dY are read from HBM; both Haar cascades are recomputed on chip.
 //
-// Kernel 1 (wt_dw_plane_kernel): one CTA per (c, n) plane.
+// Kernel 1 (wt_dw_plane_kernel): one CTA (256 threads) per (c, n) plane.
 //   deep levels (l >= 2): 32x32 tiles of the level's subbands of X (R halo) and dY are
-//     staged from on-chip carriers (level 2 from the 4x4 pixel blocks of X and dY); warp w
-//     correlates band w and reduces its 25 sums with warp shuffles after each level.
-//   full resolution: 64x64-pixel tiles; warps 0-1 run the base correlation (8x4 pixel
-//     blocks, dY read straight into registers), warps 2-3 the level-1 subband correlations
-//     (16 lanes per band, 4x4 coefficient blocks). Each thread keeps its 25 partial sums
-//     in registers for the whole plane.
+//     staged as band-pair tiles, (LL, LH) and (HL, HH), from on-chip carriers (level 2
+//     from the 4x4 pixel blocks of X and dY); threads 0-127 correlate pair 0 and threads
+//     128-255 pair 1 with packed f32x2 FMAs (2x4 coefficient blocks), and the sums are
+//     flushed after each level by recursive-halving warp reductions in a fixed order.
+//   full resolution: 64x64-pixel tiles of X (2R halo) and dY arrive by TMA; the next
+//     tile's load is issued as soon as the current one has been widened to fp32, so it
+//     overlaps the correlations. Threads 0-127 run the base correlation (4x4 pixel
+//     blocks), threads 128-255 the level-1 band-pair correlations (4x4 coefficient
+//     blocks). Each thread keeps its partial sums in registers for the whole plane.
 //   The per-plane partial vector [dW~0 | db~ | dW~^(l)_b] goes to the workspace.
 // Kernel 2 (wt_dw_reduce_kernel): per channel, sums the N partial vectors in a fixed
 //   order and applies the gradient unfolding of §4.3 Eq. 9.
