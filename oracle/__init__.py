@@ -145,10 +145,11 @@ def backward(x, dy, w0, b0, s0, wl, sl, levels: int) -> dict:
 
 
 def haar_analysis(img) -> np.ndarray:
-    """Eq. 5 on every 2x2 block of one plane [h, w] -> [4, h/2, w/2] (LL, LH, HL, HH)."""
+    """Eq. 5 on every 2x2 block of one plane [h, w] -> [4, ceil(h/2), ceil(w/2)]
+    (LL, LH, HL, HH); pixels past an odd edge are zero."""
     img = _f64(img)
     h, w = img.shape
-    out = np.empty((4, h // 2, w // 2))
+    out = np.empty((4, (h + 1) // 2, (w + 1) // 2))
     _lib().wo_haar_analysis(h, w, _ptr(img), _ptr(out))
     return out
 

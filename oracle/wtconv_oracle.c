@@ -25,7 +25,11 @@
  *   - depthwise convolution is cross-correlation with zero padding R = (k-1)/2 so that
  *     the resolution is preserved (WTConv-IO §2.1), odd k only;
  *   - the bias sits inside the base scale: s0 * (X *dw W0 + b) (Algorithm 1, return line);
- *   - the level scale multiplies after the convolution (Algorithm 1, "filter, then scale").
+ *   - the level scale multiplies after the convolution (Algorithm 1, "filter, then scale");
+ *   - a carrier with an odd number of rows (columns) is padded with one zero row (column)
+ *     at the bottom (right) before its analysis, so level l has ceil(h_{l-1} / 2) rows,
+ *     and each synthesis output is cropped back to the carrier's size (the pages are
+ *     silent on odd sizes; this is the plainest completion of Eq. 5 / Eq. 12).
  *
  * Parity pins: none of these functions is trusted on its own; the pytest suite under
  * tests/ pins them against Prop. 1, Eq. 5, Eq. 13, library convolutions with autograd,
@@ -48,7 +52,6 @@ static int wo_check(const wo_desc* d) {
     if (d->n < 0 || d->c <= 0 || d->h <= 0 || d->w <= 0) return 1;
     if (d->k < 1 || d->k > 31 || (d->k % 2) == 0) return 1;
     if (d->levels < 0 || d->levels > 30) return 1;
-    if ((d->h % (1 << d->levels)) != 0 || (d->w % (1 << d->levels)) != 0) return 1;
     return 0;
 }
 
@@ -56,22 +59,27 @@ static int wo_check(const wo_desc* d) {
  * Building blocks
  * ------------------------------------------------------------------------------- */
 
+/* Pixel (r, c) of an h x w plane, zero outside it (the padding of odd carriers). */
+static double px(const double* in, int h, int w, int r, int c) {
+    return (r < h && c < w) ? in[(size_t)r * w + c] : 0.0;
+}
+
 /*
  * One level of orthonormal 2-D Haar analysis (WTConv-IO §4.1, Eq. 5), applied to every
  * non-overlapping 2x2 block [a b; c d] of a plane of size h x w:
  *   LL = (a+b+c+d)/2, LH = (a+b-c-d)/2, HL = (a-b+c-d)/2, HH = (a-b-c+d)/2.
- * a is (2i, 2j), b is (2i, 2j+1), c is (2i+1, 2j), d is (2i+1, 2j+1).
- * out is [4][h/2][w/2] in band order (LL, LH, HL, HH).
+ * a is (2i, 2j), b is (2i, 2j+1), c is (2i+1, 2j), d is (2i+1, 2j+1); pixels past an odd
+ * edge are zero. out is [4][ceil(h/2)][ceil(w/2)] in band order (LL, LH, HL, HH).
  */
 void wo_haar_analysis(int h, int w, const double* in, double* out) {
-    const int h2 = h / 2, w2 = w / 2;
+    const int h2 = (h + 1) / 2, w2 = (w + 1) / 2;
     const size_t band = (size_t)h2 * w2;
     for (int i = 0; i < h2; ++i) {
         for (int j = 0; j < w2; ++j) {
-            const double a = in[(size_t)(2 * i) * w + 2 * j];
-            const double b = in[(size_t)(2 * i) * w + 2 * j + 1];
-            const double c = in[(size_t)(2 * i + 1) * w + 2 * j];
-            const double dd = in[(size_t)(2 * i + 1) * w + 2 * j + 1];
+            const double a = px(in, h, w, 2 * i, 2 * j);
+            const double b = px(in, h, w, 2 * i, 2 * j + 1);
+            const double c = px(in, h, w, 2 * i + 1, 2 * j);
+            const double dd = px(in, h, w, 2 * i + 1, 2 * j + 1);
             const size_t o = (size_t)i * w2 + j;
             out[0 * band + o] = 0.5 * (a + b + c + dd);
             out[1 * band + o] = 0.5 * (a + b - c - dd);
@@ -84,12 +92,12 @@ void wo_haar_analysis(int h, int w, const double* in, double* out) {
 /*
  * One level of Haar synthesis (WTConv-IO App. A, Eq. 12): the value at within-block
  * position (ry, rx) of block (i, j) is
- *   (LL + (-1)^ry LH + (-1)^rx HL + (-1)^(ry+rx) HH) / 2.
- * in is [4][h2][w2]; out is [2*h2][2*w2].
+ *   (LL + (-1)^ry LH + (-1)^rx HL + (-1)^(ry+rx) HH) / 2,
+ * cropped to an ho x wo plane (ho in {2 h2 - 1, 2 h2}): in is [4][h2][w2], out [ho][wo].
  */
-void wo_haar_synthesis(int h2, int w2, const double* in, double* out) {
+static void haar_synthesis_crop(int h2, int w2, int ho, int wo, const double* in,
+                                double* out) {
     const size_t band = (size_t)h2 * w2;
-    const int w = 2 * w2;
     for (int i = 0; i < h2; ++i) {
         for (int j = 0; j < w2; ++j) {
             const size_t o = (size_t)i * w2 + j;
@@ -97,14 +105,20 @@ void wo_haar_synthesis(int h2, int w2, const double* in, double* out) {
             const double hl = in[2 * band + o], hh = in[3 * band + o];
             for (int ry = 0; ry < 2; ++ry) {
                 for (int rx = 0; rx < 2; ++rx) {
+                    if (2 * i + ry >= ho || 2 * j + rx >= wo) continue;
                     const double sy = ry ? -1.0 : 1.0;
                     const double sx = rx ? -1.0 : 1.0;
-                    out[(size_t)(2 * i + ry) * w + 2 * j + rx] =
+                    out[(size_t)(2 * i + ry) * wo + 2 * j + rx] =
                         0.5 * (ll + sy * lh + sx * hl + sy * sx * hh);
                 }
             }
         }
     }
+}
+
+/* Eq. 12 without cropping: in is [4][h2][w2]; out is [2*h2][2*w2]. */
+void wo_haar_synthesis(int h2, int w2, const double* in, double* out) {
+    haar_synthesis_crop(h2, w2, 2 * h2, 2 * w2, in, out);
 }
 
 /*
@@ -172,19 +186,20 @@ static void dwconv_adjoint_weight(int h, int w, int k, const double* g, const do
     }
 }
 
-/* Adjoint of one synthesis level (transpose of Eq. 12, entry by entry). */
-static void synthesis_adjoint(int h2, int w2, const double* g, double* gin) {
+/* Adjoint of one cropped synthesis level (transpose of Eq. 12 and of the crop, entry by
+ * entry): g is [ho][wo], gin [4][h2][w2]. */
+static void synthesis_adjoint(int h2, int w2, int ho, int wo, const double* g, double* gin) {
     const size_t band = (size_t)h2 * w2;
-    const int w = 2 * w2;
     for (int i = 0; i < h2; ++i) {
         for (int j = 0; j < w2; ++j) {
             const size_t o = (size_t)i * w2 + j;
             double acc[4] = {0.0, 0.0, 0.0, 0.0};
             for (int ry = 0; ry < 2; ++ry) {
                 for (int rx = 0; rx < 2; ++rx) {
+                    if (2 * i + ry >= ho || 2 * j + rx >= wo) continue;
                     const double sy = ry ? -1.0 : 1.0;
                     const double sx = rx ? -1.0 : 1.0;
-                    const double gv = g[(size_t)(2 * i + ry) * w + 2 * j + rx];
+                    const double gv = g[(size_t)(2 * i + ry) * wo + 2 * j + rx];
                     acc[0] += 0.5 * gv;
                     acc[1] += 0.5 * sy * gv;
                     acc[2] += 0.5 * sx * gv;
@@ -196,20 +211,23 @@ static void synthesis_adjoint(int h2, int w2, const double* g, double* gin) {
     }
 }
 
-/* Adjoint of one analysis level (transpose of Eq. 5, entry by entry); accumulates. */
+/* Adjoint of one padded analysis level (transpose of Eq. 5 and of the zero padding,
+ * entry by entry): g is [4][ceil(h/2)][ceil(w/2)], gin [h][w]; accumulates. */
 static void analysis_adjoint(int h, int w, const double* g, double* gin) {
-    const int h2 = h / 2, w2 = w / 2;
+    const int h2 = (h + 1) / 2, w2 = (w + 1) / 2;
     const size_t band = (size_t)h2 * w2;
     for (int i = 0; i < h2; ++i) {
         for (int j = 0; j < w2; ++j) {
             const size_t o = (size_t)i * w2 + j;
             const double ll = g[0 * band + o], lh = g[1 * band + o];
             const double hl = g[2 * band + o], hh = g[3 * band + o];
-            /* column of Eq. 5 for a, b, c, d respectively */
-            gin[(size_t)(2 * i) * w + 2 * j] += 0.5 * (ll + lh + hl + hh);
-            gin[(size_t)(2 * i) * w + 2 * j + 1] += 0.5 * (ll + lh - hl - hh);
-            gin[(size_t)(2 * i + 1) * w + 2 * j] += 0.5 * (ll - lh + hl - hh);
-            gin[(size_t)(2 * i + 1) * w + 2 * j + 1] += 0.5 * (ll - lh - hl + hh);
+            /* column of Eq. 5 for a, b, c, d respectively; padded pixels have no gradient */
+            const double col[4] = {0.5 * (ll + lh + hl + hh), 0.5 * (ll + lh - hl - hh),
+                                   0.5 * (ll - lh + hl - hh), 0.5 * (ll - lh - hl + hh)};
+            for (int q = 0; q < 4; ++q) {
+                const int r = 2 * i + (q >> 1), c = 2 * j + (q & 1);
+                if (r < h && c < w) gin[(size_t)r * w + c] += col[q];
+            }
         }
     }
 }
@@ -220,7 +238,7 @@ static void analysis_adjoint(int h, int w, const double* g, double* gin) {
 
 typedef struct {
     int L, k;
-    int* hl;     /* hl[l] = h >> l, l = 0..L */
+    int* hl;     /* hl[0] = h, hl[l] = ceil(hl[l-1] / 2), l = 1..L */
     int* wl;
     double** X;  /* X[l]: carrier at level l, [hl][wl], X[0] = input */
     double** Y;  /* Y[l]: analysis coefficients of X[l-1], [4][hl][wl], l = 1..L */
@@ -255,8 +273,8 @@ static int tape_alloc(plane_tape* t, int h, int w, int k, int L) {
     t->base_conv = (double*)calloc((size_t)h * w, sizeof(double));
     if (!t->hl || !t->wl || !t->X || !t->Y || !t->Cv || !t->Z || !t->base_conv) return 2;
     for (int l = 0; l <= L; ++l) {
-        t->hl[l] = h >> l;
-        t->wl[l] = w >> l;
+        t->hl[l] = (l == 0) ? h : (t->hl[l - 1] + 1) / 2;
+        t->wl[l] = (l == 0) ? w : (t->wl[l - 1] + 1) / 2;
         if (l == 0) continue;
         const size_t sz = (size_t)t->hl[l] * t->wl[l];
         t->X[l] = (double*)calloc(sz, sizeof(double));
@@ -296,7 +314,7 @@ static void plane_down(const wo_desc* d, int ch, const double* xin, const double
 
 /*
  * Upward loop of Algorithm 1 (cascade):
- *   R^(L+1) = 0;  R^(l) = A^T( ([Z^(l)]_LL + R^(l+1)) || [Z^(l)]_H );
+ *   R^(L+1) = 0;  R^(l) = A^T( ([Z^(l)]_LL + R^(l+1)) || [Z^(l)]_H ), cropped to X^(l-1)'s size;
  * then out = s0 * base_conv + R^(1).
  */
 static int plane_up_cascade(const wo_desc* d, int ch, const double* s0, const plane_tape* t,
@@ -312,7 +330,7 @@ static int plane_up_cascade(const wo_desc* d, int ch, const double* s0, const pl
         if (!U || !Rn) { free(U); free(Rn); free(R); return 2; }
         memcpy(U, t->Z[l], 4 * band * sizeof(double));
         if (R) for (size_t e = 0; e < band; ++e) U[e] += R[e];
-        wo_haar_synthesis(hh, ww, U, Rn);
+        haar_synthesis_crop(hh, ww, t->hl[l - 1], t->wl[l - 1], U, Rn);
         free(U);
         free(R);
         R = Rn;
@@ -435,7 +453,8 @@ int wo_backward(const wo_desc* d, const double* x, const double* dy, const doubl
             for (int l = 1; l <= L; ++l) {
                 const size_t band = (size_t)t.hl[l] * t.wl[l];
                 gZ[l] = (double*)malloc(4 * band * sizeof(double));
-                synthesis_adjoint(t.hl[l], t.wl[l], gR, gZ[l]); /* grad of the concatenation */
+                /* grad of the concatenation */
+                synthesis_adjoint(t.hl[l], t.wl[l], t.hl[l - 1], t.wl[l - 1], gR, gZ[l]);
                 double* next = (double*)malloc(band * sizeof(double));
                 memcpy(next, gZ[l], band * sizeof(double)); /* R^(l+1) was added to LL */
                 free(gR_owned);

@@ -99,14 +99,19 @@ def _alg1_torch(x, w0, b0, s0, wl, sl, L):
     """Algorithm 1 written with framework primitives, as §3.1 describes the reference:
     Haar analysis as a grouped stride-2 conv2d with +-1/2 filters, the level filter as a
     depthwise conv over the 4C-channel tensor, a scale multiply, LL slicing, and the
-    synthesis as the grouped conv_transpose2d. Float64, differentiable by autograd."""
+    synthesis as the grouped conv_transpose2d. A carrier with an odd side is padded with
+    one zero row / column (F.pad) before its analysis and each synthesis output is cropped
+    back to the carrier's size. Float64, differentiable by autograd."""
     N, C, H, W = x.shape
     k = w0.shape[-1]
     r = (k - 1) // 2
     haar = _HAAR_FILTERS.unsqueeze(1).repeat(C, 1, 1, 1)  # [4C, 1, 2, 2]
     cur = x
     Z = []
+    sizes = []
     for l in range(L):
+        sizes.append(cur.shape[-2:])
+        cur = F.pad(cur, (0, cur.shape[-1] % 2, 0, cur.shape[-2] % 2))
         Y = F.conv2d(cur, haar, stride=2, groups=C)  # channel 4c + b
         Cv = F.conv2d(Y, wl[l].reshape(4 * C, 1, k, k), padding=r, groups=4 * C)
         Z.append(Cv * sl[l].reshape(1, 4 * C, 1, 1))
@@ -119,6 +124,7 @@ def _alg1_torch(x, w0, b0, s0, wl, sl, L):
             add[:, 0::4] = R
             Zl = Zl + add
         R = F.conv_transpose2d(Zl, haar, stride=2, groups=C)
+        R = R[:, :, :sizes[l][0], :sizes[l][1]]
     base = F.conv2d(x, w0.reshape(C, 1, k, k), padding=r, groups=C) + b0.reshape(1, C, 1, 1)
     out = s0.reshape(1, C, 1, 1) * base
     return out + R if R is not None else out
@@ -131,6 +137,9 @@ CASES = [  # n, c, h, w, k, L
     (1, 3, 8, 24, 1, 2),
     (1, 2, 16, 16, 7, 4),
     (2, 3, 12, 10, 5, 0),
+    (1, 2, 13, 11, 5, 2),   # odd sides: carriers padded at every level
+    (2, 2, 7, 9, 3, 3),     # 7 -> 4 -> 2 -> 1 rows, 9 -> 5 -> 3 -> 2 columns
+    (1, 1, 6, 5, 1, 2),     # 6 -> 3 -> 2: an odd carrier at level 2 only
 ]
 
 
@@ -164,6 +173,31 @@ def test_backward_matches_library_autograd(oracle_lib, n, c, h, w, k, L):
 # ---------------------------------------------------------------------------------------
 # Closed forms, special cases and invariants
 # ---------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("h,w,L", [(13, 11, 2), (7, 9, 3), (5, 6, 2), (17, 3, 2)])
+def test_odd_sizes_equal_padding_the_input(oracle_lib, h, w, L):
+    """Zero-padding every odd carrier is the same operator as zero-padding X once to a
+    multiple of 2^L and cropping the output: the padded region of each carrier is exactly
+    the analysis of zeros, and the level coefficients that reach the cropped output sit at
+    (y >> l, x >> l) inside the padded grid. Gradients: dX is the cropped dX of the padded
+    problem with dY zero-padded; parameter gradients are equal."""
+    n, c, k = 2, 2, 5
+    p = _params(n, c, h, w, k, L, seed=40 + h + w)
+    m = 1 << L
+    hp, wp = -(-h // m) * m, -(-w // m) * m
+    xp = np.zeros((n, c, hp, wp)); xp[:, :, :h, :w] = p["x"]
+    gp = np.zeros((n, c, hp, wp)); gp[:, :, :h, :w] = p["dy"]
+    for mode in ("cascade", "closed"):
+        y = oracle.forward(p["x"], p["w0"], p["b0"], p["s0"], p["wl"], p["sl"], L, mode=mode)
+        yp = oracle.forward(xp, p["w0"], p["b0"], p["s0"], p["wl"], p["sl"], L, mode=mode)
+        np.testing.assert_allclose(y, yp[:, :, :h, :w], rtol=0, atol=1e-12)
+    g = oracle.backward(p["x"], p["dy"], p["w0"], p["b0"], p["s0"], p["wl"], p["sl"], L)
+    gpad = oracle.backward(xp, gp, p["w0"], p["b0"], p["s0"], p["wl"], p["sl"], L)
+    np.testing.assert_allclose(g["dx"], gpad["dx"][:, :, :h, :w], rtol=0, atol=1e-11)
+    for key in ("dw0", "db0", "ds0", "dwl", "dsl"):
+        np.testing.assert_allclose(g[key], gpad[key], rtol=0,
+                                   atol=1e-11 * max(1.0, np.abs(gpad[key]).max()), err_msg=key)
+
 
 def _delta(k):
     d = np.zeros((k, k))
@@ -395,7 +429,7 @@ def test_invalid_arguments_rejected(oracle_lib):
                        np.zeros((1, 1, 4, 4, 4)), np.ones((1, 1, 4)), 1)  # even k
     with pytest.raises(ValueError):
         oracle.forward(np.zeros((1, 1, 6, 6)), np.zeros((1, 3, 3)), None, np.ones(1),
-                       np.zeros((2, 1, 4, 3, 3)), np.ones((2, 1, 4)), 2)  # 6 % 4 != 0
+                       np.zeros((31, 1, 4, 3, 3)), np.ones((31, 1, 4)), 31)  # L > 30
 
 
 # ---------------------------------------------------------------------------------------
