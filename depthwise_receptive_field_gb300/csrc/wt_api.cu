@@ -20,8 +20,6 @@ wt_status check_desc(const wt_desc* d) {
     if (d->io != WT_F32 && d->io != WT_BF16 && d->io != WT_F16) return WT_ERR_INVALID_ARG;
     if (d->k < 1 || (d->k % 2) == 0) return WT_ERR_INVALID_ARG;
     if (d->levels < 0 || d->levels > kMaxLevels) return WT_ERR_INVALID_ARG;
-    const int m = 1 << d->levels;
-    if ((d->h % m) != 0 || (d->w % m) != 0) return WT_ERR_INVALID_ARG;
     if ((size_t)d->n * d->c > 0x7fffffffull) return WT_ERR_INVALID_ARG;  // grid limit
     if (d->k > 7) return WT_ERR_UNSUPPORTED;
     return WT_OK;

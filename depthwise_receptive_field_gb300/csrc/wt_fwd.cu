@@ -47,6 +47,7 @@ struct FwdArgs {
     long long slot;     // floats between consecutive CTAs' slots (2 * zd_slot)
     long long planes;
     int C, H, W, L;
+    int Hp, Wp;  // the plane padded with zeros to multiples of 2^L: level l is (Hp, Wp) >> l
     int img;  // floats of one channel's weight image (a multiple of 4)
     int vec, use_tma;
     int o_bar, o_raw, o_dblk, o_w, o_b, o_x, o_z;  // shared-memory regions (floats)
@@ -122,14 +123,14 @@ __device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, floa
                                              uint64_t* bar_s, uint32_t& ph_s, long long plane) {
     constexpr int BW = SweepBox<T>::BW, BH = SweepBox<T>::BH, NB = SweepBox<T>::NBUF;
     constexpr int PR = BH / 4;  // rows of level-2 positions per box
-    const int H2 = a.H >> 2, W2 = a.W >> 2;
+    const int H2 = a.Hp >> 2, W2 = a.Wp >> 2;
     float* c2 = sm + a.o_car[2];
     float4* u2v = reinterpret_cast<float4*>(u2);
     const int tid = threadIdx.x;
     if (a.use_tma) {
         T* buf = reinterpret_cast<T*>(sm + a.o_b);
-        const int bxn = (a.W + BW - 1) / BW;
-        const int nbox = sweep_boxes(a.H, a.W, BW, BH);
+        const int bxn = (a.Wp + BW - 1) / BW;
+        const int nbox = sweep_boxes(a.Hp, a.Wp, BW, BH);
         constexpr int PC = BW / 4;  // level-2 positions per box row
         const int pi = tid / PC, pj = tid % PC;
         for (int t = 0; t < nbox; ++t) {
@@ -163,10 +164,9 @@ __device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, floa
                 const int p = base + k * kFT;
                 if (p < n) {
                     const int i2 = p / W2, j2 = p - i2 * W2;
-                    const T* q = xp + (size_t)(4 * i2) * a.W + 4 * j2;
-                    const float4 u = level2_block(IO<T>::ld4(q), IO<T>::ld4(q + a.W),
-                                                  IO<T>::ld4(q + 2 * (size_t)a.W),
-                                                  IO<T>::ld4(q + 3 * (size_t)a.W));
+                    float4 r[4];
+                    load_block4x4<T>(xp, a.H, a.W, a.vec, 4 * i2, 4 * j2, r);
+                    const float4 u = level2_block(r[0], r[1], r[2], r[3]);
                     __stcg(u2v + p, u);
                     if (a.L >= 3) c2[p] = 0.5f * u.x;
                 }
@@ -179,7 +179,7 @@ __device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, floa
 // Carriers X^(l) = LL of X^(l-1) (normalized, Eq. 5) for l = 3..L-1, in shared memory.
 __device__ __forceinline__ void deep_carriers(const FwdArgs& a, float* sm) {
     for (int l = 3; l < a.L; ++l) {
-        const int Hl = a.H >> l, Wl = a.W >> l, Wp = a.W >> (l - 1);
+        const int Hl = a.Hp >> l, Wl = a.Wp >> l, Wp = a.Wp >> (l - 1);
         const float* cp = sm + a.o_car[l - 1];
         float* cl = sm + a.o_car[l];
         for (int p = threadIdx.x; p < Hl * Wl; p += kFT) {
@@ -201,7 +201,7 @@ __device__ __forceinline__ void deep_stage(const FwdArgs& a, const float* u2, fl
     constexpr int R = FG<K>::R, BT = FG<K>::BT;
     constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, PHALF = PG<K>::PHALF;
     constexpr int NIT = (BT * BT + kFT - 1) / kFT;
-    const int Hl = a.H >> l, Wl = a.W >> l, Wp = a.W >> (l - 1);
+    const int Hl = a.Hp >> l, Wl = a.Wp >> l, Wp = a.Wp >> (l - 1);
     float* bs = sm + a.o_b;
     const float* carp = (l >= 3) ? sm + a.o_car[l - 1] : nullptr;
     const float4* u2v = reinterpret_cast<const float4*>(u2);
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
             }
             if (a.use_tma && a.L >= 2) {  // first boxes of the level-2 sweep
                 constexpr int BW = SweepBox<T>::BW, BH = SweepBox<T>::BH;
-                const int bxn = (a.W + BW - 1) / BW, nbox = sweep_boxes(a.H, a.W, BW, BH);
+                const int bxn = (a.Wp + BW - 1) / BW, nbox = sweep_boxes(a.Hp, a.Wp, BW, BH);
                 T* buf = reinterpret_cast<T*>(sm + a.o_b);
                 for (int t = 0; t < SweepBox<T>::NBUF && t < nbox; ++t) {
                     const int ny = t / bxn, nx = t - ny * bxn;
@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
             }
             deep_carriers(a, sm);
             for (int l = a.L; l >= 2; --l) {
-                const int Hl = a.H >> l, Wl = a.W >> l;
+                const int Hl = a.Hp >> l, Wl = a.Wp >> l;
                 for (int ti0 = 0; ti0 < Hl; ti0 += kCT) {
                     for (int tj0 = 0; tj0 < Wl; tj0 += kCT) {
                         deep_stage<K>(a, u2, sm, l, ti0, tj0);
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                                 const float4 z = make_float4(za.x, za.y, zb.x, zb.y);
                                 float v = 0.f;
                                 for (int m = 3; m <= a.L; ++m) {
-                                    const int sh = m - 2, Wm = a.W >> m;
+                                    const int sh = m - 2, Wm = a.Wp >> m;
                                     const float4 zm = reinterpret_cast<const float4*>(sm + a.o_zl[m])
                                         [(i2 >> sh) * Wm + (j2 >> sh)];
                                     v += synth_rt(zm, (i2 >> (m - 3)) & 1, (j2 >> (m - 3)) & 1);
@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
             if (a.L >= 2) {
                 if (!a.use_tma) {
                     // plain copy of the 16x16 level-2 block of deep sums (zero outside)
-                    const int H2 = a.H >> 2, W2 = a.W >> 2;
+                    const int H2 = a.Hp >> 2, W2 = a.Wp >> 2;
                     const float4* z2 = reinterpret_cast<const float4*>(zslot);
                     const int i0 = y0 >> 2, j0 = x0 >> 2;
                     const int i = tid >> 4, j = tid & 15;
@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
             if (a.L >= 1) {
                 // level-1 filters: 2 band pairs x 128 blocks of 2x4 coefficients, one per thread
                 const int pp = tid >> 7, bi = (tid >> 3) & 15, bj = tid & 7;
-                if (y0 / 2 + 2 * bi < a.H / 2 && x0 / 2 + 4 * bj < a.W / 2) {
+                if (y0 / 2 + 2 * bi < (a.H + 1) / 2 && x0 / 2 + 4 * bj < (a.W + 1) / 2) {
                     f2x acc[2][4];
                     conv_pair_2x4<K>(bs + pp * PTILE + (2 * bi) * PROW, bj, wsm + (1 + pp) * WS,
                                      acc);
@@ -598,6 +598,7 @@ FwdPlan fwd_plan(const wt_desc& d) {
     FwdPlan p;
     FwdArgs& a = p.a;
     const int L = d.levels;
+    const int hp = padded_side(d.h, L), wp = padded_side(d.w, L);
     int off = 0;
     a.o_bar = off;
     off += 32;  // eight mbarriers, padded to 128 bytes
@@ -625,16 +626,16 @@ FwdPlan fwd_plan(const wt_desc& d) {
     for (int l = 0; l <= kMaxLevels; ++l) a.o_car[l] = a.o_zl[l] = 0;
     for (int l = 2; l < L; ++l) {
         a.o_car[l] = cp;
-        cp += round4((d.h >> l) * (d.w >> l));
+        cp += round4((hp >> l) * (wp >> l));
     }
     for (int l = 3; l <= L; ++l) {
         a.o_zl[l] = cp;
-        cp += 4 * (d.h >> l) * (d.w >> l);
+        cp += 4 * (hp >> l) * (wp >> l);
     }
     const int total = xend > cp ? xend : cp;
     p.smem = (size_t)total * sizeof(float);
     // per CTA: deep sums and level-2 subbands, each [H/4][W/4][4] fp32
-    a.zd_slot = (L >= 2) ? ((4LL * (d.h >> 2) * (d.w >> 2) + 63) & ~63LL) : 0;
+    a.zd_slot = (L >= 2) ? ((4LL * (hp >> 2) * (wp >> 2) + 63) & ~63LL) : 0;
     a.slot = 2 * a.zd_slot;
     const long long planes = (long long)d.n * d.c;
     int occ = (int)((228 * 1024) / (p.smem + 1024));
@@ -668,6 +669,8 @@ wt_status launch_fwd_k(const wt_desc& d, const void* x, const float* w0f, const 
     a.C = d.c;
     a.H = d.h;
     a.W = d.w;
+    a.Hp = padded_side(d.h, d.levels);
+    a.Wp = padded_side(d.w, d.levels);
     a.L = d.levels;
     a.vec = (d.w % 4 == 0) ? 1 : 0;
     // TMA needs 16-byte row strides; otherwise the tile is staged with plain loads
@@ -680,7 +683,7 @@ wt_status launch_fwd_k(const wt_desc& d, const void* x, const float* w0f, const 
                             (unsigned long long)d.w * d.h * esize, XBox<K, T>::XBW,
                             XBox<K, T>::XBH);
         if (ok && d.levels >= 2) {
-            const unsigned long long w2 = d.w >> 2, h2 = d.h >> 2;
+            const unsigned long long w2 = a.Wp >> 2, h2 = a.Hp >> 2;
             ok = encode_3d(&a.tmd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.zd, 4 * w2, h2,
                            (unsigned long long)p.grid, 16 * w2, (unsigned long long)a.slot * 4,
                            64, 16);

@@ -32,6 +32,14 @@ auto with_io_type(wt_dtype io, F&& f) {
     }
 }
 
+// A plane side padded with zeros up to a multiple of 2^L: the kernels run every level on
+// the padded plane, which equals zero-padding each odd carrier by one row / column before
+// its analysis and cropping each synthesis output (only the H x W outputs are stored).
+inline int padded_side(int n, int levels) {
+    const int m = 1 << levels;
+    return (n + m - 1) / m * m;
+}
+
 // Bytes per element of an I/O dtype.
 inline size_t io_bytes(wt_dtype io) { return io == WT_F32 ? 4 : 2; }
 

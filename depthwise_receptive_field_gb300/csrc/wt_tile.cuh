@@ -51,83 +51,6 @@ __device__ __forceinline__ void load_row(const float* p, float (&v)[4 * N]) {
     }
 }
 
-// acc[o][q] = sum_{u,v} w[u][v] win[o+u][q+v] for a 4x4 output block (acc overwritten).
-template <int K>
-__device__ __forceinline__ void conv4x4(const float* win, int pitch, const float* wsm,
-                                        float (&acc)[4][4]) {
-    constexpr int KK = FG<K>::KK, R = FG<K>::R, CNC = FG<K>::CNC;
-    float w[KK];
-#pragma unroll
-    for (int q = 0; q < KK; ++q) w[q] = wsm[q];
-#pragma unroll
-    for (int o = 0; o < 4; ++o)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[o][q] = 0.f;
-#pragma unroll
-    for (int r = 0; r < 4 + 2 * R; ++r) {
-        float v[4 * CNC];
-        load_row<CNC>(win + r * pitch, v);
-#pragma unroll
-        for (int o = 0; o < 4; ++o) {
-            const int u = r - o;
-            if (u < 0 || u >= K) continue;
-#pragma unroll
-            for (int vv = 0; vv < K; ++vv)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) acc[o][q] = fmaf(w[u * K + vv], v[q + vv], acc[o][q]);
-        }
-    }
-}
-
-// acc[o][q] += sum_{u,v} w[u][v] win[o+u][q+v] for an 8-row x 4-col output block.
-template <int K>
-__device__ __forceinline__ void conv8x4(const float* win, int pitch, const float* wsm,
-                                        float (&acc)[8][4]) {
-    constexpr int KK = FG<K>::KK, BWR = FG<K>::BWR, BNC = FG<K>::BNC;
-    float w[KK];
-#pragma unroll
-    for (int q = 0; q < KK; ++q) w[q] = wsm[q];
-#pragma unroll
-    for (int r = 0; r < BWR; ++r) {
-        float v[4 * BNC];
-        load_row<BNC>(win + r * pitch, v);
-#pragma unroll
-        for (int o = 0; o < 8; ++o) {
-            const int u = r - o;
-            if (u < 0 || u >= K) continue;
-#pragma unroll
-            for (int vv = 0; vv < K; ++vv)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) acc[o][q] = fmaf(w[u * K + vv], v[q + vv], acc[o][q]);
-        }
-    }
-}
-
-// Weight-gradient correlation: acc[u*K+v] += sum_{o,q} g[o][q] win[o+u][q+v] over a block
-// of ROWS x 4 gradient values (ROWS = 4 or 8); acc may be longer than K*K (extra entries
-// are left alone).
-template <int K, int ROWS, int NA>
-__device__ __forceinline__ void corr_rows(const float* win, int pitch, const float (&g)[ROWS][4],
-                                          float (&acc)[NA]) {
-    static_assert(NA >= K * K, "accumulator too short");
-    constexpr int R = FG<K>::R, NC = (4 + 2 * R + 3) / 4;
-#pragma unroll
-    for (int r = 0; r < ROWS + 2 * R; ++r) {
-        float v[4 * NC];
-        load_row<NC>(win + r * pitch, v);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int o = 0; o < ROWS; ++o) {
-                const int u = r - o;
-                if (u < 0 || u >= K) continue;
-#pragma unroll
-                for (int vv = 0; vv < K; ++vv)
-                    acc[u * K + vv] = fmaf(g[o][q], v[q + vv], acc[u * K + vv]);
-            }
-    }
-}
-
 // ---------------------------------------------------------------------------------
 // Band-pair tiles for packed (f32x2) filtering: the four subbands are stored as two
 // tiles of interleaved pairs, (LL, LH) and (HL, HH), so that one packed FMA applies the
@@ -450,49 +373,43 @@ __device__ __forceinline__ void stage_tile(const T* xp, int H, int W, int vec, f
     }
 }
 
-// Level-1 unnormalized subbands of the staged tile with an R-coefficient halo,
-// band-major [4][BT][BPITCH] (cell (ci, cj) <-> coefficient (y0/2 - R + ci, x0/2 - R + cj)).
-template <int K>
-__device__ __forceinline__ void bands_from_tile(const float* xs, float* bs) {
-    constexpr int PAD = FG<K>::PAD, XP = FG<K>::XPITCH, BT = FG<K>::BT;
-    constexpr int BP = FG<K>::BPITCH, BAND = FG<K>::BAND;
-    for (int idx = threadIdx.x; idx < BT * BT; idx += blockDim.x) {
-        const int ci = idx / BT, cj = idx - ci * BT;
-        const float* p = xs + (2 * ci) * XP + PAD + 2 * cj;
-        float a, b, c, d;
-        if constexpr ((PAD & 1) == 0) {
-            const float2 t0 = *reinterpret_cast<const float2*>(p);
-            const float2 t1 = *reinterpret_cast<const float2*>(p + XP);
-            a = t0.x; b = t0.y; c = t1.x; d = t1.y;
-        } else {
-            a = p[0]; b = p[1]; c = p[XP]; d = p[XP + 1];
+// The 4x4 pixel block of a plane at (r0, c0), zero outside H x W (the padding of a plane
+// whose sides are not multiples of 2^L); vector loads when the block lies inside the plane
+// and rows start on 4-element boundaries (vec: W % 4 == 0).
+template <typename T>
+__device__ __forceinline__ void load_block4x4(const T* xp, int H, int W, int vec, int r0, int c0,
+                                              float4 (&r)[4]) {
+    if (vec && r0 + 3 < H && c0 + 3 < W) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) r[q] = IO<T>::ld4(xp + (size_t)(r0 + q) * W + c0);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float e[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                e[m] = (r0 + q < H && c0 + m < W) ? IO<T>::ld(xp + (size_t)(r0 + q) * W + c0 + m)
+                                                  : 0.f;
+            r[q] = make_float4(e[0], e[1], e[2], e[3]);
         }
-        const float4 u = haar_u(a, b, c, d);
-        float* q = bs + ci * BP + cj;
-        q[0] = u.x;
-        q[BAND] = u.y;
-        q[2 * BAND] = u.z;
-        q[3 * BAND] = u.w;
     }
 }
 
 // Level-l (l >= 2) carrier 2x2 block feeding subband cell (gi, gj): from X itself when
-// l == 2 (its 4x4 pixel block, through the level-1 carrier), else from the carrier
-// X^(l-1) of width Wp in shared memory. Values are Eq. 5's normalized low-pass carrier.
+// l == 2 (its 4x4 pixel block, through the level-1 carrier; zero outside the H x W plane),
+// else from the carrier X^(l-1) of width Wp in shared memory. Values are Eq. 5's
+// normalized low-pass carrier.
 template <typename T>
-__device__ __forceinline__ void carrier_block(int l, const T* xp, int W, const float* carp,
-                                              int Wp, int gi, int gj, float& ca, float& cb,
-                                              float& cc, float& cd) {
+__device__ __forceinline__ void carrier_block(int l, const T* xp, int H, int W, int vec,
+                                              const float* carp, int Wp, int gi, int gj,
+                                              float& ca, float& cb, float& cc, float& cd) {
     if (l == 2) {
-        const T* p = xp + (size_t)(4 * gi) * W + 4 * gj;
-        const float4 r0 = IO<T>::ld4(p);
-        const float4 r1 = IO<T>::ld4(p + W);
-        const float4 r2 = IO<T>::ld4(p + 2 * (size_t)W);
-        const float4 r3 = IO<T>::ld4(p + 3 * (size_t)W);
-        ca = 0.5f * (r0.x + r0.y + r1.x + r1.y);
-        cb = 0.5f * (r0.z + r0.w + r1.z + r1.w);
-        cc = 0.5f * (r2.x + r2.y + r3.x + r3.y);
-        cd = 0.5f * (r2.z + r2.w + r3.z + r3.w);
+        float4 r[4];
+        load_block4x4<T>(xp, H, W, vec, 4 * gi, 4 * gj, r);
+        ca = 0.5f * (r[0].x + r[0].y + r[1].x + r[1].y);
+        cb = 0.5f * (r[0].z + r[0].w + r[1].z + r[1].w);
+        cc = 0.5f * (r[2].x + r[2].y + r[3].x + r[3].y);
+        cd = 0.5f * (r[2].z + r[2].w + r[3].z + r[3].w);
     } else {
         const float* q = carp + (size_t)(2 * gi) * Wp + 2 * gj;
         ca = q[0];

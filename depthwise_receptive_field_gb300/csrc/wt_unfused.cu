@@ -513,6 +513,9 @@ wt_status check_variant(const wt_desc* desc, int variant) {
     if (variant < WT_VARIANT_REFERENCE || variant > WT_VARIANT_FOLDED) return WT_ERR_INVALID_ARG;
     if (desc->io != WT_F32) return WT_ERR_UNSUPPORTED;
     if (desc->levels > kMaxLevels) return WT_ERR_UNSUPPORTED;
+    // the staged pipelines materialize every level at exactly half the size of the last
+    const int m = 1 << desc->levels;
+    if ((desc->h % m) != 0 || (desc->w % m) != 0) return WT_ERR_UNSUPPORTED;
     return WT_OK;
 }
 

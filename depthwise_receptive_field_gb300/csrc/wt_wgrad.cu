@@ -39,6 +39,7 @@ struct DwArgs {
     float* part;  // [C][N][KP]
     int* err;     // set when a TMA wait times out (may be null)
     int N, C, H, W, L;
+    int Hp, Wp;  // the plane padded with zeros to multiples of 2^L: level l is (Hp, Wp) >> l
     int vec, use_tma;
     int KP;
     int o_bar, o_rawx, o_rawg, o_acc, o_red, o_xb, o_gb, o_x, o_g;  // shared memory (floats)
@@ -58,7 +59,7 @@ __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const T* xp, cons
     constexpr int R = FG<K>::R, BT = FG<K>::BT;
     constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, PHALF = PG<K>::PHALF;
     constexpr int NIT = (BT * BT + kDT - 1) / kDT;
-    const int Hl = a.H >> l, Wl = a.W >> l, Wp = a.W >> (l - 1);
+    const int Hl = a.Hp >> l, Wl = a.Wp >> l, Wp = a.Wp >> (l - 1);
     float* xb = sm + a.o_xb;
     float* gb = sm + a.o_gb;
     const float* cpx = (l >= 3) ? sm + a.o_carx[l - 1] : nullptr;
@@ -75,11 +76,11 @@ __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const T* xp, cons
         float4 ux = f4_zero(), ug = f4_zero();
         if (gi >= 0 && gi < Hl && gj >= 0 && gj < Wl) {
             float ca, cb, cc, cd;
-            carrier_block<T>(l, xp, a.W, cpx, Wp, gi, gj, ca, cb, cc, cd);
+            carrier_block<T>(l, xp, a.H, a.W, a.vec, cpx, Wp, gi, gj, ca, cb, cc, cd);
             ux = haar_u(ca, cb, cc, cd);
             if (inner) {
                 if (clx) clx[gi * Wl + gj] = 0.5f * ux.x;
-                carrier_block<T>(l, gp, a.W, cpy, Wp, gi, gj, ca, cb, cc, cd);
+                carrier_block<T>(l, gp, a.H, a.W, a.vec, cpy, Wp, gi, gj, ca, cb, cc, cd);
                 ug = haar_u(ca, cb, cc, cd);
                 if (cly) cly[gi * Wl + gj] = 0.5f * ug.x;
             }
@@ -224,7 +225,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
 
     // ---- deep levels l = 2..L: band pair pp = tid / 128, 2x4 block per thread ----
     for (int l = 2; l <= a.L; ++l) {
-        const int Hl = a.H >> l, Wl = a.W >> l;
+        const int Hl = a.Hp >> l, Wl = a.Wp >> l;
         const int pp = tid >> 7, bi = (tid >> 3) & 15, bj = tid & 7;
         f2x accd[KK];
 #pragma unroll
@@ -317,7 +318,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
             }
         } else {
             const int t2 = tid - 128, pp = t2 >> 6, bi = (t2 >> 3) & 7, bj = t2 & 7;
-            if (y0 / 2 + 4 * bi < a.H / 2 && x0 / 2 + 4 * bj < a.W / 2) {
+            if (y0 / 2 + 4 * bi < (a.H + 1) / 2 && x0 / 2 + 4 * bj < (a.W + 1) / 2) {
                 f2x g[4][4];
 #pragma unroll
                 for (int o = 0; o < 4; ++o) {
@@ -444,7 +445,8 @@ void dw_layout(const wt_desc& d, DwArgs& a, size_t& smem_bytes) {
     int cp = alias0;
     for (int l = 0; l <= kMaxLevels; ++l) a.o_carx[l] = a.o_cary[l] = 0;
     for (int l = 2; l < L; ++l) {
-        const int sz = round4((d.h >> l) * (d.w >> l));
+        const int sz = round4((padded_side(d.h, d.levels) >> l) *
+                              (padded_side(d.w, d.levels) >> l));
         a.o_carx[l] = cp;
         cp += sz;
         a.o_cary[l] = cp;
@@ -468,6 +470,8 @@ bool dw_prepare(const wt_desc& d, const void* x, const void* dy, float* part, in
     a.C = d.c;
     a.H = d.h;
     a.W = d.w;
+    a.Hp = padded_side(d.h, d.levels);
+    a.Wp = padded_side(d.w, d.levels);
     a.L = d.levels;
     a.vec = (d.w % 4 == 0) ? 1 : 0;
     a.use_tma = 0;

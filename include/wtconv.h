@@ -29,9 +29,15 @@
  *    happen later surface on the next synchronizing CUDA call, as usual.
  *  - Gradients are written, never accumulated into.
  *  - x, y, dy and dx must be 16-byte aligned; parameter pointers 4-byte aligned.
- *  - Accepted shapes: N, C, H, W >= 1; k odd, 1 <= k <= 7; 0 <= L <= 12; H and W
- *    divisible by 2^L. Everything else returns WT_ERR_INVALID_ARG (or
- *    WT_ERR_UNSUPPORTED for a k the kernels were not built for).
+ *  - Accepted shapes: N, C, H, W >= 1; k odd, 1 <= k <= 7; 0 <= L <= 12. Everything else
+ *    returns WT_ERR_INVALID_ARG (or WT_ERR_UNSUPPORTED for a k the kernels were not built
+ *    for, or a plane too large for the kernels' shared memory at that L).
+ *  - Odd sides: a carrier with an odd number of rows (columns) is padded with one zero
+ *    row (column) at the bottom (right) before its Haar analysis, so level l has
+ *    ceil(H_{l-1} / 2) rows, and every synthesis output is cropped back to its carrier's
+ *    size (the pages are silent on odd sizes; this is the plain completion of Eq. 5 and
+ *    Eq. 12). It equals running the layer on X zero-padded to multiples of 2^L and keeping
+ *    the top-left H x W outputs, which is how the kernels compute it.
  *  - Results are deterministic: no atomics; every reduction runs in a fixed order.
  */
 #ifndef WTCONV_H_

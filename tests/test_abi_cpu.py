@@ -39,8 +39,8 @@ BAD = [
     dict(k=0),
     dict(levels=-1),
     dict(levels=13),
-    dict(h=30, levels=2),   # 30 % 4 != 0
-    dict(w=12, levels=3),   # 12 % 8 != 0
+    dict(h=0),
+    dict(w=-3),
     dict(n=0),
     dict(c=0),
     dict(io=7),
@@ -58,6 +58,18 @@ def test_invalid_descriptors_rejected(lib, override):
     # the compute entry points validate the same way before touching the device
     st = lib.wtconv_forward(ctypes.byref(d), 16, 16, None, 16, 16, None, 0, None)
     assert st == B.WT_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("h,w,L", [(30, 32, 2), (32, 12, 3), (13, 11, 2), (7, 9, 3)])
+def test_odd_sides_are_accepted(lib, h, w, L):
+    """Sides that are not multiples of 2^L are padded per level (not rejected); the staged
+    pipelines, which materialize exact halvings, report them as unsupported."""
+    d = B.make_desc(2, 3, h, w, 5, L, B.WT_F32)
+    fwd, bwd_d, bwd_w = B.wtconv_workspace_size(d)
+    assert fwd == bwd_d and fwd >= 256 and bwd_w > 256
+    with pytest.raises(B.WTConvError) as e:
+        B.wtconv_variant_workspace_size(d, B.WT_VARIANT_REFERENCE)
+    assert e.value.status == B.WT_ERR_UNSUPPORTED
 
 
 def test_unbuilt_kernel_size_is_unsupported(lib):
@@ -142,7 +154,7 @@ def test_variant_validation(lib):
     assert e.value.status == B.WT_ERR_UNSUPPORTED
     with pytest.raises(B.WTConvError) as e:
         B.wtconv_variant_workspace_size(B.make_desc(2, 3, 60, 64, 5, 3, B.WT_F32), 0)
-    assert e.value.status == B.WT_ERR_INVALID_ARG
+    assert e.value.status == B.WT_ERR_UNSUPPORTED
     # null input pointer: rejected before any launch
     with pytest.raises(B.WTConvError) as e:
         B.wtconv_forward_variant(d, 0, None, 16, None, 16, 16, 16, 16, 256, sizes[0], stream=0)

@@ -81,7 +81,17 @@ F16 = [  # fp16 I/O (the pages' half-precision measurements): TMA path and plain
 ]
 
 
-@pytest.mark.parametrize("n,c,h,w,k,L,dtype", EDGE + F16)
+ODD = [  # sides that are not multiples of 2^L: carriers zero-padded per level
+    (2, 3, 13, 11, 5, 2, "f32"),      # both sides odd, plain staging
+    (1, 2, 37, 64, 5, 3, "bf16"),     # odd H on the TMA path (W * 2 bytes % 16 == 0)
+    (2, 2, 7, 9, 3, 3, "f32"),        # 7 -> 4 -> 2 -> 1 rows
+    (1, 2, 100, 60, 7, 4, "bf16"),    # W * 2 bytes % 16 != 0: plain staging, k = 7
+    (1, 1, 5, 5, 5, 5, "f32"),        # more levels than the plane has halvings
+    (2, 2, 130, 66, 5, 5, "f16"),     # several tiles with odd carriers at deep levels
+]
+
+
+@pytest.mark.parametrize("n,c,h,w,k,L,dtype", EDGE + F16 + ODD)
 def test_edge_shapes(n, c, h, w, k, L, dtype):
     wl = shape_workload(n, c, h, w, k, L, dtype, seed=1000 + h + w + k + L)
     errs, _ = run_and_compare(wl, bias_and_scale=True)
