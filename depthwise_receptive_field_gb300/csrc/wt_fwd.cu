@@ -44,13 +44,15 @@ struct FwdArgs {
     float* zd;         // scratch: per CTA the deep sums, then the level-2 subbands
     int* err;          // first word of the workspace: set on a stuck TMA wait
     long long zd_slot;  // floats of each of the two arrays of a CTA's slot
-    long long slot;     // floats between consecutive CTAs' slots (2 * zd_slot)
+    long long slot;     // floats between consecutive CTAs' slots (2 * zd_slot + deep state)
     long long planes;
     int C, H, W, L;
     int Hp, Wp;  // the plane padded with zeros to multiples of 2^L: level l is (Hp, Wp) >> l
     int img;  // floats of one channel's weight image (a multiple of 4)
     int vec, use_tma;
     int o_bar, o_raw, o_dblk, o_w, o_b, o_x, o_z;  // shared-memory regions (floats)
+    // deep-level state, in shared memory or (deep_global) in the CTA's workspace slot:
+    int deep_global;
     int o_car[kMaxLevels + 1];                    // carriers X^(l), l = 2..L-1
     int o_zl[kMaxLevels + 1];                     // Z^(l), l = 3..L, interleaved [Hl][Wl][4]
 };
@@ -118,16 +120,17 @@ __device__ __forceinline__ float4 level2_block(const float4& r0, const float4& r
 // memory. TMA path: the first NBUF boxes were issued at the start of the plane; box t + NBUF
 // reuses box t's buffer once every thread is past it. Returns false if a TMA wait timed
 // out (the vote makes the result uniform over the CTA).
-template <typename T>
-__device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, float* sm, float* u2,
-                                             uint64_t* bar_s, uint32_t& ph_s, long long plane) {
+template <typename T, bool FAST>
+__device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, float* sm, float* deep,
+                                             float* u2, uint64_t* bar_s, uint32_t& ph_s,
+                                             long long plane) {
     constexpr int BW = SweepBox<T>::BW, BH = SweepBox<T>::BH, NB = SweepBox<T>::NBUF;
     constexpr int PR = BH / 4;  // rows of level-2 positions per box
     const int H2 = a.Hp >> 2, W2 = a.Wp >> 2;
-    float* c2 = sm + a.o_car[2];
+    float* c2 = deep + a.o_car[2];
     float4* u2v = reinterpret_cast<float4*>(u2);
     const int tid = threadIdx.x;
-    if (a.use_tma) {
+    if (FAST || a.use_tma) {
         T* buf = reinterpret_cast<T*>(sm + a.o_b);
         const int bxn = (a.Wp + BW - 1) / BW;
         const int nbox = sweep_boxes(a.Hp, a.Wp, BW, BH);
@@ -177,11 +180,11 @@ __device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, floa
 }
 
 // Carriers X^(l) = LL of X^(l-1) (normalized, Eq. 5) for l = 3..L-1, in shared memory.
-__device__ __forceinline__ void deep_carriers(const FwdArgs& a, float* sm) {
+__device__ __forceinline__ void deep_carriers(const FwdArgs& a, float* deep) {
     for (int l = 3; l < a.L; ++l) {
         const int Hl = a.Hp >> l, Wl = a.Wp >> l, Wp = a.Wp >> (l - 1);
-        const float* cp = sm + a.o_car[l - 1];
-        float* cl = sm + a.o_car[l];
+        const float* cp = deep + a.o_car[l - 1];
+        float* cl = deep + a.o_car[l];
         for (int p = threadIdx.x; p < Hl * Wl; p += kFT) {
             const int i = p / Wl, j = p - i * Wl;
             const float* q = cp + (size_t)(2 * i) * Wp + 2 * j;
@@ -196,14 +199,14 @@ __device__ __forceinline__ void deep_carriers(const FwdArgs& a, float* sm) {
 // from the sweep's output (L2-resident), deeper levels transform the carrier X^(l-1) in
 // shared memory. The trip count is a compile-time constant so that all loads issue early.
 template <int K>
-__device__ __forceinline__ void deep_stage(const FwdArgs& a, const float* u2, float* sm, int l,
-                                           int ti0, int tj0) {
+__device__ __forceinline__ void deep_stage(const FwdArgs& a, const float* u2, float* sm,
+                                           const float* deep, int l, int ti0, int tj0) {
     constexpr int R = FG<K>::R, BT = FG<K>::BT;
     constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, PHALF = PG<K>::PHALF;
     constexpr int NIT = (BT * BT + kFT - 1) / kFT;
     const int Hl = a.Hp >> l, Wl = a.Wp >> l, Wp = a.Wp >> (l - 1);
     float* bs = sm + a.o_b;
-    const float* carp = (l >= 3) ? sm + a.o_car[l - 1] : nullptr;
+    const float* carp = (l >= 3) ? deep + a.o_car[l - 1] : nullptr;
     const float4* u2v = reinterpret_cast<const float4*>(u2);
 #pragma unroll
     for (int it = 0; it < NIT; ++it) {
@@ -226,7 +229,94 @@ __device__ __forceinline__ void deep_stage(const FwdArgs& a, const float* u2, fl
     }
 }
 
-template <int K, typename T>
+// Deep levels of one plane, after the level-2 sweep: carriers X^(l >= 3), levels L..3
+// filtered into the deep state, then level 2, whose filtered subbands are combined at once
+// with the deeper levels into Eq. 7's sum over levels 2..L at level-1 resolution, written
+// to the scratch slot: level-2 position (i2, j2) holds the sums for level-1 positions
+// (2 i2 + a, 2 j2 + b) as (a, b) = (0,0), (0,1), (1,0), (1,1). The deep state (carriers,
+// Z^(l >= 3)) is in shared memory (DG = false: deep is the shared-memory base) or in the
+// CTA's workspace slot (DG = true).
+template <int K, bool DG>
+__device__ __forceinline__ void deep_levels(const FwdArgs& a, float* sm, float* deep_g,
+                                            const float* u2, float* zslot) {
+    constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, WS = PG<K>::WS;
+    constexpr int ZROW = PG<K>::ZROW, ZTILE = PG<K>::ZTILE;
+    float* deep = DG ? deep_g : sm;
+    const float* wsm = sm + a.o_w;
+    float* bs = sm + a.o_b;
+    float* zs = sm + a.o_z;
+    const int tid = threadIdx.x;
+    deep_carriers(a, deep);
+    for (int l = a.L; l >= 2; --l) {
+        const int Hl = a.Hp >> l, Wl = a.Wp >> l;
+        for (int ti0 = 0; ti0 < Hl; ti0 += kCT) {
+            for (int tj0 = 0; tj0 < Wl; tj0 += kCT) {
+                deep_stage<K>(a, u2, sm, deep, l, ti0, tj0);
+                __syncthreads();
+                {
+                    // band pair pp = tid / 128, 2x4 output block (bi, bj)
+                    const int pp = tid >> 7, bi = (tid >> 3) & 15, bj = tid & 7;
+                    const int gi0 = ti0 + 2 * bi, gj0 = tj0 + 4 * bj;
+                    if (gi0 < Hl && gj0 < Wl) {
+                        f2x acc[2][4];
+                        conv_pair_2x4<K>(bs + pp * PTILE + (2 * bi) * PROW, bj,
+                                         wsm + (1 + 2 * (l - 1) + pp) * WS, acc);
+                        if (l >= 3) {
+                            float* zl = deep + a.o_zl[l];
+#pragma unroll
+                            for (int o = 0; o < 2; ++o) {
+                                if (gi0 + o >= Hl) continue;
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    if (gj0 + q < Wl)
+                                        *reinterpret_cast<float2*>(
+                                            zl + ((gi0 + o) * Wl + gj0 + q) * 4 + 2 * pp) =
+                                            upk2(acc[o][q]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int o = 0; o < 2; ++o) {
+                                float* zr = zs + pp * ZTILE + (2 * bi + o) * ZROW + 8 * bj;
+                                const float2 q0 = upk2(acc[o][0]), q1 = upk2(acc[o][1]);
+                                const float2 q2 = upk2(acc[o][2]), q3 = upk2(acc[o][3]);
+                                reinterpret_cast<float4*>(zr)[0] = make_float4(q0.x, q0.y, q1.x, q1.y);
+                                reinterpret_cast<float4*>(zr)[1] = make_float4(q2.x, q2.y, q3.x, q3.y);
+                            }
+                        }
+                    }
+                }
+                __syncthreads();
+                if (l == 2) {
+                    // deep sums of this level-2 tile's positions
+                    float4* dsum = reinterpret_cast<float4*>(zslot);
+#pragma unroll
+                    for (int k = 0; k < (kCT * kCT) / kFT; ++k) {
+                        const int p = tid + k * kFT, ti = p >> 5, tj = p & 31;
+                        const int i2 = ti0 + ti, j2 = tj0 + tj;
+                        if (i2 >= Hl || j2 >= Wl) continue;
+                        const float2 za = *reinterpret_cast<const float2*>(zs + ti * ZROW + 2 * tj);
+                        const float2 zb = *reinterpret_cast<const float2*>(zs + ZTILE + ti * ZROW + 2 * tj);
+                        const float4 z = make_float4(za.x, za.y, zb.x, zb.y);
+                        float v = 0.f;
+                        for (int m = 3; m <= a.L; ++m) {
+                            const int sh = m - 2, Wm = a.Wp >> m;
+                            const float4 zm = reinterpret_cast<const float4*>(deep + a.o_zl[m])
+                                [(i2 >> sh) * Wm + (j2 >> sh)];
+                            v += synth_rt(zm, (i2 >> (m - 3)) & 1, (j2 >> (m - 3)) & 1);
+                        }
+                        dsum[(size_t)i2 * Wl + j2] =
+                            make_float4(synth<0, 0>(z) + v, synth<0, 1>(z) + v,
+                                        synth<1, 0>(z) + v, synth<1, 1>(z) + v);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// FAST: the plane is TMA-staged, has 4-aligned rows, needs no padding and keeps its deep
+// state in shared memory, so those checks and the other paths are compiled out.
+template <int K, typename T, bool FAST>
 __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_constant__ FwdArgs a) {
     constexpr int R = FG<K>::R, PAD = FG<K>::PAD, XP = FG<K>::XPITCH;
     constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, WS = PG<K>::WS;
@@ -246,13 +336,16 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
     float* zs = sm + a.o_z;
     float* zslot = a.zd + (size_t)blockIdx.x * a.slot;  // deep sums [H/4][W/4][4]
     float* u2 = zslot + a.zd_slot;                          // level-2 subbands, same shape
+    const bool use_tma = FAST || a.use_tma;
+    const bool deep_global = !FAST && a.deep_global;
+    float* deep = deep_global ? zslot + 2 * a.zd_slot : sm;  // carriers and Z^(l >= 3)
     const size_t plane_elems = (size_t)a.H * a.W;
     const int tid = threadIdx.x;
     const bool leader = tid == 0;
     const int tiles_x = (a.W + kTile - 1) / kTile;
     const int ntiles = tiles_x * ((a.H + kTile - 1) / kTile);
 
-    if (a.use_tma && leader) {
+    if (use_tma && leader) {
         mbar_init(bar_x, 1);
         mbar_init(bar_d, 1);
         mbar_init(bar_d + 1, 1);
@@ -266,7 +359,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
     // weights of the current plane are in shared memory (uniform over the CTA)
     auto weights_ready = [&]() -> bool {
         bool ok = true;
-        if (a.use_tma) {
+        if (use_tma) {
             ok = mbar_wait_bounded(bar_w, ph_w);
             ph_w ^= 1;
         }
@@ -280,17 +373,17 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
         __syncthreads();  // the previous plane is done with shared memory
         const float bias = (a.b0f != nullptr) ? __ldg(a.b0f + c) : 0.f;
         const float* wimg = a.wimg + (size_t)c * a.img;
-        if (!a.use_tma)
+        if (!use_tma)
             for (int e = tid; e < a.img; e += kFT) wsm[e] = __ldg(wimg + e);
         if (leader) {
-            if (a.use_tma) {  // this channel's weights and the first tile of this plane
+            if (use_tma) {  // this channel's weights and the first tile of this plane
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(bar_w, (uint32_t)a.img * 4u);
                 bulk_load(wsm, wimg, (uint32_t)a.img * 4u, bar_w);
                 mbar_arrive_expect_tx(bar_x, XBox<K, T>::BYTES);
                 tma_load_3d(raw, &a.tmx, -XBox<K, T>::XOFF, -2 * R, (int)plane, bar_x);
             }
-            if (a.use_tma && a.L >= 2) {  // first boxes of the level-2 sweep
+            if (use_tma && a.L >= 2) {  // first boxes of the level-2 sweep
                 constexpr int BW = SweepBox<T>::BW, BH = SweepBox<T>::BH;
                 const int bxn = (a.Wp + BW - 1) / BW, nbox = sweep_boxes(a.Hp, a.Wp, BW, BH);
                 T* buf = reinterpret_cast<T*>(sm + a.o_b);
@@ -311,76 +404,14 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
         // (i2, j2) holds the sums for level-1 positions (2i2 + a, 2j2 + b) as
         // (a, b) = (0,0), (0,1), (1,0), (1,1).
         if (a.L >= 2) {
-            if (!level2_sweep<T>(a, xp, sm, u2, bar_s, ph_s, plane) || !weights_ready()) {
+            if (!level2_sweep<T, FAST>(a, xp, sm, deep, u2, bar_s, ph_s, plane) || !weights_ready()) {
                 failed = true;
                 break;
             }
-            deep_carriers(a, sm);
-            for (int l = a.L; l >= 2; --l) {
-                const int Hl = a.Hp >> l, Wl = a.Wp >> l;
-                for (int ti0 = 0; ti0 < Hl; ti0 += kCT) {
-                    for (int tj0 = 0; tj0 < Wl; tj0 += kCT) {
-                        deep_stage<K>(a, u2, sm, l, ti0, tj0);
-                        __syncthreads();
-                        {
-                            // band pair pp = tid / 128, 2x4 output block (bi, bj)
-                            const int pp = tid >> 7, bi = (tid >> 3) & 15, bj = tid & 7;
-                            const int gi0 = ti0 + 2 * bi, gj0 = tj0 + 4 * bj;
-                            if (gi0 < Hl && gj0 < Wl) {
-                                f2x acc[2][4];
-                                conv_pair_2x4<K>(bs + pp * PTILE + (2 * bi) * PROW, bj,
-                                                 wsm + (1 + 2 * (l - 1) + pp) * WS, acc);
-                                if (l >= 3) {
-                                    float* zl = sm + a.o_zl[l];
-#pragma unroll
-                                    for (int o = 0; o < 2; ++o) {
-                                        if (gi0 + o >= Hl) continue;
-#pragma unroll
-                                        for (int q = 0; q < 4; ++q)
-                                            if (gj0 + q < Wl)
-                                                *reinterpret_cast<float2*>(
-                                                    zl + ((gi0 + o) * Wl + gj0 + q) * 4 + 2 * pp) =
-                                                    upk2(acc[o][q]);
-                                    }
-                                } else {
-#pragma unroll
-                                    for (int o = 0; o < 2; ++o) {
-                                        float* zr = zs + pp * ZTILE + (2 * bi + o) * ZROW + 8 * bj;
-                                        const float2 q0 = upk2(acc[o][0]), q1 = upk2(acc[o][1]);
-                                        const float2 q2 = upk2(acc[o][2]), q3 = upk2(acc[o][3]);
-                                        reinterpret_cast<float4*>(zr)[0] = make_float4(q0.x, q0.y, q1.x, q1.y);
-                                        reinterpret_cast<float4*>(zr)[1] = make_float4(q2.x, q2.y, q3.x, q3.y);
-                                    }
-                                }
-                            }
-                        }
-                        __syncthreads();
-                        if (l == 2) {
-                            // deep sums of this level-2 tile's positions
-                            float4* dsum = reinterpret_cast<float4*>(zslot);
-#pragma unroll
-                            for (int k = 0; k < (kCT * kCT) / kFT; ++k) {
-                                const int p = tid + k * kFT, ti = p >> 5, tj = p & 31;
-                                const int i2 = ti0 + ti, j2 = tj0 + tj;
-                                if (i2 >= Hl || j2 >= Wl) continue;
-                                const float2 za = *reinterpret_cast<const float2*>(zs + ti * ZROW + 2 * tj);
-                                const float2 zb = *reinterpret_cast<const float2*>(zs + ZTILE + ti * ZROW + 2 * tj);
-                                const float4 z = make_float4(za.x, za.y, zb.x, zb.y);
-                                float v = 0.f;
-                                for (int m = 3; m <= a.L; ++m) {
-                                    const int sh = m - 2, Wm = a.Wp >> m;
-                                    const float4 zm = reinterpret_cast<const float4*>(sm + a.o_zl[m])
-                                        [(i2 >> sh) * Wm + (j2 >> sh)];
-                                    v += synth_rt(zm, (i2 >> (m - 3)) & 1, (j2 >> (m - 3)) & 1);
-                                }
-                                dsum[(size_t)i2 * Wl + j2] =
-                                    make_float4(synth<0, 0>(z) + v, synth<0, 1>(z) + v,
-                                                synth<1, 0>(z) + v, synth<1, 1>(z) + v);
-                            }
-                        }
-                    }
-                }
-            }
+            if (deep_global)
+                deep_levels<K, true>(a, sm, zslot + 2 * a.zd_slot, u2, zslot);
+            else
+                deep_levels<K, false>(a, sm, sm, u2, zslot);
             fence_proxy_async_global();
             __syncthreads();
         }
@@ -390,7 +421,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
             failed = true;
             break;
         }
-        if (a.L >= 2 && a.use_tma && leader) {  // deep sums of the first tile
+        if (a.L >= 2 && use_tma && leader) {  // deep sums of the first tile
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(bar_d, kDBytes);
             tma_load_3d(dblk, &a.tmd, 0, 0, (int)blockIdx.x, bar_d);
@@ -401,7 +432,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
             const int y0 = ty * kTile, x0 = tx * kTile;
             float* dcur = dblk + (t & 1) * (kDBytes / 4);
             if (a.L >= 2) {
-                if (!a.use_tma) {
+                if (!use_tma) {
                     // plain copy of the 16x16 level-2 block of deep sums (zero outside)
                     const int H2 = a.Hp >> 2, W2 = a.Wp >> 2;
                     const float4* z2 = reinterpret_cast<const float4*>(zslot);
@@ -412,7 +443,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                     reinterpret_cast<float4*>(dcur)[tid] = v;
                 }
             }
-            if (a.use_tma) {
+            if (use_tma) {
                 // a timed-out wait converts stale data; the vote after the pass ends the kernel
                 const bool ok = mbar_wait_bounded(bar_x, ph_x);
                 ph_x ^= 1;
@@ -474,7 +505,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                 if (a.L >= 1) {
                     float4 d = f4_zero();
                     if (a.L >= 2) {
-                        if (a.use_tma) ok_d = mbar_wait_bounded(bar_d + db, (ph_d >> db) & 1u);
+                        if (use_tma) ok_d = mbar_wait_bounded(bar_d + db, (ph_d >> db) & 1u);
                         d = reinterpret_cast<const float4*>(dcur)[tid];
                     }
                     const float dv[2][2] = {{d.x, d.y}, {d.z, d.w}};
@@ -522,7 +553,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                                 IO<T>::st(yp + (size_t)(gy + o) * a.W + gx + q, acc[o][q]);
                 }
             }
-            if (a.L >= 2 && a.use_tma) ph_d ^= 1u << db;
+            if (a.L >= 2 && use_tma) ph_d ^= 1u << db;
             if (__syncthreads_or(!ok_d)) {
                 failed = true;
                 break;
@@ -592,6 +623,8 @@ struct FwdPlan {
 };
 
 constexpr size_t kErrWordBytes = 256;  // the workspace starts with the error word
+// shared memory per CTA that still lets two CTAs share an SM
+constexpr size_t kTwoCtaSmem = 228 * 1024 / 2 - 1024;
 
 template <int K, typename T>
 FwdPlan fwd_plan(const wt_desc& d) {
@@ -622,21 +655,36 @@ FwdPlan fwd_plan(const wt_desc& d) {
     a.o_x = alias0;
     a.o_dblk = round32(alias0 + FG<K>::XROWS * FG<K>::XPITCH);
     const int xend = a.o_dblk + ((L >= 2) ? 2 * kDBytes / 4 : 0);
-    int cp = alias0;
+    // deep-level state: carriers X^(2..L-1), then Z^(3..L), each 16-byte aligned
+    int deep = 0;
     for (int l = 0; l <= kMaxLevels; ++l) a.o_car[l] = a.o_zl[l] = 0;
     for (int l = 2; l < L; ++l) {
-        a.o_car[l] = cp;
-        cp += round4((hp >> l) * (wp >> l));
+        a.o_car[l] = deep;
+        deep += round4((hp >> l) * (wp >> l));
     }
     for (int l = 3; l <= L; ++l) {
-        a.o_zl[l] = cp;
-        cp += 4 * (hp >> l) * (wp >> l);
+        a.o_zl[l] = deep;
+        deep += 4 * (hp >> l) * (wp >> l);
     }
-    const int total = xend > cp ? xend : cp;
+    // it stays in shared memory unless it would lower the occupancy the tiles alone allow
+    // (two CTAs per SM when they fit it, else one) or not fit at all; then it moves to the
+    // CTA's workspace slot, and shared memory holds the tiles only
+    const int local_end = alias0 + deep > xend ? alias0 + deep : xend;
+    const size_t limit =
+        ((size_t)xend * sizeof(float) <= kTwoCtaSmem) ? kTwoCtaSmem : kMaxSmemPerBlock;
+    a.deep_global = (deep > 0 && (size_t)local_end * sizeof(float) > limit) ? 1 : 0;
+    int total = xend;
+    if (!a.deep_global) {
+        for (int l = 2; l <= L; ++l) {
+            a.o_car[l] += alias0;
+            a.o_zl[l] += alias0;
+        }
+        total = local_end;
+    }
     p.smem = (size_t)total * sizeof(float);
-    // per CTA: deep sums and level-2 subbands, each [H/4][W/4][4] fp32
+    // per CTA: deep sums and level-2 subbands, each [H/4][W/4][4] fp32 (+ the deep state)
     a.zd_slot = (L >= 2) ? ((4LL * (hp >> 2) * (wp >> 2) + 63) & ~63LL) : 0;
-    a.slot = 2 * a.zd_slot;
+    a.slot = 2 * a.zd_slot + (a.deep_global ? (((long long)deep + 63) & ~63LL) : 0);
     const long long planes = (long long)d.n * d.c;
     int occ = (int)((228 * 1024) / (p.smem + 1024));
     if (occ > 2) occ = 2;
@@ -704,7 +752,8 @@ wt_status launch_fwd_k(const wt_desc& d, const void* x, const float* w0f, const 
         if (cudaGetLastError() != cudaSuccess) return WT_ERR_CUDA;
         ++*launches;
     }
-    auto kern = wt_fwd_plane_kernel<K, T>;
+    const bool fast = a.use_tma && a.vec && a.H == a.Hp && a.W == a.Wp && !a.deep_global;
+    auto kern = fast ? wt_fwd_plane_kernel<K, T, true> : wt_fwd_plane_kernel<K, T, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) !=
         cudaSuccess)
         return WT_ERR_CUDA;

@@ -382,7 +382,7 @@ __device__ __forceinline__ void load_block4x4(const T* xp, int H, int W, int vec
     if (vec && r0 + 3 < H && c0 + 3 < W) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) r[q] = IO<T>::ld4(xp + (size_t)(r0 + q) * W + c0);
-    } else {
+    } else {  // edge of the plane or unaligned rows: element loads
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             float e[4];
@@ -397,15 +397,21 @@ __device__ __forceinline__ void load_block4x4(const T* xp, int H, int W, int vec
 
 // Level-l (l >= 2) carrier 2x2 block feeding subband cell (gi, gj): from X itself when
 // l == 2 (its 4x4 pixel block, through the level-1 carrier; zero outside the H x W plane),
-// else from the carrier X^(l-1) of width Wp in shared memory. Values are Eq. 5's
-// normalized low-pass carrier.
-template <typename T>
+// else from the carrier X^(l-1) of width Wp. Values are Eq. 5's normalized low-pass
+// carrier. EXACT: the plane has 4-aligned rows and needs no padding at level 2, so every
+// block lies inside it and is read with vector loads.
+template <typename T, bool EXACT>
 __device__ __forceinline__ void carrier_block(int l, const T* xp, int H, int W, int vec,
                                               const float* carp, int Wp, int gi, int gj,
                                               float& ca, float& cb, float& cc, float& cd) {
     if (l == 2) {
         float4 r[4];
-        load_block4x4<T>(xp, H, W, vec, 4 * gi, 4 * gj, r);
+        if (EXACT) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) r[q] = IO<T>::ld4(xp + (size_t)(4 * gi + q) * W + 4 * gj);
+        } else {
+            load_block4x4<T>(xp, H, W, vec, 4 * gi, 4 * gj, r);
+        }
         ca = 0.5f * (r[0].x + r[0].y + r[1].x + r[1].y);
         cb = 0.5f * (r[0].z + r[0].w + r[1].z + r[1].w);
         cc = 0.5f * (r[2].x + r[2].y + r[3].x + r[3].y);

@@ -43,6 +43,11 @@ struct DwArgs {
     int vec, use_tma;
     int KP;
     int o_bar, o_rawx, o_rawg, o_acc, o_red, o_xb, o_gb, o_x, o_g;  // shared memory (floats)
+    // deep carriers X^(l), dY^(l) (l = 2..L-1): in shared memory, or (deep_global) in a
+    // per-plane region of car_floats floats at car + plane * car_floats
+    int deep_global;
+    float* car;
+    long long car_floats;
     int o_carx[kMaxLevels + 1], o_cary[kMaxLevels + 1];
 };
 
@@ -53,19 +58,20 @@ constexpr int kGTile = kCT * kGRow;   // floats per pair tile
 
 // Deep stage for level l: X subbands with an R halo into the X pair tiles, dY subbands of
 // the tile's own cells into the dY pair tiles; carriers X^(l), dY^(l) for l < L.
-template <int K, typename T>
+template <int K, typename T, bool FAST>
 __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const T* xp, const T* gp,
-                                              float* sm, int l, int ti0, int tj0) {
+                                              float* sm, float* cbase, int l, int ti0,
+                                              int tj0) {
     constexpr int R = FG<K>::R, BT = FG<K>::BT;
     constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, PHALF = PG<K>::PHALF;
     constexpr int NIT = (BT * BT + kDT - 1) / kDT;
     const int Hl = a.Hp >> l, Wl = a.Wp >> l, Wp = a.Wp >> (l - 1);
     float* xb = sm + a.o_xb;
     float* gb = sm + a.o_gb;
-    const float* cpx = (l >= 3) ? sm + a.o_carx[l - 1] : nullptr;
-    const float* cpy = (l >= 3) ? sm + a.o_cary[l - 1] : nullptr;
-    float* clx = (l < a.L) ? sm + a.o_carx[l] : nullptr;
-    float* cly = (l < a.L) ? sm + a.o_cary[l] : nullptr;
+    const float* cpx = (l >= 3) ? cbase + a.o_carx[l - 1] : nullptr;
+    const float* cpy = (l >= 3) ? cbase + a.o_cary[l - 1] : nullptr;
+    float* clx = (l < a.L) ? cbase + a.o_carx[l] : nullptr;
+    float* cly = (l < a.L) ? cbase + a.o_cary[l] : nullptr;
 #pragma unroll
     for (int it = 0; it < NIT; ++it) {
         const int idx = threadIdx.x + it * kDT;
@@ -76,11 +82,11 @@ __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const T* xp, cons
         float4 ux = f4_zero(), ug = f4_zero();
         if (gi >= 0 && gi < Hl && gj >= 0 && gj < Wl) {
             float ca, cb, cc, cd;
-            carrier_block<T>(l, xp, a.H, a.W, a.vec, cpx, Wp, gi, gj, ca, cb, cc, cd);
+            carrier_block<T, FAST>(l, xp, a.H, a.W, a.vec, cpx, Wp, gi, gj, ca, cb, cc, cd);
             ux = haar_u(ca, cb, cc, cd);
             if (inner) {
                 if (clx) clx[gi * Wl + gj] = 0.5f * ux.x;
-                carrier_block<T>(l, gp, a.H, a.W, a.vec, cpy, Wp, gi, gj, ca, cb, cc, cd);
+                carrier_block<T, FAST>(l, gp, a.H, a.W, a.vec, cpy, Wp, gi, gj, ca, cb, cc, cd);
                 ug = haar_u(ca, cb, cc, cd);
                 if (cly) cly[gi * Wl + gj] = 0.5f * ug.x;
             }
@@ -98,9 +104,11 @@ __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const T* xp, cons
 }
 
 // Widen the TMA-staged raw dY tile (64x64) to the fp32 dY tile and, when `bands`, form
-// its level-1 unnormalized subbands in the dY pair tiles. One item = 2x4 pixels.
+// its level-1 unnormalized subbands in the dY pair tiles. One item = 2x4 pixels. Returns
+// this thread's sum of the dY values it converted.
 template <typename T>
-__device__ __forceinline__ void convert_raw_dy(const T* raw, float* gs, float* gb, bool bands) {
+__device__ __forceinline__ float convert_raw_dy(const T* raw, float* gs, float* gb, bool bands) {
+    float sum = 0.f;
     for (int idx = threadIdx.x; idx < kCT * (kCT / 2); idx += blockDim.x) {
         const int ci = idx >> 4, m = idx & 15;
         const T* r0 = raw + (2 * ci) * kTile + 4 * m;
@@ -109,6 +117,7 @@ __device__ __forceinline__ void convert_raw_dy(const T* raw, float* gs, float* g
         float* d0 = gs + (2 * ci) * kTile + 4 * m;
         *reinterpret_cast<float4*>(d0) = make_float4(a0.x, a0.y, a1.x, a1.y);
         *reinterpret_cast<float4*>(d0 + kTile) = make_float4(b0.x, b0.y, b1.x, b1.y);
+        sum += ((a0.x + a0.y) + (a1.x + a1.y)) + ((b0.x + b0.y) + (b1.x + b1.y));
         if (bands) {
             const float4 u = haar_u(a0.x, a0.y, b0.x, b0.y);
             const float4 v = haar_u(a1.x, a1.y, b1.x, b1.y);
@@ -117,12 +126,15 @@ __device__ __forceinline__ void convert_raw_dy(const T* raw, float* gs, float* g
             *reinterpret_cast<float4*>(q + kGTile) = make_float4(u.z, u.w, v.z, v.w);
         }
     }
+    return sum;
 }
 
 // Non-TMA staging of the dY tile (fp32 tile + pair tiles), zero outside the plane.
+// Returns this thread's sum of the dY values it staged.
 template <typename T>
-__device__ __forceinline__ void stage_dy_plain(const T* gp, int H, int W, float* gs, float* gb,
-                                               bool bands, int y0, int x0) {
+__device__ __forceinline__ float stage_dy_plain(const T* gp, int H, int W, float* gs, float* gb,
+                                                bool bands, int y0, int x0) {
+    float sum = 0.f;
     for (int idx = threadIdx.x; idx < kCT * kCT; idx += blockDim.x) {
         const int ci = idx / kCT, cj = idx - ci * kCT;
         float v[4];
@@ -133,6 +145,7 @@ __device__ __forceinline__ void stage_dy_plain(const T* gp, int H, int W, float*
         }
         float* d0 = gs + (2 * ci) * kTile + 2 * cj;
         d0[0] = v[0]; d0[1] = v[1]; d0[kTile] = v[2]; d0[kTile + 1] = v[3];
+        sum += (v[0] + v[1]) + (v[2] + v[3]);
         if (bands) {
             const float4 u = haar_u(v[0], v[1], v[2], v[3]);
             float* q = gb + ci * kGRow + 4 * pchunk(cj >> 1, kGHalf) + 2 * (cj & 1);
@@ -140,6 +153,18 @@ __device__ __forceinline__ void stage_dy_plain(const T* gp, int H, int W, float*
             *reinterpret_cast<float2*>(q + kGTile) = make_float2(u.z, u.w);
         }
     }
+    return sum;
+}
+
+// One compensated (Kahan) step of this thread's running sum red[tid] (with its
+// compensation in red[blockDim.x + tid]): sum += v.
+__device__ __forceinline__ void kahan_add(float* red, float v) {
+    const int t = threadIdx.x, n = blockDim.x;
+    const float s = red[t], c = red[n + t];
+    const float y = v - c;
+    const float u = s + y;
+    red[n + t] = (u - s) - y;
+    red[t] = u;
 }
 
 // Recursive-halving warp reduction of 32 values: lane l ends with the warp total of
@@ -183,7 +208,9 @@ __device__ __forceinline__ void warp_totals_to(const f2x (&acc)[NQ], float extra
     }
 }
 
-template <int K, typename T>
+// FAST: the plane is TMA-staged, has 4-aligned rows, needs no padding and keeps its deep
+// carriers in shared memory, so those checks and the other paths are compiled out.
+template <int K, typename T, bool FAST>
 __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(const __grid_constant__ DwArgs a) {
     constexpr int R = FG<K>::R, KK = FG<K>::KK, PAD = FG<K>::PAD, XP = FG<K>::XPITCH;
     constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE;
@@ -198,8 +225,9 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
     float* gb = sm + a.o_gb;
     float* xs = sm + a.o_x;
     float* gs = sm + a.o_g;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const bool leader = tid == 0;
+    const bool use_tma = FAST || a.use_tma;
 
     const int c = blockIdx.x, n = blockIdx.y;
     const long long plane = (long long)n * a.C + c;
@@ -211,12 +239,12 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
     constexpr int BYTES = XBox<K, T>::BYTES + kTile * kTile * (int)sizeof(T);
 
     for (int e = tid; e < a.KP; e += kDT) acc_sm[e] = 0.f;
-    if (a.use_tma && leader) {
+    if (use_tma && leader) {
         mbar_init(bar, 1);
         fence_mbar_init();
     }
     __syncthreads();
-    if (a.use_tma && leader) {  // first tile, in flight during the deep levels
+    if (use_tma && leader) {  // first tile, in flight during the deep levels
         mbar_arrive_expect_tx(bar, BYTES);
         tma_load_3d(rawx, &a.tmx, -XBox<K, T>::XOFF, -2 * R, (int)plane, bar);
         tma_load_3d(rawg, &a.tmg, 0, 0, (int)plane, bar);
@@ -224,6 +252,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
     uint32_t ph = 0;
 
     // ---- deep levels l = 2..L: band pair pp = tid / 128, 2x4 block per thread ----
+    float* cbase = (!FAST && a.deep_global) ? a.car + plane * a.car_floats : sm;  // carriers
     for (int l = 2; l <= a.L; ++l) {
         const int Hl = a.Hp >> l, Wl = a.Wp >> l;
         const int pp = tid >> 7, bi = (tid >> 3) & 15, bj = tid & 7;
@@ -232,7 +261,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
         for (int q = 0; q < KK; ++q) accd[q] = 0ull;
         for (int ti0 = 0; ti0 < Hl; ti0 += kCT) {
             for (int tj0 = 0; tj0 < Wl; tj0 += kCT) {
-                dw_deep_stage<K, T>(a, xp, gp, sm, l, ti0, tj0);
+                dw_deep_stage<K, T, FAST>(a, xp, gp, sm, cbase, l, ti0, tj0);
                 __syncthreads();
                 if (ti0 + 2 * bi < Hl && tj0 + 4 * bj < Wl) {
                     f2x g[2][4];
@@ -268,12 +297,18 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
     f2x acc[KK];
 #pragma unroll
     for (int q = 0; q < KK; ++q) acc[q] = 0ull;
-    float dbs = 0.f;
+    // sum of dY, taken while converting the dY tiles: a register partial over at most 16
+    // tiles, folded into a compensated (Kahan) running sum so that planes of millions of
+    // pixels keep the fp32 sum accurate to a few ulps. The running sum and its compensation
+    // live in this thread's two words of `red` (idle until the final flush).
+    red[tid] = 0.f;
+    red[kDT + tid] = 0.f;
+    float dpart = 0.f;
     bool failed = false;
     for (int t = 0; t < ntiles; ++t) {
         const int ty = t / tiles_x, tx = t - ty * tiles_x;
         const int y0 = ty * kTile, x0 = tx * kTile;
-        if (a.use_tma) {
+        if (use_tma) {
             const bool ok = mbar_wait_bounded(bar, ph);
             ph ^= 1;
             if (__syncthreads_or(!ok)) {
@@ -281,7 +316,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
                 break;
             }
             convert_raw<K, T>(rawx, xs, xb, a.L >= 1);
-            convert_raw_dy<T>(rawg, gs, gb, a.L >= 1);
+            dpart += convert_raw_dy<T>(rawg, gs, gb, a.L >= 1);
             __syncthreads();
             if (leader && t + 1 < ntiles) {
                 const int ny = (t + 1) / tiles_x, nx = (t + 1) - ny * tiles_x;
@@ -293,12 +328,16 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
             }
         } else {
             stage_tile<K, T>(xp, a.H, a.W, a.vec, xs, y0, x0);
-            stage_dy_plain<T>(gp, a.H, a.W, gs, gb, a.L >= 1, y0, x0);
+            dpart += stage_dy_plain<T>(gp, a.H, a.W, gs, gb, a.L >= 1, y0, x0);
             __syncthreads();
             if (a.L >= 1) {
                 pair_bands_from_tile<K>(xs, xb);
                 __syncthreads();
             }
+        }
+        if ((t & 15) == 15 || t + 1 == ntiles) {
+            kahan_add(red, dpart);
+            dpart = 0.f;
         }
         if (base_role) {
             const int nb = (a.L == 0) ? 1 : 2;
@@ -312,7 +351,6 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
                     const float4 tv = *reinterpret_cast<const float4*>(gs + (4 * by + o) * kTile + 4 * bx);
                     g[o][0] = pk2(tv.x, tv.y);
                     g[o][1] = pk2(tv.z, tv.w);
-                    dbs += (tv.x + tv.y) + (tv.z + tv.w);
                 }
                 corr_base_4x4<K>(xs + (4 * by + R) * XP + 4 * bx + R + PAD, XP, g, acc);
             }
@@ -341,14 +379,20 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
     }
 
     // ---- flush: fixed-order reductions into acc_sm, then the partial vector ----
+    const float dbs = red[tid] - red[kDT + tid];
+    __syncthreads();  // every thread has read its sum before `red` takes the warp totals
     warp_totals_to<KK, 2 * KK + 1>(acc, dbs, red + warp * 128);
     __syncthreads();
     const int nbase = (a.L == 0) ? 8 : 4;
     for (int e = tid; e <= KK; e += kDT) {
-        // base taps: even + odd column halves of each base warp; e == KK: the bias sum
+        // base taps: even + odd column halves of each base warp; e == KK: the sum of dY,
+        // which every warp holds a share of (it is taken while converting the dY tiles)
         float s = 0.f;
-        for (int w = 0; w < nbase; ++w)
-            s += (e < KK) ? (red[w * 128 + 2 * e] + red[w * 128 + 2 * e + 1]) : red[w * 128 + 2 * KK];
+        if (e < KK) {
+            for (int w = 0; w < nbase; ++w) s += red[w * 128 + 2 * e] + red[w * 128 + 2 * e + 1];
+        } else {
+            for (int w = 0; w < kDT / 32; ++w) s += red[w * 128 + 2 * KK];
+        }
         acc_sm[e] += s;
     }
     if (a.L >= 1) {
@@ -413,6 +457,9 @@ int round4(int v) { return (v + 3) & ~3; }
 int round32(int v) { return (v + 31) & ~31; }
 
 constexpr size_t kDwErrBytes = 256;  // the workspace starts with a status word
+constexpr size_t kTwoCtaSmem = 228 * 1024 / 2 - 1024;  // two CTAs per SM still fit
+
+size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
 
 template <int K, typename T>
 void dw_layout(const wt_desc& d, DwArgs& a, size_t& smem_bytes) {
@@ -442,7 +489,7 @@ void dw_layout(const wt_desc& d, DwArgs& a, size_t& smem_bytes) {
     off = round4(off);
     a.o_g = off;
     off += kTile * kTile;
-    int cp = alias0;
+    int cp = 0;
     for (int l = 0; l <= kMaxLevels; ++l) a.o_carx[l] = a.o_cary[l] = 0;
     for (int l = 2; l < L; ++l) {
         const int sz = round4((padded_side(d.h, d.levels) >> l) *
@@ -452,16 +499,31 @@ void dw_layout(const wt_desc& d, DwArgs& a, size_t& smem_bytes) {
         a.o_cary[l] = cp;
         cp += sz;
     }
-    const int total = off > cp ? off : cp;
+    // the carriers stay in shared memory unless they would lower the occupancy the tiles
+    // alone allow (two CTAs per SM for k <= 5 when the tiles fit it, else one) or not fit
+    // at all; then they move to the workspace
+    const size_t two = (K >= 7) ? kMaxSmemPerBlock : kTwoCtaSmem;
+    const size_t limit = ((size_t)off * sizeof(float) <= two) ? two : kMaxSmemPerBlock;
+    const int local_end = alias0 + cp > off ? alias0 + cp : off;
+    a.deep_global = (cp > 0 && (size_t)local_end * sizeof(float) > limit) ? 1 : 0;
+    a.car_floats = a.deep_global ? (((long long)cp + 63) & ~63LL) : 0;
+    if (!a.deep_global)
+        for (int l = 2; l < L; ++l) {
+            a.o_carx[l] += alias0;
+            a.o_cary[l] += alias0;
+        }
+    const int total = a.deep_global ? off : local_end;
     smem_bytes = (size_t)total * sizeof(float);
 }
 
 // Fill the kernel arguments (layout, pointers, tensor maps) for one launch.
 template <int K, typename T>
-bool dw_prepare(const wt_desc& d, const void* x, const void* dy, float* part, int* err,
-                DwArgs& a, size_t& smem) {
+bool dw_prepare(const wt_desc& d, const void* x, const void* dy, float* part, float* car,
+                int* err, DwArgs& a, size_t& smem) {
     dw_layout<K, T>(d, a, smem);
     if (smem > kMaxSmemPerBlock) return false;
+    if (a.deep_global && car == nullptr) return false;
+    a.car = car;
     a.x = x;
     a.dy = dy;
     a.part = part;
@@ -492,7 +554,8 @@ bool dw_prepare(const wt_desc& d, const void* x, const void* dy, float* part, in
 template <int K, typename T>
 wt_status launch_dw_plane(const DwArgs& a, size_t smem, const wt_desc& d, cudaStream_t stream,
                           int* launches) {
-    auto kern = wt_dw_plane_kernel<K, T>;
+    const bool fast = a.use_tma && a.vec && a.H == a.Hp && a.W == a.Wp && !a.deep_global;
+    auto kern = fast ? wt_dw_plane_kernel<K, T, true> : wt_dw_plane_kernel<K, T, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return WT_ERR_CUDA;
@@ -508,13 +571,17 @@ wt_status launch_dw_k(const wt_desc& d, const void* x, const void* dy, const flo
                       float* dw0, float* db0, float* ds0, float* dwl, float* dsl, void* ws,
                       size_t ws_bytes, cudaStream_t stream, int* launches) {
     const int KP = FG<K>::KK + 1 + 4 * FG<K>::KK * d.levels;
-    const size_t need = kDwErrBytes + (size_t)d.c * d.n * KP * sizeof(float);
+    const size_t part_bytes = round256((size_t)d.c * d.n * KP * sizeof(float));
+    DwArgs a;
+    size_t smem = 0;
+    dw_layout<K, T>(d, a, smem);
+    const size_t need = kDwErrBytes + part_bytes +
+                        (size_t)d.c * d.n * (size_t)a.car_floats * sizeof(float);
     if (ws == nullptr || ws_bytes < need) return WT_ERR_WORKSPACE;
     int* err = reinterpret_cast<int*>(ws);
     float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + kDwErrBytes);
-    DwArgs a;
-    size_t smem = 0;
-    if (!dw_prepare<K, T>(d, x, dy, part, err, a, smem)) return WT_ERR_UNSUPPORTED;
+    float* car = reinterpret_cast<float*>(static_cast<char*>(ws) + kDwErrBytes + part_bytes);
+    if (!dw_prepare<K, T>(d, x, dy, part, car, err, a, smem)) return WT_ERR_UNSUPPORTED;
     if (cudaMemsetAsync(err, 0, sizeof(int), stream) != cudaSuccess) return WT_ERR_CUDA;
     wt_status st = launch_dw_plane<K, T>(a, smem, d, stream, launches);
     if (st != WT_OK) return st;
@@ -530,7 +597,8 @@ wt_status launch_dw_partials_k(const wt_desc& d, const void* x, const void* dy, 
                                cudaStream_t stream, int* launches) {
     DwArgs a;
     size_t smem = 0;
-    if (!dw_prepare<K, T>(d, x, dy, part, nullptr, a, smem)) return WT_ERR_UNSUPPORTED;
+    // (no carrier region here: shapes whose carriers need the workspace are unsupported)
+    if (!dw_prepare<K, T>(d, x, dy, part, nullptr, nullptr, a, smem)) return WT_ERR_UNSUPPORTED;
     return launch_dw_plane<K, T>(a, smem, d, stream, launches);
 }
 
@@ -571,25 +639,36 @@ size_t dw_partial_floats(const wt_desc& d) {
     return (size_t)KK + 1 + 4 * (size_t)KK * d.levels;
 }
 
-size_t backward_weight_ws_bytes(const wt_desc& d) {
-    return kDwErrBytes + (size_t)d.c * d.n * dw_partial_floats(d) * sizeof(float);
-}
-
-size_t backward_weight_smem_bytes(const wt_desc& d) {
-    DwArgs a;
-    size_t smem = 0;
+namespace {
+// Layout of the plane kernel for d (shared memory bytes and the carriers' placement).
+bool dw_plan(const wt_desc& d, DwArgs& a, size_t& smem) {
     switch (d.k) {
 #define WT_CASE(KV)                                                                          \
     case KV:                                                                                 \
         with_io_type(d.io, [&](auto t) { dw_layout<KV, decltype(t)>(d, a, smem); return 0; }); \
-        break;
+        return true;
         WT_CASE(1)
         WT_CASE(3)
         WT_CASE(5)
         WT_CASE(7)
 #undef WT_CASE
-        default: return 0;
+        default: return false;
     }
+}
+}  // namespace
+
+size_t backward_weight_ws_bytes(const wt_desc& d) {
+    DwArgs a;
+    size_t smem = 0;
+    if (!dw_plan(d, a, smem)) return 0;
+    return kDwErrBytes + round256((size_t)d.c * d.n * dw_partial_floats(d) * sizeof(float)) +
+           (size_t)d.c * d.n * (size_t)a.car_floats * sizeof(float);
+}
+
+size_t backward_weight_smem_bytes(const wt_desc& d) {
+    DwArgs a;
+    size_t smem = 0;
+    if (!dw_plan(d, a, smem)) return 0;
     return smem;
 }
 

@@ -91,7 +91,15 @@ ODD = [  # sides that are not multiples of 2^L: carriers zero-padded per level
 ]
 
 
-@pytest.mark.parametrize("n,c,h,w,k,L,dtype", EDGE + F16 + ODD)
+LARGE = [  # planes whose deep-level state no longer fits in shared memory
+    (1, 2, 512, 512, 5, 5, "bf16"),   # the pages' largest sweep plane at L = 5
+    (1, 1, 1024, 1024, 3, 5, "f32"),
+    (1, 1, 512, 512, 7, 5, "f16"),
+    (1, 1, 520, 500, 5, 4, "f32"),    # large and not a multiple of 2^L
+]
+
+
+@pytest.mark.parametrize("n,c,h,w,k,L,dtype", EDGE + F16 + ODD + LARGE)
 def test_edge_shapes(n, c, h, w, k, L, dtype):
     wl = shape_workload(n, c, h, w, k, L, dtype, seed=1000 + h + w + k + L)
     errs, _ = run_and_compare(wl, bias_and_scale=True)
