@@ -254,8 +254,12 @@ __device__ __forceinline__ void deep_levels(const FwdArgs& a, float* sm, float* 
                 deep_stage<K>(a, u2, sm, deep, l, ti0, tj0);
                 __syncthreads();
                 {
-                    // band pair pp = tid / 128, 2x4 output block (bi, bj)
-                    const int pp = tid >> 7, bi = (tid >> 3) & 15, bj = tid & 7;
+                    // band pair pp, 2x4 output block (bi, bj); at level 2 warp w takes rows
+                    // 4w..4w+3 of both pairs, the rows whose deep sums it forms below
+                    const int lane = tid & 31;
+                    const int pp = (l == 2) ? lane >> 4 : tid >> 7;
+                    const int bi = (l == 2) ? 2 * (tid >> 5) + ((lane >> 3) & 1) : (tid >> 3) & 15;
+                    const int bj = tid & 7;
                     const int gi0 = ti0 + 2 * bi, gj0 = tj0 + 4 * bj;
                     if (gi0 < Hl && gj0 < Wl) {
                         f2x acc[2][4];
@@ -285,13 +289,13 @@ __device__ __forceinline__ void deep_levels(const FwdArgs& a, float* sm, float* 
                         }
                     }
                 }
-                __syncthreads();
                 if (l == 2) {
-                    // deep sums of this level-2 tile's positions
+                    // deep sums of this level-2 tile's positions: warp w, rows 4w..4w+3
+                    __syncwarp();
                     float4* dsum = reinterpret_cast<float4*>(zslot);
 #pragma unroll
                     for (int k = 0; k < (kCT * kCT) / kFT; ++k) {
-                        const int p = tid + k * kFT, ti = p >> 5, tj = p & 31;
+                        const int ti = 4 * (tid >> 5) + k, tj = tid & 31;
                         const int i2 = ti0 + ti, j2 = tj0 + tj;
                         if (i2 >= Hl || j2 >= Wl) continue;
                         const float2 za = *reinterpret_cast<const float2*>(zs + ti * ZROW + 2 * tj);
@@ -309,6 +313,7 @@ __device__ __forceinline__ void deep_levels(const FwdArgs& a, float* sm, float* 
                                         synth<1, 0>(z) + v, synth<1, 1>(z) + v);
                     }
                 }
+                __syncthreads();  // the band-pair tiles are free for the next stage
             }
         }
     }
@@ -474,8 +479,12 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                 }
             }
             if (a.L >= 1) {
-                // level-1 filters: 2 band pairs x 128 blocks of 2x4 coefficients, one per thread
-                const int pp = tid >> 7, bi = (tid >> 3) & 15, bj = tid & 7;
+                // level-1 filters: 2 band pairs x 128 blocks of 2x4 coefficients, one per
+                // thread. Warp w filters coefficient rows 4w..4w+3 of both pairs, exactly the
+                // rows that its own threads' 4x4 pixel blocks synthesize below, so a warp
+                // barrier hands them over.
+                const int lane = tid & 31;
+                const int pp = lane >> 4, bi = 2 * (tid >> 5) + ((lane >> 3) & 1), bj = lane & 7;
                 if (y0 / 2 + 2 * bi < (a.H + 1) / 2 && x0 / 2 + 4 * bj < (a.W + 1) / 2) {
                     f2x acc[2][4];
                     conv_pair_2x4<K>(bs + pp * PTILE + (2 * bi) * PROW, bj, wsm + (1 + pp) * WS,
@@ -489,7 +498,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                         reinterpret_cast<float4*>(zr)[1] = make_float4(q2.x, q2.y, q3.x, q3.y);
                     }
                 }
-                __syncthreads();
+                __syncwarp();
             }
             // the deep sums are waited for just before their use; the wait is voted on at the
             // end of the tile
