@@ -43,6 +43,7 @@ struct FwdArgs {
     const float* wimg;  // per channel, the shared-memory image of its folded weights
     float* zd;         // scratch: per CTA the deep sums, then the level-2 subbands
     int* err;          // first word of the workspace: set on a stuck TMA wait
+    int* next;         // second word: the next plane to hand out (zeroed before the launch)
     long long zd_slot;  // floats of each of the two arrays of a CTA's slot
     long long slot;     // floats between consecutive CTAs' slots (2 * zd_slot + deep state)
     long long planes;
@@ -99,21 +100,6 @@ struct SweepBox {
     static constexpr int NBUF = 4;
     static_assert((BW / 4) * (BH / 4) <= 256, "one level-2 position per thread");
 };
-
-__device__ __forceinline__ int sweep_boxes(int H, int W, int bw, int bh) {
-    return ((W + bw - 1) / bw) * ((H + bh - 1) / bh);
-}
-
-// Level-2 subbands (unnormalized) and carrier of the 4x4 pixel block r0..r3 (Eq. 5 applied
-// to the pixels gives X^(1) = LL; applied again to the 2x2 block of X^(1) it gives level 2).
-__device__ __forceinline__ float4 level2_block(const float4& r0, const float4& r1,
-                                               const float4& r2, const float4& r3) {
-    const float ca = 0.5f * (r0.x + r0.y + r1.x + r1.y);
-    const float cb = 0.5f * (r0.z + r0.w + r1.z + r1.w);
-    const float cc = 0.5f * (r2.x + r2.y + r3.x + r3.y);
-    const float cd = 0.5f * (r2.z + r2.w + r3.z + r3.w);
-    return haar_u(ca, cb, cc, cd);
-}
 
 // Level-2 sweep: the unnormalized subbands of every level-2 position go to u2
 // [H/4][W/4][4] (LL, LH, HL, HH) and, when L >= 3, the carrier X^(2) = LL / 2 to shared
@@ -371,7 +357,10 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
         return !__syncthreads_or(!ok);
     };
 
-    for (long long plane = blockIdx.x; plane < a.planes; plane += gridDim.x) {
+    // planes: first blockIdx.x, then whichever is next in the shared counter (planes are
+    // independent, so the order does not change any result), else a fixed stride
+    int* s_next = reinterpret_cast<int*>(sm + a.o_bar + 16);
+    for (long long plane = blockIdx.x; plane < a.planes;) {
         const int c = (int)(plane % a.C);
         const T* xp = reinterpret_cast<const T*>(a.x) + plane * plane_elems;
         T* yp = reinterpret_cast<T*>(a.y) + plane * plane_elems;
@@ -569,6 +558,10 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
             }
         }
         if (failed) break;
+        if (leader)
+            *s_next = (a.next != nullptr) ? (int)gridDim.x + atomicAdd(a.next, 1) : -1;
+        __syncthreads();
+        plane = (a.next != nullptr) ? (long long)*s_next : plane + gridDim.x;
     }
     if (failed && leader && a.err != nullptr) atomicExch(a.err, kErrTmaTimeout);
 }
@@ -719,6 +712,7 @@ wt_status launch_fwd_k(const wt_desc& d, const void* x, const float* w0f, const 
     a.y = y;
     a.b0f = flip ? nullptr : b0f;
     a.err = reinterpret_cast<int*>(ws);
+    a.next = a.err + 1;
     float* wimg = reinterpret_cast<float*>(static_cast<char*>(ws) + kErrWordBytes);
     a.wimg = wimg;
     a.zd = reinterpret_cast<float*>(static_cast<char*>(ws) + kErrWordBytes + p.img_bytes);
@@ -752,7 +746,7 @@ wt_status launch_fwd_k(const wt_desc& d, const void* x, const float* w0f, const 
         }
         a.use_tma = ok ? 1 : 0;
     }
-    if (cudaMemsetAsync(a.err, 0, sizeof(int), stream) != cudaSuccess) return WT_ERR_CUDA;
+    if (cudaMemsetAsync(a.err, 0, 2 * sizeof(int), stream) != cudaSuccess) return WT_ERR_CUDA;
     {
         const long long n = (long long)d.c * a.img;
         const int blocks = (int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);

@@ -62,9 +62,13 @@ wt_status launch_backward_weight(const wt_desc& d, const void* x, const void* dy
                                  cudaStream_t stream, int* launches);
 size_t backward_weight_ws_bytes(const wt_desc& d);
 // pieces of the backward-weight path: the per-plane partial kernel alone (partials
-// [C][d.n][KP] to `part`) and the reduce + unfold kernel alone over [C][groups][KP]
+// [C][d.n][KP] to `part`; its CTAs' level-2 scratch slots, backward_weight_slot_bytes each,
+// in [slots, slots + slots_bytes), the grid shrinking to the slots that fit) and the
+// reduce + unfold kernel alone over [C][groups][KP]
 wt_status launch_dw_partials(const wt_desc& d, const void* x, const void* dy, float* part,
-                             cudaStream_t stream, int* launches);
+                             float* slots, size_t slots_bytes, cudaStream_t stream,
+                             int* launches);
+size_t backward_weight_slot_bytes(const wt_desc& d);
 wt_status launch_dw_reduce(const wt_desc& d, const float* part, int groups, const float* w0,
                            const float* b0, const float* s0, const float* wl, const float* sl,
                            float* dw0, float* db0, float* ds0, float* dwl, float* dsl,

@@ -7,9 +7,10 @@
 // the library (kNoAllocScratchBytes, 4 MiB). Every GPU that loads the library holds that
 // array until the process exits.
 //
-// The scratch holds the per-channel running totals [C][KP] followed by the per-plane
-// partial vectors of one chunk of images [C][nc][KP] (KP = k*k + 1 + 4 k*k L). The batch
-// is processed in chunks of nc images, as many as fit; each chunk runs the ordinary
+// The scratch holds the per-channel running totals [C][KP], the per-plane partial vectors
+// of one chunk of images [C][nc][KP] (KP = k*k + 1 + 4 k*k L), and the level-2 scratch
+// slots of the plane kernel's CTAs (when L >= 2; the kernel runs as many CTAs as slots
+// fit). The batch is processed in chunks of nc images; each chunk runs the ordinary
 // per-plane partial kernel, then a small kernel folds the chunk into the totals (the
 // first chunk overwrites them, so nothing needs clearing beforehand), and finally the
 // ordinary reduce + unfold kernel turns the totals into gradients.
@@ -94,19 +95,32 @@ extern "C" wt_status wtconv_backward_weight_noalloc(const wt_desc* desc, const v
                              !aligned4(dwl) || !aligned4(dsl)))
         return WT_ERR_INVALID_ARG;
 
-    // sizes: totals [C][KP], then one chunk of partial vectors [C][nc][KP]
+    // sizes: totals [C][KP], then one chunk of partial vectors [C][nc][KP], then the
+    // plane kernel's level-2 scratch slots (as many CTAs' as fit, up to one per plane of
+    // the chunk or two per SM, whichever is fewer; at least one)
     const size_t KP = dw_partial_floats(*desc);
     const size_t per_image = (size_t)desc->c * KP;
     const size_t totals_floats = (per_image + 63) & ~size_t(63);
-    if (totals_floats + per_image > kNoAllocScratchFloats) return WT_ERR_WORKSPACE;
-    size_t nc_max = (kNoAllocScratchFloats - totals_floats) / per_image;
+    const size_t slot_floats = backward_weight_slot_bytes(*desc) / sizeof(float);
+    if (totals_floats + per_image + slot_floats > kNoAllocScratchFloats) return WT_ERR_WORKSPACE;
+    size_t want_slots = (size_t)desc->c * desc->n < 304 ? (size_t)desc->c * desc->n : 304;
+    if (slot_floats == 0) want_slots = 0;
+    size_t nc_max = 1;
+    if (kNoAllocScratchFloats > totals_floats + want_slots * slot_floats + per_image)
+        nc_max = (kNoAllocScratchFloats - totals_floats - want_slots * slot_floats) / per_image;
     if (nc_max > (size_t)desc->n) nc_max = (size_t)desc->n;
+    const size_t part_floats = (nc_max * per_image + 63) & ~size_t(63);
 
     float* scratch = nullptr;
     st = scratch_on_current_device(&scratch);
     if (st != WT_OK) return st;
     float* totals = scratch;
     float* part = scratch + totals_floats;
+    float* slots = part + part_floats;
+    const size_t slots_bytes =
+        (kNoAllocScratchFloats > totals_floats + part_floats)
+            ? (kNoAllocScratchFloats - totals_floats - part_floats) * sizeof(float)
+            : 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     const size_t esize = io_bytes(desc->io);
@@ -118,7 +132,7 @@ extern "C" wt_status wtconv_backward_weight_noalloc(const wt_desc* desc, const v
         sub.n = nc;
         const char* xb = static_cast<const char*>(x) + (size_t)n0 * image_bytes;
         const char* gb = static_cast<const char*>(dy) + (size_t)n0 * image_bytes;
-        st = launch_dw_partials(sub, xb, gb, part, s, &launches);
+        st = launch_dw_partials(sub, xb, gb, part, slots, slots_bytes, s, &launches);
         if (st != WT_OK) return st;
         const size_t n_tot = per_image;
         const unsigned blocks = (unsigned)((n_tot + 255) / 256 < 1024 ? (n_tot + 255) / 256 : 1024);

@@ -395,34 +395,20 @@ __device__ __forceinline__ void load_block4x4(const T* xp, int H, int W, int vec
     }
 }
 
-// Level-l (l >= 2) carrier 2x2 block feeding subband cell (gi, gj): from X itself when
-// l == 2 (its 4x4 pixel block, through the level-1 carrier; zero outside the H x W plane),
-// else from the carrier X^(l-1) of width Wp. Values are Eq. 5's normalized low-pass
-// carrier. EXACT: the plane has 4-aligned rows and needs no padding at level 2, so every
-// block lies inside it and is read with vector loads.
-template <typename T, bool EXACT>
-__device__ __forceinline__ void carrier_block(int l, const T* xp, int H, int W, int vec,
-                                              const float* carp, int Wp, int gi, int gj,
-                                              float& ca, float& cb, float& cc, float& cd) {
-    if (l == 2) {
-        float4 r[4];
-        if (EXACT) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) r[q] = IO<T>::ld4(xp + (size_t)(4 * gi + q) * W + 4 * gj);
-        } else {
-            load_block4x4<T>(xp, H, W, vec, 4 * gi, 4 * gj, r);
-        }
-        ca = 0.5f * (r[0].x + r[0].y + r[1].x + r[1].y);
-        cb = 0.5f * (r[0].z + r[0].w + r[1].z + r[1].w);
-        cc = 0.5f * (r[2].x + r[2].y + r[3].x + r[3].y);
-        cd = 0.5f * (r[2].z + r[2].w + r[3].z + r[3].w);
-    } else {
-        const float* q = carp + (size_t)(2 * gi) * Wp + 2 * gj;
-        ca = q[0];
-        cb = q[1];
-        cc = q[Wp];
-        cd = q[Wp + 1];
-    }
+// Number of bw x bh boxes that tile an H x W plane.
+__device__ __forceinline__ int sweep_boxes(int H, int W, int bw, int bh) {
+    return ((W + bw - 1) / bw) * ((H + bh - 1) / bh);
+}
+
+// Level-2 subbands (unnormalized) and carrier of the 4x4 pixel block r0..r3 (Eq. 5 applied
+// to the pixels gives X^(1) = LL; applied again to the 2x2 block of X^(1) it gives level 2).
+__device__ __forceinline__ float4 level2_block(const float4& r0, const float4& r1,
+                                               const float4& r2, const float4& r3) {
+    const float ca = 0.5f * (r0.x + r0.y + r1.x + r1.y);
+    const float cb = 0.5f * (r0.z + r0.w + r1.z + r1.w);
+    const float cc = 0.5f * (r2.x + r2.y + r3.x + r3.y);
+    const float cd = 0.5f * (r2.z + r2.w + r3.z + r3.w);
+    return haar_u(ca, cb, cc, cd);
 }
 
 }  // namespace wt

@@ -8,12 +8,17 @@
 // and the base-path gradients are dW~^(0)[u][v] = sum dY[y][x] X[y+u-R][x+v-R],
 // db~ = sum dY. Only X and dY are read from HBM; both Haar cascades are recomputed on chip.
 //
-// Kernel 1 (wt_dw_plane_kernel): one CTA (256 threads) per (c, n) plane.
+// Kernel 1 (wt_dw_plane_kernel): a persistent grid of 256-thread CTAs walks the (n, c)
+// planes. Per plane:
+//   level-2 sweep (L >= 2): X and dY stream through shared memory in TMA boxes (two box
+//     pairs in flight); every 4x4 pixel block becomes its four level-2 subbands (Eq. 5
+//     twice), stored for both tensors in the CTA's workspace slot (L2-resident), and the
+//     carriers X^(2), dY^(2) for the deeper levels.
 //   deep levels (l >= 2): 32x32 tiles of the level's subbands of X (R halo) and dY are
-//     staged as band-pair tiles, (LL, LH) and (HL, HH), from on-chip carriers (level 2
-//     from the 4x4 pixel blocks of X and dY); threads 0-127 correlate pair 0 and threads
-//     128-255 pair 1 with packed f32x2 FMAs (2x4 coefficient blocks), and the sums are
-//     flushed after each level by recursive-halving warp reductions in a fixed order.
+//     staged as band-pair tiles, (LL, LH) and (HL, HH) (level 2 from the slot, deeper
+//     levels from the carriers); threads 0-127 correlate pair 0 and 128-255 pair 1 with
+//     packed f32x2 FMAs (2x4 coefficient blocks), flushed after each level by
+//     recursive-halving warp reductions in a fixed order.
 //   full resolution: 64x64-pixel tiles of X (2R halo) and dY arrive by TMA; the next
 //     tile's load is issued as soon as the current one has been widened to fp32, so it
 //     overlaps the correlations. Threads 0-127 run the base correlation (4x4 pixel
@@ -34,21 +39,36 @@ constexpr int kDT = 256;  // threads per CTA
 struct DwArgs {
     CUtensorMap tmx;  // X: dims {W, H, planes}, box {XBW, XBH, 1} (2R halo)
     CUtensorMap tmg;  // dY: dims {W, H, planes}, box {64, 64, 1}
+    CUtensorMap tsx;  // X for the level-2 sweep: box {64, DwSweep::BH, 1}
+    CUtensorMap tsg;  // dY for the level-2 sweep: box {64, DwSweep::BH, 1}
     const void* x;
     const void* dy;
-    float* part;  // [C][N][KP]
-    int* err;     // set when a TMA wait times out (may be null)
+    float* part;      // [C][N][KP]
+    int* err;         // set when a TMA wait times out (may be null)
+    int* next;        // the next plane to hand out (zeroed before the launch; may be null)
+    float* slots;     // per CTA: level-2 subbands of X, of dY (u2 floats each), carriers
+    long long slot_floats, u2_floats;
+    long long planes;
     int N, C, H, W, L;
     int Hp, Wp;  // the plane padded with zeros to multiples of 2^L: level l is (Hp, Wp) >> l
     int vec, use_tma;
     int KP;
     int o_bar, o_rawx, o_rawg, o_acc, o_red, o_xb, o_gb, o_x, o_g;  // shared memory (floats)
-    // deep carriers X^(l), dY^(l) (l = 2..L-1): in shared memory, or (deep_global) in a
-    // per-plane region of car_floats floats at car + plane * car_floats
+    // deep carriers X^(l), dY^(l) (l = 2..L-1): in shared memory, or (deep_global) in the
+    // CTA's slot after the two subband arrays
     int deep_global;
-    float* car;
-    long long car_floats;
     int o_carx[kMaxLevels + 1], o_cary[kMaxLevels + 1];
+};
+
+// Boxes of the level-2 sweep: 64 columns x BH rows of X or dY, 8 KB in either dtype; two
+// (X, dY) box pairs are in flight, in the band-pair tiles (idle at that time).
+template <typename T>
+struct DwSweep {
+    static constexpr int BW = 64;
+    static constexpr int BH = sizeof(T) == 2 ? 64 : 32;
+    static constexpr int BYTES = BW * BH * (int)sizeof(T);
+    static constexpr int BOXF = BYTES / 4;  // floats per box
+    static constexpr int NB = 2;            // box pairs in flight
 };
 
 // dY subband-pair tiles (no halo): 32 rows x 32 cells, 16-byte chunks split even/odd.
@@ -57,9 +77,10 @@ constexpr int kGRow = 8 * kGHalf;     // floats per row
 constexpr int kGTile = kCT * kGRow;   // floats per pair tile
 
 // Deep stage for level l: X subbands with an R halo into the X pair tiles, dY subbands of
-// the tile's own cells into the dY pair tiles; carriers X^(l), dY^(l) for l < L.
-template <int K, typename T, bool FAST>
-__device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const T* xp, const T* gp,
+// the tile's own cells into the dY pair tiles. Level 2 reads the sweep's stored subbands,
+// deeper levels transform the carriers X^(l-1), dY^(l-1) and write X^(l), dY^(l) for l < L.
+template <int K>
+__device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const float* u2x, const float* u2g,
                                               float* sm, float* cbase, int l, int ti0,
                                               int tj0) {
     constexpr int R = FG<K>::R, BT = FG<K>::BT;
@@ -70,8 +91,10 @@ __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const T* xp, cons
     float* gb = sm + a.o_gb;
     const float* cpx = (l >= 3) ? cbase + a.o_carx[l - 1] : nullptr;
     const float* cpy = (l >= 3) ? cbase + a.o_cary[l - 1] : nullptr;
-    float* clx = (l < a.L) ? cbase + a.o_carx[l] : nullptr;
-    float* cly = (l < a.L) ? cbase + a.o_cary[l] : nullptr;
+    float* clx = (l >= 3 && l < a.L) ? cbase + a.o_carx[l] : nullptr;
+    float* cly = (l >= 3 && l < a.L) ? cbase + a.o_cary[l] : nullptr;
+    const float4* ux4 = reinterpret_cast<const float4*>(u2x);
+    const float4* ug4 = reinterpret_cast<const float4*>(u2g);
 #pragma unroll
     for (int it = 0; it < NIT; ++it) {
         const int idx = threadIdx.x + it * kDT;
@@ -81,14 +104,18 @@ __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const T* xp, cons
         const bool inner = si >= R && si < R + kCT && sj >= R && sj < R + kCT;
         float4 ux = f4_zero(), ug = f4_zero();
         if (gi >= 0 && gi < Hl && gj >= 0 && gj < Wl) {
-            float ca, cb, cc, cd;
-            carrier_block<T, FAST>(l, xp, a.H, a.W, a.vec, cpx, Wp, gi, gj, ca, cb, cc, cd);
-            ux = haar_u(ca, cb, cc, cd);
-            if (inner) {
-                if (clx) clx[gi * Wl + gj] = 0.5f * ux.x;
-                carrier_block<T, FAST>(l, gp, a.H, a.W, a.vec, cpy, Wp, gi, gj, ca, cb, cc, cd);
-                ug = haar_u(ca, cb, cc, cd);
-                if (cly) cly[gi * Wl + gj] = 0.5f * ug.x;
+            if (l == 2) {
+                ux = __ldcg(ux4 + (size_t)gi * Wl + gj);
+                if (inner) ug = __ldcg(ug4 + (size_t)gi * Wl + gj);
+            } else {
+                const float* q = cpx + (size_t)(2 * gi) * Wp + 2 * gj;
+                ux = haar_u(q[0], q[1], q[Wp], q[Wp + 1]);
+                if (inner) {
+                    if (clx) clx[gi * Wl + gj] = 0.5f * ux.x;
+                    const float* r = cpy + (size_t)(2 * gi) * Wp + 2 * gj;
+                    ug = haar_u(r[0], r[1], r[Wp], r[Wp + 1]);
+                    if (cly) cly[gi * Wl + gj] = 0.5f * ug.x;
+                }
             }
         }
         float* q = xb + si * PROW + 4 * pchunk(sj >> 1, PHALF) + 2 * (sj & 1);
@@ -101,6 +128,78 @@ __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const T* xp, cons
             *reinterpret_cast<float2*>(r + kGTile) = make_float2(ug.z, ug.w);
         }
     }
+}
+
+// Level-2 sweep of X and dY: the unnormalized level-2 subbands of every position go to
+// u2x / u2g [H/4][W/4][4] (LL, LH, HL, HH) and, when L >= 3, the carriers X^(2) = LL / 2
+// and dY^(2) to carx / cary. TMA path: the first NB box pairs were issued at the start of
+// the plane; pair t + NB reuses pair t's buffers once every thread is past them. Returns
+// false if a TMA wait timed out (the vote makes the result uniform over the CTA).
+template <typename T, bool FAST>
+__device__ __forceinline__ bool dw_sweep(const DwArgs& a, const T* xp, const T* gp, float* sm,
+                                         float* carx, float* cary, float* u2x, float* u2g,
+                                         uint64_t* bar_s, uint32_t& ph_s, long long plane) {
+    using S = DwSweep<T>;
+    constexpr int BW = S::BW, BH = S::BH, NB = S::NB, PR = BH / 4, PC = BW / 4;
+    const int H2 = a.Hp >> 2, W2 = a.Wp >> 2;
+    float4* ux4 = reinterpret_cast<float4*>(u2x);
+    float4* ug4 = reinterpret_cast<float4*>(u2g);
+    const int tid = threadIdx.x;
+    if (FAST || a.use_tma) {
+        T* buf = reinterpret_cast<T*>(sm + a.o_xb);  // X boxes 0..NB-1, then dY boxes
+        const int bxn = (a.Wp + BW - 1) / BW;
+        const int nbox = sweep_boxes(a.Hp, a.Wp, BW, BH);
+        const int pi = tid / PC, pj = tid % PC;
+        for (int t = 0; t < nbox; ++t) {
+            const int b = t % NB;
+            const bool ok = mbar_wait_bounded(bar_s + b, (ph_s >> b) & 1u);
+            ph_s ^= 1u << b;
+            if (__syncthreads_or(!ok)) return false;
+            if (tid == 0 && t >= 1 && t - 1 + NB < nbox) {
+                // every thread is past pair t - 1: refill its buffers with pair t - 1 + NB
+                const int nt = t - 1 + NB, nb = (t - 1) % NB;
+                const int ny = nt / bxn, nx = nt - ny * bxn;
+                mbar_arrive_expect_tx(bar_s + nb, 2 * S::BYTES);
+                tma_load_3d(buf + nb * (BW * BH), &a.tsx, nx * BW, ny * BH, (int)plane, bar_s + nb);
+                tma_load_3d(buf + (NB + nb) * (BW * BH), &a.tsg, nx * BW, ny * BH, (int)plane,
+                            bar_s + nb);
+            }
+            const int by = t / bxn, bx = t - by * bxn;
+            const int i2 = by * PR + pi, j2 = bx * PC + pj;
+            if (pi < PR && i2 < H2 && j2 < W2) {
+                const T* q = buf + b * (BW * BH) + (4 * pi) * BW + 4 * pj;
+                const float4 ux = level2_block(ld4_smem<T>(q), ld4_smem<T>(q + BW),
+                                               ld4_smem<T>(q + 2 * BW), ld4_smem<T>(q + 3 * BW));
+                const T* r = q + NB * (BW * BH);
+                const float4 ug = level2_block(ld4_smem<T>(r), ld4_smem<T>(r + BW),
+                                               ld4_smem<T>(r + 2 * BW), ld4_smem<T>(r + 3 * BW));
+                const size_t o = (size_t)i2 * W2 + j2;
+                __stcg(ux4 + o, ux);
+                __stcg(ug4 + o, ug);
+                if (carx != nullptr) {
+                    carx[o] = 0.5f * ux.x;
+                    cary[o] = 0.5f * ug.x;
+                }
+            }
+        }
+    } else {
+        const int n = H2 * W2;
+        for (int p = tid; p < n; p += kDT) {
+            const int i2 = p / W2, j2 = p - i2 * W2;
+            float4 r[4];
+            load_block4x4<T>(xp, a.H, a.W, a.vec, 4 * i2, 4 * j2, r);
+            const float4 ux = level2_block(r[0], r[1], r[2], r[3]);
+            load_block4x4<T>(gp, a.H, a.W, a.vec, 4 * i2, 4 * j2, r);
+            const float4 ug = level2_block(r[0], r[1], r[2], r[3]);
+            __stcg(ux4 + p, ux);
+            __stcg(ug4 + p, ug);
+            if (carx != nullptr) {
+                carx[p] = 0.5f * ux.x;
+                cary[p] = 0.5f * ug.x;
+            }
+        }
+    }
+    return true;
 }
 
 // Widen the TMA-staged raw dY tile (64x64) to the fp32 dY tile and, when `bands`, form
@@ -214,13 +313,16 @@ template <int K, typename T, bool FAST>
 __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(const __grid_constant__ DwArgs a) {
     constexpr int R = FG<K>::R, KK = FG<K>::KK, PAD = FG<K>::PAD, XP = FG<K>::XPITCH;
     constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE;
+    using S = DwSweep<T>;
     extern __shared__ __align__(128) float4 smem_f4[];
     float* sm = reinterpret_cast<float*>(smem_f4);
+    // mbarriers: the full-resolution tile pair, then the level-2 sweep's box pairs
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + a.o_bar);
+    uint64_t* bar_s = bar + 1;
     T* rawx = reinterpret_cast<T*>(sm + a.o_rawx);
     T* rawg = reinterpret_cast<T*>(sm + a.o_rawg);
     float* acc_sm = sm + a.o_acc;
-    float* red = sm + a.o_red;  // [8 warps][64]
+    float* red = sm + a.o_red;  // [8 warps][128]
     float* xb = sm + a.o_xb;
     float* gb = sm + a.o_gb;
     float* xs = sm + a.o_x;
@@ -228,46 +330,172 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
     const int tid = threadIdx.x, warp = tid >> 5;
     const bool leader = tid == 0;
     const bool use_tma = FAST || a.use_tma;
-
-    const int c = blockIdx.x, n = blockIdx.y;
-    const long long plane = (long long)n * a.C + c;
+    float* slot = a.slots + (size_t)blockIdx.x * a.slot_floats;
+    float* u2x = slot;
+    float* u2g = slot + a.u2_floats;
+    float* cbase = (!FAST && a.deep_global) ? slot + 2 * a.u2_floats : sm;  // carriers
+    float* carx = (a.L >= 3) ? cbase + a.o_carx[2] : nullptr;
+    float* cary = (a.L >= 3) ? cbase + a.o_cary[2] : nullptr;
     const size_t plane_elems = (size_t)a.H * a.W;
-    const T* xp = reinterpret_cast<const T*>(a.x) + plane * plane_elems;
-    const T* gp = reinterpret_cast<const T*>(a.dy) + plane * plane_elems;
     const int tiles_x = (a.W + kTile - 1) / kTile;
     const int ntiles = tiles_x * ((a.H + kTile - 1) / kTile);
     constexpr int BYTES = XBox<K, T>::BYTES + kTile * kTile * (int)sizeof(T);
 
-    for (int e = tid; e < a.KP; e += kDT) acc_sm[e] = 0.f;
     if (use_tma && leader) {
         mbar_init(bar, 1);
+        for (int b = 0; b < S::NB; ++b) mbar_init(bar_s + b, 1);
         fence_mbar_init();
     }
     __syncthreads();
-    if (use_tma && leader) {  // first tile, in flight during the deep levels
-        mbar_arrive_expect_tx(bar, BYTES);
-        tma_load_3d(rawx, &a.tmx, -XBox<K, T>::XOFF, -2 * R, (int)plane, bar);
-        tma_load_3d(rawg, &a.tmg, 0, 0, (int)plane, bar);
-    }
-    uint32_t ph = 0;
+    uint32_t ph = 0, ph_s = 0;
+    bool failed = false;
 
-    // ---- deep levels l = 2..L: band pair pp = tid / 128, 2x4 block per thread ----
-    float* cbase = (!FAST && a.deep_global) ? a.car + plane * a.car_floats : sm;  // carriers
-    for (int l = 2; l <= a.L; ++l) {
-        const int Hl = a.Hp >> l, Wl = a.Wp >> l;
-        const int pp = tid >> 7, bi = (tid >> 3) & 15, bj = tid & 7;
-        f2x accd[KK];
+    // planes: first blockIdx.x, then whichever is next in the shared counter (planes are
+    // independent, so the order does not change any result), else a fixed stride
+    int* s_next = reinterpret_cast<int*>(sm + a.o_bar + 16);
+    for (long long plane = blockIdx.x; plane < a.planes;) {
+        const int n = (int)(plane / a.C), c = (int)(plane - (long long)n * a.C);
+        const T* xp = reinterpret_cast<const T*>(a.x) + plane * plane_elems;
+        const T* gp = reinterpret_cast<const T*>(a.dy) + plane * plane_elems;
+        __syncthreads();  // the previous plane is done with shared memory
+        for (int e = tid; e < a.KP; e += kDT) acc_sm[e] = 0.f;
+        if (use_tma && leader) {
+            // the first full-resolution tile pair, in flight during the deep levels, and the
+            // first box pairs of the level-2 sweep
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar, BYTES);
+            tma_load_3d(rawx, &a.tmx, -XBox<K, T>::XOFF, -2 * R, (int)plane, bar);
+            tma_load_3d(rawg, &a.tmg, 0, 0, (int)plane, bar);
+            if (a.L >= 2) {
+                constexpr int BW = S::BW, BH = S::BH;
+                const int bxn = (a.Wp + BW - 1) / BW, nbox = sweep_boxes(a.Hp, a.Wp, BW, BH);
+                T* buf = reinterpret_cast<T*>(sm + a.o_xb);
+                for (int t = 0; t < S::NB && t < nbox; ++t) {
+                    const int ny = t / bxn, nx = t - ny * bxn;
+                    mbar_arrive_expect_tx(bar_s + t, 2 * S::BYTES);
+                    tma_load_3d(buf + t * (BW * BH), &a.tsx, nx * BW, ny * BH, (int)plane,
+                                bar_s + t);
+                    tma_load_3d(buf + (S::NB + t) * (BW * BH), &a.tsg, nx * BW, ny * BH,
+                                (int)plane, bar_s + t);
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---- deep levels l = 2..L: band pair pp = tid / 128, 2x4 block per thread ----
+        if (a.L >= 2) {
+            if (!dw_sweep<T, FAST>(a, xp, gp, sm, carx, cary, u2x, u2g, bar_s, ph_s, plane)) {
+                failed = true;
+                break;
+            }
+            __syncthreads();
+        }
+        for (int l = 2; l <= a.L; ++l) {
+            const int Hl = a.Hp >> l, Wl = a.Wp >> l;
+            const int pp = tid >> 7, bi = (tid >> 3) & 15, bj = tid & 7;
+            f2x accd[KK];
 #pragma unroll
-        for (int q = 0; q < KK; ++q) accd[q] = 0ull;
-        for (int ti0 = 0; ti0 < Hl; ti0 += kCT) {
-            for (int tj0 = 0; tj0 < Wl; tj0 += kCT) {
-                dw_deep_stage<K, T, FAST>(a, xp, gp, sm, cbase, l, ti0, tj0);
+            for (int q = 0; q < KK; ++q) accd[q] = 0ull;
+            for (int ti0 = 0; ti0 < Hl; ti0 += kCT) {
+                for (int tj0 = 0; tj0 < Wl; tj0 += kCT) {
+                    dw_deep_stage<K>(a, u2x, u2g, sm, cbase, l, ti0, tj0);
+                    __syncthreads();
+                    if (ti0 + 2 * bi < Hl && tj0 + 4 * bj < Wl) {
+                        f2x g[2][4];
+#pragma unroll
+                        for (int o = 0; o < 2; ++o) {
+                            const float* gr = gb + pp * kGTile + (2 * bi + o) * kGRow;
+                            const float4 t0 = *reinterpret_cast<const float4*>(gr + 4 * bj);
+                            const float4 t1 = *reinterpret_cast<const float4*>(gr + 4 * (kGHalf + bj));
+                            g[o][0] = pk2(t0.x, t0.y);
+                            g[o][1] = pk2(t0.z, t0.w);
+                            g[o][2] = pk2(t1.x, t1.y);
+                            g[o][3] = pk2(t1.z, t1.w);
+                        }
+                        corr_pair<K, 2>(xb + pp * PTILE + (2 * bi) * PROW, bj, g, accd);
+                    }
+                    __syncthreads();
+                }
+            }
+            // flush: warps 4pp..4pp+3 hold band pair pp; fixed-order sum into acc_sm
+            warp_totals_to<KK, 2 * KK>(accd, 0.f, red + warp * 128);
+            __syncthreads();
+            for (int e = tid; e < 4 * KK; e += kDT) {
+                const int p2 = e / (2 * KK), k = e - p2 * 2 * KK;  // k = 2*tap + band-in-pair
+                float s = 0.f;
+                for (int w = 0; w < 4; ++w) s += red[(4 * p2 + w) * 128 + k];
+                acc_sm[KK + 1 + (l - 1) * 4 * KK + (2 * p2 + (k & 1)) * KK + (k >> 1)] += s;
+            }
+            __syncthreads();
+        }
+
+        // ---- full resolution: warps 0-3 base path, warps 4-7 level-1 band pairs ----
+        const bool base_role = (a.L == 0) || (tid < 128);
+        f2x acc[KK];
+#pragma unroll
+        for (int q = 0; q < KK; ++q) acc[q] = 0ull;
+        // sum of dY, taken while converting the dY tiles: a register partial over at most 16
+        // tiles, folded into a compensated (Kahan) running sum so that planes of millions of
+        // pixels keep the fp32 sum accurate to a few ulps. The running sum and its
+        // compensation live in this thread's two words of `red` (idle until the flush).
+        red[tid] = 0.f;
+        red[kDT + tid] = 0.f;
+        float dpart = 0.f;
+        for (int t = 0; t < ntiles; ++t) {
+            const int ty = t / tiles_x, tx = t - ty * tiles_x;
+            const int y0 = ty * kTile, x0 = tx * kTile;
+            if (use_tma) {
+                const bool ok = mbar_wait_bounded(bar, ph);
+                ph ^= 1;
+                if (__syncthreads_or(!ok)) {
+                    failed = true;
+                    break;
+                }
+                convert_raw<K, T>(rawx, xs, xb, a.L >= 1);
+                dpart += convert_raw_dy<T>(rawg, gs, gb, a.L >= 1);
                 __syncthreads();
-                if (ti0 + 2 * bi < Hl && tj0 + 4 * bj < Wl) {
-                    f2x g[2][4];
+                if (leader && t + 1 < ntiles) {
+                    const int ny = (t + 1) / tiles_x, nx = (t + 1) - ny * tiles_x;
+                    mbar_arrive_expect_tx(bar, BYTES);
+                    tma_load_3d(rawx, &a.tmx, nx * kTile - XBox<K, T>::XOFF, ny * kTile - 2 * R,
+                                (int)plane, bar);
+                    tma_load_3d(rawg, &a.tmg, nx * kTile, ny * kTile, (int)plane, bar);
+                }
+            } else {
+                stage_tile<K, T>(xp, a.H, a.W, a.vec, xs, y0, x0);
+                dpart += stage_dy_plain<T>(gp, a.H, a.W, gs, gb, a.L >= 1, y0, x0);
+                __syncthreads();
+                if (a.L >= 1) {
+                    pair_bands_from_tile<K>(xs, xb);
+                    __syncthreads();
+                }
+            }
+            if ((t & 15) == 15 || t + 1 == ntiles) {
+                kahan_add(red, dpart);
+                dpart = 0.f;
+            }
+            if (base_role) {
+                const int nb = (a.L == 0) ? 1 : 2;
+                for (int k = 0; k < nb; ++k) {
+                    const int blk = tid + kDT / 2 * k;  // L == 0: tid covers all 256 blocks
+                    const int by = blk >> 4, bx = blk & 15;
+                    if (y0 + 4 * by >= a.H || x0 + 4 * bx >= a.W) continue;
+                    f2x g[4][2];
 #pragma unroll
-                    for (int o = 0; o < 2; ++o) {
-                        const float* gr = gb + pp * kGTile + (2 * bi + o) * kGRow;
+                    for (int o = 0; o < 4; ++o) {
+                        const float4 tv = *reinterpret_cast<const float4*>(gs + (4 * by + o) * kTile + 4 * bx);
+                        g[o][0] = pk2(tv.x, tv.y);
+                        g[o][1] = pk2(tv.z, tv.w);
+                    }
+                    corr_base_4x4<K>(xs + (4 * by + R) * XP + 4 * bx + R + PAD, XP, g, acc);
+                }
+            } else {
+                const int t2 = tid - 128, pp = t2 >> 6, bi = (t2 >> 3) & 7, bj = t2 & 7;
+                if (y0 / 2 + 4 * bi < (a.H + 1) / 2 && x0 / 2 + 4 * bj < (a.W + 1) / 2) {
+                    f2x g[4][4];
+#pragma unroll
+                    for (int o = 0; o < 4; ++o) {
+                        const float* gr = gb + pp * kGTile + (4 * bi + o) * kGRow;
                         const float4 t0 = *reinterpret_cast<const float4*>(gr + 4 * bj);
                         const float4 t1 = *reinterpret_cast<const float4*>(gr + 4 * (kGHalf + bj));
                         g[o][0] = pk2(t0.x, t0.y);
@@ -275,137 +503,47 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
                         g[o][2] = pk2(t1.x, t1.y);
                         g[o][3] = pk2(t1.z, t1.w);
                     }
-                    corr_pair<K, 2>(xb + pp * PTILE + (2 * bi) * PROW, bj, g, accd);
+                    corr_pair<K, 4>(xb + pp * PTILE + (4 * bi) * PROW, bj, g, acc);
                 }
-                __syncthreads();
             }
+            __syncthreads();
         }
-        // flush: warps 4pp..4pp+3 hold band pair pp; fixed-order sum into acc_sm
-        warp_totals_to<KK, 2 * KK>(accd, 0.f, red + warp * 128);
+        if (failed) break;
+
+        // ---- flush: fixed-order reductions into acc_sm, then the partial vector ----
+        const float dbs = red[tid] - red[kDT + tid];
+        __syncthreads();  // every thread has read its sum before `red` takes the warp totals
+        warp_totals_to<KK, 2 * KK + 1>(acc, dbs, red + warp * 128);
         __syncthreads();
-        for (int e = tid; e < 4 * KK; e += kDT) {
-            const int p2 = e / (2 * KK), k = e - p2 * 2 * KK;  // k = 2*tap + band-in-pair
+        const int nbase = (a.L == 0) ? 8 : 4;
+        for (int e = tid; e <= KK; e += kDT) {
+            // base taps: even + odd column halves of each base warp; e == KK: the sum of dY,
+            // which every warp holds a share of (it is taken while converting the dY tiles)
             float s = 0.f;
-            for (int w = 0; w < 4; ++w) s += red[(4 * p2 + w) * 128 + k];
-            acc_sm[KK + 1 + (l - 1) * 4 * KK + (2 * p2 + (k & 1)) * KK + (k >> 1)] += s;
+            if (e < KK) {
+                for (int w = 0; w < nbase; ++w) s += red[w * 128 + 2 * e] + red[w * 128 + 2 * e + 1];
+            } else {
+                for (int w = 0; w < kDT / 32; ++w) s += red[w * 128 + 2 * KK];
+            }
+            acc_sm[e] += s;
         }
-        __syncthreads();
-    }
-
-    // ---- full resolution: warps 0-3 base path, warps 4-7 level-1 band pairs ----
-    const bool base_role = (a.L == 0) || (tid < 128);
-    f2x acc[KK];
-#pragma unroll
-    for (int q = 0; q < KK; ++q) acc[q] = 0ull;
-    // sum of dY, taken while converting the dY tiles: a register partial over at most 16
-    // tiles, folded into a compensated (Kahan) running sum so that planes of millions of
-    // pixels keep the fp32 sum accurate to a few ulps. The running sum and its compensation
-    // live in this thread's two words of `red` (idle until the final flush).
-    red[tid] = 0.f;
-    red[kDT + tid] = 0.f;
-    float dpart = 0.f;
-    bool failed = false;
-    for (int t = 0; t < ntiles; ++t) {
-        const int ty = t / tiles_x, tx = t - ty * tiles_x;
-        const int y0 = ty * kTile, x0 = tx * kTile;
-        if (use_tma) {
-            const bool ok = mbar_wait_bounded(bar, ph);
-            ph ^= 1;
-            if (__syncthreads_or(!ok)) {
-                failed = true;
-                break;
-            }
-            convert_raw<K, T>(rawx, xs, xb, a.L >= 1);
-            dpart += convert_raw_dy<T>(rawg, gs, gb, a.L >= 1);
-            __syncthreads();
-            if (leader && t + 1 < ntiles) {
-                const int ny = (t + 1) / tiles_x, nx = (t + 1) - ny * tiles_x;
-                fence_proxy_async_smem();
-                mbar_arrive_expect_tx(bar, BYTES);
-                tma_load_3d(rawx, &a.tmx, nx * kTile - XBox<K, T>::XOFF, ny * kTile - 2 * R,
-                            (int)plane, bar);
-                tma_load_3d(rawg, &a.tmg, nx * kTile, ny * kTile, (int)plane, bar);
-            }
-        } else {
-            stage_tile<K, T>(xp, a.H, a.W, a.vec, xs, y0, x0);
-            dpart += stage_dy_plain<T>(gp, a.H, a.W, gs, gb, a.L >= 1, y0, x0);
-            __syncthreads();
-            if (a.L >= 1) {
-                pair_bands_from_tile<K>(xs, xb);
-                __syncthreads();
-            }
-        }
-        if ((t & 15) == 15 || t + 1 == ntiles) {
-            kahan_add(red, dpart);
-            dpart = 0.f;
-        }
-        if (base_role) {
-            const int nb = (a.L == 0) ? 1 : 2;
-            for (int k = 0; k < nb; ++k) {
-                const int blk = tid + kDT / 2 * k;  // L == 0: tid covers all 256 blocks
-                const int by = blk >> 4, bx = blk & 15;
-                if (y0 + 4 * by >= a.H || x0 + 4 * bx >= a.W) continue;
-                f2x g[4][2];
-#pragma unroll
-                for (int o = 0; o < 4; ++o) {
-                    const float4 tv = *reinterpret_cast<const float4*>(gs + (4 * by + o) * kTile + 4 * bx);
-                    g[o][0] = pk2(tv.x, tv.y);
-                    g[o][1] = pk2(tv.z, tv.w);
-                }
-                corr_base_4x4<K>(xs + (4 * by + R) * XP + 4 * bx + R + PAD, XP, g, acc);
-            }
-        } else {
-            const int t2 = tid - 128, pp = t2 >> 6, bi = (t2 >> 3) & 7, bj = t2 & 7;
-            if (y0 / 2 + 4 * bi < (a.H + 1) / 2 && x0 / 2 + 4 * bj < (a.W + 1) / 2) {
-                f2x g[4][4];
-#pragma unroll
-                for (int o = 0; o < 4; ++o) {
-                    const float* gr = gb + pp * kGTile + (4 * bi + o) * kGRow;
-                    const float4 t0 = *reinterpret_cast<const float4*>(gr + 4 * bj);
-                    const float4 t1 = *reinterpret_cast<const float4*>(gr + 4 * (kGHalf + bj));
-                    g[o][0] = pk2(t0.x, t0.y);
-                    g[o][1] = pk2(t0.z, t0.w);
-                    g[o][2] = pk2(t1.x, t1.y);
-                    g[o][3] = pk2(t1.z, t1.w);
-                }
-                corr_pair<K, 4>(xb + pp * PTILE + (4 * bi) * PROW, bj, g, acc);
+        if (a.L >= 1) {
+            for (int e = tid; e < 4 * KK; e += kDT) {
+                // band pair pp lives in warps 4 + 2pp and 5 + 2pp
+                const int p2 = e / (2 * KK), k = e - p2 * 2 * KK;
+                const float s = red[(4 + 2 * p2) * 128 + k] + red[(5 + 2 * p2) * 128 + k];
+                acc_sm[KK + 1 + (2 * p2 + (k & 1)) * KK + (k >> 1)] += s;
             }
         }
         __syncthreads();
+        float* out = a.part + ((size_t)c * a.N + n) * a.KP;
+        for (int e = tid; e < a.KP; e += kDT) out[e] = acc_sm[e];
+        if (leader)
+            *s_next = (a.next != nullptr) ? (int)gridDim.x + atomicAdd(a.next, 1) : -1;
+        __syncthreads();
+        plane = (a.next != nullptr) ? (long long)*s_next : plane + gridDim.x;
     }
-    if (failed) {
-        if (leader && a.err != nullptr) atomicExch(a.err, kErrTmaTimeout);
-        return;
-    }
-
-    // ---- flush: fixed-order reductions into acc_sm, then the partial vector ----
-    const float dbs = red[tid] - red[kDT + tid];
-    __syncthreads();  // every thread has read its sum before `red` takes the warp totals
-    warp_totals_to<KK, 2 * KK + 1>(acc, dbs, red + warp * 128);
-    __syncthreads();
-    const int nbase = (a.L == 0) ? 8 : 4;
-    for (int e = tid; e <= KK; e += kDT) {
-        // base taps: even + odd column halves of each base warp; e == KK: the sum of dY,
-        // which every warp holds a share of (it is taken while converting the dY tiles)
-        float s = 0.f;
-        if (e < KK) {
-            for (int w = 0; w < nbase; ++w) s += red[w * 128 + 2 * e] + red[w * 128 + 2 * e + 1];
-        } else {
-            for (int w = 0; w < kDT / 32; ++w) s += red[w * 128 + 2 * KK];
-        }
-        acc_sm[e] += s;
-    }
-    if (a.L >= 1) {
-        for (int e = tid; e < 4 * KK; e += kDT) {
-            // band pair pp lives in warps 4 + 2pp and 5 + 2pp
-            const int p2 = e / (2 * KK), k = e - p2 * 2 * KK;
-            const float s = red[(4 + 2 * p2) * 128 + k] + red[(5 + 2 * p2) * 128 + k];
-            acc_sm[KK + 1 + (2 * p2 + (k & 1)) * KK + (k >> 1)] += s;
-        }
-    }
-    __syncthreads();
-    float* out = a.part + ((size_t)c * a.N + n) * a.KP;
-    for (int e = tid; e < a.KP; e += kDT) out[e] = acc_sm[e];
+    if (failed && leader && a.err != nullptr) atomicExch(a.err, kErrTmaTimeout);
 }
 
 // Per channel: fixed-order sum of the N partial vectors, then §4.3 Eq. 9.
@@ -461,14 +599,25 @@ constexpr size_t kTwoCtaSmem = 228 * 1024 / 2 - 1024;  // two CTAs per SM still 
 
 size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// Shared-memory layout, slot layout and grid of the plane kernel for d.
+struct DwPlan {
+    DwArgs a;
+    size_t smem = 0;
+    int grid = 0;            // persistent CTAs
+    size_t slot_bytes = 0;   // workspace per CTA (0 when L < 2)
+};
+
 template <int K, typename T>
-void dw_layout(const wt_desc& d, DwArgs& a, size_t& smem_bytes) {
+DwPlan dw_layout(const wt_desc& d) {
     constexpr int KK = FG<K>::KK;
+    DwPlan p;
+    DwArgs& a = p.a;
     const int L = d.levels;
+    const int hp = padded_side(d.h, L), wp = padded_side(d.w, L);
     a.KP = KK + 1 + 4 * KK * L;
     int off = 0;
     a.o_bar = off;
-    off += 32;
+    off += 32;  // mbarriers, padded to 128 bytes
     a.o_rawx = off;
     off += round32((XBox<K, T>::BYTES + 3) / 4);
     a.o_rawg = off;
@@ -482,18 +631,20 @@ void dw_layout(const wt_desc& d, DwArgs& a, size_t& smem_bytes) {
     off = round4(off);
     a.o_gb = off;
     off += 2 * kGTile;
+    // the level-2 sweep's box pairs reuse the band-pair tiles (and the space after them)
+    const int sweep_end = a.o_xb + 2 * DwSweep<T>::NB * DwSweep<T>::BOXF;
+    if (off < sweep_end) off = sweep_end;
     // the fp32 X and dY tiles share their region with the deep-level carriers
-    const int alias0 = off;
-    a.o_x = off;
-    off += FG<K>::XROWS * FG<K>::XPITCH;
+    const int alias0 = round32(off);
+    a.o_x = alias0;
+    off = alias0 + FG<K>::XROWS * FG<K>::XPITCH;
     off = round4(off);
     a.o_g = off;
     off += kTile * kTile;
     int cp = 0;
     for (int l = 0; l <= kMaxLevels; ++l) a.o_carx[l] = a.o_cary[l] = 0;
     for (int l = 2; l < L; ++l) {
-        const int sz = round4((padded_side(d.h, d.levels) >> l) *
-                              (padded_side(d.w, d.levels) >> l));
+        const int sz = round4((hp >> l) * (wp >> l));
         a.o_carx[l] = cp;
         cp += sz;
         a.o_cary[l] = cp;
@@ -501,33 +652,47 @@ void dw_layout(const wt_desc& d, DwArgs& a, size_t& smem_bytes) {
     }
     // the carriers stay in shared memory unless they would lower the occupancy the tiles
     // alone allow (two CTAs per SM for k <= 5 when the tiles fit it, else one) or not fit
-    // at all; then they move to the workspace
+    // at all; then they move to the CTA's workspace slot
     const size_t two = (K >= 7) ? kMaxSmemPerBlock : kTwoCtaSmem;
     const size_t limit = ((size_t)off * sizeof(float) <= two) ? two : kMaxSmemPerBlock;
     const int local_end = alias0 + cp > off ? alias0 + cp : off;
     a.deep_global = (cp > 0 && (size_t)local_end * sizeof(float) > limit) ? 1 : 0;
-    a.car_floats = a.deep_global ? (((long long)cp + 63) & ~63LL) : 0;
     if (!a.deep_global)
         for (int l = 2; l < L; ++l) {
             a.o_carx[l] += alias0;
             a.o_cary[l] += alias0;
         }
     const int total = a.deep_global ? off : local_end;
-    smem_bytes = (size_t)total * sizeof(float);
+    p.smem = (size_t)total * sizeof(float);
+    // per CTA: the level-2 subbands of X and of dY, [H/4][W/4][4] fp32 each (+ carriers)
+    a.u2_floats = (L >= 2) ? ((4LL * (hp >> 2) * (wp >> 2) + 63) & ~63LL) : 0;
+    a.slot_floats = 2 * a.u2_floats + (a.deep_global ? (((long long)cp + 63) & ~63LL) : 0);
+    p.slot_bytes = (size_t)a.slot_floats * sizeof(float);
+    const long long planes = (long long)d.n * d.c;
+    int occ = (int)((228 * 1024) / (p.smem + 1024));
+    const int occ_max = (K >= 7) ? 1 : 2;
+    if (occ > occ_max) occ = occ_max;
+    if (occ < 1) occ = 1;
+    long long grid = (long long)kNumSMs * occ;
+    if (grid > planes) grid = planes;
+    p.grid = (int)grid;
+    return p;
 }
 
-// Fill the kernel arguments (layout, pointers, tensor maps) for one launch.
+// Fill the kernel arguments (pointers, tensor maps) for one launch with `grid` CTAs.
 template <int K, typename T>
-bool dw_prepare(const wt_desc& d, const void* x, const void* dy, float* part, float* car,
-                int* err, DwArgs& a, size_t& smem) {
-    dw_layout<K, T>(d, a, smem);
-    if (smem > kMaxSmemPerBlock) return false;
-    if (a.deep_global && car == nullptr) return false;
-    a.car = car;
+bool dw_prepare(const wt_desc& d, const void* x, const void* dy, float* part, float* slots,
+                int* err, DwPlan& p) {
+    DwArgs& a = p.a;
+    if (p.smem > kMaxSmemPerBlock) return false;
+    if (p.slot_bytes > 0 && slots == nullptr) return false;
+    a.slots = slots;
     a.x = x;
     a.dy = dy;
     a.part = part;
     a.err = err;
+    a.next = (err != nullptr) ? err + 1 : nullptr;
+    a.planes = (long long)d.n * d.c;
     a.N = d.n;
     a.C = d.c;
     a.H = d.h;
@@ -543,23 +708,28 @@ bool dw_prepare(const wt_desc& d, const void* x, const void* dy, float* part, fl
         const unsigned long long planes = (unsigned long long)d.n * d.c;
         const unsigned long long s1 = (unsigned long long)d.w * esize;
         const unsigned long long s2 = (unsigned long long)d.w * d.h * esize;
-        const bool ok =
+        bool ok =
             encode_3d(&a.tmx, dt, x, d.w, d.h, planes, s1, s2, XBox<K, T>::XBW, XBox<K, T>::XBH) &&
             encode_3d(&a.tmg, dt, dy, d.w, d.h, planes, s1, s2, kTile, kTile);
+        if (ok && d.levels >= 2)
+            ok = encode_3d(&a.tsx, dt, x, d.w, d.h, planes, s1, s2, DwSweep<T>::BW,
+                           DwSweep<T>::BH) &&
+                 encode_3d(&a.tsg, dt, dy, d.w, d.h, planes, s1, s2, DwSweep<T>::BW,
+                           DwSweep<T>::BH);
         a.use_tma = ok ? 1 : 0;
     }
     return true;
 }
 
 template <int K, typename T>
-wt_status launch_dw_plane(const DwArgs& a, size_t smem, const wt_desc& d, cudaStream_t stream,
-                          int* launches) {
+wt_status launch_dw_plane(const DwPlan& p, cudaStream_t stream, int* launches) {
+    const DwArgs& a = p.a;
     const bool fast = a.use_tma && a.vec && a.H == a.Hp && a.W == a.Wp && !a.deep_global;
     auto kern = fast ? wt_dw_plane_kernel<K, T, true> : wt_dw_plane_kernel<K, T, false>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) !=
         cudaSuccess)
         return WT_ERR_CUDA;
-    kern<<<dim3((unsigned)d.c, (unsigned)d.n), kDT, smem, stream>>>(a);
+    kern<<<(unsigned)p.grid, kDT, p.smem, stream>>>(a);
     if (cudaGetLastError() != cudaSuccess) return WT_ERR_CUDA;
     ++*launches;
     return WT_OK;
@@ -572,45 +742,50 @@ wt_status launch_dw_k(const wt_desc& d, const void* x, const void* dy, const flo
                       size_t ws_bytes, cudaStream_t stream, int* launches) {
     const int KP = FG<K>::KK + 1 + 4 * FG<K>::KK * d.levels;
     const size_t part_bytes = round256((size_t)d.c * d.n * KP * sizeof(float));
-    DwArgs a;
-    size_t smem = 0;
-    dw_layout<K, T>(d, a, smem);
-    const size_t need = kDwErrBytes + part_bytes +
-                        (size_t)d.c * d.n * (size_t)a.car_floats * sizeof(float);
+    DwPlan p = dw_layout<K, T>(d);
+    const size_t need = kDwErrBytes + part_bytes + (size_t)p.grid * p.slot_bytes;
     if (ws == nullptr || ws_bytes < need) return WT_ERR_WORKSPACE;
     int* err = reinterpret_cast<int*>(ws);
     float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + kDwErrBytes);
-    float* car = reinterpret_cast<float*>(static_cast<char*>(ws) + kDwErrBytes + part_bytes);
-    if (!dw_prepare<K, T>(d, x, dy, part, car, err, a, smem)) return WT_ERR_UNSUPPORTED;
-    if (cudaMemsetAsync(err, 0, sizeof(int), stream) != cudaSuccess) return WT_ERR_CUDA;
-    wt_status st = launch_dw_plane<K, T>(a, smem, d, stream, launches);
+    float* slots = reinterpret_cast<float*>(static_cast<char*>(ws) + kDwErrBytes + part_bytes);
+    if (!dw_prepare<K, T>(d, x, dy, part, slots, err, p)) return WT_ERR_UNSUPPORTED;
+    if (cudaMemsetAsync(err, 0, 2 * sizeof(int), stream) != cudaSuccess) return WT_ERR_CUDA;
+    wt_status st = launch_dw_plane<K, T>(p, stream, launches);
     if (st != WT_OK) return st;
-    wt_dw_reduce_kernel<<<(unsigned)d.c, 128, (size_t)a.KP * sizeof(float), stream>>>(
-        part, d.c, d.n, a.KP, K, d.levels, w0, b0, s0, wl, sl, dw0, db0, ds0, dwl, dsl);
+    wt_dw_reduce_kernel<<<(unsigned)d.c, 128, (size_t)p.a.KP * sizeof(float), stream>>>(
+        part, d.c, d.n, p.a.KP, K, d.levels, w0, b0, s0, wl, sl, dw0, db0, ds0, dwl, dsl);
     if (cudaGetLastError() != cudaSuccess) return WT_ERR_CUDA;
     ++*launches;
     return WT_OK;
 }
 
+// Partial vectors only (no reduce), with the CTAs' slots in [slots, slots + slot_bytes_max):
+// the grid shrinks to the slots that fit.
 template <int K, typename T>
 wt_status launch_dw_partials_k(const wt_desc& d, const void* x, const void* dy, float* part,
-                               cudaStream_t stream, int* launches) {
-    DwArgs a;
-    size_t smem = 0;
-    // (no carrier region here: shapes whose carriers need the workspace are unsupported)
-    if (!dw_prepare<K, T>(d, x, dy, part, nullptr, nullptr, a, smem)) return WT_ERR_UNSUPPORTED;
-    return launch_dw_plane<K, T>(a, smem, d, stream, launches);
+                               float* slots, size_t slots_bytes, cudaStream_t stream,
+                               int* launches) {
+    DwPlan p = dw_layout<K, T>(d);
+    if (p.slot_bytes > 0) {
+        const size_t fit = slots_bytes / p.slot_bytes;
+        if (fit == 0) return WT_ERR_WORKSPACE;
+        if ((size_t)p.grid > fit) p.grid = (int)fit;
+    }
+    if (!dw_prepare<K, T>(d, x, dy, part, slots, nullptr, p)) return WT_ERR_UNSUPPORTED;
+    return launch_dw_plane<K, T>(p, stream, launches);
 }
 
 }  // namespace
 
 wt_status launch_dw_partials(const wt_desc& d, const void* x, const void* dy, float* part,
-                             cudaStream_t stream, int* launches) {
+                             float* slots, size_t slots_bytes, cudaStream_t stream,
+                             int* launches) {
     switch (d.k) {
 #define WT_CASE(KV)                                                                           \
     case KV:                                                                                  \
         return with_io_type(d.io, [&](auto t) {                                               \
-            return launch_dw_partials_k<KV, decltype(t)>(d, x, dy, part, stream, launches);   \
+            return launch_dw_partials_k<KV, decltype(t)>(d, x, dy, part, slots, slots_bytes,  \
+                                                         stream, launches);                   \
         });
         WT_CASE(1)
         WT_CASE(3)
@@ -640,12 +815,12 @@ size_t dw_partial_floats(const wt_desc& d) {
 }
 
 namespace {
-// Layout of the plane kernel for d (shared memory bytes and the carriers' placement).
-bool dw_plan(const wt_desc& d, DwArgs& a, size_t& smem) {
+// Plan of the plane kernel for d (shared memory, slots, grid).
+bool dw_plan(const wt_desc& d, DwPlan& p) {
     switch (d.k) {
 #define WT_CASE(KV)                                                                          \
     case KV:                                                                                 \
-        with_io_type(d.io, [&](auto t) { dw_layout<KV, decltype(t)>(d, a, smem); return 0; }); \
+        p = with_io_type(d.io, [&](auto t) { return dw_layout<KV, decltype(t)>(d); });       \
         return true;
         WT_CASE(1)
         WT_CASE(3)
@@ -658,18 +833,22 @@ bool dw_plan(const wt_desc& d, DwArgs& a, size_t& smem) {
 }  // namespace
 
 size_t backward_weight_ws_bytes(const wt_desc& d) {
-    DwArgs a;
-    size_t smem = 0;
-    if (!dw_plan(d, a, smem)) return 0;
+    DwPlan p;
+    if (!dw_plan(d, p)) return 0;
     return kDwErrBytes + round256((size_t)d.c * d.n * dw_partial_floats(d) * sizeof(float)) +
-           (size_t)d.c * d.n * (size_t)a.car_floats * sizeof(float);
+           (size_t)p.grid * p.slot_bytes;
+}
+
+size_t backward_weight_slot_bytes(const wt_desc& d) {
+    DwPlan p;
+    if (!dw_plan(d, p)) return 0;
+    return p.slot_bytes;
 }
 
 size_t backward_weight_smem_bytes(const wt_desc& d) {
-    DwArgs a;
-    size_t smem = 0;
-    if (!dw_plan(d, a, smem)) return 0;
-    return smem;
+    DwPlan p;
+    if (!dw_plan(d, p)) return 0;
+    return p.smem;
 }
 
 wt_status launch_backward_weight(const wt_desc& d, const void* x, const void* dy,

@@ -110,11 +110,18 @@ def test_workspace_sizes_for_workloads(lib, name):
         slot = 2 * half
         assert fwd >= 256 + img + slot and (fwd - 256 - img) % slot == 0
         assert fwd <= 256 + img + 2 * 152 * slot  # at most 2 CTAs per SM
-    # backward-weight: a 256-byte status word, then one partial vector
-    # [dW0 | db | dW^(l)] per (channel, image)
+    # backward-weight: a 256-byte status word, one partial vector [dW0 | db | dW^(l)] per
+    # (channel, image), then per resident CTA (persistent grid, at most 2 per SM) a slot
+    # holding the level-2 subbands of X and of dY, each [H/4][W/4][4] fp32 (L >= 2)
     kk = wl.k * wl.k
     per_partial = (kk + 1 + 4 * kk * wl.levels) * 4
-    assert bwd_w == 256 + (wl.c * wl.n * per_partial + 255) // 256 * 256
+    parts = 256 + (wl.c * wl.n * per_partial + 255) // 256 * 256
+    if wl.levels < 2:
+        assert bwd_w == parts
+    else:
+        dslot = 2 * ((4 * (wl.h >> 2) * (wl.w >> 2) + 63) // 64 * 64 * 4)
+        assert bwd_w >= parts + dslot and (bwd_w - parts) % dslot == 0
+        assert bwd_w <= parts + 2 * 152 * dslot
 
 
 def _header_prototypes():
