@@ -291,8 +291,15 @@ __device__ __forceinline__ void convert_raw(const T* raw, float* xs, float* bs, 
     for (int idx = threadIdx.x; idx < BT * NCR; idx += blockDim.x) {
         const int ci = idx / NCR, m = idx - ci * NCR;
         const T* r0 = raw + (2 * ci) * RW + C0 + 4 * m;
-        const float2 a0 = ld2_smem<T>(r0), a1 = ld2_smem<T>(r0 + 2);
-        const float2 b0 = ld2_smem<T>(r0 + RW), b1 = ld2_smem<T>(r0 + RW + 2);
+        float2 a0, a1, b0, b1;
+        if constexpr (C0 % 4 == 0) {  // 4-element aligned: one vector load per row
+            const float4 ra = ld4_smem<T>(r0), rb = ld4_smem<T>(r0 + RW);
+            a0 = make_float2(ra.x, ra.y); a1 = make_float2(ra.z, ra.w);
+            b0 = make_float2(rb.x, rb.y); b1 = make_float2(rb.z, rb.w);
+        } else {
+            a0 = ld2_smem<T>(r0); a1 = ld2_smem<T>(r0 + 2);
+            b0 = ld2_smem<T>(r0 + RW); b1 = ld2_smem<T>(r0 + RW + 2);
+        }
         float* d0 = xs + (2 * ci) * XP + PAD + 4 * m;
         if constexpr ((PAD & 1) == 0) {
             reinterpret_cast<float2*>(d0)[0] = a0;

@@ -211,8 +211,9 @@ __device__ __forceinline__ float convert_raw_dy(const T* raw, float* gs, float* 
     for (int idx = threadIdx.x; idx < kCT * (kCT / 2); idx += blockDim.x) {
         const int ci = idx >> 4, m = idx & 15;
         const T* r0 = raw + (2 * ci) * kTile + 4 * m;
-        const float2 a0 = ld2_smem<T>(r0), a1 = ld2_smem<T>(r0 + 2);
-        const float2 b0 = ld2_smem<T>(r0 + kTile), b1 = ld2_smem<T>(r0 + kTile + 2);
+        const float4 ra = ld4_smem<T>(r0), rb = ld4_smem<T>(r0 + kTile);
+        const float2 a0 = make_float2(ra.x, ra.y), a1 = make_float2(ra.z, ra.w);
+        const float2 b0 = make_float2(rb.x, rb.y), b1 = make_float2(rb.z, rb.w);
         float* d0 = gs + (2 * ci) * kTile + 4 * m;
         *reinterpret_cast<float4*>(d0) = make_float4(a0.x, a0.y, a1.x, a1.y);
         *reinterpret_cast<float4*>(d0 + kTile) = make_float4(b0.x, b0.y, b1.x, b1.y);
