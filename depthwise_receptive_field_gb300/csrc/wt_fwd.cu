@@ -90,15 +90,17 @@ __global__ void wt_fwd_weight_image_kernel(const float* w0f, const float* wlf, i
     }
 }
 
-// Box of the level-2 sweep: 64 columns x BH rows of X, 8 KB in either dtype; NBUF boxes
+// Box of the level-2 sweep: 64 columns x BH rows of X, 16 KB in either dtype; NBUF boxes
 // are in flight (they occupy the band-pair and filtered-subband tiles, idle at that time).
+// Each thread handles PPT level-2 positions of a box.
 template <typename T>
 struct SweepBox {
     static constexpr int BW = 64;
-    static constexpr int BH = sizeof(T) == 2 ? 64 : 32;
+    static constexpr int BH = 16384 / (BW * (int)sizeof(T));
     static constexpr int BYTES = BW * BH * (int)sizeof(T);
-    static constexpr int NBUF = 4;
-    static_assert((BW / 4) * (BH / 4) <= 256, "one level-2 position per thread");
+    static constexpr int NBUF = 2;
+    static constexpr int PPT = (BW / 4) * (BH / 4) / 256;
+    static_assert(PPT * 256 == (BW / 4) * (BH / 4), "whole positions per thread");
 };
 
 // Level-2 sweep: the unnormalized subbands of every level-2 position go to u2
@@ -136,13 +138,18 @@ __device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, floa
                 tma_load_3d(buf + nb * (BW * BH), &a.tms, nx * BW, ny * BH, (int)plane, bar_s + nb);
             }
             const int by = t / bxn, bx = t - by * bxn;
-            const int i2 = by * PR + pi, j2 = bx * PC + pj;
-            if (pi < PR && i2 < H2 && j2 < W2) {
-                const T* q = buf + b * (BW * BH) + (4 * pi) * BW + 4 * pj;
-                const float4 u = level2_block(ld4_smem<T>(q), ld4_smem<T>(q + BW),
-                                              ld4_smem<T>(q + 2 * BW), ld4_smem<T>(q + 3 * BW));
-                __stcg(u2v + (size_t)i2 * W2 + j2, u);
-                if (a.L >= 3) c2[i2 * W2 + j2] = 0.5f * u.x;
+#pragma unroll
+            for (int k = 0; k < SweepBox<T>::PPT; ++k) {
+                const int pk = pi + (256 / PC) * k;  // position row within the box
+                const int i2 = by * PR + pk, j2 = bx * PC + pj;
+                if (i2 < H2 && j2 < W2) {
+                    const T* q = buf + b * (BW * BH) + (4 * pk) * BW + 4 * pj;
+                    const float4 u = level2_block(ld4_smem<T>(q), ld4_smem<T>(q + BW),
+                                                  ld4_smem<T>(q + 2 * BW),
+                                                  ld4_smem<T>(q + 3 * BW));
+                    __stcg(u2v + (size_t)i2 * W2 + j2, u);
+                    if (a.L >= 3) c2[i2 * W2 + j2] = 0.5f * u.x;
+                }
             }
         }
     } else {
