@@ -51,7 +51,10 @@ struct FwdArgs {
     int Hp, Wp;  // the plane padded with zeros to multiples of 2^L: level l is (Hp, Wp) >> l
     int img;  // floats of one channel's weight image (a multiple of 4)
     int vec, use_tma;
-    int o_bar, o_raw, o_dblk, o_w, o_b, o_x, o_z;  // shared-memory regions (floats)
+    // shared-memory regions (floats): mbarriers, raw X tiles (2), weight image, band-pair
+    // tiles (2), filtered level-1 band pairs, deep-sum blocks (2)
+    int o_bar, o_raw, o_dblk, o_w, o_b, o_z;
+    int raw_f, b_f;  // floats per raw-tile buffer and per band-pair buffer
     // deep-level state, in shared memory or (deep_global) in the CTA's workspace slot:
     int deep_global;
     int o_car[kMaxLevels + 1];                    // carriers X^(l), l = 2..L-1
@@ -237,7 +240,8 @@ __device__ __forceinline__ void deep_levels(const FwdArgs& a, float* sm, float* 
     float* deep = DG ? deep_g : sm;
     const float* wsm = sm + a.o_w;
     float* bs = sm + a.o_b;
-    float* zs = sm + a.o_z;
+    float* zs = sm + a.o_b + a.b_f;  // the second band-pair buffer holds the filtered pairs
+    static_assert(PG<K>::ZTILE <= PG<K>::PTILE, "filtered pairs fit a band-pair buffer");
     const int tid = threadIdx.x;
     deep_carriers(a, deep);
     for (int l = a.L; l >= 2; --l) {
@@ -316,21 +320,19 @@ __device__ __forceinline__ void deep_levels(const FwdArgs& a, float* sm, float* 
 // state in shared memory, so those checks and the other paths are compiled out.
 template <int K, typename T, bool FAST>
 __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_constant__ FwdArgs a) {
-    constexpr int R = FG<K>::R, PAD = FG<K>::PAD, XP = FG<K>::XPITCH;
+    constexpr int R = FG<K>::R;
     constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, WS = PG<K>::WS;
     constexpr int ZROW = PG<K>::ZROW, ZTILE = PG<K>::ZTILE;
     extern __shared__ __align__(128) float4 smem_f4[];
     float* sm = reinterpret_cast<float*>(smem_f4);
-    // mbarriers: X tile, deep-sum blocks (2 buffers), weights, level-2 sweep boxes
+    // mbarriers: X tiles (2 buffers), deep-sum blocks (2 buffers), weights, level-2 sweep
     uint64_t* bar_x = reinterpret_cast<uint64_t*>(sm + a.o_bar);
-    uint64_t* bar_d = bar_x + 1;
-    uint64_t* bar_w = bar_x + 3;
-    uint64_t* bar_s = bar_x + 4;
-    T* raw = reinterpret_cast<T*>(sm + a.o_raw);
+    uint64_t* bar_d = bar_x + 2;
+    uint64_t* bar_w = bar_x + 4;
+    uint64_t* bar_s = bar_x + 5;
+    static_assert(SweepBox<T>::NBUF <= 2, "mbarrier slots");
     float* dblk = sm + a.o_dblk;  // two buffers of kDBytes
     float* wsm = sm + a.o_w;
-    float* xs = sm + a.o_x;
-    float* bs = sm + a.o_b;
     float* zs = sm + a.o_z;
     float* zslot = a.zd + (size_t)blockIdx.x * a.slot;  // deep sums [H/4][W/4][4]
     float* u2 = zslot + a.zd_slot;                          // level-2 subbands, same shape
@@ -345,6 +347,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
 
     if (use_tma && leader) {
         mbar_init(bar_x, 1);
+        mbar_init(bar_x + 1, 1);
         mbar_init(bar_d, 1);
         mbar_init(bar_d + 1, 1);
         mbar_init(bar_w, 1);
@@ -382,7 +385,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                 mbar_arrive_expect_tx(bar_w, (uint32_t)a.img * 4u);
                 bulk_load(wsm, wimg, (uint32_t)a.img * 4u, bar_w);
                 mbar_arrive_expect_tx(bar_x, XBox<K, T>::BYTES);
-                tma_load_3d(raw, &a.tmx, -XBox<K, T>::XOFF, -2 * R, (int)plane, bar_x);
+                tma_load_3d(sm + a.o_raw, &a.tmx, -XBox<K, T>::XOFF, -2 * R, (int)plane, bar_x);
             }
             if (use_tma && a.L >= 2) {  // first boxes of the level-2 sweep
                 constexpr int BW = SweepBox<T>::BW, BH = SweepBox<T>::BH;
@@ -427,13 +430,27 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
             mbar_arrive_expect_tx(bar_d, kDBytes);
             tma_load_3d(dblk, &a.tmd, 0, 0, (int)blockIdx.x, bar_d);
         }
+        // Tiles: raw X tiles and band-pair tiles are double-buffered, so one barrier per
+        // tile suffices: when every thread has passed barrier A(t), all of tile t - 1 is
+        // done, its buffers are free for tile t + 1 (issued right there) and a thread may
+        // widen tile t + 1 while others still filter tile t.
         const int by = tid >> 4, bx = tid & 15;  // 4x4-pixel block of this thread
+        bool ok_prev = true;                      // deep-sum wait of the previous tile
         for (int t = 0; t < ntiles; ++t) {
             const int ty = t / tiles_x, tx = t - ty * tiles_x;
             const int y0 = ty * kTile, x0 = tx * kTile;
-            float* dcur = dblk + (t & 1) * (kDBytes / 4);
-            if (a.L >= 2) {
-                if (!use_tma) {
+            const int rb = t & 1;
+            T* raw = reinterpret_cast<T*>(sm + a.o_raw + rb * a.raw_f);
+            float* bs = sm + a.o_b + rb * a.b_f;
+            float* dcur = dblk + rb * (kDBytes / 4);
+            bool ok_x = true;
+            if (use_tma) {
+                // a timed-out wait converts stale data; the vote below ends the kernel
+                ok_x = mbar_wait_bounded(bar_x + rb, (ph_x >> rb) & 1u);
+                ph_x ^= 1u << rb;
+            } else {
+                stage_raw<K, T>(xp, a.H, a.W, raw, y0, x0);
+                if (a.L >= 2) {
                     // plain copy of the 16x16 level-2 block of deep sums (zero outside)
                     const int H2 = a.Hp >> 2, W2 = a.Wp >> 2;
                     const float4* z2 = reinterpret_cast<const float4*>(zslot);
@@ -443,35 +460,23 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                     if (i0 + i < H2 && j0 + j < W2) v = z2[(size_t)(i0 + i) * W2 + j0 + j];
                     reinterpret_cast<float4*>(dcur)[tid] = v;
                 }
-            }
-            if (use_tma) {
-                // a timed-out wait converts stale data; the vote after the pass ends the kernel
-                const bool ok = mbar_wait_bounded(bar_x, ph_x);
-                ph_x ^= 1;
-                convert_raw<K, T>(raw, xs, bs, a.L >= 1);
-                if (__syncthreads_or(!ok)) {
-                    failed = true;
-                    break;
-                }
-                if (leader && t + 1 < ntiles) {  // next tile: X and its deep sums
-                    const int ny = (t + 1) / tiles_x, nx = (t + 1) - ny * tiles_x;
-                    fence_proxy_async_smem();
-                    mbar_arrive_expect_tx(bar_x, XBox<K, T>::BYTES);
-                    tma_load_3d(raw, &a.tmx, nx * kTile - XBox<K, T>::XOFF, ny * kTile - 2 * R,
-                                (int)plane, bar_x);
-                    if (a.L >= 2) {
-                        const int nb = (t + 1) & 1;
-                        mbar_arrive_expect_tx(bar_d + nb, kDBytes);
-                        tma_load_3d(dblk + nb * (kDBytes / 4), &a.tmd, nx * kTile,
-                                    (ny * kTile) >> 2, (int)blockIdx.x, bar_d + nb);
-                    }
-                }
-            } else {
-                stage_tile<K, T>(xp, a.H, a.W, a.vec, xs, y0, x0);
                 __syncthreads();
-                if (a.L >= 1) {
-                    pair_bands_from_tile<K>(xs, bs);
-                    __syncthreads();
+            }
+            if (a.L >= 1) convert_bands<K, T>(raw, bs);
+            if (__syncthreads_or(!(ok_x && ok_prev))) {  // barrier A(t)
+                failed = true;
+                break;
+            }
+            if (use_tma && leader && t + 1 < ntiles) {  // tile t + 1: X and its deep sums
+                const int ny = (t + 1) / tiles_x, nx = (t + 1) - ny * tiles_x, nb = rb ^ 1;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar_x + nb, XBox<K, T>::BYTES);
+                tma_load_3d(sm + a.o_raw + nb * a.raw_f, &a.tmx, nx * kTile - XBox<K, T>::XOFF,
+                            ny * kTile - 2 * R, (int)plane, bar_x + nb);
+                if (a.L >= 2) {
+                    mbar_arrive_expect_tx(bar_d + nb, kDBytes);
+                    tma_load_3d(dblk + nb * (kDBytes / 4), &a.tmd, nx * kTile,
+                                (ny * kTile) >> 2, (int)blockIdx.x, bar_d + nb);
                 }
             }
             if (a.L >= 1) {
@@ -497,8 +502,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                 __syncwarp();
             }
             // the deep sums are waited for just before their use; the wait is voted on at the
-            // end of the tile
-            const int db = t & 1;
+            // next barrier
             bool ok_d = true;
             const int gy = y0 + 4 * by, gx = x0 + 4 * bx;
             if (gy < a.H && gx < a.W) {
@@ -506,11 +510,11 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                 const f2x bias2 = pk2(bias, bias);
 #pragma unroll
                 for (int o = 0; o < 4; ++o) acc2[o][0] = acc2[o][1] = bias2;
-                conv_base_4x4<K>(xs + (4 * by + R) * XP + 4 * bx + R + PAD, XP, wsm, acc2);
+                conv_base_4x4_raw<K, T>(raw, by, bx, wsm, acc2);
                 if (a.L >= 1) {
                     float4 d = f4_zero();
                     if (a.L >= 2) {
-                        if (use_tma) ok_d = mbar_wait_bounded(bar_d + db, (ph_d >> db) & 1u);
+                        if (use_tma) ok_d = mbar_wait_bounded(bar_d + rb, (ph_d >> rb) & 1u);
                         d = reinterpret_cast<const float4*>(dcur)[tid];
                     }
                     const float dv[2][2] = {{d.x, d.y}, {d.z, d.w}};
@@ -558,12 +562,11 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                                 IO<T>::st(yp + (size_t)(gy + o) * a.W + gx + q, acc[o][q]);
                 }
             }
-            if (a.L >= 2 && use_tma) ph_d ^= 1u << db;
-            if (__syncthreads_or(!ok_d)) {
-                failed = true;
-                break;
-            }
+            if (a.L >= 2 && use_tma) ph_d ^= 1u << rb;
+            ok_prev = ok_d;
         }
+        // the last tile's deep-sum wait, and every thread done with this plane's tiles
+        if (!failed && __syncthreads_or(!ok_prev)) failed = true;
         if (failed) break;
         if (leader)
             *s_next = (a.next != nullptr) ? (int)gridDim.x + atomicAdd(a.next, 1) : -1;
@@ -643,26 +646,25 @@ FwdPlan fwd_plan(const wt_desc& d) {
     const int hp = padded_side(d.h, L), wp = padded_side(d.w, L);
     int off = 0;
     a.o_bar = off;
-    off += 32;  // eight mbarriers, padded to 128 bytes
+    off += 32;  // seven mbarriers and the next-plane word, padded to 128 bytes
     a.o_raw = off;
-    off += round32((XBox<K, T>::BYTES + 3) / 4);
+    a.raw_f = round32((XBox<K, T>::BYTES + 3) / 4);
+    off += 2 * a.raw_f;
     a.o_w = off;
     a.img = PG<K>::WS * (1 + 2 * L);
     off += a.img;
     off = round32(off);
     a.o_b = off;
-    off += 2 * PG<K>::PTILE;
-    off = round4(off);
-    a.o_z = off;
-    off += 2 * PG<K>::ZTILE;
-    // the level-2 sweep's boxes reuse the band-pair and filtered-subband tiles
+    a.b_f = round32(2 * PG<K>::PTILE);
+    off += 2 * a.b_f;
+    // the level-2 sweep's boxes reuse the band-pair tiles
     const int sweep_end = a.o_b + SweepBox<T>::NBUF * SweepBox<T>::BYTES / 4;
     if (off < sweep_end) off = round32(sweep_end);
-    // the full-resolution phase's X tile + deep-sum blocks and the deep phase's carriers +
-    // Z^(l >= 3) share a region
+    // the full-resolution phase's filtered pairs + deep-sum blocks and the deep phase's
+    // carriers + Z^(l >= 3) share a region
     const int alias0 = round32(off);
-    a.o_x = alias0;
-    a.o_dblk = round32(alias0 + FG<K>::XROWS * FG<K>::XPITCH);
+    a.o_z = alias0;
+    a.o_dblk = round32(alias0 + 2 * PG<K>::ZTILE);
     const int xend = a.o_dblk + ((L >= 2) ? 2 * kDBytes / 4 : 0);
     // deep-level state: carriers X^(2..L-1), then Z^(3..L), each 16-byte aligned
     int deep = 0;

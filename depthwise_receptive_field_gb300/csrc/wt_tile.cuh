@@ -402,6 +402,112 @@ __device__ __forceinline__ void load_block4x4(const T* xp, int H, int W, int vec
     }
 }
 
+// The level-1 band-pair tiles alone from the raw tile (the base filter reads the raw tile
+// itself): one item = two horizontally adjacent cells (a 2x4 pixel block).
+template <int K, typename T>
+__device__ __forceinline__ void convert_bands(const T* raw, float* bs) {
+    constexpr int BT = FG<K>::BT;
+    constexpr int NCR = PG<K>::NCR, PROW = PG<K>::PROW, PTILE = PG<K>::PTILE;
+    constexpr int PHALF = PG<K>::PHALF;
+    constexpr int RW = XBox<K, T>::XBW, C0 = XBox<K, T>::C0;
+    for (int idx = threadIdx.x; idx < BT * NCR; idx += blockDim.x) {
+        const int ci = idx / NCR, m = idx - ci * NCR;
+        const T* r0 = raw + (2 * ci) * RW + C0 + 4 * m;
+        float2 a0, a1, b0, b1;
+        if constexpr (C0 % 4 == 0) {  // 4-element aligned: one vector load per row
+            const float4 ra = ld4_smem<T>(r0), rb = ld4_smem<T>(r0 + RW);
+            a0 = make_float2(ra.x, ra.y); a1 = make_float2(ra.z, ra.w);
+            b0 = make_float2(rb.x, rb.y); b1 = make_float2(rb.z, rb.w);
+        } else {
+            a0 = ld2_smem<T>(r0); a1 = ld2_smem<T>(r0 + 2);
+            b0 = ld2_smem<T>(r0 + RW); b1 = ld2_smem<T>(r0 + RW + 2);
+        }
+        const float4 u = haar_u(a0.x, a0.y, b0.x, b0.y);
+        const float4 v = haar_u(a1.x, a1.y, b1.x, b1.y);
+        float* q = bs + ci * PROW + 4 * pchunk(m, PHALF);
+        *reinterpret_cast<float4*>(q) = make_float4(u.x, u.y, v.x, v.y);
+        *reinterpret_cast<float4*>(q + PTILE) = make_float4(u.z, u.w, v.z, v.w);
+    }
+}
+
+// Non-TMA staging of a raw tile: element (rr, cc) of the XBox layout is pixel
+// (y0 - 2R + rr, x0 - XOFF + cc) of the plane, zero outside it (element loads: any row
+// alignment).
+template <int K, typename T>
+__device__ __forceinline__ void stage_raw(const T* xp, int H, int W, T* raw, int y0, int x0) {
+    constexpr int R = FG<K>::R, RW = XBox<K, T>::XBW, RH = XBox<K, T>::XBH;
+    constexpr int XOFF = XBox<K, T>::XOFF;
+    for (int idx = threadIdx.x; idx < RH * RW; idx += blockDim.x) {
+        const int rr = idx / RW, cc = idx - rr * RW;
+        const int gy = y0 - 2 * R + rr, gx = x0 - XOFF + cc;
+        raw[idx] = (gy >= 0 && gy < H && gx >= 0 && gx < W) ? xp[(size_t)gy * W + gx]
+                                                             : static_cast<T>(0.f);
+    }
+}
+
+// N consecutive raw elements starting P (0 or 1) past the 2-element-aligned pointer p,
+// widened to float: 32-bit loads for 16-bit types, 64-bit loads for fp32.
+template <typename T, int N, int P>
+__device__ __forceinline__ void load_raw_run(const T* p, float (&v)[N]) {
+    constexpr int NW = (N + P + 1) / 2;  // 2-element words
+    float e[2 * NW];
+#pragma unroll
+    for (int j = 0; j < NW; ++j) {
+        const float2 t = ld2_smem<T>(p + 2 * j);
+        e[2 * j] = t.x;
+        e[2 * j + 1] = t.y;
+    }
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = e[i + P];
+}
+
+// Packed base k x k filter of the 4x4 pixel block (by, bx) of a tile, read from the raw tile
+// (widened in registers), accumulating onto acc[o][p] = (pixel (o, 2p), pixel (o, 2p+1)).
+// Window row r is raw row 4by + R + r; window column j is raw column 4bx + XOFF - R + j.
+// wdup = KK taps as (w, w) pairs.
+template <int K, typename T>
+__device__ __forceinline__ void conv_base_4x4_raw(const T* raw, int by, int bx,
+                                                  const float* wdup, f2x (&acc)[4][2]) {
+    constexpr int R = FG<K>::R, KK = FG<K>::KK;
+    constexpr int RW = XBox<K, T>::XBW, S = XBox<K, T>::XOFF - R;
+    constexpr int P = S & 1, NV = 4 + 2 * R;
+    f2x w[KK];
+#pragma unroll
+    for (int q = 0; q + 1 < KK; q += 2) {
+        const float4 t = *reinterpret_cast<const float4*>(wdup + 2 * q);
+        w[q] = pk2(t.x, t.y);
+        w[q + 1] = pk2(t.z, t.w);
+    }
+    if constexpr (KK & 1) {
+        const float2 t = *reinterpret_cast<const float2*>(wdup + 2 * (KK - 1));
+        w[KK - 1] = pk2(t.x, t.y);
+    }
+    const T* base = raw + (4 * by + R) * RW + 4 * bx + (S - P);
+#pragma unroll
+    for (int r = 0; r < 4 + 2 * R; ++r) {
+        float v[NV];
+        load_raw_run<T, NV, P>(base + r * RW, v);
+        f2x A[NV / 2], B[NV / 2 - 1];
+#pragma unroll
+        for (int m = 0; m < NV / 2; ++m) A[m] = pk2(v[2 * m], v[2 * m + 1]);
+#pragma unroll
+        for (int m = 0; m < NV / 2 - 1; ++m) B[m] = pk2(v[2 * m + 1], v[2 * m + 2]);
+#pragma unroll
+        for (int o = 0; o < 4; ++o) {
+            const int u = r - o;
+            if (u < 0 || u >= K) continue;
+#pragma unroll
+            for (int vv = 0; vv < K; ++vv)
+#pragma unroll
+                for (int pp = 0; pp < 2; ++pp) {
+                    const int idx = 2 * pp + vv;
+                    const f2x in = (idx & 1) ? B[(idx - 1) >> 1] : A[idx >> 1];
+                    acc[o][pp] = fma2(w[u * K + vv], in, acc[o][pp]);
+                }
+        }
+    }
+}
+
 // Number of bw x bh boxes that tile an H x W plane.
 __device__ __forceinline__ int sweep_boxes(int H, int W, int bw, int bh) {
     return ((W + bw - 1) / bw) * ((H + bh - 1) / bh);
