@@ -508,6 +508,61 @@ __device__ __forceinline__ void conv_base_4x4_raw(const T* raw, int by, int bx,
     }
 }
 
+// Packed base weight-gradient correlation of the 4x4 pixel block (by, bx), read from the raw
+// tiles and widened in registers: X in the layout above (window row r is raw row
+// 4by + R + r, window column j raw column 4bx + XOFF - R + j) and the 64x64 dY tile.
+// With g[o][p] = (dY[o][2p], dY[o][2p+1]), acc[u*K+v] accumulates the even- and odd-column
+// partial sums of sum_{o,q} dY[o][q] X[o+u][q+v] (add the two halves at the end).
+template <int K, typename T>
+__device__ __forceinline__ void corr_base_4x4_raw(const T* rawx, const T* rawg, int by, int bx,
+                                                  f2x (&acc)[K * K]) {
+    constexpr int R = FG<K>::R;
+    constexpr int RW = XBox<K, T>::XBW, S = XBox<K, T>::XOFF - R;
+    constexpr int P = S & 1, NV = 4 + 2 * R;
+    f2x g[4][2];
+#pragma unroll
+    for (int o = 0; o < 4; ++o) {
+        const float4 t = ld4_smem<T>(rawg + (4 * by + o) * kTile + 4 * bx);
+        g[o][0] = pk2(t.x, t.y);
+        g[o][1] = pk2(t.z, t.w);
+    }
+    const T* base = rawx + (4 * by + R) * RW + 4 * bx + (S - P);
+#pragma unroll
+    for (int r = 0; r < 4 + 2 * R; ++r) {
+        float v[NV];
+        load_raw_run<T, NV, P>(base + r * RW, v);
+        f2x A[NV / 2], B[NV / 2 - 1];
+#pragma unroll
+        for (int m = 0; m < NV / 2; ++m) A[m] = pk2(v[2 * m], v[2 * m + 1]);
+#pragma unroll
+        for (int m = 0; m < NV / 2 - 1; ++m) B[m] = pk2(v[2 * m + 1], v[2 * m + 2]);
+#pragma unroll
+        for (int o = 0; o < 4; ++o) {
+            const int u = r - o;
+            if (u < 0 || u >= K) continue;
+#pragma unroll
+            for (int vv = 0; vv < K; ++vv)
+#pragma unroll
+                for (int pp = 0; pp < 2; ++pp) {
+                    const int idx = 2 * pp + vv;
+                    const f2x in = (idx & 1) ? B[(idx - 1) >> 1] : A[idx >> 1];
+                    acc[u * K + vv] = fma2(g[o][pp], in, acc[u * K + vv]);
+                }
+        }
+    }
+}
+
+// Non-TMA staging of a 64x64 raw tile without halo: element (rr, cc) is pixel
+// (y0 + rr, x0 + cc) of the plane, zero outside it.
+template <typename T>
+__device__ __forceinline__ void stage_raw_tile(const T* p, int H, int W, T* raw, int y0, int x0) {
+    for (int idx = threadIdx.x; idx < kTile * kTile; idx += blockDim.x) {
+        const int rr = idx / kTile, cc = idx - rr * kTile;
+        const int gy = y0 + rr, gx = x0 + cc;
+        raw[idx] = (gy < H && gx < W) ? p[(size_t)gy * W + gx] : static_cast<T>(0.f);
+    }
+}
+
 // Number of bw x bh boxes that tile an H x W plane.
 __device__ __forceinline__ int sweep_boxes(int H, int W, int bw, int bh) {
     return ((W + bw - 1) / bw) * ((H + bh - 1) / bh);

@@ -12,18 +12,19 @@
 // planes. Per plane:
 //   level-2 sweep (L >= 2): X and dY stream through shared memory in TMA boxes (two box
 //     pairs in flight); every 4x4 pixel block becomes its four level-2 subbands (Eq. 5
-//     twice), stored for both tensors in the CTA's workspace slot (L2-resident), and the
-//     carriers X^(2), dY^(2) for the deeper levels.
+//     twice), stored for both tensors in the CTA's workspace slot (L2-resident); LL / 2 of
+//     it is the carrier X^(2), dY^(2) of level 3.
 //   deep levels (l >= 2): 32x32 tiles of the level's subbands of X (R halo) and dY are
 //     staged as band-pair tiles, (LL, LH) and (HL, HH) (level 2 from the slot, deeper
 //     levels from the carriers); threads 0-127 correlate pair 0 and 128-255 pair 1 with
 //     packed f32x2 FMAs (2x4 coefficient blocks), flushed after each level by
 //     recursive-halving warp reductions in a fixed order.
-//   full resolution: 64x64-pixel tiles of X (2R halo) and dY arrive by TMA; the next
-//     tile's load is issued as soon as the current one has been widened to fp32, so it
-//     overlaps the correlations. Threads 0-127 run the base correlation (4x4 pixel
-//     blocks), threads 128-255 the level-1 band-pair correlations (4x4 coefficient
-//     blocks). Each thread keeps its partial sums in registers for the whole plane.
+//   full resolution: 64x64-pixel tiles of X (2R halo) and dY arrive by TMA into two
+//     buffers; the next tile's load is issued as soon as the current one's level-1
+//     band pairs are formed, so it overlaps the correlations. Threads 0-127 run the base
+//     correlation (4x4 pixel blocks, read from the raw tiles and widened in registers),
+//     threads 128-255 the level-1 band-pair correlations (4x4 coefficient blocks). Each
+//     thread keeps its partial sums in registers for the whole plane.
 //   The per-plane partial vector [dW~0 | db~ | dW~^(l)_b] goes to the workspace.
 // Kernel 2 (wt_dw_reduce_kernel): per channel, sums the N partial vectors in a fixed
 //   order and applies the gradient unfolding of §4.3 Eq. 9.
@@ -53,9 +54,13 @@ struct DwArgs {
     int Hp, Wp;  // the plane padded with zeros to multiples of 2^L: level l is (Hp, Wp) >> l
     int vec, use_tma;
     int KP;
-    int o_bar, o_rawx, o_rawg, o_acc, o_red, o_xb, o_gb, o_x, o_g;  // shared memory (floats)
-    // deep carriers X^(l), dY^(l) (l = 2..L-1): in shared memory, or (deep_global) in the
-    // CTA's slot after the two subband arrays
+    // shared memory (floats): mbarriers, raw X tiles (2 buffers of rawx_f), raw dY tiles
+    // (2 of rawg_f), the partial vector, warp totals, X and dY band-pair tiles
+    int o_bar, o_rawx, o_rawg, o_acc, o_red, o_xb, o_gb;
+    int rawx_f, rawg_f;
+    // deep carriers X^(l), dY^(l) (l = 3..L-1; X^(2) is LL / 2 of the stored level-2
+    // subbands): in shared memory, or (deep_global) in the CTA's slot after the two subband
+    // arrays
     int deep_global;
     int o_carx[kMaxLevels + 1], o_cary[kMaxLevels + 1];
 };
@@ -77,8 +82,9 @@ constexpr int kGRow = 8 * kGHalf;     // floats per row
 constexpr int kGTile = kCT * kGRow;   // floats per pair tile
 
 // Deep stage for level l: X subbands with an R halo into the X pair tiles, dY subbands of
-// the tile's own cells into the dY pair tiles. Level 2 reads the sweep's stored subbands,
-// deeper levels transform the carriers X^(l-1), dY^(l-1) and write X^(l), dY^(l) for l < L.
+// the tile's own cells into the dY pair tiles. Level 2 reads the sweep's stored subbands;
+// deeper levels transform the carriers X^(l-1), dY^(l-1) (level 3: LL / 2 of the stored
+// level-2 subbands) and write X^(l), dY^(l) for l < L.
 template <int K>
 __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const float* u2x, const float* u2g,
                                               float* sm, float* cbase, int l, int ti0,
@@ -89,8 +95,16 @@ __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const float* u2x,
     const int Hl = a.Hp >> l, Wl = a.Wp >> l, Wp = a.Wp >> (l - 1);
     float* xb = sm + a.o_xb;
     float* gb = sm + a.o_gb;
-    const float* cpx = (l >= 3) ? cbase + a.o_carx[l - 1] : nullptr;
-    const float* cpy = (l >= 3) ? cbase + a.o_cary[l - 1] : nullptr;
+    const float* cpx = (l >= 4) ? cbase + a.o_carx[l - 1] : nullptr;
+    const float* cpy = (l >= 4) ? cbase + a.o_cary[l - 1] : nullptr;
+    // 2x2 block of the carrier of level l - 1 >= 2 at (2gi, 2gj), transformed by Eq. 5
+    auto carrier_u = [&](const float* cp, const float* u2, int gi, int gj) -> float4 {
+        const size_t o = (size_t)(2 * gi) * Wp + 2 * gj;
+        if (l == 3)
+            return haar_u(0.5f * __ldcg(u2 + 4 * o), 0.5f * __ldcg(u2 + 4 * (o + 1)),
+                          0.5f * __ldcg(u2 + 4 * (o + Wp)), 0.5f * __ldcg(u2 + 4 * (o + Wp + 1)));
+        return haar_u(cp[o], cp[o + 1], cp[o + Wp], cp[o + Wp + 1]);
+    };
     float* clx = (l >= 3 && l < a.L) ? cbase + a.o_carx[l] : nullptr;
     float* cly = (l >= 3 && l < a.L) ? cbase + a.o_cary[l] : nullptr;
     const float4* ux4 = reinterpret_cast<const float4*>(u2x);
@@ -108,12 +122,10 @@ __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const float* u2x,
                 ux = __ldcg(ux4 + (size_t)gi * Wl + gj);
                 if (inner) ug = __ldcg(ug4 + (size_t)gi * Wl + gj);
             } else {
-                const float* q = cpx + (size_t)(2 * gi) * Wp + 2 * gj;
-                ux = haar_u(q[0], q[1], q[Wp], q[Wp + 1]);
+                ux = carrier_u(cpx, u2x, gi, gj);
                 if (inner) {
                     if (clx) clx[gi * Wl + gj] = 0.5f * ux.x;
-                    const float* r = cpy + (size_t)(2 * gi) * Wp + 2 * gj;
-                    ug = haar_u(r[0], r[1], r[Wp], r[Wp + 1]);
+                    ug = carrier_u(cpy, u2g, gi, gj);
                     if (cly) cly[gi * Wl + gj] = 0.5f * ug.x;
                 }
             }
@@ -131,13 +143,12 @@ __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const float* u2x,
 }
 
 // Level-2 sweep of X and dY: the unnormalized level-2 subbands of every position go to
-// u2x / u2g [H/4][W/4][4] (LL, LH, HL, HH) and, when L >= 3, the carriers X^(2) = LL / 2
-// and dY^(2) to carx / cary. TMA path: the first NB box pairs were issued at the start of
+// u2x / u2g [H/4][W/4][4] (LL, LH, HL, HH). TMA path: the first NB box pairs were issued at the start of
 // the plane; pair t + NB reuses pair t's buffers once every thread is past them. Returns
 // false if a TMA wait timed out (the vote makes the result uniform over the CTA).
 template <typename T, bool FAST>
 __device__ __forceinline__ bool dw_sweep(const DwArgs& a, const T* xp, const T* gp, float* sm,
-                                         float* carx, float* cary, float* u2x, float* u2g,
+                                         float* u2x, float* u2g,
                                          uint64_t* bar_s, uint32_t& ph_s, long long plane) {
     using S = DwSweep<T>;
     constexpr int BW = S::BW, BH = S::BH, NB = S::NB, PR = BH / 4, PC = BW / 4;
@@ -176,10 +187,6 @@ __device__ __forceinline__ bool dw_sweep(const DwArgs& a, const T* xp, const T* 
                 const size_t o = (size_t)i2 * W2 + j2;
                 __stcg(ux4 + o, ux);
                 __stcg(ug4 + o, ug);
-                if (carx != nullptr) {
-                    carx[o] = 0.5f * ux.x;
-                    cary[o] = 0.5f * ug.x;
-                }
             }
         }
     } else {
@@ -193,64 +200,27 @@ __device__ __forceinline__ bool dw_sweep(const DwArgs& a, const T* xp, const T* 
             const float4 ug = level2_block(r[0], r[1], r[2], r[3]);
             __stcg(ux4 + p, ux);
             __stcg(ug4 + p, ug);
-            if (carx != nullptr) {
-                carx[p] = 0.5f * ux.x;
-                cary[p] = 0.5f * ug.x;
-            }
         }
     }
     return true;
 }
 
-// Widen the TMA-staged raw dY tile (64x64) to the fp32 dY tile and, when `bands`, form
-// its level-1 unnormalized subbands in the dY pair tiles. One item = 2x4 pixels. Returns
-// this thread's sum of the dY values it converted.
+// Level-1 unnormalized subbands of the raw dY tile (64x64, no halo) into the dY pair tiles
+// (when `bands`); returns this thread's sum of the dY values it read. One item = 2x4 pixels.
 template <typename T>
-__device__ __forceinline__ float convert_raw_dy(const T* raw, float* gs, float* gb, bool bands) {
+__device__ __forceinline__ float convert_raw_dy(const T* raw, float* gb, bool bands) {
     float sum = 0.f;
     for (int idx = threadIdx.x; idx < kCT * (kCT / 2); idx += blockDim.x) {
         const int ci = idx >> 4, m = idx & 15;
         const T* r0 = raw + (2 * ci) * kTile + 4 * m;
         const float4 ra = ld4_smem<T>(r0), rb = ld4_smem<T>(r0 + kTile);
-        const float2 a0 = make_float2(ra.x, ra.y), a1 = make_float2(ra.z, ra.w);
-        const float2 b0 = make_float2(rb.x, rb.y), b1 = make_float2(rb.z, rb.w);
-        float* d0 = gs + (2 * ci) * kTile + 4 * m;
-        *reinterpret_cast<float4*>(d0) = make_float4(a0.x, a0.y, a1.x, a1.y);
-        *reinterpret_cast<float4*>(d0 + kTile) = make_float4(b0.x, b0.y, b1.x, b1.y);
-        sum += ((a0.x + a0.y) + (a1.x + a1.y)) + ((b0.x + b0.y) + (b1.x + b1.y));
+        sum += ((ra.x + ra.y) + (ra.z + ra.w)) + ((rb.x + rb.y) + (rb.z + rb.w));
         if (bands) {
-            const float4 u = haar_u(a0.x, a0.y, b0.x, b0.y);
-            const float4 v = haar_u(a1.x, a1.y, b1.x, b1.y);
+            const float4 u = haar_u(ra.x, ra.y, rb.x, rb.y);
+            const float4 v = haar_u(ra.z, ra.w, rb.z, rb.w);
             float* q = gb + ci * kGRow + 4 * pchunk(m, kGHalf);
             *reinterpret_cast<float4*>(q) = make_float4(u.x, u.y, v.x, v.y);
             *reinterpret_cast<float4*>(q + kGTile) = make_float4(u.z, u.w, v.z, v.w);
-        }
-    }
-    return sum;
-}
-
-// Non-TMA staging of the dY tile (fp32 tile + pair tiles), zero outside the plane.
-// Returns this thread's sum of the dY values it staged.
-template <typename T>
-__device__ __forceinline__ float stage_dy_plain(const T* gp, int H, int W, float* gs, float* gb,
-                                                bool bands, int y0, int x0) {
-    float sum = 0.f;
-    for (int idx = threadIdx.x; idx < kCT * kCT; idx += blockDim.x) {
-        const int ci = idx / kCT, cj = idx - ci * kCT;
-        float v[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int gy = y0 + 2 * ci + (e >> 1), gx = x0 + 2 * cj + (e & 1);
-            v[e] = (gy < H && gx < W) ? IO<T>::ld(gp + (size_t)gy * W + gx) : 0.f;
-        }
-        float* d0 = gs + (2 * ci) * kTile + 2 * cj;
-        d0[0] = v[0]; d0[1] = v[1]; d0[kTile] = v[2]; d0[kTile + 1] = v[3];
-        sum += (v[0] + v[1]) + (v[2] + v[3]);
-        if (bands) {
-            const float4 u = haar_u(v[0], v[1], v[2], v[3]);
-            float* q = gb + ci * kGRow + 4 * pchunk(cj >> 1, kGHalf) + 2 * (cj & 1);
-            *reinterpret_cast<float2*>(q) = make_float2(u.x, u.y);
-            *reinterpret_cast<float2*>(q + kGTile) = make_float2(u.z, u.w);
         }
     }
     return sum;
@@ -312,22 +282,20 @@ __device__ __forceinline__ void warp_totals_to(const f2x (&acc)[NQ], float extra
 // carriers in shared memory, so those checks and the other paths are compiled out.
 template <int K, typename T, bool FAST>
 __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(const __grid_constant__ DwArgs a) {
-    constexpr int R = FG<K>::R, KK = FG<K>::KK, PAD = FG<K>::PAD, XP = FG<K>::XPITCH;
+    constexpr int R = FG<K>::R, KK = FG<K>::KK;
     constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE;
     using S = DwSweep<T>;
     extern __shared__ __align__(128) float4 smem_f4[];
     float* sm = reinterpret_cast<float*>(smem_f4);
-    // mbarriers: the full-resolution tile pair, then the level-2 sweep's box pairs
+    // mbarriers: the full-resolution tile pairs (2 buffers), then the level-2 sweep's box
+    // pairs
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + a.o_bar);
-    uint64_t* bar_s = bar + 1;
-    T* rawx = reinterpret_cast<T*>(sm + a.o_rawx);
-    T* rawg = reinterpret_cast<T*>(sm + a.o_rawg);
+    uint64_t* bar_s = bar + 2;
+    static_assert(DwSweep<T>::NB <= 4, "mbarrier slots");
     float* acc_sm = sm + a.o_acc;
     float* red = sm + a.o_red;  // [8 warps][128]
     float* xb = sm + a.o_xb;
     float* gb = sm + a.o_gb;
-    float* xs = sm + a.o_x;
-    float* gs = sm + a.o_g;
     const int tid = threadIdx.x, warp = tid >> 5;
     const bool leader = tid == 0;
     const bool use_tma = FAST || a.use_tma;
@@ -335,8 +303,6 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
     float* u2x = slot;
     float* u2g = slot + a.u2_floats;
     float* cbase = (!FAST && a.deep_global) ? slot + 2 * a.u2_floats : sm;  // carriers
-    float* carx = (a.L >= 3) ? cbase + a.o_carx[2] : nullptr;
-    float* cary = (a.L >= 3) ? cbase + a.o_cary[2] : nullptr;
     const size_t plane_elems = (size_t)a.H * a.W;
     const int tiles_x = (a.W + kTile - 1) / kTile;
     const int ntiles = tiles_x * ((a.H + kTile - 1) / kTile);
@@ -344,6 +310,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
 
     if (use_tma && leader) {
         mbar_init(bar, 1);
+        mbar_init(bar + 1, 1);
         for (int b = 0; b < S::NB; ++b) mbar_init(bar_s + b, 1);
         fence_mbar_init();
     }
@@ -365,8 +332,8 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
             // first box pairs of the level-2 sweep
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(bar, BYTES);
-            tma_load_3d(rawx, &a.tmx, -XBox<K, T>::XOFF, -2 * R, (int)plane, bar);
-            tma_load_3d(rawg, &a.tmg, 0, 0, (int)plane, bar);
+            tma_load_3d(sm + a.o_rawx, &a.tmx, -XBox<K, T>::XOFF, -2 * R, (int)plane, bar);
+            tma_load_3d(sm + a.o_rawg, &a.tmg, 0, 0, (int)plane, bar);
             if (a.L >= 2) {
                 constexpr int BW = S::BW, BH = S::BH;
                 const int bxn = (a.Wp + BW - 1) / BW, nbox = sweep_boxes(a.Hp, a.Wp, BW, BH);
@@ -385,7 +352,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
 
         // ---- deep levels l = 2..L: band pair pp = tid / 128, 2x4 block per thread ----
         if (a.L >= 2) {
-            if (!dw_sweep<T, FAST>(a, xp, gp, sm, carx, cary, u2x, u2g, bar_s, ph_s, plane)) {
+            if (!dw_sweep<T, FAST>(a, xp, gp, sm, u2x, u2g, bar_s, ph_s, plane)) {
                 failed = true;
                 break;
             }
@@ -442,34 +409,38 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
         red[tid] = 0.f;
         red[kDT + tid] = 0.f;
         float dpart = 0.f;
+        // Raw tiles are double-buffered: tile t + 1's pair is issued as soon as tile t's is
+        // converted (barrier B1), into the buffers tile t - 1 freed at its barrier B2.
         for (int t = 0; t < ntiles; ++t) {
             const int ty = t / tiles_x, tx = t - ty * tiles_x;
             const int y0 = ty * kTile, x0 = tx * kTile;
+            const int rb = t & 1;
+            const T* rawx = reinterpret_cast<const T*>(sm + a.o_rawx + rb * a.rawx_f);
+            const T* rawg = reinterpret_cast<const T*>(sm + a.o_rawg + rb * a.rawg_f);
+            bool ok = true;
             if (use_tma) {
-                const bool ok = mbar_wait_bounded(bar, ph);
-                ph ^= 1;
-                if (__syncthreads_or(!ok)) {
-                    failed = true;
-                    break;
-                }
-                convert_raw<K, T>(rawx, xs, xb, a.L >= 1);
-                dpart += convert_raw_dy<T>(rawg, gs, gb, a.L >= 1);
-                __syncthreads();
-                if (leader && t + 1 < ntiles) {
-                    const int ny = (t + 1) / tiles_x, nx = (t + 1) - ny * tiles_x;
-                    mbar_arrive_expect_tx(bar, BYTES);
-                    tma_load_3d(rawx, &a.tmx, nx * kTile - XBox<K, T>::XOFF, ny * kTile - 2 * R,
-                                (int)plane, bar);
-                    tma_load_3d(rawg, &a.tmg, nx * kTile, ny * kTile, (int)plane, bar);
-                }
+                // a timed-out wait converts stale data; the vote below ends the kernel
+                ok = mbar_wait_bounded(bar + rb, (ph >> rb) & 1u);
+                ph ^= 1u << rb;
             } else {
-                stage_tile<K, T>(xp, a.H, a.W, a.vec, xs, y0, x0);
-                dpart += stage_dy_plain<T>(gp, a.H, a.W, gs, gb, a.L >= 1, y0, x0);
+                stage_raw<K, T>(xp, a.H, a.W, const_cast<T*>(rawx), y0, x0);
+                stage_raw_tile<T>(gp, a.H, a.W, const_cast<T*>(rawg), y0, x0);
                 __syncthreads();
-                if (a.L >= 1) {
-                    pair_bands_from_tile<K>(xs, xb);
-                    __syncthreads();
-                }
+            }
+            if (a.L >= 1) convert_bands<K, T>(rawx, xb);
+            dpart += convert_raw_dy<T>(rawg, gb, a.L >= 1);
+            if (__syncthreads_or(!ok)) {  // B1(t)
+                failed = true;
+                break;
+            }
+            if (use_tma && leader && t + 1 < ntiles) {
+                const int ny = (t + 1) / tiles_x, nx = (t + 1) - ny * tiles_x, nb = rb ^ 1;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar + nb, BYTES);
+                tma_load_3d(sm + a.o_rawx + nb * a.rawx_f, &a.tmx, nx * kTile - XBox<K, T>::XOFF,
+                            ny * kTile - 2 * R, (int)plane, bar + nb);
+                tma_load_3d(sm + a.o_rawg + nb * a.rawg_f, &a.tmg, nx * kTile, ny * kTile,
+                            (int)plane, bar + nb);
             }
             if ((t & 15) == 15 || t + 1 == ntiles) {
                 kahan_add(red, dpart);
@@ -481,14 +452,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
                     const int blk = tid + kDT / 2 * k;  // L == 0: tid covers all 256 blocks
                     const int by = blk >> 4, bx = blk & 15;
                     if (y0 + 4 * by >= a.H || x0 + 4 * bx >= a.W) continue;
-                    f2x g[4][2];
-#pragma unroll
-                    for (int o = 0; o < 4; ++o) {
-                        const float4 tv = *reinterpret_cast<const float4*>(gs + (4 * by + o) * kTile + 4 * bx);
-                        g[o][0] = pk2(tv.x, tv.y);
-                        g[o][1] = pk2(tv.z, tv.w);
-                    }
-                    corr_base_4x4<K>(xs + (4 * by + R) * XP + 4 * bx + R + PAD, XP, g, acc);
+                    corr_base_4x4_raw<K, T>(rawx, rawg, by, bx, acc);
                 }
             } else {
                 const int t2 = tid - 128, pp = t2 >> 6, bi = (t2 >> 3) & 7, bj = t2 & 7;
@@ -507,7 +471,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
                     corr_pair<K, 4>(xb + pp * PTILE + (4 * bi) * PROW, bj, g, acc);
                 }
             }
-            __syncthreads();
+            __syncthreads();  // B2(t): the band-pair tiles and raw buffer rb are free
         }
         if (failed) break;
 
@@ -618,11 +582,13 @@ DwPlan dw_layout(const wt_desc& d) {
     a.KP = KK + 1 + 4 * KK * L;
     int off = 0;
     a.o_bar = off;
-    off += 32;  // mbarriers, padded to 128 bytes
+    off += 32;  // mbarriers and the next-plane word, padded to 128 bytes
     a.o_rawx = off;
-    off += round32((XBox<K, T>::BYTES + 3) / 4);
+    a.rawx_f = round32((XBox<K, T>::BYTES + 3) / 4);
+    off += 2 * a.rawx_f;
     a.o_rawg = off;
-    off += round32(kTile * kTile * (int)sizeof(T) / 4);
+    a.rawg_f = round32(kTile * kTile * (int)sizeof(T) / 4);
+    off += 2 * a.rawg_f;
     a.o_acc = off;
     off += round32(a.KP);
     a.o_red = off;
@@ -635,16 +601,12 @@ DwPlan dw_layout(const wt_desc& d) {
     // the level-2 sweep's box pairs reuse the band-pair tiles (and the space after them)
     const int sweep_end = a.o_xb + 2 * DwSweep<T>::NB * DwSweep<T>::BOXF;
     if (off < sweep_end) off = sweep_end;
-    // the fp32 X and dY tiles share their region with the deep-level carriers
-    const int alias0 = round32(off);
-    a.o_x = alias0;
-    off = alias0 + FG<K>::XROWS * FG<K>::XPITCH;
-    off = round4(off);
-    a.o_g = off;
-    off += kTile * kTile;
+    // the deep-level carriers X^(l), dY^(l), l = 3..L-1, after everything else
+    off = round32(off);
+    const int alias0 = off;
     int cp = 0;
     for (int l = 0; l <= kMaxLevels; ++l) a.o_carx[l] = a.o_cary[l] = 0;
-    for (int l = 2; l < L; ++l) {
+    for (int l = 3; l < L; ++l) {
         const int sz = round4((hp >> l) * (wp >> l));
         a.o_carx[l] = cp;
         cp += sz;
@@ -659,7 +621,7 @@ DwPlan dw_layout(const wt_desc& d) {
     const int local_end = alias0 + cp > off ? alias0 + cp : off;
     a.deep_global = (cp > 0 && (size_t)local_end * sizeof(float) > limit) ? 1 : 0;
     if (!a.deep_global)
-        for (int l = 2; l < L; ++l) {
+        for (int l = 3; l < L; ++l) {
             a.o_carx[l] += alias0;
             a.o_cary[l] += alias0;
         }
