@@ -7,18 +7,19 @@
 //   deep phase (L >= 2) -- a first sweep streams X through shared memory in TMA boxes
 //     (several in flight) and turns every 4x4 pixel block into the four subbands of level
 //     2 (§4.1 Eq. 5 twice: the level-1 carrier X^(1), then its Haar transform), stored in
-//     the CTA's scratch slot, and into the carrier X^(2) in shared memory. Levels l = 3..L
-//     then run from the carriers at their own resolution, and level 2 from the stored
-//     subbands: 32x32 output tiles of the subbands are staged with an R-coefficient halo
+//     the CTA's scratch slot; LL / 2 of them is the carrier X^(2). Levels l = 3..L then run
+//     from the carriers at their own resolution, and level 2 from the stored subbands: 32x32 output tiles of the subbands are staged with an R-coefficient halo
 //     and filtered by the four folded k x k kernels (§4.3 Eq. 8). A last pass sums Eq. 7's
 //     terms of levels 2..L at level-1 resolution (§4.2 Prop. 2: coefficient address by
 //     coordinate shifts, signs by coordinate bits) into the scratch slot.
 //   full-resolution phase -- 64x64-pixel tiles: a TMA load brings the tile of X with a
-//     2R halo (zero outside the plane) into shared memory while the previous tile is being
-//     computed; one pass widens it to fp32 and forms the four level-1 subbands; four
-//     streaming 4x4-block passes filter the subbands; a last pass computes the base k x k
-//     convolution and stores, in the same write, base + level-1 synthesis (Eq. 7's l = 1
-//     term) + the deep sum (TMA-loaded per tile).
+//     2R halo (zero outside the plane) into one of two shared-memory buffers while the
+//     previous tile is being computed; one pass forms the four level-1 subbands as two
+//     band-pair tiles (also double-buffered, so one CTA barrier per tile suffices); each
+//     warp filters the band pairs of its own coefficient rows; a last pass computes the
+//     base k x k convolution straight from the raw tile (widened in registers) and
+//     stores, in the same write, base + level-1 synthesis (Eq. 7's l = 1 term) + the deep
+//     sum (TMA-loaded per tile).
 //
 // Backward-data is the same operator on dY with every kernel rotated by 180 degrees and
 // no bias (§2.2 Eq. 1: the adjoint of analysis is synthesis; the adjoint of
@@ -55,6 +56,9 @@ struct FwdArgs {
     // tiles (2), filtered level-1 band pairs, deep-sum blocks (2)
     int o_bar, o_raw, o_dblk, o_w, o_b, o_z;
     int raw_f, b_f;  // floats per raw-tile buffer and per band-pair buffer
+    int b_step;      // floats between the two band-pair buffers (0: a single buffer)
+    int o_dz;        // the deep levels' filtered level-2 pairs (floats)
+    int car2;        // the carrier X^(2) is kept in the deep state (else re-read from u2)
     // deep-level state, in shared memory or (deep_global) in the CTA's workspace slot:
     int deep_global;
     int o_car[kMaxLevels + 1];                    // carriers X^(l), l = 2..L-1
@@ -107,9 +111,10 @@ struct SweepBox {
 };
 
 // Level-2 sweep: the unnormalized subbands of every level-2 position go to u2
-// [H/4][W/4][4] (LL, LH, HL, HH) and, when L >= 3, the carrier X^(2) = LL / 2 to shared
-// memory. TMA path: the first NBUF boxes were issued at the start of the plane; box t + NBUF
-// reuses box t's buffer once every thread is past it. Returns false if a TMA wait timed
+// [H/4][W/4][4] (LL, LH, HL, HH); LL / 2 of it is the carrier X^(2), also written to the
+// deep state when it is kept there. TMA path: the first
+// NBUF boxes were issued at the start of the plane; box t + NBUF reuses box t's buffer once
+// every thread is past it. Returns false if a TMA wait timed
 // out (the vote makes the result uniform over the CTA).
 template <typename T, bool FAST>
 __device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, float* sm, float* deep,
@@ -118,8 +123,8 @@ __device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, floa
     constexpr int BW = SweepBox<T>::BW, BH = SweepBox<T>::BH, NB = SweepBox<T>::NBUF;
     constexpr int PR = BH / 4;  // rows of level-2 positions per box
     const int H2 = a.Hp >> 2, W2 = a.Wp >> 2;
-    float* c2 = deep + a.o_car[2];
     float4* u2v = reinterpret_cast<float4*>(u2);
+    float* c2 = a.car2 ? deep + a.o_car[2] : nullptr;
     const int tid = threadIdx.x;
     if (FAST || a.use_tma) {
         T* buf = reinterpret_cast<T*>(sm + a.o_b);
@@ -151,7 +156,7 @@ __device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, floa
                                                   ld4_smem<T>(q + 2 * BW),
                                                   ld4_smem<T>(q + 3 * BW));
                     __stcg(u2v + (size_t)i2 * W2 + j2, u);
-                    if (a.L >= 3) c2[i2 * W2 + j2] = 0.5f * u.x;
+                    if (c2 != nullptr) c2[i2 * W2 + j2] = 0.5f * u.x;
                 }
             }
         }
@@ -167,7 +172,7 @@ __device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, floa
                     load_block4x4<T>(xp, a.H, a.W, a.vec, 4 * i2, 4 * j2, r);
                     const float4 u = level2_block(r[0], r[1], r[2], r[3]);
                     __stcg(u2v + p, u);
-                    if (a.L >= 3) c2[p] = 0.5f * u.x;
+                    if (c2 != nullptr) c2[p] = 0.5f * u.x;
                 }
             }
         }
@@ -175,16 +180,27 @@ __device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, floa
     return true;
 }
 
-// Carriers X^(l) = LL of X^(l-1) (normalized, Eq. 5) for l = 3..L-1, in shared memory.
-__device__ __forceinline__ void deep_carriers(const FwdArgs& a, float* deep) {
+// 2x2 block of the carrier X^(l-1), l >= 3, at (2i, 2j) of its Wp-wide grid, from cp; when
+// cp is null, X^(2) as LL / 2 of the stored level-2 subbands u2.
+__device__ __forceinline__ float4 carrier_block(const float* u2, const float* cp, int i, int j,
+                                                int Wp) {
+    const size_t o = (size_t)(2 * i) * Wp + 2 * j;
+    if (cp == nullptr)
+        return make_float4(0.5f * __ldcg(u2 + 4 * o), 0.5f * __ldcg(u2 + 4 * (o + 1)),
+                           0.5f * __ldcg(u2 + 4 * (o + Wp)), 0.5f * __ldcg(u2 + 4 * (o + Wp + 1)));
+    return make_float4(cp[o], cp[o + 1], cp[o + Wp], cp[o + Wp + 1]);
+}
+
+// Carriers X^(l) = LL of X^(l-1) (normalized, Eq. 5) for l = 3..L-1, in the deep state.
+__device__ __forceinline__ void deep_carriers(const FwdArgs& a, const float* u2, float* deep) {
     for (int l = 3; l < a.L; ++l) {
         const int Hl = a.Hp >> l, Wl = a.Wp >> l, Wp = a.Wp >> (l - 1);
-        const float* cp = deep + a.o_car[l - 1];
+        const float* cp = (l >= 4 || a.car2) ? deep + a.o_car[l - 1] : nullptr;
         float* cl = deep + a.o_car[l];
         for (int p = threadIdx.x; p < Hl * Wl; p += kFT) {
             const int i = p / Wl, j = p - i * Wl;
-            const float* q = cp + (size_t)(2 * i) * Wp + 2 * j;
-            cl[p] = 0.5f * (q[0] + q[1] + q[Wp] + q[Wp + 1]);
+            const float4 q = carrier_block(u2, cp, i, j, Wp);
+            cl[p] = 0.5f * (q.x + q.y + q.z + q.w);
         }
         __syncthreads();
     }
@@ -192,17 +208,18 @@ __device__ __forceinline__ void deep_carriers(const FwdArgs& a, float* deep) {
 
 // Deep stage for level l: subbands of the 32x32 output tile at (ti0, tj0) with an R halo
 // (zero outside the level grid) into the two band-pair tiles. Level 2 reads its subbands
-// from the sweep's output (L2-resident), deeper levels transform the carrier X^(l-1) in
-// shared memory. The trip count is a compile-time constant so that all loads issue early.
-template <int K>
-__device__ __forceinline__ void deep_stage(const FwdArgs& a, const float* u2, float* sm,
-                                           const float* deep, int l, int ti0, int tj0) {
+// from the sweep's output (L2-resident), deeper levels transform the carrier X^(l-1) of the
+// deep state (X^(2), when not kept there, is LL / 2 of the sweep's output). The source is
+// chosen outside the loop, whose trip count is a compile-time constant so that all loads
+// issue early.
+template <int K, int SRC>  // SRC 0: level-2 subbands; 1: carrier cp; 2: X^(2) from u2
+__device__ __forceinline__ void deep_stage_from(const FwdArgs& a, const float* u2,
+                                                const float* cp, float* bs, int l, int ti0,
+                                                int tj0) {
     constexpr int R = FG<K>::R, BT = FG<K>::BT;
     constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, PHALF = PG<K>::PHALF;
     constexpr int NIT = (BT * BT + kFT - 1) / kFT;
     const int Hl = a.Hp >> l, Wl = a.Wp >> l, Wp = a.Wp >> (l - 1);
-    float* bs = sm + a.o_b;
-    const float* carp = (l >= 3) ? deep + a.o_car[l - 1] : nullptr;
     const float4* u2v = reinterpret_cast<const float4*>(u2);
 #pragma unroll
     for (int it = 0; it < NIT; ++it) {
@@ -212,17 +229,29 @@ __device__ __forceinline__ void deep_stage(const FwdArgs& a, const float* u2, fl
         const int gi = ti0 - R + si, gj = tj0 - R + sj;
         float4 u = f4_zero();
         if (gi >= 0 && gi < Hl && gj >= 0 && gj < Wl) {
-            if (l == 2) {
+            if constexpr (SRC == 0) {
                 u = __ldcg(u2v + (size_t)gi * Wl + gj);
             } else {
-                const float* q = carp + (size_t)(2 * gi) * Wp + 2 * gj;
-                u = haar_u(q[0], q[1], q[Wp], q[Wp + 1]);
+                const float4 q = carrier_block(u2, SRC == 1 ? cp : nullptr, gi, gj, Wp);
+                u = haar_u(q.x, q.y, q.z, q.w);
             }
         }
         float* q = bs + si * PROW + 4 * pchunk(sj >> 1, PHALF) + 2 * (sj & 1);
         *reinterpret_cast<float2*>(q) = make_float2(u.x, u.y);
         *reinterpret_cast<float2*>(q + PTILE) = make_float2(u.z, u.w);
     }
+}
+
+template <int K>
+__device__ __forceinline__ void deep_stage(const FwdArgs& a, const float* u2, float* sm,
+                                           const float* deep, int l, int ti0, int tj0) {
+    float* bs = sm + a.o_b;
+    if (l == 2)
+        deep_stage_from<K, 0>(a, u2, nullptr, bs, l, ti0, tj0);
+    else if (l >= 4 || a.car2)
+        deep_stage_from<K, 1>(a, u2, deep + a.o_car[l - 1], bs, l, ti0, tj0);
+    else
+        deep_stage_from<K, 2>(a, u2, nullptr, bs, l, ti0, tj0);
 }
 
 // Deep levels of one plane, after the level-2 sweep: carriers X^(l >= 3), levels L..3
@@ -240,10 +269,9 @@ __device__ __forceinline__ void deep_levels(const FwdArgs& a, float* sm, float* 
     float* deep = DG ? deep_g : sm;
     const float* wsm = sm + a.o_w;
     float* bs = sm + a.o_b;
-    float* zs = sm + a.o_b + a.b_f;  // the second band-pair buffer holds the filtered pairs
-    static_assert(PG<K>::ZTILE <= PG<K>::PTILE, "filtered pairs fit a band-pair buffer");
+    float* zs = sm + a.o_dz;  // filtered level-2 pairs
     const int tid = threadIdx.x;
-    deep_carriers(a, deep);
+    deep_carriers(a, u2, deep);
     for (int l = a.L; l >= 2; --l) {
         const int Hl = a.Hp >> l, Wl = a.Wp >> l;
         for (int ti0 = 0; ti0 < Hl; ti0 += kCT) {
@@ -441,7 +469,8 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
             const int y0 = ty * kTile, x0 = tx * kTile;
             const int rb = t & 1;
             T* raw = reinterpret_cast<T*>(sm + a.o_raw + rb * a.raw_f);
-            float* bs = sm + a.o_b + rb * a.b_f;
+            float* bs = sm + a.o_b + rb * a.b_step;
+            if (a.b_step == 0 && t > 0) __syncthreads();  // one band-pair buffer: tile t - 1 is done
             float* dcur = dblk + rb * (kDBytes / 4);
             bool ok_x = true;
             if (use_tma) {
@@ -638,12 +667,14 @@ constexpr size_t kErrWordBytes = 256;  // the workspace starts with the error wo
 // shared memory per CTA that still lets two CTAs share an SM
 constexpr size_t kTwoCtaSmem = 228 * 1024 / 2 - 1024;
 
+// Shared-memory layout of one CTA for nbs band-pair buffers (2: one barrier per tile; 1: an
+// extra barrier before each tile's band pass) and car2 (keep the carrier X^(2) in the deep
+// state, else read it as LL / 2 of the stored level-2 subbands). Returns the floats used
+// with the deep state in shared memory (local_end) and without it (xend); `deep` = floats
+// of the deep state.
 template <int K, typename T>
-FwdPlan fwd_plan(const wt_desc& d) {
-    FwdPlan p;
-    FwdArgs& a = p.a;
-    const int L = d.levels;
-    const int hp = padded_side(d.h, L), wp = padded_side(d.w, L);
+void fwd_layout(FwdArgs& a, int L, int hp, int wp, int nbs, int car2, int& xend, int& local_end,
+                int& deep) {
     int off = 0;
     a.o_bar = off;
     off += 32;  // seven mbarriers and the next-plane word, padded to 128 bytes
@@ -656,7 +687,18 @@ FwdPlan fwd_plan(const wt_desc& d) {
     off = round32(off);
     a.o_b = off;
     a.b_f = round32(2 * PG<K>::PTILE);
-    off += 2 * a.b_f;
+    a.b_step = (nbs == 2) ? a.b_f : 0;
+    off += nbs * a.b_f;
+    // the deep levels' filtered level-2 pairs: the second band-pair buffer, else the second
+    // raw buffer (idle during the deep phase) when large enough, else their own space
+    if (nbs == 2) {
+        a.o_dz = a.o_b + a.b_f;
+    } else if (a.raw_f >= 2 * PG<K>::ZTILE) {
+        a.o_dz = a.o_raw + a.raw_f;
+    } else {
+        a.o_dz = off;
+        off += 2 * PG<K>::ZTILE;
+    }
     // the level-2 sweep's boxes reuse the band-pair tiles
     const int sweep_end = a.o_b + SweepBox<T>::NBUF * SweepBox<T>::BYTES / 4;
     if (off < sweep_end) off = round32(sweep_end);
@@ -665,11 +707,12 @@ FwdPlan fwd_plan(const wt_desc& d) {
     const int alias0 = round32(off);
     a.o_z = alias0;
     a.o_dblk = round32(alias0 + 2 * PG<K>::ZTILE);
-    const int xend = a.o_dblk + ((L >= 2) ? 2 * kDBytes / 4 : 0);
-    // deep-level state: carriers X^(2..L-1), then Z^(3..L), each 16-byte aligned
-    int deep = 0;
+    xend = a.o_dblk + ((L >= 2) ? 2 * kDBytes / 4 : 0);
+    // deep-level state: carriers X^(2 or 3..L-1), then Z^(3..L), each 16-byte aligned
+    a.car2 = (car2 && L >= 3) ? 1 : 0;
+    deep = 0;
     for (int l = 0; l <= kMaxLevels; ++l) a.o_car[l] = a.o_zl[l] = 0;
-    for (int l = 2; l < L; ++l) {
+    for (int l = a.car2 ? 2 : 3; l < L; ++l) {
         a.o_car[l] = deep;
         deep += round4((hp >> l) * (wp >> l));
     }
@@ -677,21 +720,63 @@ FwdPlan fwd_plan(const wt_desc& d) {
         a.o_zl[l] = deep;
         deep += 4 * (hp >> l) * (wp >> l);
     }
-    // it stays in shared memory unless it would lower the occupancy the tiles alone allow
-    // (two CTAs per SM when they fit it, else one) or not fit at all; then it moves to the
-    // CTA's workspace slot, and shared memory holds the tiles only
-    const int local_end = alias0 + deep > xend ? alias0 + deep : xend;
-    const size_t limit =
-        ((size_t)xend * sizeof(float) <= kTwoCtaSmem) ? kTwoCtaSmem : kMaxSmemPerBlock;
-    a.deep_global = (deep > 0 && (size_t)local_end * sizeof(float) > limit) ? 1 : 0;
-    int total = xend;
-    if (!a.deep_global) {
-        for (int l = 2; l <= L; ++l) {
-            a.o_car[l] += alias0;
-            a.o_zl[l] += alias0;
-        }
-        total = local_end;
+    local_end = alias0 + deep > xend ? alias0 + deep : xend;
+    for (int l = 2; l <= L; ++l) {  // offsets for the shared-memory placement
+        a.o_car[l] += alias0;
+        a.o_zl[l] += alias0;
     }
+}
+
+template <int K, typename T>
+FwdPlan fwd_plan(const wt_desc& d) {
+    FwdPlan p;
+    FwdArgs& a = p.a;
+    const int L = d.levels;
+    const int hp = padded_side(d.h, L), wp = padded_side(d.w, L);
+    // Layout choice, first fit: two CTAs per SM with the deep state in shared memory (two
+    // band-pair buffers before one, X^(2) kept before re-read); else two CTAs per SM with
+    // the deep state in the CTA's workspace slot; else one CTA per SM, deep state in shared
+    // memory if it fits, else in the slot.
+    static const int kOrder[4][2] = {{2, 1}, {2, 0}, {1, 1}, {1, 0}};
+    int xend = 0, local_end = 0, deep = 0, total = 0;
+    bool chosen = false;
+    for (int i = 0; i < 4 && !chosen; ++i) {
+        fwd_layout<K, T>(a, L, hp, wp, kOrder[i][0], kOrder[i][1], xend, local_end, deep);
+        if ((size_t)local_end * sizeof(float) <= kTwoCtaSmem) {
+            a.deep_global = 0;
+            total = local_end;
+            chosen = true;
+        }
+    }
+    for (int nbs = 2; nbs >= 1 && !chosen; --nbs) {
+        fwd_layout<K, T>(a, L, hp, wp, nbs, 0, xend, local_end, deep);
+        if ((size_t)xend * sizeof(float) <= kTwoCtaSmem) {
+            a.deep_global = 1;
+            total = xend;
+            chosen = true;
+        }
+    }
+    for (int i = 0; i < 4 && !chosen; ++i) {
+        fwd_layout<K, T>(a, L, hp, wp, kOrder[i][0], kOrder[i][1], xend, local_end, deep);
+        if ((size_t)local_end * sizeof(float) <= kMaxSmemPerBlock) {
+            a.deep_global = 0;
+            total = local_end;
+            chosen = true;
+        }
+    }
+    if (!chosen) {
+        fwd_layout<K, T>(a, L, hp, wp, 2, 0, xend, local_end, deep);
+        a.deep_global = 1;
+        total = xend;
+    }
+    if (a.deep_global) {  // the deep state moves to the slot, offsets from its start
+        const int alias0 = a.o_z;
+        for (int l = 2; l <= L; ++l) {
+            a.o_car[l] -= alias0;
+            a.o_zl[l] -= alias0;
+        }
+    }
+    if (deep == 0) a.deep_global = 0;
     p.smem = (size_t)total * sizeof(float);
     // per CTA: deep sums and level-2 subbands, each [H/4][W/4][4] fp32 (+ the deep state)
     a.zd_slot = (L >= 2) ? ((4LL * (hp >> 2) * (wp >> 2) + 63) & ~63LL) : 0;

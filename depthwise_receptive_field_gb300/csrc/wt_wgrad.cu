@@ -57,6 +57,7 @@ struct DwArgs {
     // shared memory (floats): mbarriers, raw X tiles (2 buffers of rawx_f), raw dY tiles
     // (2 of rawg_f), the partial vector, warp totals, X and dY band-pair tiles
     int o_bar, o_rawx, o_rawg, o_acc, o_red, o_xb, o_gb;
+    int o_kah;  // per thread: running sum of dY and its compensation
     int rawx_f, rawg_f;
     // deep carriers X^(l), dY^(l) (l = 3..L-1; X^(2) is LL / 2 of the stored level-2
     // subbands): in shared memory, or (deep_global) in the CTA's slot after the two subband
@@ -109,6 +110,37 @@ __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const float* u2x,
     float* cly = (l >= 3 && l < a.L) ? cbase + a.o_cary[l] : nullptr;
     const float4* ux4 = reinterpret_cast<const float4*>(u2x);
     const float4* ug4 = reinterpret_cast<const float4*>(u2g);
+    if (l == 2) {  // all loads first, then all stores (loads from L2 overlap)
+        float4 uxv[NIT], ugv[NIT];
+#pragma unroll
+        for (int it = 0; it < NIT; ++it) {
+            const int idx = threadIdx.x + it * kDT;
+            const int si = idx / BT, sj = idx - si * BT;
+            const int gi = ti0 - R + si, gj = tj0 - R + sj;
+            const bool inner = si >= R && si < R + kCT && sj >= R && sj < R + kCT;
+            const bool in = idx < BT * BT && gi >= 0 && gi < Hl && gj >= 0 && gj < Wl;
+            uxv[it] = in ? __ldcg(ux4 + (size_t)gi * Wl + gj) : f4_zero();
+            ugv[it] = (in && inner) ? __ldcg(ug4 + (size_t)gi * Wl + gj) : f4_zero();
+        }
+#pragma unroll
+        for (int it = 0; it < NIT; ++it) {
+            const int idx = threadIdx.x + it * kDT;
+            if (idx >= BT * BT) break;
+            const int si = idx / BT, sj = idx - si * BT;
+            const bool inner = si >= R && si < R + kCT && sj >= R && sj < R + kCT;
+            const float4 ux = uxv[it], ug = ugv[it];
+            float* q = xb + si * PROW + 4 * pchunk(sj >> 1, PHALF) + 2 * (sj & 1);
+            *reinterpret_cast<float2*>(q) = make_float2(ux.x, ux.y);
+            *reinterpret_cast<float2*>(q + PTILE) = make_float2(ux.z, ux.w);
+            if (inner) {
+                const int ci = si - R, cj = sj - R;
+                float* r = gb + ci * kGRow + 4 * pchunk(cj >> 1, kGHalf) + 2 * (cj & 1);
+                *reinterpret_cast<float2*>(r) = make_float2(ug.x, ug.y);
+                *reinterpret_cast<float2*>(r + kGTile) = make_float2(ug.z, ug.w);
+            }
+        }
+        return;
+    }
 #pragma unroll
     for (int it = 0; it < NIT; ++it) {
         const int idx = threadIdx.x + it * kDT;
@@ -226,15 +258,16 @@ __device__ __forceinline__ float convert_raw_dy(const T* raw, float* gb, bool ba
     return sum;
 }
 
-// One compensated (Kahan) step of this thread's running sum red[tid] (with its
-// compensation in red[blockDim.x + tid]): sum += v.
-__device__ __forceinline__ void kahan_add(float* red, float v) {
+// One compensated (Kahan) step of this thread's running sum kah[tid] (with its
+// compensation in kah[blockDim.x + tid]): sum += v. In shared memory, not registers: the
+// correlation loops need every register.
+__device__ __forceinline__ void kahan_add(float* kah, float v) {
     const int t = threadIdx.x, n = blockDim.x;
-    const float s = red[t], c = red[n + t];
+    const float s = kah[t], c = kah[n + t];
     const float y = v - c;
     const float u = s + y;
-    red[n + t] = (u - s) - y;
-    red[t] = u;
+    kah[n + t] = (u - s) - y;
+    kah[t] = u;
 }
 
 // Recursive-halving warp reduction of 32 values: lane l ends with the warp total of
@@ -404,10 +437,10 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
         for (int q = 0; q < KK; ++q) acc[q] = 0ull;
         // sum of dY, taken while converting the dY tiles: a register partial over at most 16
         // tiles, folded into a compensated (Kahan) running sum so that planes of millions of
-        // pixels keep the fp32 sum accurate to a few ulps. The running sum and its
-        // compensation live in this thread's two words of `red` (idle until the flush).
-        red[tid] = 0.f;
-        red[kDT + tid] = 0.f;
+        // pixels keep the fp32 sum accurate to a few ulps
+        float* kah = sm + a.o_kah;
+        kah[tid] = 0.f;
+        kah[kDT + tid] = 0.f;
         float dpart = 0.f;
         // Raw tiles are double-buffered: tile t + 1's pair is issued as soon as tile t's is
         // converted (barrier B1), into the buffers tile t - 1 freed at its barrier B2.
@@ -443,7 +476,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
                             (int)plane, bar + nb);
             }
             if ((t & 15) == 15 || t + 1 == ntiles) {
-                kahan_add(red, dpart);
+                kahan_add(kah, dpart);
                 dpart = 0.f;
             }
             if (base_role) {
@@ -476,7 +509,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
         if (failed) break;
 
         // ---- flush: fixed-order reductions into acc_sm, then the partial vector ----
-        const float dbs = red[tid] - red[kDT + tid];
+        const float dbs = kah[tid] - kah[kDT + tid];
         __syncthreads();  // every thread has read its sum before `red` takes the warp totals
         warp_totals_to<KK, 2 * KK + 1>(acc, dbs, red + warp * 128);
         __syncthreads();
@@ -591,8 +624,24 @@ DwPlan dw_layout(const wt_desc& d) {
     off += 2 * a.rawg_f;
     a.o_acc = off;
     off += round32(a.KP);
-    a.o_red = off;
-    off += 8 * 128;
+    // warp totals of the flushes, 8 x 128 floats, with the dY sum's Kahan words in their
+    // first 2 x 256 (read before the full-resolution flush overwrites them); where that
+    // would cost the second CTA per SM, the totals use the second raw X buffer instead (idle
+    // at flush time: the deep levels run before tile 1 is issued, the full-resolution flush
+    // after the last tile) and the Kahan words get their own 2 x 256
+    static_assert(8 * 128 <= (XBox<K, T>::BYTES) / 4, "warp totals fit a raw X buffer");
+    const int tiles_rest = 2 * PG<K>::PTILE + 4 + 2 * kGTile;  // band-pair tiles (+ padding)
+    const int sweep_min = 2 * DwSweep<T>::NB * DwSweep<T>::BOXF;
+    const int tail = tiles_rest > sweep_min ? tiles_rest : sweep_min;
+    if ((size_t)(off + 8 * 128 + tail + 32) * sizeof(float) <= kTwoCtaSmem) {
+        a.o_red = off;
+        a.o_kah = off;
+        off += 8 * 128;
+    } else {
+        a.o_red = a.o_rawx + a.rawx_f;
+        a.o_kah = off;
+        off += 2 * kDT;
+    }
     a.o_xb = off;
     off += 2 * PG<K>::PTILE;
     off = round4(off);

@@ -99,7 +99,14 @@ LARGE = [  # planes whose deep-level state no longer fits in shared memory
 ]
 
 
-@pytest.mark.parametrize("n,c,h,w,k,L,dtype", EDGE + F16 + ODD + LARGE)
+LAYOUT = [  # the forward's shared-memory layouts (band-pair buffers, where X^(2) lives)
+    (1, 2, 192, 128, 7, 4, "f32"),    # one band-pair buffer (a barrier more per tile)
+    (1, 1, 256, 256, 7, 5, "bf16"),   # two buffers, X^(2) re-read from the level-2 subbands
+    (1, 1, 256, 256, 5, 5, "f32"),    # the same in fp32
+]
+
+
+@pytest.mark.parametrize("n,c,h,w,k,L,dtype", EDGE + F16 + ODD + LARGE + LAYOUT)
 def test_edge_shapes(n, c, h, w, k, L, dtype):
     wl = shape_workload(n, c, h, w, k, L, dtype, seed=1000 + h + w + k + L)
     errs, _ = run_and_compare(wl, bias_and_scale=True)
