@@ -54,6 +54,7 @@ struct DwArgs {
     int Hp, Wp;  // the plane padded with zeros to multiples of 2^L: level l is (Hp, Wp) >> l
     int vec, use_tma;
     int KP;
+    int nsw;  // level-2 sweep box pairs in flight (2..kMaxSweep)
     // shared memory (floats): mbarriers, raw X tiles (2 buffers of rawx_f), raw dY tiles
     // (2 of rawg_f), the partial vector, warp totals, X and dY band-pair tiles
     int o_bar, o_rawx, o_rawg, o_acc, o_red, o_xb, o_gb;
@@ -66,15 +67,16 @@ struct DwArgs {
     int o_carx[kMaxLevels + 1], o_cary[kMaxLevels + 1];
 };
 
-// Boxes of the level-2 sweep: 64 columns x BH rows of X or dY, 8 KB in either dtype; two
-// (X, dY) box pairs are in flight, in the band-pair tiles (idle at that time).
+// Boxes of the level-2 sweep: 64 columns x BH rows of X or dY, 8 KB in either dtype; 2 to
+// kMaxSweep (X, dY) box pairs are in flight (DwArgs::nsw, as many as shared memory allows),
+// over the band-pair tiles and the carriers (idle at that time).
+constexpr int kMaxSweep = 4;
 template <typename T>
 struct DwSweep {
     static constexpr int BW = 64;
     static constexpr int BH = sizeof(T) == 2 ? 64 : 32;
     static constexpr int BYTES = BW * BH * (int)sizeof(T);
     static constexpr int BOXF = BYTES / 4;  // floats per box
-    static constexpr int NB = 2;            // box pairs in flight
 };
 
 // dY subband-pair tiles (no halo): 32 rows x 32 cells, 16-byte chunks split even/odd.
@@ -183,7 +185,8 @@ __device__ __forceinline__ bool dw_sweep(const DwArgs& a, const T* xp, const T* 
                                          float* u2x, float* u2g,
                                          uint64_t* bar_s, uint32_t& ph_s, long long plane) {
     using S = DwSweep<T>;
-    constexpr int BW = S::BW, BH = S::BH, NB = S::NB, PR = BH / 4, PC = BW / 4;
+    constexpr int BW = S::BW, BH = S::BH, PR = BH / 4, PC = BW / 4;
+    const int NB = a.nsw;
     const int H2 = a.Hp >> 2, W2 = a.Wp >> 2;
     float4* ux4 = reinterpret_cast<float4*>(u2x);
     float4* ug4 = reinterpret_cast<float4*>(u2g);
@@ -193,14 +196,13 @@ __device__ __forceinline__ bool dw_sweep(const DwArgs& a, const T* xp, const T* 
         const int bxn = (a.Wp + BW - 1) / BW;
         const int nbox = sweep_boxes(a.Hp, a.Wp, BW, BH);
         const int pi = tid / PC, pj = tid % PC;
-        for (int t = 0; t < nbox; ++t) {
-            const int b = t % NB;
+        for (int t = 0, b = 0, nb = NB - 1; t < nbox; ++t) {  // b = t % NB, nb = (t - 1) % NB
             const bool ok = mbar_wait_bounded(bar_s + b, (ph_s >> b) & 1u);
             ph_s ^= 1u << b;
             if (__syncthreads_or(!ok)) return false;
             if (tid == 0 && t >= 1 && t - 1 + NB < nbox) {
                 // every thread is past pair t - 1: refill its buffers with pair t - 1 + NB
-                const int nt = t - 1 + NB, nb = (t - 1) % NB;
+                const int nt = t - 1 + NB;
                 const int ny = nt / bxn, nx = nt - ny * bxn;
                 mbar_arrive_expect_tx(bar_s + nb, 2 * S::BYTES);
                 tma_load_3d(buf + nb * (BW * BH), &a.tsx, nx * BW, ny * BH, (int)plane, bar_s + nb);
@@ -220,6 +222,8 @@ __device__ __forceinline__ bool dw_sweep(const DwArgs& a, const T* xp, const T* 
                 __stcg(ux4 + o, ux);
                 __stcg(ug4 + o, ug);
             }
+            nb = b;
+            b = (b + 1 == NB) ? 0 : b + 1;
         }
     } else {
         const int n = H2 * W2;
@@ -324,7 +328,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
     // pairs
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + a.o_bar);
     uint64_t* bar_s = bar + 2;
-    static_assert(DwSweep<T>::NB <= 4, "mbarrier slots");
+    static_assert(2 + kMaxSweep <= 8, "mbarriers below the next-plane word");
     float* acc_sm = sm + a.o_acc;
     float* red = sm + a.o_red;  // [8 warps][128]
     float* xb = sm + a.o_xb;
@@ -344,7 +348,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
     if (use_tma && leader) {
         mbar_init(bar, 1);
         mbar_init(bar + 1, 1);
-        for (int b = 0; b < S::NB; ++b) mbar_init(bar_s + b, 1);
+        for (int b = 0; b < a.nsw; ++b) mbar_init(bar_s + b, 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -371,12 +375,12 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
                 constexpr int BW = S::BW, BH = S::BH;
                 const int bxn = (a.Wp + BW - 1) / BW, nbox = sweep_boxes(a.Hp, a.Wp, BW, BH);
                 T* buf = reinterpret_cast<T*>(sm + a.o_xb);
-                for (int t = 0; t < S::NB && t < nbox; ++t) {
+                for (int t = 0; t < a.nsw && t < nbox; ++t) {
                     const int ny = t / bxn, nx = t - ny * bxn;
                     mbar_arrive_expect_tx(bar_s + t, 2 * S::BYTES);
                     tma_load_3d(buf + t * (BW * BH), &a.tsx, nx * BW, ny * BH, (int)plane,
                                 bar_s + t);
-                    tma_load_3d(buf + (S::NB + t) * (BW * BH), &a.tsg, nx * BW, ny * BH,
+                    tma_load_3d(buf + (a.nsw + t) * (BW * BH), &a.tsg, nx * BW, ny * BH,
                                 (int)plane, bar_s + t);
                 }
             }
@@ -631,7 +635,7 @@ DwPlan dw_layout(const wt_desc& d) {
     // after the last tile) and the Kahan words get their own 2 x 256
     static_assert(8 * 128 <= (XBox<K, T>::BYTES) / 4, "warp totals fit a raw X buffer");
     const int tiles_rest = 2 * PG<K>::PTILE + 4 + 2 * kGTile;  // band-pair tiles (+ padding)
-    const int sweep_min = 2 * DwSweep<T>::NB * DwSweep<T>::BOXF;
+    const int sweep_min = 2 * 2 * DwSweep<T>::BOXF;  // two box pairs
     const int tail = tiles_rest > sweep_min ? tiles_rest : sweep_min;
     if ((size_t)(off + 8 * 128 + tail + 32) * sizeof(float) <= kTwoCtaSmem) {
         a.o_red = off;
@@ -647,10 +651,7 @@ DwPlan dw_layout(const wt_desc& d) {
     off = round4(off);
     a.o_gb = off;
     off += 2 * kGTile;
-    // the level-2 sweep's box pairs reuse the band-pair tiles (and the space after them)
-    const int sweep_end = a.o_xb + 2 * DwSweep<T>::NB * DwSweep<T>::BOXF;
-    if (off < sweep_end) off = sweep_end;
-    // the deep-level carriers X^(l), dY^(l), l = 3..L-1, after everything else
+    // the deep-level carriers X^(l), dY^(l), l = 3..L-1, after the band-pair tiles
     off = round32(off);
     const int alias0 = off;
     int cp = 0;
@@ -662,19 +663,41 @@ DwPlan dw_layout(const wt_desc& d) {
         a.o_cary[l] = cp;
         cp += sz;
     }
-    // the carriers stay in shared memory unless they would lower the occupancy the tiles
-    // alone allow (two CTAs per SM for k <= 5 when the tiles fit it, else one) or not fit
-    // at all; then they move to the CTA's workspace slot
+    // The level-2 sweep's nsw box pairs overlay the band-pair tiles, the carriers and
+    // whatever space follows (all idle during the sweep). First fit, preferring carriers in
+    // shared memory (the FAST instantiation) and then more box pairs: two CTAs per SM (k <=
+    // 5) with carriers in shared memory and 4 or 3 pairs; with carriers in the CTA's
+    // workspace slot and 4 or 3 pairs; either placement with 2 pairs; else one CTA per SM.
     const size_t two = (K >= 7) ? kMaxSmemPerBlock : kTwoCtaSmem;
-    const size_t limit = ((size_t)off * sizeof(float) <= two) ? two : kMaxSmemPerBlock;
-    const int local_end = alias0 + cp > off ? alias0 + cp : off;
-    a.deep_global = (cp > 0 && (size_t)local_end * sizeof(float) > limit) ? 1 : 0;
+    auto end_of = [&](int nsw, bool dg) {
+        const int e = dg ? alias0 : alias0 + cp;
+        const int sw = a.o_xb + 2 * nsw * DwSweep<T>::BOXF;
+        return e > sw ? e : sw;
+    };
+    static const int kTry[6][2] = {{4, 0}, {3, 0}, {4, 1}, {3, 1}, {2, 0}, {2, 1}};
+    int total = -1;
+    for (size_t lim : {two, kMaxSmemPerBlock}) {
+        for (int i = 0; i < 6 && total < 0; ++i) {
+            const bool dg = kTry[i][1] != 0;
+            if (dg && cp == 0) continue;
+            if ((size_t)end_of(kTry[i][0], dg) * sizeof(float) <= lim) {
+                a.nsw = kTry[i][0];
+                a.deep_global = dg ? 1 : 0;
+                total = end_of(a.nsw, dg);
+            }
+        }
+        if (total >= 0) break;
+    }
+    if (total < 0) {  // too large for shared memory: reported as unsupported by the caller
+        a.nsw = 2;
+        a.deep_global = cp > 0 ? 1 : 0;
+        total = end_of(2, a.deep_global != 0);
+    }
     if (!a.deep_global)
         for (int l = 3; l < L; ++l) {
             a.o_carx[l] += alias0;
             a.o_cary[l] += alias0;
         }
-    const int total = a.deep_global ? off : local_end;
     p.smem = (size_t)total * sizeof(float);
     // per CTA: the level-2 subbands of X and of dY, [H/4][W/4][4] fp32 each (+ carriers)
     a.u2_floats = (L >= 2) ? ((4LL * (hp >> 2) * (wp >> 2) + 63) & ~63LL) : 0;
