@@ -81,6 +81,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
+// One arrival on `bar` (release semantics: this thread's earlier shared-memory accesses are
+// ordered before a waiter's acquire).
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 // Bulk copy of `bytes` contiguous bytes from global to shared memory, completing on `bar`
 // (both addresses 16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,

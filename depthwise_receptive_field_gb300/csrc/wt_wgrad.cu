@@ -10,8 +10,9 @@
 //
 // Kernel 1 (wt_dw_plane_kernel): a persistent grid of 256-thread CTAs walks the (n, c)
 // planes. Per plane:
-//   level-2 sweep (L >= 2): X and dY stream through shared memory in TMA boxes (two box
-//     pairs in flight); every 4x4 pixel block becomes its four level-2 subbands (Eq. 5
+//   level-2 sweep (L >= 2): X and dY stream through shared memory in TMA boxes (2 to 4
+//     box pairs in flight, as shared memory allows; each warp releases a pair on an
+//     mbarrier, and the pair is refilled once all eight have, with no CTA barrier); every 4x4 pixel block becomes its four level-2 subbands (Eq. 5
 //     twice), stored for both tensors in the CTA's workspace slot (L2-resident); LL / 2 of
 //     it is the carrier X^(2), dY^(2) of level 3.
 //   deep levels (l >= 2): 32x32 tiles of the level's subbands of X (R halo) and dY are
@@ -177,13 +178,18 @@ __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const float* u2x,
 }
 
 // Level-2 sweep of X and dY: the unnormalized level-2 subbands of every position go to
-// u2x / u2g [H/4][W/4][4] (LL, LH, HL, HH). TMA path: the first NB box pairs were issued at the start of
-// the plane; pair t + NB reuses pair t's buffers once every thread is past them. Returns
-// false if a TMA wait timed out (the vote makes the result uniform over the CTA).
+// u2x / u2g [H/4][W/4][4] (LL, LH, HL, HH). TMA path: the first NB box pairs were issued at
+// the start of the plane; pair t + NB reuses pair t's buffers. With NB >= 3 a CTA barrier
+// after each pair's wait frees the previous pair's buffers. With NB = 2 there is no CTA
+// barrier per pair: every warp arrives on bar_e[b] (8 arrivals) when it is done with
+// buffer b, and thread 0 waits for that before refilling it, so warps may run apart. Every
+// wait is bounded; a timeout sets *s_abort, after which no thread waits again, and the vote
+// at the end returns false (uniform over the CTA).
 template <typename T, bool FAST>
 __device__ __forceinline__ bool dw_sweep(const DwArgs& a, const T* xp, const T* gp, float* sm,
-                                         float* u2x, float* u2g,
-                                         uint64_t* bar_s, uint32_t& ph_s, long long plane) {
+                                         float* u2x, float* u2g, uint64_t* bar_s,
+                                         uint64_t* bar_e, uint32_t& ph_s, uint32_t& ph_e,
+                                         volatile int* s_abort, long long plane) {
     using S = DwSweep<T>;
     constexpr int BW = S::BW, BH = S::BH, PR = BH / 4, PC = BW / 4;
     const int NB = a.nsw;
@@ -196,19 +202,8 @@ __device__ __forceinline__ bool dw_sweep(const DwArgs& a, const T* xp, const T* 
         const int bxn = (a.Wp + BW - 1) / BW;
         const int nbox = sweep_boxes(a.Hp, a.Wp, BW, BH);
         const int pi = tid / PC, pj = tid % PC;
-        for (int t = 0, b = 0, nb = NB - 1; t < nbox; ++t) {  // b = t % NB, nb = (t - 1) % NB
-            const bool ok = mbar_wait_bounded(bar_s + b, (ph_s >> b) & 1u);
-            ph_s ^= 1u << b;
-            if (__syncthreads_or(!ok)) return false;
-            if (tid == 0 && t >= 1 && t - 1 + NB < nbox) {
-                // every thread is past pair t - 1: refill its buffers with pair t - 1 + NB
-                const int nt = t - 1 + NB;
-                const int ny = nt / bxn, nx = nt - ny * bxn;
-                mbar_arrive_expect_tx(bar_s + nb, 2 * S::BYTES);
-                tma_load_3d(buf + nb * (BW * BH), &a.tsx, nx * BW, ny * BH, (int)plane, bar_s + nb);
-                tma_load_3d(buf + (NB + nb) * (BW * BH), &a.tsg, nx * BW, ny * BH, (int)plane,
-                            bar_s + nb);
-            }
+        // this thread's level-2 position of pair t (in buffers b)
+        auto pair = [&](int t, int b) {
             const int by = t / bxn, bx = t - by * bxn;
             const int i2 = by * PR + pi, j2 = bx * PC + pj;
             if (pi < PR && i2 < H2 && j2 < W2) {
@@ -222,9 +217,56 @@ __device__ __forceinline__ bool dw_sweep(const DwArgs& a, const T* xp, const T* 
                 __stcg(ux4 + o, ux);
                 __stcg(ug4 + o, ug);
             }
+        };
+        auto refill = [&](int nt, int nb) {  // pair nt into buffers nb
+            const int ny = nt / bxn, nx = nt - ny * bxn;
+            mbar_arrive_expect_tx(bar_s + nb, 2 * S::BYTES);
+            tma_load_3d(buf + nb * (BW * BH), &a.tsx, nx * BW, ny * BH, (int)plane, bar_s + nb);
+            tma_load_3d(buf + (NB + nb) * (BW * BH), &a.tsg, nx * BW, ny * BH, (int)plane,
+                        bar_s + nb);
+        };
+        if (NB >= 3) {
+            // three or more pairs in flight: one CTA barrier per pair (measured faster here
+            // than the per-warp releases below, which win with two pairs)
+            for (int t = 0, b = 0, nb = NB - 1; t < nbox; ++t) {
+                const bool okb = mbar_wait_bounded(bar_s + b, (ph_s >> b) & 1u);
+                ph_s ^= 1u << b;
+                if (__syncthreads_or(!okb)) return false;
+                // every thread is past pair t - 1: refill its buffers with pair t - 1 + NB
+                if (tid == 0 && t >= 1 && t - 1 + NB < nbox) refill(t - 1 + NB, nb);
+                pair(t, b);
+                nb = b;
+                b = (b + 1 == NB) ? 0 : b + 1;
+            }
+            return true;
+        }
+        bool ok = true;
+        for (int t = 0, b = 0, nb = NB - 1; t < nbox; ++t) {  // b = t % NB, nb = (t - 1) % NB
+            if (tid == 0 && t >= 1) {
+                // pair t - 1 + NB into the buffers of pair t - 1 once every warp released them
+                const int nt = t - 1 + NB;
+                if (nt < nbox && ok && *s_abort == 0) {
+                    ok = mbar_wait_bounded(bar_e + nb, (ph_e >> nb) & 1u);
+                    if (ok)
+                        refill(nt, nb);
+                    else
+                        *s_abort = 1;
+                }
+                ph_e ^= 1u << nb;  // the release of pair t - 1 (waited for or not)
+            }
+            if (ok && *s_abort == 0) {
+                ok = mbar_wait_bounded(bar_s + b, (ph_s >> b) & 1u);
+                if (!ok) *s_abort = 1;
+            }
+            ph_s ^= 1u << b;
+            if (ok) pair(t, b);
+            __syncwarp();
+            if ((tid & 31) == 0) mbar_arrive(bar_e + b);
             nb = b;
             b = (b + 1 == NB) ? 0 : b + 1;
         }
+        if (tid == 0) ph_e ^= 1u << ((nbox - 1) % NB);  // the release of the last pair
+        if (__syncthreads_or(!ok)) return false;
     } else {
         const int n = H2 * W2;
         for (int p = tid; p < n; p += kDT) {
@@ -327,8 +369,9 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
     // mbarriers: the full-resolution tile pairs (2 buffers), then the level-2 sweep's box
     // pairs
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + a.o_bar);
-    uint64_t* bar_s = bar + 2;
-    static_assert(2 + kMaxSweep <= 8, "mbarriers below the next-plane word");
+    uint64_t* bar_s = bar + 2;           // sweep pairs loaded
+    uint64_t* bar_e = bar_s + kMaxSweep;  // sweep pairs released by all 8 warps
+    static_assert(2 + 2 * kMaxSweep <= 12, "mbarriers below the next-plane word");
     float* acc_sm = sm + a.o_acc;
     float* red = sm + a.o_red;  // [8 warps][128]
     float* xb = sm + a.o_xb;
@@ -348,16 +391,21 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
     if (use_tma && leader) {
         mbar_init(bar, 1);
         mbar_init(bar + 1, 1);
-        for (int b = 0; b < a.nsw; ++b) mbar_init(bar_s + b, 1);
+        for (int b = 0; b < a.nsw; ++b) {
+            mbar_init(bar_s + b, 1);
+            mbar_init(bar_e + b, kDT / 32);
+        }
         fence_mbar_init();
     }
+    volatile int* s_abort = reinterpret_cast<volatile int*>(sm + a.o_bar + 26);  // a wait timed out
+    if (leader) *s_abort = 0;
     __syncthreads();
-    uint32_t ph = 0, ph_s = 0;
+    uint32_t ph = 0, ph_s = 0, ph_e = 0;
     bool failed = false;
 
     // planes: first blockIdx.x, then whichever is next in the shared counter (planes are
     // independent, so the order does not change any result), else a fixed stride
-    int* s_next = reinterpret_cast<int*>(sm + a.o_bar + 16);
+    int* s_next = reinterpret_cast<int*>(sm + a.o_bar + 24);
     for (long long plane = blockIdx.x; plane < a.planes;) {
         const int n = (int)(plane / a.C), c = (int)(plane - (long long)n * a.C);
         const T* xp = reinterpret_cast<const T*>(a.x) + plane * plane_elems;
@@ -389,7 +437,8 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
 
         // ---- deep levels l = 2..L: band pair pp = tid / 128, 2x4 block per thread ----
         if (a.L >= 2) {
-            if (!dw_sweep<T, FAST>(a, xp, gp, sm, u2x, u2g, bar_s, ph_s, plane)) {
+            if (!dw_sweep<T, FAST>(a, xp, gp, sm, u2x, u2g, bar_s, bar_e, ph_s, ph_e, s_abort,
+                                   plane)) {
                 failed = true;
                 break;
             }

@@ -120,8 +120,11 @@ def test_c3_stage1_f16_sampled():
     assert_within(errs, wl.dtype, wl.name)
 
 
-def test_backward_is_deterministic():
-    wl = WORKLOADS["c3_stage1_bf16"]
+@pytest.mark.parametrize("wl", [
+    WORKLOADS["c3_stage1_bf16"],                           # level-2 sweep: 4 pairs, CTA barriers
+    shape_workload(2, 6, 256, 256, 5, 5, "f32", seed=77),  # 2 pairs, per-warp releases
+], ids=lambda w: w.name)
+def test_backward_is_deterministic(wl):
     inp = make_inputs(wl)
     a = gpu_run(inp, wl.levels, True)
     b = gpu_run(inp, wl.levels, True)
