@@ -38,6 +38,7 @@ struct FwdArgs {
     CUtensorMap tmx;  // X: dims {W, H, planes}, box {XBW, XBH, 1}
     CUtensorMap tmd;  // deep sum: dims {4*W2, H2, slots}, box {64, 16, 1}
     CUtensorMap tms;  // X for the level-2 sweep: dims {W, H, planes}, box {64, SweepBox::BH, 1}
+    CUtensorMap tmu;  // level-2 subbands in the slots: dims {4*W2, H2, slots}, box {4*BT, BT, 1}
     const void* x;
     void* y;
     const float* b0f;
@@ -59,6 +60,7 @@ struct FwdArgs {
     int b_step;      // floats between the two band-pair buffers (0: a single buffer)
     int o_dz;        // the deep levels' filtered level-2 pairs (floats)
     int car2;        // the carrier X^(2) is kept in the deep state (else re-read from u2)
+    int o_u;         // level-2 tiles are TMA-staged here (over the carriers), or -1
     // deep-level state, in shared memory or (deep_global) in the CTA's workspace slot:
     int deep_global;
     int o_car[kMaxLevels + 1];                    // carriers X^(l), l = 2..L-1
@@ -112,14 +114,16 @@ struct SweepBox {
 
 // Level-2 sweep: the unnormalized subbands of every level-2 position go to u2
 // [H/4][W/4][4] (LL, LH, HL, HH); LL / 2 of it is the carrier X^(2), also written to the
-// deep state when it is kept there. TMA path: the first
-// NBUF boxes were issued at the start of the plane; box t + NBUF reuses box t's buffer once
-// every thread is past it. Returns false if a TMA wait timed
-// out (the vote makes the result uniform over the CTA).
+// deep state when it is kept there. TMA path: the first NBUF boxes were issued at the start
+// of the plane; box t + NBUF reuses box t's buffer. Each warp releases a box on bar_e[b]
+// (8 arrivals) and thread 0 refills the buffer once all have, so there is no CTA barrier
+// per box. Every wait is bounded; a timeout sets *s_abort, after which no thread waits
+// again, and the vote at the end returns false (uniform over the CTA).
 template <typename T, bool FAST>
 __device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, float* sm, float* deep,
-                                             float* u2, uint64_t* bar_s, uint32_t& ph_s,
-                                             long long plane) {
+                                             float* u2, uint64_t* bar_s, uint64_t* bar_e,
+                                             uint32_t& ph_s, uint32_t& ph_e,
+                                             volatile int* s_abort, long long plane) {
     constexpr int BW = SweepBox<T>::BW, BH = SweepBox<T>::BH, NB = SweepBox<T>::NBUF;
     constexpr int PR = BH / 4;  // rows of level-2 positions per box
     const int H2 = a.Hp >> 2, W2 = a.Wp >> 2;
@@ -132,19 +136,30 @@ __device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, floa
         const int nbox = sweep_boxes(a.Hp, a.Wp, BW, BH);
         constexpr int PC = BW / 4;  // level-2 positions per box row
         const int pi = tid / PC, pj = tid % PC;
+        bool ok = true;
         for (int t = 0; t < nbox; ++t) {
             const int b = t % NB;
-            const bool ok = mbar_wait_bounded(bar_s + b, (ph_s >> b) & 1u);
-            ph_s ^= 1u << b;
-            if (__syncthreads_or(!ok)) return false;
-            if (tid == 0 && t >= 1 && t - 1 + NB < nbox) {
-                // every thread is past box t - 1: refill its buffer with box t - 1 + NB
+            if (tid == 0 && t >= 1) {
                 const int nt = t - 1 + NB, nb = (t - 1) % NB;
-                const int ny = nt / bxn, nx = nt - ny * bxn;
-                fence_proxy_async_smem();
-                mbar_arrive_expect_tx(bar_s + nb, SweepBox<T>::BYTES);
-                tma_load_3d(buf + nb * (BW * BH), &a.tms, nx * BW, ny * BH, (int)plane, bar_s + nb);
+                if (nt < nbox && ok && *s_abort == 0) {
+                    ok = mbar_wait_bounded(bar_e + nb, (ph_e >> nb) & 1u);
+                    if (ok) {
+                        const int ny = nt / bxn, nx = nt - ny * bxn;
+                        fence_proxy_async_smem();
+                        mbar_arrive_expect_tx(bar_s + nb, SweepBox<T>::BYTES);
+                        tma_load_3d(buf + nb * (BW * BH), &a.tms, nx * BW, ny * BH, (int)plane,
+                                    bar_s + nb);
+                    } else {
+                        *s_abort = 1;
+                    }
+                }
+                ph_e ^= 1u << nb;
             }
+            if (ok && *s_abort == 0) {
+                ok = mbar_wait_bounded(bar_s + b, (ph_s >> b) & 1u);
+                if (!ok) *s_abort = 1;
+            }
+            ph_s ^= 1u << b;
             const int by = t / bxn, bx = t - by * bxn;
 #pragma unroll
             for (int k = 0; k < SweepBox<T>::PPT; ++k) {
@@ -155,11 +170,18 @@ __device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, floa
                     const float4 u = level2_block(ld4_smem<T>(q), ld4_smem<T>(q + BW),
                                                   ld4_smem<T>(q + 2 * BW),
                                                   ld4_smem<T>(q + 3 * BW));
-                    __stcg(u2v + (size_t)i2 * W2 + j2, u);
-                    if (c2 != nullptr) c2[i2 * W2 + j2] = 0.5f * u.x;
+                    if (ok) {
+                        __stcg(u2v + (size_t)i2 * W2 + j2, u);
+                        if (c2 != nullptr) c2[i2 * W2 + j2] = 0.5f * u.x;
+                    }
                 }
             }
+            __syncwarp();
+            if ((tid & 31) == 0) mbar_arrive(bar_e + b);
         }
+        if (tid == 0) ph_e ^= 1u << ((nbox - 1) % NB);
+        if (a.o_u >= 0) fence_proxy_async_global();  // u2 is read back by TMA (level-2 staging)
+        if (__syncthreads_or(!ok)) return false;
     } else {
         const int n = H2 * W2;
         for (int base = tid; base < n; base += 4 * kFT) {
@@ -177,6 +199,7 @@ __device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, floa
             }
         }
     }
+    if (a.o_u >= 0) fence_proxy_async_global();  // u2 is read back by TMA (level-2 staging)
     return true;
 }
 
@@ -254,6 +277,22 @@ __device__ __forceinline__ void deep_stage(const FwdArgs& a, const float* u2, fl
         deep_stage_from<K, 2>(a, u2, nullptr, bs, l, ti0, tj0);
 }
 
+// A TMA-staged level-2 tile ([BT][BT] quadruples (LL, LH, HL, HH), zero outside the level
+// grid) into the two band-pair tiles.
+template <int K>
+__device__ __forceinline__ void repack_level2(const float* ubuf, float* bs) {
+    constexpr int BT = FG<K>::BT;
+    constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, PHALF = PG<K>::PHALF;
+    const float4* u4 = reinterpret_cast<const float4*>(ubuf);
+    for (int idx = threadIdx.x; idx < BT * BT; idx += kFT) {
+        const int si = idx / BT, sj = idx - si * BT;
+        const float4 u = u4[idx];
+        float* q = bs + si * PROW + 4 * pchunk(sj >> 1, PHALF) + 2 * (sj & 1);
+        *reinterpret_cast<float2*>(q) = make_float2(u.x, u.y);
+        *reinterpret_cast<float2*>(q + PTILE) = make_float2(u.z, u.w);
+    }
+}
+
 // Deep levels of one plane, after the level-2 sweep: carriers X^(l >= 3), levels L..3
 // filtered into the deep state, then level 2, whose filtered subbands are combined at once
 // with the deeper levels into Eq. 7's sum over levels 2..L at level-1 resolution, written
@@ -261,9 +300,11 @@ __device__ __forceinline__ void deep_stage(const FwdArgs& a, const float* u2, fl
 // (2 i2 + a, 2 j2 + b) as (a, b) = (0,0), (0,1), (1,0), (1,1). The deep state (carriers,
 // Z^(l >= 3)) is in shared memory (DG = false: deep is the shared-memory base) or in the
 // CTA's workspace slot (DG = true).
-template <int K, bool DG>
-__device__ __forceinline__ void deep_levels(const FwdArgs& a, float* sm, float* deep_g,
-                                            const float* u2, float* zslot) {
+template <int K, bool DG, bool STAGED>
+__device__ __forceinline__ bool deep_levels(const FwdArgs& a, float* sm, float* deep_g,
+                                            const float* u2, float* zslot, uint64_t* bar_u,
+                                            uint32_t& ph_u) {
+    constexpr int R = FG<K>::R;
     constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, WS = PG<K>::WS;
     constexpr int ZROW = PG<K>::ZROW, ZTILE = PG<K>::ZTILE;
     float* deep = DG ? deep_g : sm;
@@ -271,13 +312,47 @@ __device__ __forceinline__ void deep_levels(const FwdArgs& a, float* sm, float* 
     float* bs = sm + a.o_b;
     float* zs = sm + a.o_dz;  // filtered level-2 pairs
     const int tid = threadIdx.x;
+    // level-2 tiles by TMA from the slot into the staging buffer (over the dead carriers),
+    // the next tile's load in flight while the current one is filtered
+    constexpr bool tma2 = STAGED && !DG;
+    float* ubuf = sm + (tma2 ? a.o_u : 0);
+    auto issue2 = [&](int ti0, int tj0) {
+        mbar_arrive_expect_tx(bar_u, 16u * FG<K>::BT * FG<K>::BT);
+        tma_load_3d(ubuf, &a.tmu, 4 * (tj0 - R), ti0 - R, (int)blockIdx.x, bar_u);
+    };
+    bool ok = true;
     deep_carriers(a, u2, deep);
     for (int l = a.L; l >= 2; --l) {
         const int Hl = a.Hp >> l, Wl = a.Wp >> l;
+        if (l == 2 && tma2) {
+            // every thread's generic accesses to the carriers are ordered before the load
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0) issue2(0, 0);
+        }
         for (int ti0 = 0; ti0 < Hl; ti0 += kCT) {
             for (int tj0 = 0; tj0 < Wl; tj0 += kCT) {
-                deep_stage<K>(a, u2, sm, deep, l, ti0, tj0);
-                __syncthreads();
+                if (l == 2 && tma2) {
+                    // a timed-out wait repacks stale data; the vote below ends the kernel
+                    ok = mbar_wait_bounded(bar_u, ph_u) && ok;
+                    ph_u ^= 1;
+                    repack_level2<K>(ubuf, bs);
+                } else {
+                    deep_stage<K>(a, u2, sm, deep, l, ti0, tj0);
+                }
+                if (l == 2 && tma2) {
+                    if (__syncthreads_or(!ok)) return false;
+                } else {
+                    __syncthreads();
+                }
+                if (l == 2 && tma2 && tid == 0) {  // the next level-2 tile
+                    const int nj = tj0 + kCT < Wl ? tj0 + kCT : 0;
+                    const int ni = tj0 + kCT < Wl ? ti0 : ti0 + kCT;
+                    if (ni < Hl) {
+                        fence_proxy_async_smem();
+                        issue2(ni, nj);
+                    }
+                }
                 {
                     // band pair pp, 2x4 output block (bi, bj); at level 2 warp w takes rows
                     // 4w..4w+3 of both pairs, the rows whose deep sums it forms below
@@ -342,11 +417,14 @@ __device__ __forceinline__ void deep_levels(const FwdArgs& a, float* sm, float* 
             }
         }
     }
+    return true;
 }
 
-// FAST: the plane is TMA-staged, has 4-aligned rows, needs no padding and keeps its deep
-// state in shared memory, so those checks and the other paths are compiled out.
-template <int K, typename T, bool FAST>
+// MODE >= 1 (FAST): the plane is TMA-staged, has 4-aligned rows, needs no padding and
+// keeps its deep state in shared memory, so those checks and the other paths are compiled
+// out. MODE 2 also TMA-stages the level-2 tiles (compiled only where the layout can pick it:
+// kept out of the other instantiations, whose deep levels it would slow down).
+template <int K, typename T, int MODE>
 __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_constant__ FwdArgs a) {
     constexpr int R = FG<K>::R;
     constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, WS = PG<K>::WS;
@@ -354,16 +432,20 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
     extern __shared__ __align__(128) float4 smem_f4[];
     float* sm = reinterpret_cast<float*>(smem_f4);
     // mbarriers: X tiles (2 buffers), deep-sum blocks (2 buffers), weights, level-2 sweep
+    // boxes loaded (NBUF) and released by all 8 warps (NBUF), level-2 tiles
     uint64_t* bar_x = reinterpret_cast<uint64_t*>(sm + a.o_bar);
     uint64_t* bar_d = bar_x + 2;
     uint64_t* bar_w = bar_x + 4;
     uint64_t* bar_s = bar_x + 5;
-    static_assert(SweepBox<T>::NBUF <= 2, "mbarrier slots");
+    uint64_t* bar_e = bar_s + SweepBox<T>::NBUF;
+    uint64_t* bar_u = bar_e + SweepBox<T>::NBUF;  // level-2 tiles from the slot
+    static_assert(SweepBox<T>::NBUF <= 2, "mbarriers below the next-plane word");
     float* dblk = sm + a.o_dblk;  // two buffers of kDBytes
     float* wsm = sm + a.o_w;
     float* zs = sm + a.o_z;
     float* zslot = a.zd + (size_t)blockIdx.x * a.slot;  // deep sums [H/4][W/4][4]
     float* u2 = zslot + a.zd_slot;                          // level-2 subbands, same shape
+    constexpr bool FAST = MODE >= 1;
     const bool use_tma = FAST || a.use_tma;
     const bool deep_global = !FAST && a.deep_global;
     float* deep = deep_global ? zslot + 2 * a.zd_slot : sm;  // carriers and Z^(l >= 3)
@@ -379,11 +461,17 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
         mbar_init(bar_d, 1);
         mbar_init(bar_d + 1, 1);
         mbar_init(bar_w, 1);
-        for (int b = 0; b < SweepBox<T>::NBUF; ++b) mbar_init(bar_s + b, 1);
+        for (int b = 0; b < SweepBox<T>::NBUF; ++b) {
+            mbar_init(bar_s + b, 1);
+            mbar_init(bar_e + b, kFT / 32);
+        }
+        mbar_init(bar_u, 1);
         fence_mbar_init();
     }
+    volatile int* s_abort = reinterpret_cast<volatile int*>(sm + a.o_bar + 26);
+    if (leader) *s_abort = 0;
     __syncthreads();
-    uint32_t ph_x = 0, ph_d = 0, ph_w = 0, ph_s = 0;
+    uint32_t ph_x = 0, ph_d = 0, ph_w = 0, ph_s = 0, ph_e = 0, ph_u = 0;
     bool failed = false;
     // weights of the current plane are in shared memory (uniform over the CTA)
     auto weights_ready = [&]() -> bool {
@@ -397,7 +485,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
 
     // planes: first blockIdx.x, then whichever is next in the shared counter (planes are
     // independent, so the order does not change any result), else a fixed stride
-    int* s_next = reinterpret_cast<int*>(sm + a.o_bar + 16);
+    int* s_next = reinterpret_cast<int*>(sm + a.o_bar + 24);
     for (long long plane = blockIdx.x; plane < a.planes;) {
         const int c = (int)(plane % a.C);
         const T* xp = reinterpret_cast<const T*>(a.x) + plane * plane_elems;
@@ -436,14 +524,18 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
         // (i2, j2) holds the sums for level-1 positions (2i2 + a, 2j2 + b) as
         // (a, b) = (0,0), (0,1), (1,0), (1,1).
         if (a.L >= 2) {
-            if (!level2_sweep<T, FAST>(a, xp, sm, deep, u2, bar_s, ph_s, plane) || !weights_ready()) {
+            if (!level2_sweep<T, FAST>(a, xp, sm, deep, u2, bar_s, bar_e, ph_s, ph_e, s_abort, plane) || !weights_ready()) {
                 failed = true;
                 break;
             }
-            if (deep_global)
-                deep_levels<K, true>(a, sm, zslot + 2 * a.zd_slot, u2, zslot);
-            else
-                deep_levels<K, false>(a, sm, sm, u2, zslot);
+            const bool dok =
+                deep_global ? deep_levels<K, true, false>(a, sm, zslot + 2 * a.zd_slot, u2, zslot,
+                                                          bar_u, ph_u)
+                            : deep_levels<K, false, MODE == 2>(a, sm, sm, u2, zslot, bar_u, ph_u);
+            if (!dok) {
+                failed = true;
+                break;
+            }
             fence_proxy_async_global();
             __syncthreads();
         }
@@ -673,8 +765,8 @@ constexpr size_t kTwoCtaSmem = 228 * 1024 / 2 - 1024;
 // with the deep state in shared memory (local_end) and without it (xend); `deep` = floats
 // of the deep state.
 template <int K, typename T>
-void fwd_layout(FwdArgs& a, int L, int hp, int wp, int nbs, int car2, int& xend, int& local_end,
-                int& deep) {
+void fwd_layout(FwdArgs& a, int L, int hp, int wp, int nbs, int car2, int stage_u, int& xend,
+                int& local_end, int& deep) {
     int off = 0;
     a.o_bar = off;
     off += 32;  // seven mbarriers and the next-plane word, padded to 128 bytes
@@ -708,19 +800,44 @@ void fwd_layout(FwdArgs& a, int L, int hp, int wp, int nbs, int car2, int& xend,
     a.o_z = alias0;
     a.o_dblk = round32(alias0 + 2 * PG<K>::ZTILE);
     xend = a.o_dblk + ((L >= 2) ? 2 * kDBytes / 4 : 0);
-    // deep-level state: carriers X^(2 or 3..L-1), then Z^(3..L), each 16-byte aligned
     a.car2 = (car2 && L >= 3) ? 1 : 0;
     deep = 0;
     for (int l = 0; l <= kMaxLevels; ++l) a.o_car[l] = a.o_zl[l] = 0;
-    for (int l = a.car2 ? 2 : 3; l < L; ++l) {
-        a.o_car[l] = deep;
-        deep += round4((hp >> l) * (wp >> l));
+    // level-2 tiles (BT x BT subband quadruples) TMA-staged over the carriers, which are dead
+    // by the time level 2 runs. Only where that measured faster than loading them directly:
+    // 16-bit I/O, k <= 5 and at least two level-2 tiles (so that a load is in flight while
+    // a tile is filtered; with one tile the extra barrier and the repack cost more).
+    const int l2_tiles = ((hp >> 2) + kCT - 1) / kCT * (((wp >> 2) + kCT - 1) / kCT);
+    const bool su = stage_u && L >= 2 && sizeof(T) == 2 && K <= 5 && l2_tiles >= 2;
+    // deep-level state, each part 16-byte aligned: the carriers X^(2 or 3..L-1) and
+    // Z^(3..L); with staging Z first, so that the staging buffer can overlay the carriers
+    auto place_z = [&]() {
+        for (int l = 3; l <= L; ++l) {
+            a.o_zl[l] = deep;
+            deep += 4 * (hp >> l) * (wp >> l);
+        }
+    };
+    auto place_car = [&]() {
+        for (int l = a.car2 ? 2 : 3; l < L; ++l) {
+            a.o_car[l] = deep;
+            deep += round4((hp >> l) * (wp >> l));
+        }
+    };
+    a.o_u = -1;
+    int dend;
+    if (su) {
+        place_z();
+        const int zsize = deep;
+        place_car();
+        a.o_u = alias0 + round32(zsize);  // a TMA destination: 128-byte aligned
+        const int u_end = round32(zsize) + 4 * FG<K>::BT * FG<K>::BT;
+        dend = deep > u_end ? deep : u_end;
+    } else {
+        place_car();
+        place_z();
+        dend = deep;
     }
-    for (int l = 3; l <= L; ++l) {
-        a.o_zl[l] = deep;
-        deep += 4 * (hp >> l) * (wp >> l);
-    }
-    local_end = alias0 + deep > xend ? alias0 + deep : xend;
+    local_end = alias0 + dend > xend ? alias0 + dend : xend;
     for (int l = 2; l <= L; ++l) {  // offsets for the shared-memory placement
         a.o_car[l] += alias0;
         a.o_zl[l] += alias0;
@@ -734,14 +851,17 @@ FwdPlan fwd_plan(const wt_desc& d) {
     const int L = d.levels;
     const int hp = padded_side(d.h, L), wp = padded_side(d.w, L);
     // Layout choice, first fit: two CTAs per SM with the deep state in shared memory (two
-    // band-pair buffers before one, X^(2) kept before re-read); else two CTAs per SM with
-    // the deep state in the CTA's workspace slot; else one CTA per SM, deep state in shared
-    // memory if it fits, else in the slot.
-    static const int kOrder[4][2] = {{2, 1}, {2, 0}, {1, 1}, {1, 0}};
+    // band-pair buffers before one, X^(2) kept before re-read, level-2 tiles TMA-staged
+    // before loaded directly); else two CTAs per SM with the deep state in the CTA's
+    // workspace slot; else one CTA per SM, deep state in shared memory if it fits, else in
+    // the slot.
+    static const int kOrder[8][3] = {{2, 1, 1}, {2, 1, 0}, {2, 0, 1}, {2, 0, 0},
+                                     {1, 1, 1}, {1, 1, 0}, {1, 0, 1}, {1, 0, 0}};
     int xend = 0, local_end = 0, deep = 0, total = 0;
     bool chosen = false;
-    for (int i = 0; i < 4 && !chosen; ++i) {
-        fwd_layout<K, T>(a, L, hp, wp, kOrder[i][0], kOrder[i][1], xend, local_end, deep);
+    for (int i = 0; i < 8 && !chosen; ++i) {
+        fwd_layout<K, T>(a, L, hp, wp, kOrder[i][0], kOrder[i][1], kOrder[i][2], xend,
+                         local_end, deep);
         if ((size_t)local_end * sizeof(float) <= kTwoCtaSmem) {
             a.deep_global = 0;
             total = local_end;
@@ -749,15 +869,16 @@ FwdPlan fwd_plan(const wt_desc& d) {
         }
     }
     for (int nbs = 2; nbs >= 1 && !chosen; --nbs) {
-        fwd_layout<K, T>(a, L, hp, wp, nbs, 0, xend, local_end, deep);
+        fwd_layout<K, T>(a, L, hp, wp, nbs, 0, 0, xend, local_end, deep);
         if ((size_t)xend * sizeof(float) <= kTwoCtaSmem) {
             a.deep_global = 1;
             total = xend;
             chosen = true;
         }
     }
-    for (int i = 0; i < 4 && !chosen; ++i) {
-        fwd_layout<K, T>(a, L, hp, wp, kOrder[i][0], kOrder[i][1], xend, local_end, deep);
+    for (int i = 0; i < 8 && !chosen; ++i) {
+        fwd_layout<K, T>(a, L, hp, wp, kOrder[i][0], kOrder[i][1], kOrder[i][2], xend,
+                         local_end, deep);
         if ((size_t)local_end * sizeof(float) <= kMaxSmemPerBlock) {
             a.deep_global = 0;
             total = local_end;
@@ -765,7 +886,7 @@ FwdPlan fwd_plan(const wt_desc& d) {
         }
     }
     if (!chosen) {
-        fwd_layout<K, T>(a, L, hp, wp, 2, 0, xend, local_end, deep);
+        fwd_layout<K, T>(a, L, hp, wp, 2, 0, 0, xend, local_end, deep);
         a.deep_global = 1;
         total = xend;
     }
@@ -837,9 +958,14 @@ wt_status launch_fwd_k(const wt_desc& d, const void* x, const float* w0f, const 
                                (unsigned long long)d.w * esize,
                                (unsigned long long)d.w * d.h * esize, SweepBox<T>::BW,
                                SweepBox<T>::BH);
+            if (ok && a.o_u >= 0)  // the slots' level-2 subbands, BT x BT positions a box
+                ok = encode_3d(&a.tmu, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.zd + a.zd_slot,
+                               4 * w2, h2, (unsigned long long)p.grid, 16 * w2,
+                               (unsigned long long)a.slot * 4, 4 * FG<K>::BT, FG<K>::BT);
         }
         a.use_tma = ok ? 1 : 0;
     }
+    if (!a.use_tma) a.o_u = -1;  // the level-2 tiles are then loaded directly
     if (cudaMemsetAsync(a.err, 0, 2 * sizeof(int), stream) != cudaSuccess) return WT_ERR_CUDA;
     {
         const long long n = (long long)d.c * a.img;
@@ -850,7 +976,15 @@ wt_status launch_fwd_k(const wt_desc& d, const void* x, const float* w0f, const 
         ++*launches;
     }
     const bool fast = a.use_tma && a.vec && a.H == a.Hp && a.W == a.Wp && !a.deep_global;
-    auto kern = fast ? wt_fwd_plane_kernel<K, T, true> : wt_fwd_plane_kernel<K, T, false>;
+    auto kern = fast ? wt_fwd_plane_kernel<K, T, 1> : wt_fwd_plane_kernel<K, T, 0>;
+    bool staged = false;
+    if constexpr (K <= 5 && sizeof(T) == 2) {
+        if (fast && a.o_u >= 0) {
+            kern = wt_fwd_plane_kernel<K, T, 2>;
+            staged = true;
+        }
+    }
+    if (!staged) a.o_u = -1;  // level-2 tiles loaded directly
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) !=
         cudaSuccess)
         return WT_ERR_CUDA;

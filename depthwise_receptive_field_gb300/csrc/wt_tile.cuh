@@ -107,15 +107,16 @@ __device__ __forceinline__ void conv_pair_2x4(const float* rows, int bj, const f
             v[2 * m] = pk2(t.x, t.y);
             v[2 * m + 1] = pk2(t.z, t.w);
         }
+        // taps outermost: consecutive packed FMAs update different accumulators
 #pragma unroll
-        for (int o = 0; o < 2; ++o) {
-            const int u = r - o;
-            if (u < 0 || u >= K) continue;
+        for (int vv = 0; vv < K; ++vv)
 #pragma unroll
-            for (int vv = 0; vv < K; ++vv)
+            for (int o = 0; o < 2; ++o) {
+                const int u = r - o;
+                if (u < 0 || u >= K) continue;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) acc[o][q] = fma2(w[u * K + vv], v[q + vv], acc[o][q]);
-        }
+            }
     }
 }
 
@@ -492,19 +493,20 @@ __device__ __forceinline__ void conv_base_4x4_raw(const T* raw, int by, int bx,
         for (int m = 0; m < NV / 2; ++m) A[m] = pk2(v[2 * m], v[2 * m + 1]);
 #pragma unroll
         for (int m = 0; m < NV / 2 - 1; ++m) B[m] = pk2(v[2 * m + 1], v[2 * m + 2]);
+        // taps outermost: consecutive packed FMAs update different accumulators
 #pragma unroll
-        for (int o = 0; o < 4; ++o) {
-            const int u = r - o;
-            if (u < 0 || u >= K) continue;
+        for (int vv = 0; vv < K; ++vv)
 #pragma unroll
-            for (int vv = 0; vv < K; ++vv)
+            for (int o = 0; o < 4; ++o) {
+                const int u = r - o;
+                if (u < 0 || u >= K) continue;
 #pragma unroll
                 for (int pp = 0; pp < 2; ++pp) {
                     const int idx = 2 * pp + vv;
                     const f2x in = (idx & 1) ? B[(idx - 1) >> 1] : A[idx >> 1];
                     acc[o][pp] = fma2(w[u * K + vv], in, acc[o][pp]);
                 }
-        }
+            }
     }
 }
 

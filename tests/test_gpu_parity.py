@@ -103,6 +103,9 @@ LAYOUT = [  # the forward's shared-memory layouts (band-pair buffers, where X^(2
     (1, 2, 192, 128, 7, 4, "f32"),    # one band-pair buffer (a barrier more per tile)
     (1, 1, 256, 256, 7, 5, "bf16"),   # two buffers, X^(2) re-read from the level-2 subbands
     (1, 1, 256, 256, 5, 5, "f32"),    # the same in fp32
+    (1, 2, 256, 192, 3, 4, "bf16"),   # level-2 tiles TMA-staged from the slot (2x2 tiles)
+    (1, 1, 160, 256, 5, 3, "f16"),    # the same, ragged last tile row
+    (1, 2, 150, 136, 5, 3, "bf16"),   # the same on a padded plane (general kernel)
 ]
 
 
