@@ -104,13 +104,6 @@ __device__ __forceinline__ float4 haar_u(float a, float b, float c, float d) {
 
 __device__ __forceinline__ float4 f4_zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 
-__device__ __forceinline__ void f4_fma(float4& acc, const float4& w, const float4& v) {
-    acc.x = fmaf(w.x, v.x, acc.x);
-    acc.y = fmaf(w.y, v.y, acc.y);
-    acc.z = fmaf(w.z, v.z, acc.z);
-    acc.w = fmaf(w.w, v.w, acc.w);
-}
-
 // Synthesis of one coefficient tuple at within-block parity (ry, rx) (App. A Eq. 12/13;
 // the 1/2 is folded into the weights): z.LL + s_y z.LH + s_x z.HL + s_y s_x z.HH.
 template <int RY, int RX>
@@ -126,11 +119,6 @@ __device__ __forceinline__ float synth_rt(const float4& z, int by, int bx) {
     const float t1 = by ? (z.z - z.w) : (z.z + z.w);
     return bx ? (t0 - t1) : (t0 + t1);
 }
-
-// Column index of a float4 cell in a "split" row: even cells first, then odd cells.
-// Threads that own 2-wide cell blocks then read consecutive 16-byte words (no bank
-// conflicts for LDS.128 / LDS.64).
-__device__ __forceinline__ int split_col(int c, int half) { return (c >> 1) + (c & 1) * half; }
 
 }  // namespace wt
 

@@ -490,7 +490,10 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
         const int c = (int)(plane % a.C);
         const T* xp = reinterpret_cast<const T*>(a.x) + plane * plane_elems;
         T* yp = reinterpret_cast<T*>(a.y) + plane * plane_elems;
-        __syncthreads();  // the previous plane is done with shared memory
+        // the previous plane is done with shared memory; every thread's generic accesses are
+        // ordered before the TMA writes issued below and during this plane
+        fence_proxy_async_smem();
+        __syncthreads();
         const float bias = (a.b0f != nullptr) ? __ldg(a.b0f + c) : 0.f;
         const float* wimg = a.wimg + (size_t)c * a.img;
         if (!use_tma)
@@ -537,6 +540,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                 break;
             }
             fence_proxy_async_global();
+            fence_proxy_async_smem();  // the deep state's space is reused by TMA (deep sums)
             __syncthreads();
         }
 
@@ -590,7 +594,6 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
             }
             if (use_tma && leader && t + 1 < ntiles) {  // tile t + 1: X and its deep sums
                 const int ny = (t + 1) / tiles_x, nx = (t + 1) - ny * tiles_x, nb = rb ^ 1;
-                fence_proxy_async_smem();
                 mbar_arrive_expect_tx(bar_x + nb, XBox<K, T>::BYTES);
                 tma_load_3d(sm + a.o_raw + nb * a.raw_f, &a.tmx, nx * kTile - XBox<K, T>::XOFF,
                             ny * kTile - 2 * R, (int)plane, bar_x + nb);

@@ -21,35 +21,8 @@ template <int K>
 struct FG {
     static constexpr int R = (K - 1) / 2;
     static constexpr int KK = K * K;
-    static constexpr int KKP = (KK + 3) & ~3;              // padded kernel stride (16 B)
-    static constexpr int PAD = (4 - (R % 4)) % 4;          // aligns 8x4 windows to 16 B
-    static constexpr int XROWS = kTile + 4 * R;
-    static constexpr int XCOLS = kTile + 4 * R;
-    static constexpr int BWR = 8 + 2 * R;                  // window rows of an 8x4 block
-    static constexpr int BNC = (4 + 2 * R + 3) / 4;        // float4 per window row (4-wide)
-    static constexpr int XPITCH_A = PAD + XCOLS;
-    static constexpr int XPITCH_B = PAD + (kTile - 4) + R + 4 * BNC;
-    static constexpr int XPITCH = ((XPITCH_A > XPITCH_B ? XPITCH_A : XPITCH_B) + 3) & ~3;
-    static constexpr int BT = kCT + 2 * R;                 // coefficient tile side with halo
-    static constexpr int CNC = (4 + 2 * R + 3) / 4;        // float4 per window row (4x4 block)
-    static constexpr int BPITCH_B = (kCT - 4) + 4 * CNC;
-    static constexpr int BPITCH = ((BT > BPITCH_B ? BT : BPITCH_B) + 3) & ~3;
-    static constexpr int BAND = BT * BPITCH;               // floats per haloed band tile
-    static constexpr int ZAND = kCT * kCT;                 // floats per un-haloed band tile
-    static constexpr int STAGE_STORE = (2 * R + PAD) % 4;  // alignment of staged 4-groups
+    static constexpr int BT = kCT + 2 * R;  // coefficient tile side with halo
 };
-
-template <int N>
-__device__ __forceinline__ void load_row(const float* p, float (&v)[4 * N]) {
-#pragma unroll
-    for (int m = 0; m < N; ++m) {
-        const float4 t = *reinterpret_cast<const float4*>(p + 4 * m);
-        v[4 * m] = t.x;
-        v[4 * m + 1] = t.y;
-        v[4 * m + 2] = t.z;
-        v[4 * m + 3] = t.w;
-    }
-}
 
 // ---------------------------------------------------------------------------------
 // Band-pair tiles for packed (f32x2) filtering: the four subbands are stored as two
@@ -120,50 +93,6 @@ __device__ __forceinline__ void conv_pair_2x4(const float* rows, int bj, const f
     }
 }
 
-// Packed base k x k filter of a 4x4 pixel block from the fp32 tile, accumulating onto
-// acc[o][p] = (pixel (o, 2p), pixel (o, 2p+1)). The odd-offset input pairs are formed in
-// registers. wdup = KK taps as (w, w) pairs.
-template <int K>
-__device__ __forceinline__ void conv_base_4x4(const float* win, int pitch, const float* wdup,
-                                              f2x (&acc)[4][2]) {
-    constexpr int R = FG<K>::R, KK = FG<K>::KK, CNC = FG<K>::CNC;
-    constexpr int NV = 4 * CNC;
-    f2x w[KK];
-#pragma unroll
-    for (int q = 0; q + 1 < KK; q += 2) {
-        const float4 t = *reinterpret_cast<const float4*>(wdup + 2 * q);
-        w[q] = pk2(t.x, t.y);
-        w[q + 1] = pk2(t.z, t.w);
-    }
-    if constexpr (KK & 1) {
-        const float2 t = *reinterpret_cast<const float2*>(wdup + 2 * (KK - 1));
-        w[KK - 1] = pk2(t.x, t.y);
-    }
-#pragma unroll
-    for (int r = 0; r < 4 + 2 * R; ++r) {
-        float v[NV];
-        load_row<CNC>(win + r * pitch, v);
-        f2x A[NV / 2], B[NV / 2 - 1];
-#pragma unroll
-        for (int m = 0; m < NV / 2; ++m) A[m] = pk2(v[2 * m], v[2 * m + 1]);
-#pragma unroll
-        for (int m = 0; m < NV / 2 - 1; ++m) B[m] = pk2(v[2 * m + 1], v[2 * m + 2]);
-#pragma unroll
-        for (int o = 0; o < 4; ++o) {
-            const int u = r - o;
-            if (u < 0 || u >= K) continue;
-#pragma unroll
-            for (int vv = 0; vv < K; ++vv)
-#pragma unroll
-                for (int pp = 0; pp < 2; ++pp) {
-                    const int idx = 2 * pp + vv;
-                    const f2x in = (idx & 1) ? B[(idx - 1) >> 1] : A[idx >> 1];
-                    acc[o][pp] = fma2(w[u * K + vv], in, acc[o][pp]);
-                }
-        }
-    }
-}
-
 // Packed weight-gradient correlation of a ROWS x 4 block of one band pair:
 // acc[u*K+v] += sum_{o,q} g[o][q] (.) cell[o+u][q+v], two bands at once. `rows` = pair
 // tile + (first window row) * PROW; the window starts at cell 4*bj.
@@ -191,39 +120,6 @@ __device__ __forceinline__ void corr_pair(const float* rows, int bj, const f2x (
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
                     acc[u * K + vv] = fma2(g[o][q], v[q + vv], acc[u * K + vv]);
-        }
-    }
-}
-
-// Packed base weight-gradient correlation of a 4x4 pixel block: with g[o][p] =
-// (dY[o][2p], dY[o][2p+1]), acc[u*K+v] accumulates the even- and odd-column partial sums
-// of sum_{o,q} dY[o][q] X[o+u][q+v] (add the two halves at the end).
-template <int K>
-__device__ __forceinline__ void corr_base_4x4(const float* win, int pitch, const f2x (&g)[4][2],
-                                              f2x (&acc)[K * K]) {
-    constexpr int R = FG<K>::R, CNC = FG<K>::CNC;
-    constexpr int NV = 4 * CNC;
-#pragma unroll
-    for (int r = 0; r < 4 + 2 * R; ++r) {
-        float v[NV];
-        load_row<CNC>(win + r * pitch, v);
-        f2x A[NV / 2], B[NV / 2 - 1];
-#pragma unroll
-        for (int m = 0; m < NV / 2; ++m) A[m] = pk2(v[2 * m], v[2 * m + 1]);
-#pragma unroll
-        for (int m = 0; m < NV / 2 - 1; ++m) B[m] = pk2(v[2 * m + 1], v[2 * m + 2]);
-#pragma unroll
-        for (int o = 0; o < 4; ++o) {
-            const int u = r - o;
-            if (u < 0 || u >= K) continue;
-#pragma unroll
-            for (int vv = 0; vv < K; ++vv)
-#pragma unroll
-                for (int pp = 0; pp < 2; ++pp) {
-                    const int idx = 2 * pp + vv;
-                    const f2x in = (idx & 1) ? B[(idx - 1) >> 1] : A[idx >> 1];
-                    acc[u * K + vv] = fma2(g[o][pp], in, acc[u * K + vv]);
-                }
         }
     }
 }
@@ -278,107 +174,6 @@ __device__ __forceinline__ float4 ld4_smem<__half>(const __half* p) {
     const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
     const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
     return make_float4(a.x, a.y, b.x, b.y);
-}
-
-// Widen the TMA-staged raw tile to the fp32 tile (column c at c + PAD) and, when `bands`,
-// form the level-1 unnormalized subbands with an R halo in the two band-pair tiles.
-// One item = two horizontally adjacent cells (a 2x4 pixel block).
-template <int K, typename T>
-__device__ __forceinline__ void convert_raw(const T* raw, float* xs, float* bs, bool bands) {
-    constexpr int PAD = FG<K>::PAD, XP = FG<K>::XPITCH, BT = FG<K>::BT;
-    constexpr int NCR = PG<K>::NCR, PROW = PG<K>::PROW, PTILE = PG<K>::PTILE;
-    constexpr int PHALF = PG<K>::PHALF;
-    constexpr int RW = XBox<K, T>::XBW, C0 = XBox<K, T>::C0;
-    for (int idx = threadIdx.x; idx < BT * NCR; idx += blockDim.x) {
-        const int ci = idx / NCR, m = idx - ci * NCR;
-        const T* r0 = raw + (2 * ci) * RW + C0 + 4 * m;
-        float2 a0, a1, b0, b1;
-        if constexpr (C0 % 4 == 0) {  // 4-element aligned: one vector load per row
-            const float4 ra = ld4_smem<T>(r0), rb = ld4_smem<T>(r0 + RW);
-            a0 = make_float2(ra.x, ra.y); a1 = make_float2(ra.z, ra.w);
-            b0 = make_float2(rb.x, rb.y); b1 = make_float2(rb.z, rb.w);
-        } else {
-            a0 = ld2_smem<T>(r0); a1 = ld2_smem<T>(r0 + 2);
-            b0 = ld2_smem<T>(r0 + RW); b1 = ld2_smem<T>(r0 + RW + 2);
-        }
-        float* d0 = xs + (2 * ci) * XP + PAD + 4 * m;
-        if constexpr ((PAD & 1) == 0) {
-            reinterpret_cast<float2*>(d0)[0] = a0;
-            reinterpret_cast<float2*>(d0)[1] = a1;
-            reinterpret_cast<float2*>(d0 + XP)[0] = b0;
-            reinterpret_cast<float2*>(d0 + XP)[1] = b1;
-        } else {
-            d0[0] = a0.x; d0[1] = a0.y; d0[2] = a1.x; d0[3] = a1.y;
-            d0[XP] = b0.x; d0[XP + 1] = b0.y; d0[XP + 2] = b1.x; d0[XP + 3] = b1.y;
-        }
-        if (bands) {
-            const float4 u = haar_u(a0.x, a0.y, b0.x, b0.y);
-            const float4 v = haar_u(a1.x, a1.y, b1.x, b1.y);
-            float* q = bs + ci * PROW + 4 * pchunk(m, PHALF);
-            *reinterpret_cast<float4*>(q) = make_float4(u.x, u.y, v.x, v.y);
-            *reinterpret_cast<float4*>(q + PTILE) = make_float4(u.z, u.w, v.z, v.w);
-        }
-    }
-}
-
-// Non-TMA path: level-1 band-pair tiles from the staged fp32 tile.
-template <int K>
-__device__ __forceinline__ void pair_bands_from_tile(const float* xs, float* bs) {
-    constexpr int PAD = FG<K>::PAD, XP = FG<K>::XPITCH, BT = FG<K>::BT;
-    constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, PHALF = PG<K>::PHALF;
-    for (int idx = threadIdx.x; idx < BT * BT; idx += blockDim.x) {
-        const int ci = idx / BT, cj = idx - ci * BT;
-        const float* p = xs + (2 * ci) * XP + PAD + 2 * cj;
-        const float4 u = haar_u(p[0], p[1], p[XP], p[XP + 1]);
-        float* q = bs + ci * PROW + 4 * pchunk(cj >> 1, PHALF) + 2 * (cj & 1);
-        *reinterpret_cast<float2*>(q) = make_float2(u.x, u.y);
-        *reinterpret_cast<float2*>(q + PTILE) = make_float2(u.z, u.w);
-    }
-}
-
-// Stage pixels [y0-2R, y0+64+2R) x [x0-2R, x0+64+2R) of a plane into xs (pitch XPITCH,
-// column c stored at c + PAD), zero outside the plane. vec: W % 4 == 0 (aligned rows).
-template <int K, typename T>
-__device__ __forceinline__ void stage_tile(const T* xp, int H, int W, int vec, float* xs,
-                                           int y0, int x0) {
-    constexpr int R = FG<K>::R, PAD = FG<K>::PAD, XP = FG<K>::XPITCH;
-    constexpr int ROWS = FG<K>::XROWS, COLS = FG<K>::XCOLS;
-    const int c_lo = x0 - 2 * R;
-    if (vec) {
-        const int g_lo = c_lo >= 0 ? (c_lo & ~3) : -((-c_lo + 3) & ~3);
-        const int ng = (x0 + kTile + 2 * R - g_lo + 3) >> 2;
-        for (int idx = threadIdx.x; idx < ROWS * ng; idx += blockDim.x) {
-            const int r = idx / ng, g = idx - r * ng;
-            const int gy = y0 - 2 * R + r, gx = g_lo + 4 * g;
-            float4 v = f4_zero();
-            if (gy >= 0 && gy < H && gx >= 0 && gx < W) v = IO<T>::ld4(xp + (size_t)gy * W + gx);
-            const int cc = gx - c_lo;
-            float* dst = xs + r * XP + PAD + cc;
-            if (cc >= 0 && cc + 3 < COLS) {
-                if constexpr (FG<K>::STAGE_STORE == 0) {
-                    *reinterpret_cast<float4*>(dst) = v;
-                } else if constexpr (FG<K>::STAGE_STORE == 2) {
-                    reinterpret_cast<float2*>(dst)[0] = make_float2(v.x, v.y);
-                    reinterpret_cast<float2*>(dst)[1] = make_float2(v.z, v.w);
-                } else {
-                    dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
-                }
-            } else {
-                const float e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    if (cc + q >= 0 && cc + q < COLS) dst[q] = e[q];
-            }
-        }
-    } else {
-        for (int idx = threadIdx.x; idx < ROWS * COLS; idx += blockDim.x) {
-            const int r = idx / COLS, cc = idx - r * COLS;
-            const int gy = y0 - 2 * R + r, gx = c_lo + cc;
-            float v = 0.f;
-            if (gy >= 0 && gy < H && gx >= 0 && gx < W) v = IO<T>::ld(xp + (size_t)gy * W + gx);
-            xs[r * XP + PAD + cc] = v;
-        }
-    }
 }
 
 // The 4x4 pixel block of a plane at (r0, c0), zero outside H x W (the padding of a plane

@@ -410,7 +410,10 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
         const int n = (int)(plane / a.C), c = (int)(plane - (long long)n * a.C);
         const T* xp = reinterpret_cast<const T*>(a.x) + plane * plane_elems;
         const T* gp = reinterpret_cast<const T*>(a.dy) + plane * plane_elems;
-        __syncthreads();  // the previous plane is done with shared memory
+        // the previous plane is done with shared memory; every thread's generic accesses are
+        // ordered before the TMA writes issued below and during this plane
+        fence_proxy_async_smem();
+        __syncthreads();
         for (int e = tid; e < a.KP; e += kDT) acc_sm[e] = 0.f;
         if (use_tma && leader) {
             // the first full-resolution tile pair, in flight during the deep levels, and the
@@ -482,6 +485,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
             }
             __syncthreads();
         }
+        fence_proxy_async_smem();  // warp totals may sit in raw X buffer 1, refilled by TMA
 
         // ---- full resolution: warps 0-3 base path, warps 4-7 level-1 band pairs ----
         const bool base_role = (a.L == 0) || (tid < 128);
@@ -521,7 +525,6 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
             }
             if (use_tma && leader && t + 1 < ntiles) {
                 const int ny = (t + 1) / tiles_x, nx = (t + 1) - ny * tiles_x, nb = rb ^ 1;
-                fence_proxy_async_smem();
                 mbar_arrive_expect_tx(bar + nb, BYTES);
                 tma_load_3d(sm + a.o_rawx + nb * a.rawx_f, &a.tmx, nx * kTile - XBox<K, T>::XOFF,
                             ny * kTile - 2 * R, (int)plane, bar + nb);
