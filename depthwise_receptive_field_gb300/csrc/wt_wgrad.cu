@@ -11,10 +11,9 @@
 // Kernel 1 (wt_dw_plane_kernel): a persistent grid of 256-thread CTAs walks the (n, c)
 // planes. Per plane:
 //   level-2 sweep (L >= 2): X and dY stream through shared memory in TMA boxes (2 to 4
-//     box pairs in flight, as shared memory allows; each warp releases a pair on an
-//     mbarrier, and the pair is refilled once all eight have, with no CTA barrier); every 4x4 pixel block becomes its four level-2 subbands (Eq. 5
-//     twice), stored for both tensors in the CTA's workspace slot (L2-resident); LL / 2 of
-//     it is the carrier X^(2), dY^(2) of level 3.
+//     box pairs in flight, as shared memory allows); every 4x4 pixel block becomes its
+//     four level-2 subbands (Eq. 5 twice), stored for both tensors in the CTA's
+//     workspace slot (L2-resident); LL / 2 of it is the carrier X^(2), dY^(2) of level 3.
 //   deep levels (l >= 2): 32x32 tiles of the level's subbands of X (R halo) and dY are
 //     staged as band-pair tiles, (LL, LH) and (HL, HH) (level 2 from the slot, deeper
 //     levels from the carriers); threads 0-127 correlate pair 0 and 128-255 pair 1 with
@@ -29,7 +28,8 @@
 //   The per-plane partial vector [dW~0 | db~ | dW~^(l)_b] goes to the workspace.
 // Kernel 2 (wt_dw_reduce_kernel): per channel, sums the N partial vectors in a fixed
 //   order and applies the gradient unfolding of §4.3 Eq. 9.
-// No atomics anywhere: results are bitwise reproducible.
+// No atomics on data (only the counter that hands out planes): results are bitwise
+// reproducible.
 #include "wt_internal.h"
 #include "wt_tile.cuh"
 #include "wt_tma.cuh"

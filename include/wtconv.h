@@ -38,7 +38,9 @@
  *    size (the pages are silent on odd sizes; this is the plain completion of Eq. 5 and
  *    Eq. 12). It equals running the layer on X zero-padded to multiples of 2^L and keeping
  *    the top-left H x W outputs, which is how the kernels compute it.
- *  - Results are deterministic: no atomics; every reduction runs in a fixed order.
+ *  - Results are deterministic: no atomics on data (one atomic counter hands out planes to
+ *    the persistent CTAs, which does not change any result); every reduction runs in a
+ *    fixed order.
  */
 #ifndef WTCONV_H_
 #define WTCONV_H_
