@@ -17,14 +17,35 @@ TOL = {"f32": 1e-5, "bf16": 2e-2, "f16": 2e-3}
 TOL_PARAM = {"f32": 1e-5, "bf16": 1e-4, "f16": 1e-4}
 
 
-def rel_err(got, ref) -> float:
+def rel_err(got, ref, floor: float = 0.0) -> float:
+    """max |got - ref| / max(max |ref|, floor)."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
-    scale = np.abs(ref).max()
+    scale = max(float(np.abs(ref).max()), floor)
     if scale == 0:
         return float(np.abs(got).max())
     return float(np.abs(got - ref).max() / scale)
+
+
+# db0 = s0 * sum(dY) is a plain sum, whose floating-point error is bounded by the sum of the
+# absolute terms, not by the sum: a channel whose dY nearly cancels (a single 42x72 plane
+# summing to -0.057 out of 2404 in absolute terms) has a tiny reference and an ordinary
+# fp32 error of a few 1e-6. Its scale is therefore floored at 1e-3 of s0 * sum|dY| (the
+# largest channel's). The fp32 gate then allows an absolute error of 1e-8 * s0 * sum|dY|,
+# still below the unit roundoff (6e-8) times that magnitude: an accurately summed result
+# is still required.
+DB0_FLOOR = 1e-3
+
+
+def db0_floor(inp: dict, c_idx=None) -> float:
+    dy = inp["dy"].to(torch.float64)
+    s0 = inp["s0"].to(torch.float64)
+    if c_idx is not None:
+        ci = torch.as_tensor(c_idx)
+        dy, s0 = dy[:, ci], s0[ci]
+    mag = (s0.abs() * dy.abs().sum(dim=(0, 2, 3))).max().item()
+    return DB0_FLOOR * mag
 
 
 def to64(t):
@@ -76,8 +97,11 @@ def oracle_run(inp: dict, levels: int, backward: bool, n_idx=None, c_idx=None) -
     return out
 
 
-def compare(gpu: dict, ref: dict, dtype: str, levels: int, c_idx=None, n_idx=None) -> dict:
-    """Per-tensor relative errors (gpu sliced to the oracle's sub-batch when sampled)."""
+def compare(gpu: dict, ref: dict, dtype: str, levels: int, c_idx=None, n_idx=None,
+            floors=None) -> dict:
+    """Per-tensor relative errors (gpu sliced to the oracle's sub-batch when sampled);
+    floors: optional per-tensor lower bounds of the error scale."""
+    floors = floors or {}
     errs = {}
     for name, r in ref.items():
         g = gpu[name]
@@ -93,7 +117,7 @@ def compare(gpu: dict, ref: dict, dtype: str, levels: int, c_idx=None, n_idx=Non
                 g = g[:, list(c_idx)]
         if name in ("dwl", "dsl") and levels == 0:
             continue
-        errs[name] = rel_err(g, r)
+        errs[name] = rel_err(g, r, floors.get(name, 0.0))
     return errs
 
 
@@ -107,5 +131,6 @@ def run_and_compare(wl: Workload, *, bias_and_scale=False, sample_channels=None,
     inp = make_inputs(wl, bias_and_scale=bias_and_scale)
     gpu = gpu_run(inp, wl.levels, wl.backward, fused=fused)
     ref = oracle_run(inp, wl.levels, wl.backward, c_idx=sample_channels)
-    errs = compare(gpu, ref, wl.dtype, wl.levels, c_idx=sample_channels)
+    floors = {"db0": db0_floor(inp, sample_channels)} if wl.backward else None
+    errs = compare(gpu, ref, wl.dtype, wl.levels, c_idx=sample_channels, floors=floors)
     return errs, gpu

@@ -156,3 +156,28 @@ def test_workspace_errors():
     with pytest.raises(B.WTConvError) as ei:
         B.wtconv_forward(desc, x.data_ptr() + 4, p.w0, None, p.wl, torch.empty_like(x))
     assert ei.value.status == B.WT_ERR_INVALID_ARG
+
+
+def _random_case(seed):
+    """A seeded random configuration: shape, k, L, I/O dtype (small planes, so that the
+    oracle finishes quickly), covering odd sides, rows that TMA can and cannot stage, every
+    built k and both one- and multi-tile planes."""
+    rng = np.random.default_rng(seed)
+    k = int(rng.choice([1, 3, 5, 7]))
+    dtype = str(rng.choice(["f32", "bf16", "f16"]))
+    h = int(rng.integers(1, 161))
+    w = int(rng.integers(1, 161))
+    levels = int(rng.integers(0, 7))
+    n = int(rng.integers(1, 3))
+    c = int(rng.integers(1, 4))
+    if rng.random() < 0.5:  # rows of a multiple of 16 bytes: the TMA-staged kernels
+        w = max(8, w - w % 8)
+    return n, c, h, w, k, levels, dtype
+
+
+@pytest.mark.parametrize("seed", range(32))
+def test_random_shapes(seed):
+    n, c, h, w, k, L, dtype = _random_case(seed)
+    wl = shape_workload(n, c, h, w, k, L, dtype, seed=5000 + seed)
+    errs, _ = run_and_compare(wl, bias_and_scale=True)
+    assert_within(errs, wl.dtype, wl.name)
