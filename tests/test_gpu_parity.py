@@ -181,3 +181,25 @@ def test_random_shapes(seed):
     wl = shape_workload(n, c, h, w, k, L, dtype, seed=5000 + seed)
     errs, _ = run_and_compare(wl, bias_and_scale=True)
     assert_within(errs, wl.dtype, wl.name)
+
+
+def _random_large_case(seed):
+    """Seeded random larger planes: multi-tile level-2 grids and deep states that may move
+    to the workspace slot or fall back to one CTA per SM."""
+    rng = np.random.default_rng(10_000 + seed)
+    k = int(rng.choice([3, 5, 7]))
+    dtype = str(rng.choice(["f32", "bf16", "f16"]))
+    h = int(rng.integers(130, 601))
+    w = int(rng.integers(130, 601))
+    if rng.random() < 0.6:
+        w -= w % 8
+    levels = int(rng.integers(2, 9))
+    return 1, 1, h, w, k, levels, dtype
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_large_planes(seed):
+    n, c, h, w, k, L, dtype = _random_large_case(seed)
+    wl = shape_workload(n, c, h, w, k, L, dtype, seed=6000 + seed)
+    errs, _ = run_and_compare(wl, bias_and_scale=True)
+    assert_within(errs, wl.dtype, wl.name)
