@@ -241,20 +241,25 @@ __device__ __forceinline__ void stage_raw(const T* xp, int H, int W, T* raw, int
     }
 }
 
-// N consecutive raw elements starting P (0 or 1) past the 2-element-aligned pointer p,
-// widened to float: 32-bit loads for 16-bit types, 64-bit loads for fp32.
-template <typename T, int N, int P>
-__device__ __forceinline__ void load_raw_run(const T* p, float (&v)[N]) {
-    constexpr int NW = (N + P + 1) / 2;  // 2-element words
-    float e[2 * NW];
+// N consecutive raw elements v[i] = p[S + i], widened to float, read as 4-element vectors
+// from the 4-element-aligned offset S & ~3: 8-byte loads for 16-bit types, 16-byte loads for
+// fp32 (p must be that aligned). A half-warp's 16 pixel blocks then read one contiguous
+// 128 / 256 bytes per load, with no bank conflicts between the two half-warps' rows.
+template <typename T, int N, int S>
+__device__ __forceinline__ void load_raw_vec(const T* p, float (&v)[N]) {
+    constexpr int A0 = S & ~3;
+    constexpr int NL = (S - A0 + N + 3) / 4;
+    float e[4 * NL];
 #pragma unroll
-    for (int j = 0; j < NW; ++j) {
-        const float2 t = ld2_smem<T>(p + 2 * j);
-        e[2 * j] = t.x;
-        e[2 * j + 1] = t.y;
+    for (int j = 0; j < NL; ++j) {
+        const float4 t = ld4_smem<T>(p + A0 + 4 * j);
+        e[4 * j] = t.x;
+        e[4 * j + 1] = t.y;
+        e[4 * j + 2] = t.z;
+        e[4 * j + 3] = t.w;
     }
 #pragma unroll
-    for (int i = 0; i < N; ++i) v[i] = e[i + P];
+    for (int i = 0; i < N; ++i) v[i] = e[S - A0 + i];
 }
 
 // Packed base k x k filter of the 4x4 pixel block (by, bx) of a tile, read from the raw tile
@@ -266,7 +271,7 @@ __device__ __forceinline__ void conv_base_4x4_raw(const T* raw, int by, int bx,
                                                   const float* wdup, f2x (&acc)[4][2]) {
     constexpr int R = FG<K>::R, KK = FG<K>::KK;
     constexpr int RW = XBox<K, T>::XBW, S = XBox<K, T>::XOFF - R;
-    constexpr int P = S & 1, NV = 4 + 2 * R;
+    constexpr int NV = 4 + 2 * R;
     f2x w[KK];
 #pragma unroll
     for (int q = 0; q + 1 < KK; q += 2) {
@@ -278,11 +283,11 @@ __device__ __forceinline__ void conv_base_4x4_raw(const T* raw, int by, int bx,
         const float2 t = *reinterpret_cast<const float2*>(wdup + 2 * (KK - 1));
         w[KK - 1] = pk2(t.x, t.y);
     }
-    const T* base = raw + (4 * by + R) * RW + 4 * bx + (S - P);
+    const T* base = raw + (4 * by + R) * RW + 4 * bx;
 #pragma unroll
     for (int r = 0; r < 4 + 2 * R; ++r) {
         float v[NV];
-        load_raw_run<T, NV, P>(base + r * RW, v);
+        load_raw_vec<T, NV, S>(base + r * RW, v);
         f2x A[NV / 2], B[NV / 2 - 1];
 #pragma unroll
         for (int m = 0; m < NV / 2; ++m) A[m] = pk2(v[2 * m], v[2 * m + 1]);
@@ -315,7 +320,7 @@ __device__ __forceinline__ void corr_base_4x4_raw(const T* rawx, const T* rawg, 
                                                   f2x (&acc)[K * K]) {
     constexpr int R = FG<K>::R;
     constexpr int RW = XBox<K, T>::XBW, S = XBox<K, T>::XOFF - R;
-    constexpr int P = S & 1, NV = 4 + 2 * R;
+    constexpr int NV = 4 + 2 * R;
     f2x g[4][2];
 #pragma unroll
     for (int o = 0; o < 4; ++o) {
@@ -323,11 +328,11 @@ __device__ __forceinline__ void corr_base_4x4_raw(const T* rawx, const T* rawg, 
         g[o][0] = pk2(t.x, t.y);
         g[o][1] = pk2(t.z, t.w);
     }
-    const T* base = rawx + (4 * by + R) * RW + 4 * bx + (S - P);
+    const T* base = rawx + (4 * by + R) * RW + 4 * bx;
 #pragma unroll
     for (int r = 0; r < 4 + 2 * R; ++r) {
         float v[NV];
-        load_raw_run<T, NV, P>(base + r * RW, v);
+        load_raw_vec<T, NV, S>(base + r * RW, v);
         f2x A[NV / 2], B[NV / 2 - 1];
 #pragma unroll
         for (int m = 0; m < NV / 2; ++m) A[m] = pk2(v[2 * m], v[2 * m + 1]);
