@@ -206,8 +206,11 @@ __device__ __forceinline__ void convert_bands(const T* raw, float* bs) {
     constexpr int NCR = PG<K>::NCR, PROW = PG<K>::PROW, PTILE = PG<K>::PTILE;
     constexpr int PHALF = PG<K>::PHALF;
     constexpr int RW = XBox<K, T>::XBW, C0 = XBox<K, T>::C0;
+    // items in storage order (unit u of a pair-tile row holds chunk m, pchunk(m) = u), so
+    // that a quarter-warp's 16-byte stores are contiguous (no bank conflicts)
     for (int idx = threadIdx.x; idx < BT * NCR; idx += blockDim.x) {
-        const int ci = idx / NCR, m = idx - ci * NCR;
+        const int ci = idx / NCR, u = idx - ci * NCR;
+        const int m = (u < PHALF) ? 2 * u : 2 * (u - PHALF) + 1;
         const T* r0 = raw + (2 * ci) * RW + C0 + 4 * m;
         float2 a0, a1, b0, b1;
         if constexpr (C0 % 4 == 0) {  // 4-element aligned: one vector load per row
@@ -218,11 +221,11 @@ __device__ __forceinline__ void convert_bands(const T* raw, float* bs) {
             a0 = ld2_smem<T>(r0); a1 = ld2_smem<T>(r0 + 2);
             b0 = ld2_smem<T>(r0 + RW); b1 = ld2_smem<T>(r0 + RW + 2);
         }
-        const float4 u = haar_u(a0.x, a0.y, b0.x, b0.y);
-        const float4 v = haar_u(a1.x, a1.y, b1.x, b1.y);
-        float* q = bs + ci * PROW + 4 * pchunk(m, PHALF);
-        *reinterpret_cast<float4*>(q) = make_float4(u.x, u.y, v.x, v.y);
-        *reinterpret_cast<float4*>(q + PTILE) = make_float4(u.z, u.w, v.z, v.w);
+        const float4 h0 = haar_u(a0.x, a0.y, b0.x, b0.y);
+        const float4 h1 = haar_u(a1.x, a1.y, b1.x, b1.y);
+        float* q = bs + ci * PROW + 4 * u;
+        *reinterpret_cast<float4*>(q) = make_float4(h0.x, h0.y, h1.x, h1.y);
+        *reinterpret_cast<float4*>(q + PTILE) = make_float4(h0.z, h0.w, h1.z, h1.w);
     }
 }
 

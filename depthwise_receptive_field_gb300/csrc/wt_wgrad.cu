@@ -288,17 +288,20 @@ __device__ __forceinline__ bool dw_sweep(const DwArgs& a, const T* xp, const T* 
 template <typename T>
 __device__ __forceinline__ float convert_raw_dy(const T* raw, float* gb, bool bands) {
     float sum = 0.f;
+    // items in storage order (unit u of a pair-tile row holds chunk m), so that a
+    // quarter-warp's 16-byte stores are contiguous (no bank conflicts)
     for (int idx = threadIdx.x; idx < kCT * (kCT / 2); idx += blockDim.x) {
-        const int ci = idx >> 4, m = idx & 15;
+        const int ci = idx >> 4, u = idx & 15;
+        const int m = (u < kGHalf) ? 2 * u : 2 * (u - kGHalf) + 1;
         const T* r0 = raw + (2 * ci) * kTile + 4 * m;
         const float4 ra = ld4_smem<T>(r0), rb = ld4_smem<T>(r0 + kTile);
         sum += ((ra.x + ra.y) + (ra.z + ra.w)) + ((rb.x + rb.y) + (rb.z + rb.w));
         if (bands) {
-            const float4 u = haar_u(ra.x, ra.y, rb.x, rb.y);
-            const float4 v = haar_u(ra.z, ra.w, rb.z, rb.w);
-            float* q = gb + ci * kGRow + 4 * pchunk(m, kGHalf);
-            *reinterpret_cast<float4*>(q) = make_float4(u.x, u.y, v.x, v.y);
-            *reinterpret_cast<float4*>(q + kGTile) = make_float4(u.z, u.w, v.z, v.w);
+            const float4 h0 = haar_u(ra.x, ra.y, rb.x, rb.y);
+            const float4 h1 = haar_u(ra.z, ra.w, rb.z, rb.w);
+            float* q = gb + ci * kGRow + 4 * u;
+            *reinterpret_cast<float4*>(q) = make_float4(h0.x, h0.y, h1.x, h1.y);
+            *reinterpret_cast<float4*>(q + kGTile) = make_float4(h0.z, h0.w, h1.z, h1.w);
         }
     }
     return sum;
