@@ -380,11 +380,13 @@ __device__ __forceinline__ bool deep_levels(const FwdArgs& a, float* sm, float* 
                         } else {
 #pragma unroll
                             for (int o = 0; o < 2; ++o) {
-                                float* zr = zs + pp * ZTILE + (2 * bi + o) * ZROW + 8 * bj;
+                                float* zr = zs + pp * ZTILE + (2 * bi + o) * ZROW;
                                 const float2 q0 = upk2(acc[o][0]), q1 = upk2(acc[o][1]);
                                 const float2 q2 = upk2(acc[o][2]), q3 = upk2(acc[o][3]);
-                                reinterpret_cast<float4*>(zr)[0] = make_float4(q0.x, q0.y, q1.x, q1.y);
-                                reinterpret_cast<float4*>(zr)[1] = make_float4(q2.x, q2.y, q3.x, q3.y);
+                                *reinterpret_cast<float4*>(zr + 4 * zunit(2 * bj)) =
+                                    make_float4(q0.x, q0.y, q1.x, q1.y);
+                                *reinterpret_cast<float4*>(zr + 4 * zunit(2 * bj + 1)) =
+                                    make_float4(q2.x, q2.y, q3.x, q3.y);
                             }
                         }
                     }
@@ -398,8 +400,9 @@ __device__ __forceinline__ bool deep_levels(const FwdArgs& a, float* sm, float* 
                         const int ti = 4 * (tid >> 5) + k, tj = tid & 31;
                         const int i2 = ti0 + ti, j2 = tj0 + tj;
                         if (i2 >= Hl || j2 >= Wl) continue;
-                        const float2 za = *reinterpret_cast<const float2*>(zs + ti * ZROW + 2 * tj);
-                        const float2 zb = *reinterpret_cast<const float2*>(zs + ZTILE + ti * ZROW + 2 * tj);
+                        const float* zc = zs + ti * ZROW + 4 * zunit(tj >> 1) + 2 * (tj & 1);
+                        const float2 za = *reinterpret_cast<const float2*>(zc);
+                        const float2 zb = *reinterpret_cast<const float2*>(zc + ZTILE);
                         const float4 z = make_float4(za.x, za.y, zb.x, zb.y);
                         float v = 0.f;
                         for (int m = 3; m <= a.L; ++m) {
@@ -616,11 +619,13 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                                      acc);
 #pragma unroll
                     for (int o = 0; o < 2; ++o) {
-                        float* zr = zs + pp * ZTILE + (2 * bi + o) * ZROW + 8 * bj;
+                        float* zr = zs + pp * ZTILE + (2 * bi + o) * ZROW;
                         const float2 q0 = upk2(acc[o][0]), q1 = upk2(acc[o][1]);
                         const float2 q2 = upk2(acc[o][2]), q3 = upk2(acc[o][3]);
-                        reinterpret_cast<float4*>(zr)[0] = make_float4(q0.x, q0.y, q1.x, q1.y);
-                        reinterpret_cast<float4*>(zr)[1] = make_float4(q2.x, q2.y, q3.x, q3.y);
+                        *reinterpret_cast<float4*>(zr + 4 * zunit(2 * bj)) =
+                            make_float4(q0.x, q0.y, q1.x, q1.y);
+                        *reinterpret_cast<float4*>(zr + 4 * zunit(2 * bj + 1)) =
+                            make_float4(q2.x, q2.y, q3.x, q3.y);
                     }
                 }
                 __syncwarp();
@@ -646,9 +651,9 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                     for (int i = 0; i < 2; ++i) {
                         // (LL, LH) and (HL, HH) of coefficients (2by+i, 2bx) and (2by+i, 2bx+1)
                         const float4 za = *reinterpret_cast<const float4*>(
-                            zs + (2 * by + i) * ZROW + 4 * bx);
+                            zs + (2 * by + i) * ZROW + 4 * zunit(bx));
                         const float4 zb = *reinterpret_cast<const float4*>(
-                            zs + ZTILE + (2 * by + i) * ZROW + 4 * bx);
+                            zs + ZTILE + (2 * by + i) * ZROW + 4 * zunit(bx));
                         const f2x s0 = add2(pk2(za.x, za.y), pk2(zb.x, zb.y));  // LL+HL, LH+HH
                         const f2x m0 = sub2(pk2(za.x, za.y), pk2(zb.x, zb.y));  // LL-HL, LH-HH
                         const f2x s1 = add2(pk2(za.z, za.w), pk2(zb.z, zb.w));

@@ -46,6 +46,12 @@ struct PG {
 
 __device__ __forceinline__ int pchunk(int c, int half) { return (c >> 1) + (c & 1) * half; }
 
+// Filtered pair tiles (ZROW floats = 16 16-byte units a row): chunk c (two coefficients of a
+// band pair) is stored at unit c ^ (c / 8), a permutation. Writers store chunks 2j and
+// 2j + 1 (j = 0..7 in a quarter-warp), readers chunk j or j + 8: each of these sets of 8
+// lands on 8 distinct bank groups, so neither side has bank conflicts.
+__device__ __forceinline__ int zunit(int c) { return c ^ ((c >> 3) & 1); }
+
 // Packed k x k filter of a 2x4 block of one band pair: acc[o][q] = sum_{u,v} w[u][v] (.)
 // cell[o+u][q+v], two bands at once. `rows` = pair tile + (first window row) * PROW;
 // the block's window starts at cell 4*bj. wsl = KK taps as (w_b0, w_b1) pairs.
