@@ -277,6 +277,103 @@ __device__ __forceinline__ void deep_stage(const FwdArgs& a, const float* u2, fl
         deep_stage_from<K, 2>(a, u2, nullptr, bs, l, ti0, tj0);
 }
 
+// Small deep levels share one stage/filter round. A group is the levels l, l-1, ..., lo >= 3
+// whose grids fit one output tile, stacked in the band-pair tiles: level m takes
+// 2 ceil(Hm/2) + 2R rows from row offset off_m and 4 ceil(Wm/4) + 2R columns, exactly the
+// cells its 2x4-block filter reads; the stack fits the tile's BT rows and the blocks of all
+// its levels fit one pass of the CTA's threads. Returns lo (lo = l + 1: no group, level l
+// is filtered tile by tile).
+template <int K>
+__device__ __forceinline__ int deep_group(const FwdArgs& a, int l) {
+    constexpr int R = FG<K>::R, BT = FG<K>::BT;
+    int lo = l + 1, rows = 0, blocks = 0;
+    for (int m = l; m >= 3; --m) {
+        const int Hm = a.Hp >> m, Wm = a.Wp >> m;
+        if (Hm > kCT || Wm > kCT) break;
+        const int nbi = (Hm + 1) >> 1, nbj = (Wm + 3) >> 2;
+        if (rows + 2 * nbi + 2 * R > BT || blocks + 2 * nbi * nbj > kFT) break;
+        rows += 2 * nbi + 2 * R;
+        blocks += 2 * nbi * nbj;
+        lo = m;
+    }
+    // a lone level that fills the tile gains nothing from the compact round
+    if (lo == l && rows == BT && 4 * (((a.Wp >> l) + 3) >> 2) + 2 * R == BT) lo = l + 1;
+    return lo;
+}
+
+// Stage a group (levels l..lo): every level's subbands, transformed from its carrier
+// X^(m-1) by Eq. 5, with an R halo and zeros outside its grid.
+template <int K>
+__device__ __forceinline__ void deep_group_stage(const FwdArgs& a, const float* u2,
+                                                 const float* deep, float* bs, int l, int lo) {
+    constexpr int R = FG<K>::R;
+    constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, PHALF = PG<K>::PHALF;
+    int off = 0;
+    for (int m = l; m >= lo; --m) {
+        const int Hm = a.Hp >> m, Wm = a.Wp >> m, Wp = a.Wp >> (m - 1);
+        const int rows = 2 * ((Hm + 1) >> 1) + 2 * R, cols = 4 * ((Wm + 3) >> 2) + 2 * R;
+        const float* cp = (m >= 4 || a.car2) ? deep + a.o_car[m - 1] : nullptr;
+        for (int idx = threadIdx.x; idx < rows * cols; idx += kFT) {
+            const int si = idx / cols, sj = idx - si * cols;
+            const int gi = si - R, gj = sj - R;
+            float4 u = f4_zero();
+            if (gi >= 0 && gi < Hm && gj >= 0 && gj < Wm) {
+                const float4 q = carrier_block(u2, cp, gi, gj, Wp);
+                u = haar_u(q.x, q.y, q.z, q.w);
+            }
+            float* q = bs + (off + si) * PROW + 4 * pchunk(sj >> 1, PHALF) + 2 * (sj & 1);
+            *reinterpret_cast<float2*>(q) = make_float2(u.x, u.y);
+            *reinterpret_cast<float2*>(q + PTILE) = make_float2(u.z, u.w);
+        }
+        off += rows;
+    }
+}
+
+// Filter a staged group: thread t takes one 2x4 block of one band pair of one level (the
+// levels' blocks numbered one after another), and writes its Z^(m) quadruples.
+template <int K>
+__device__ __forceinline__ void deep_group_filter(const FwdArgs& a, const float* bs,
+                                                  const float* wsm, float* deep, int l,
+                                                  int lo) {
+    constexpr int R = FG<K>::R;
+    constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, WS = PG<K>::WS;
+    int t = threadIdx.x, off = 0, lev = 0, Hm = 0, Wm = 0, nbj = 1, nb = 1;
+    for (int m = l; m >= lo; --m) {
+        const int h = a.Hp >> m, w = a.Wp >> m;
+        const int bi_n = (h + 1) >> 1, bj_n = (w + 3) >> 2;
+        if (lev == 0) {
+            if (t < 2 * bi_n * bj_n) {
+                lev = m;
+                Hm = h;
+                Wm = w;
+                nbj = bj_n;
+                nb = bi_n * bj_n;
+            } else {
+                t -= 2 * bi_n * bj_n;
+                off += 2 * bi_n + 2 * R;
+            }
+        }
+    }
+    if (lev == 0) return;
+    const int pp = t >= nb ? 1 : 0;
+    const int r = t - pp * nb;
+    const int bi = r / nbj, bj = r - bi * nbj;
+    f2x acc[2][4];
+    conv_pair_2x4<K>(bs + pp * PTILE + (off + 2 * bi) * PROW, bj,
+                     wsm + (1 + 2 * (lev - 1) + pp) * WS, acc);
+    float* zl = deep + a.o_zl[lev];
+    const int gi0 = 2 * bi, gj0 = 4 * bj;
+#pragma unroll
+    for (int o = 0; o < 2; ++o) {
+        if (gi0 + o >= Hm) continue;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (gj0 + q < Wm)
+                *reinterpret_cast<float2*>(zl + ((gi0 + o) * Wm + gj0 + q) * 4 + 2 * pp) =
+                    upk2(acc[o][q]);
+    }
+}
+
 // A TMA-staged level-2 tile ([BT][BT] quadruples (LL, LH, HL, HH), zero outside the level
 // grid) into the two band-pair tiles.
 template <int K>
@@ -324,6 +421,17 @@ __device__ __forceinline__ bool deep_levels(const FwdArgs& a, float* sm, float* 
     deep_carriers(a, u2, deep);
     for (int l = a.L; l >= 2; --l) {
         const int Hl = a.Hp >> l, Wl = a.Wp >> l;
+        if (l >= 3) {
+            const int lo = deep_group<K>(a, l);
+            if (lo <= l) {
+                deep_group_stage<K>(a, u2, deep, bs, l, lo);
+                __syncthreads();
+                deep_group_filter<K>(a, bs, wsm, deep, l, lo);
+                __syncthreads();  // the band-pair tiles are free for the next stage
+                l = lo;
+                continue;
+            }
+        }
         if (l == 2 && tma2) {
             // every thread's generic accesses to the carriers are ordered before the load
             fence_proxy_async_smem();
