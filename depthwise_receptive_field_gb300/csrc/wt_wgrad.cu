@@ -113,6 +113,39 @@ __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const float* u2x,
     float* cly = (l >= 3 && l < a.L) ? cbase + a.o_cary[l] : nullptr;
     const float4* ux4 = reinterpret_cast<const float4*>(u2x);
     const float4* ug4 = reinterpret_cast<const float4*>(u2g);
+    // a level whose grid is smaller than one tile: only the cells its correlations read,
+    // 2 ceil(Hl/2) + 2R rows by 4 ceil(Wl/4) + 2R columns of X subbands (the dY subbands
+    // are the inner part), zero outside the grid
+    const int crow = 2 * ((Hl + 1) >> 1) + 2 * R, ccol = 4 * ((Wl + 3) >> 2) + 2 * R;
+    if (Hl <= kCT && Wl <= kCT && crow * ccol < BT * BT) {
+        for (int idx = threadIdx.x; idx < crow * ccol; idx += kDT) {
+            const int si = idx / ccol, sj = idx - si * ccol;
+            const int gi = si - R, gj = sj - R;
+            const bool inner = si >= R && si < crow - R && sj >= R && sj < ccol - R;
+            float4 ux = f4_zero(), ug = f4_zero();
+            if (gi >= 0 && gi < Hl && gj >= 0 && gj < Wl) {
+                if (l == 2) {
+                    ux = __ldcg(ux4 + (size_t)gi * Wl + gj);
+                    if (inner) ug = __ldcg(ug4 + (size_t)gi * Wl + gj);
+                } else {
+                    ux = carrier_u(cpx, u2x, gi, gj);
+                    if (clx) clx[gi * Wl + gj] = 0.5f * ux.x;
+                    ug = carrier_u(cpy, u2g, gi, gj);
+                    if (cly) cly[gi * Wl + gj] = 0.5f * ug.x;
+                }
+            }
+            float* q = xb + si * PROW + 4 * pchunk(sj >> 1, PHALF) + 2 * (sj & 1);
+            *reinterpret_cast<float2*>(q) = make_float2(ux.x, ux.y);
+            *reinterpret_cast<float2*>(q + PTILE) = make_float2(ux.z, ux.w);
+            if (inner) {
+                const int ci = si - R, cj = sj - R;
+                float* r = gb + ci * kGRow + 4 * pchunk(cj >> 1, kGHalf) + 2 * (cj & 1);
+                *reinterpret_cast<float2*>(r) = make_float2(ug.x, ug.y);
+                *reinterpret_cast<float2*>(r + kGTile) = make_float2(ug.z, ug.w);
+            }
+        }
+        return;
+    }
     if (l == 2) {  // all loads first, then all stores (loads from L2 overlap)
         float4 uxv[NIT], ugv[NIT];
 #pragma unroll
