@@ -92,7 +92,7 @@ constexpr int kGTile = kCT * kGRow;   // floats per pair tile
 template <int K>
 __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const float* u2x, const float* u2g,
                                               float* sm, float* cbase, int l, int ti0,
-                                              int tj0) {
+                                              int tj0, int xoff = 0, int goff = 0) {
     constexpr int R = FG<K>::R, BT = FG<K>::BT;
     constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, PHALF = PG<K>::PHALF;
     constexpr int NIT = (BT * BT + kDT - 1) / kDT;
@@ -115,9 +115,10 @@ __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const float* u2x,
     const float4* ug4 = reinterpret_cast<const float4*>(u2g);
     // a level whose grid is smaller than one tile: only the cells its correlations read,
     // 2 ceil(Hl/2) + 2R rows by 4 ceil(Wl/4) + 2R columns of X subbands (the dY subbands
-    // are the inner part), zero outside the grid
+    // are the inner part), zero outside the grid; from rows xoff and goff of the tiles
+    // when the level is part of a group
     const int crow = 2 * ((Hl + 1) >> 1) + 2 * R, ccol = 4 * ((Wl + 3) >> 2) + 2 * R;
-    if (Hl <= kCT && Wl <= kCT && crow * ccol < BT * BT) {
+    if (Hl <= kCT && Wl <= kCT && (crow * ccol < BT * BT || xoff + goff > 0)) {
         for (int idx = threadIdx.x; idx < crow * ccol; idx += kDT) {
             const int si = idx / ccol, sj = idx - si * ccol;
             const int gi = si - R, gj = sj - R;
@@ -134,12 +135,12 @@ __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const float* u2x,
                     if (cly) cly[gi * Wl + gj] = 0.5f * ug.x;
                 }
             }
-            float* q = xb + si * PROW + 4 * pchunk(sj >> 1, PHALF) + 2 * (sj & 1);
+            float* q = xb + (xoff + si) * PROW + 4 * pchunk(sj >> 1, PHALF) + 2 * (sj & 1);
             *reinterpret_cast<float2*>(q) = make_float2(ux.x, ux.y);
             *reinterpret_cast<float2*>(q + PTILE) = make_float2(ux.z, ux.w);
             if (inner) {
                 const int ci = si - R, cj = sj - R;
-                float* r = gb + ci * kGRow + 4 * pchunk(cj >> 1, kGHalf) + 2 * (cj & 1);
+                float* r = gb + (goff + ci) * kGRow + 4 * pchunk(cj >> 1, kGHalf) + 2 * (cj & 1);
                 *reinterpret_cast<float2*>(r) = make_float2(ug.x, ug.y);
                 *reinterpret_cast<float2*>(r + kGTile) = make_float2(ug.z, ug.w);
             }
@@ -208,6 +209,28 @@ __device__ __forceinline__ void dw_deep_stage(const DwArgs& a, const float* u2x,
             *reinterpret_cast<float2*>(r + kGTile) = make_float2(ug.z, ug.w);
         }
     }
+}
+
+// Small deep levels share one stage/correlate/flush round. A group is the levels l..hi whose
+// grids fit one tile, stacked in the pair tiles (X: 2 ceil(Hm/2) + 2R rows each, dY:
+// 2 ceil(Hm/2) rows each) and given whole warps per band pair (ceil(blocks / 32) each, at
+// most the CTA's 8). Returns hi (hi = l: level l alone, hi < l: level l spans tiles).
+template <int K>
+__device__ __forceinline__ int dw_group(const DwArgs& a, int l) {
+    constexpr int R = FG<K>::R, BT = FG<K>::BT;
+    int hi = l - 1, rows = 0, grows = 0, warps = 0;
+    for (int m = l; m <= a.L; ++m) {
+        const int Hm = a.Hp >> m, Wm = a.Wp >> m;
+        if (Hm > kCT || Wm > kCT) break;
+        const int nbi = (Hm + 1) >> 1, nbj = (Wm + 3) >> 2;
+        const int nw = 2 * ((nbi * nbj + 31) >> 5);
+        if (rows + 2 * nbi + 2 * R > BT || grows + 2 * nbi > kCT || warps + nw > kDT / 32) break;
+        rows += 2 * nbi + 2 * R;
+        grows += 2 * nbi;
+        warps += nw;
+        hi = m;
+    }
+    return hi;
 }
 
 // Level-2 sweep of X and dY: the unnormalized level-2 subbands of every position go to
@@ -485,6 +508,87 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
         }
         for (int l = 2; l <= a.L; ++l) {
             const int Hl = a.Hp >> l, Wl = a.Wp >> l;
+            const int hi = dw_group<K>(a, l);
+            if (hi > l) {
+                // stage levels l..hi (level m + 1 >= 4 reads the carrier level m writes)
+                int xoff = 0, goff = 0;
+                for (int m = l; m <= hi; ++m) {
+                    dw_deep_stage<K>(a, u2x, u2g, sm, cbase, m, 0, 0, xoff, goff);
+                    const int nbi = ((a.Hp >> m) + 1) >> 1;
+                    xoff += 2 * nbi + 2 * R;
+                    goff += 2 * nbi;
+                    if (m >= 3 && m < hi) __syncthreads();
+                }
+                __syncthreads();
+                // this warp's unit: level lev, band pair pp, blocks from 32 * (warp - w0)
+                int lev = 0, pp = 0, w0 = 0, nbj = 1, nbk = 0, Hm = 0, Wm = 0;
+                xoff = goff = 0;
+                {
+                    int wn = 0, xo = 0, go = 0;
+                    for (int m = l; m <= hi; ++m) {
+                        const int h = a.Hp >> m, w = a.Wp >> m;
+                        const int bi_n = (h + 1) >> 1, bj_n = (w + 3) >> 2;
+                        const int nw = (bi_n * bj_n + 31) >> 5;
+                        for (int q = 0; q < 2; ++q) {
+                            if (lev == 0 && warp < wn + nw) {
+                                lev = m;
+                                pp = q;
+                                w0 = wn;
+                                nbj = bj_n;
+                                nbk = bi_n * bj_n;
+                                Hm = h;
+                                Wm = w;
+                                xoff = xo;
+                                goff = go;
+                            }
+                            wn += nw;
+                        }
+                        xo += 2 * bi_n + 2 * R;
+                        go += 2 * bi_n;
+                    }
+                }
+                if (lev != 0) {
+                    f2x accd[KK];
+#pragma unroll
+                    for (int q = 0; q < KK; ++q) accd[q] = 0ull;
+                    const int r = 32 * (warp - w0) + (tid & 31);
+                    const int bi = r / nbj, bj = r - bi * nbj;
+                    if (r < nbk && 2 * bi < Hm && 4 * bj < Wm) {
+                        f2x g[2][4];
+#pragma unroll
+                        for (int o = 0; o < 2; ++o) {
+                            const float* gr = gb + pp * kGTile + (goff + 2 * bi + o) * kGRow;
+                            const float4 t0 = *reinterpret_cast<const float4*>(gr + 4 * bj);
+                            const float4 t1 = *reinterpret_cast<const float4*>(gr + 4 * (kGHalf + bj));
+                            g[o][0] = pk2(t0.x, t0.y);
+                            g[o][1] = pk2(t0.z, t0.w);
+                            g[o][2] = pk2(t1.x, t1.y);
+                            g[o][3] = pk2(t1.z, t1.w);
+                        }
+                        corr_pair<K, 2>(xb + pp * PTILE + (xoff + 2 * bi) * PROW, bj, g, accd);
+                    }
+                    warp_totals_to<KK, 2 * KK>(accd, 0.f, red + warp * 128);
+                }
+                __syncthreads();
+                // fixed-order sum of each unit's warps into acc_sm
+                {
+                    int wn = 0;
+                    for (int m = l; m <= hi; ++m) {
+                        const int bi_n = ((a.Hp >> m) + 1) >> 1, bj_n = ((a.Wp >> m) + 3) >> 2;
+                        const int nw = (bi_n * bj_n + 31) >> 5;
+                        for (int e = tid; e < 4 * KK; e += kDT) {
+                            const int p2 = e / (2 * KK), k = e - p2 * 2 * KK;
+                            float sacc = 0.f;
+                            for (int w = 0; w < nw; ++w) sacc += red[(wn + p2 * nw + w) * 128 + k];
+                            acc_sm[KK + 1 + (m - 1) * 4 * KK + (2 * p2 + (k & 1)) * KK + (k >> 1)] += sacc;
+                        }
+                        wn += 2 * nw;
+                    }
+                }
+                __syncthreads();
+                l = hi;
+                continue;
+            }
             const int pp = tid >> 7, bi = (tid >> 3) & 15, bj = tid & 7;
             f2x accd[KK];
 #pragma unroll
