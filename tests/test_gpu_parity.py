@@ -109,7 +109,18 @@ LAYOUT = [  # the forward's shared-memory layouts (band-pair buffers, where X^(2
 ]
 
 
-@pytest.mark.parametrize("n,c,h,w,k,L,dtype", EDGE + F16 + ODD + LARGE + LAYOUT)
+GROUP = [  # small deep levels sharing one stage/filter round (stacked in the tiles)
+    (1, 2, 256, 256, 5, 8, "f32"),    # forward levels 8..5 in one round; dW 4-5 and 6-8
+    (2, 3, 56, 56, 5, 3, "bf16"),     # stage-1 plane: dW levels 2 and 3 together
+    (1, 2, 64, 512, 5, 5, "bf16"),    # wide plane: only the last two levels fit a tile
+    (1, 1, 2048, 64, 3, 6, "f16"),    # tall plane
+    (1, 2, 128, 128, 7, 5, "bf16"),   # k = 7: larger halos, fewer levels per round
+    (1, 2, 128, 128, 1, 6, "f32"),    # k = 1: no halo
+    (2, 3, 112, 80, 3, 6, "bf16"),    # padded plane (general kernels)
+]
+
+
+@pytest.mark.parametrize("n,c,h,w,k,L,dtype", EDGE + F16 + ODD + LARGE + LAYOUT + GROUP)
 def test_edge_shapes(n, c, h, w, k, L, dtype):
     wl = shape_workload(n, c, h, w, k, L, dtype, seed=1000 + h + w + k + L)
     errs, _ = run_and_compare(wl, bias_and_scale=True)
