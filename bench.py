@@ -204,9 +204,32 @@ def time_oracle_step(s: dict, levels: int) -> float:
     return time.perf_counter() - t0
 
 
-def cpu_baseline(wl, target_s: float = 10.0) -> dict:
+def host_cpu() -> dict:
+    """The host's CPU model and logical core count (Linux /proc/cpuinfo)."""
+    import platform
+    model = None
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                key, val = key.strip(), val.strip()
+                if key == "model name" and model is None:
+                    model = val
+                elif key in ("CPU implementer", "CPU part") and key not in fields:
+                    fields[key] = val
+    except OSError:
+        pass
+    if model is None:
+        model = platform.machine() + "".join(f", {k} {v}" for k, v in fields.items())
+    return {"cpu_model": model, "os_cpu_count": os.cpu_count()}
+
+
+def cpu_baseline(wl, target_s: float = 10.0, single_s: float = 3.0) -> dict:
     """The oracle, as it stands, on a bounded sample of the workload: up to 8 images of
-    all channels, passes repeated until about `target_s` seconds of CPU work."""
+    all channels on all host cores, passes repeated until about `target_s` seconds of CPU
+    work; then one image of up to 64 channels on one thread for about `single_s` seconds
+    (the plain-loop figure)."""
     import oracle
     oracle.build()
     cores = oracle.num_threads()
@@ -217,11 +240,27 @@ def cpu_baseline(wl, target_s: float = 10.0) -> dict:
     while total < target_s and passes < 50:
         total += time_oracle_step(s, wl.levels)
         passes += 1
+    chans = max(1, min(wl.c, 64))
+    s1 = oracle_sample(wl, 1, chans)
+    elems1 = s1["x"].numel()
+    total1, passes1 = 0.0, 0
+    oracle.set_num_threads(1)
+    try:
+        while total1 < single_s and passes1 < 50:
+            total1 += time_oracle_step(s1, wl.levels)
+            passes1 += 1
+    finally:
+        oracle.set_num_threads(cores)
     return {"value": elems * passes / total / 1e9, "unit": "Gelem/s", "cores": cores,
             "kind": "oracle",
             "sample": f"{images} of {wl.n} images x all {wl.c} channels ({elems} elements), "
                       f"{passes} fwd+bwd passes in {total:.1f} s, float64 plain loops, "
-                      "OpenMP over planes (fwd) and channels (bwd)"}
+                      "OpenMP over planes (fwd) and channels (bwd)",
+            "single_thread": {
+                "value": elems1 * passes1 / total1 / 1e9, "unit": "Gelem/s", "cores": 1,
+                "sample": f"1 of {wl.n} images x {chans} of {wl.c} channels ({elems1} "
+                          f"elements), {passes1} fwd+bwd passes in {total1:.1f} s"},
+            "host": host_cpu()}
 
 
 def run_reference(args, wl):

@@ -72,6 +72,8 @@ def _lib():
             lib.wo_haar_synthesis.argtypes = [ctypes.c_int, ctypes.c_int, dp, dp]
             lib.wo_dwconv.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, dp, dp, dp]
             lib.wo_num_threads.restype = ctypes.c_int
+            lib.wo_set_num_threads.argtypes = [ctypes.c_int]
+            lib.wo_set_num_threads.restype = None
             _LIB = lib
     return _LIB
 
@@ -93,6 +95,11 @@ def _ptr(a):
 def num_threads() -> int:
     """OpenMP threads the oracle uses (OMP_NUM_THREADS, else all cores)."""
     return int(_lib().wo_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """OpenMP threads for the following calls (the timed CPU baseline's single-thread leg)."""
+    _lib().wo_set_num_threads(int(n))
 
 
 def _desc(x, k, levels):

@@ -523,3 +523,12 @@ int wo_num_threads(void) {
     return 1;
 #endif
 }
+
+/* Threads for the following calls (n >= 1); only the timed CPU baseline changes it. */
+void wo_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

@@ -67,3 +67,17 @@ def test_single_rank_is_identity():
 def test_fp32_peak_from_unit_counts():
     import bench
     assert bench.fp32_peak_tflops(2070.0) == pytest.approx(152 * 128 * 2 * 2.07e9 / 1e12)
+
+
+def test_cpu_baseline_legs():
+    """The bench's oracle baseline: an all-cores leg and a one-thread leg on bounded
+    samples, the host's CPU described, and the oracle's thread count restored after."""
+    import bench
+    import oracle
+    from depthwise_receptive_field_gb300.inputs import WORKLOADS
+    before = oracle.num_threads()
+    r = bench.cpu_baseline(WORKLOADS["c2_fp32_train"], target_s=0.05, single_s=0.05)
+    assert r["kind"] == "oracle" and r["cores"] == before and r["value"] > 0
+    assert r["single_thread"]["cores"] == 1 and r["single_thread"]["value"] > 0
+    assert r["host"]["os_cpu_count"] == os.cpu_count() and r["host"]["cpu_model"]
+    assert oracle.num_threads() == before
