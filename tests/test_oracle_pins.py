@@ -350,6 +350,33 @@ def test_finite_differences(oracle_lib, L):
             assert abs(fd - g[gname][idx]) <= 1e-6 * max(1.0, abs(fd)), (key, idx, fd, g[gname][idx])
 
 
+@pytest.mark.parametrize("shape", [(2, 3, 20, 28, 5, 3), (1, 2, 32, 32, 7, 4),
+                                   (1, 2, 24, 40, 1, 2)])
+def test_gradients_along_whole_tensor_directions(oracle_lib, shape):
+    """Algorithm 1 is affine in each of X, W^(0), b, s^(0), W^(l), s^(l) with the others
+    held (every stage is a convolution, a Haar step, a scale or a sum), so for a random
+    direction D of one of them <dY, F(P + D) - F(P)> equals <dP, D> up to rounding, at
+    sizes and odd carrier sides that finite differences element by element do not reach."""
+    n, c, h, w, k, L = shape
+    p = _params(n, c, h, w, k, L, seed=90 + k)
+    base = {key: p[key].double().numpy().copy() for key in ("x", "w0", "b0", "s0", "wl", "sl")}
+    dy = p["dy"].double().numpy()
+    g = oracle.backward(base["x"], dy, base["w0"], base["b0"], base["s0"], base["wl"],
+                        base["sl"], L)
+    names = {"x": "dx", "w0": "dw0", "b0": "db0", "s0": "ds0", "wl": "dwl", "sl": "dsl"}
+    y0 = oracle.forward(base["x"], base["w0"], base["b0"], base["s0"], base["wl"], base["sl"], L)
+    rng = np.random.default_rng(k)
+    for key, gname in names.items():
+        d = rng.standard_normal(base[key].shape)
+        q = dict(base)
+        q[key] = base[key] + d
+        y1 = oracle.forward(q["x"], q["w0"], q["b0"], q["s0"], q["wl"], q["sl"], L)
+        lhs = float(((y1 - y0) * dy).sum())
+        rhs = float((g[gname] * d).sum())
+        scale = float((np.abs(y1 - y0) * np.abs(dy)).sum())
+        assert abs(lhs - rhs) <= 1e-12 * scale, (key, lhs, rhs)
+
+
 def _operator_matrix(fn, size):
     cols = []
     for e in range(size):
