@@ -7,7 +7,7 @@ import torch
 from depthwise_receptive_field_gb300 import binding as B
 from depthwise_receptive_field_gb300 import layer
 from depthwise_receptive_field_gb300.inputs import WORKLOADS, make_inputs, shape_workload
-from parity_util import assert_within, gpu_run, run_and_compare
+from parity_util import assert_within, gpu_run, run_and_compare, run_and_compare_full
 
 pytestmark = pytest.mark.gpu
 
@@ -45,17 +45,19 @@ def test_c3_stage1_bf16_full():
 
 
 @pytest.mark.parametrize("levels", [0, 1, 2, 3, 4])
-def test_c4_level_sweep_sampled(levels):
-    """Full 32x128x128x128 bf16 shape, checked on three channels (all batch entries)."""
+def test_c4_level_sweep_full(levels):
+    """The 32x128x128x128 bf16 level sweep (L = 0 is the plain depthwise conv), every
+    output element and every parameter gradient against the oracle."""
     wl = WORKLOADS["c4_sweep_bf16"].with_levels(levels)
-    errs, _ = run_and_compare(wl, sample_channels=[0, 77, 127])
+    errs, _ = run_and_compare_full(wl, chunk=32)
     assert_within(errs, wl.dtype, wl.name)
 
 
-def test_c5_large_sampled():
-    """Full 16x256x256x256 bf16 L=5 shape (the benchmarked one), three channels checked."""
+def test_c5_large_full():
+    """The 16x256x256x256 bf16 L = 5 workload (the benchmarked one), every output element
+    and every parameter gradient against the oracle."""
     wl = WORKLOADS["c5_large_bf16"]
-    errs, _ = run_and_compare(wl, sample_channels=[0, 131, 255])
+    errs, _ = run_and_compare_full(wl, chunk=32)
     assert_within(errs, wl.dtype, wl.name)
 
 
@@ -127,10 +129,10 @@ def test_edge_shapes(n, c, h, w, k, L, dtype):
     assert_within(errs, wl.dtype, wl.name)
 
 
-def test_c3_stage1_f16_sampled():
-    """The stage-1 shape with fp16 I/O, four channels checked (all batch entries)."""
+def test_c3_stage1_f16_full():
+    """The stage-1 shape with fp16 I/O, every element against the oracle."""
     wl = WORKLOADS["c3_stage1_bf16"].with_dtype("f16")
-    errs, _ = run_and_compare(wl, sample_channels=[0, 31, 64, 95])
+    errs, _ = run_and_compare_full(wl, chunk=48)
     assert_within(errs, wl.dtype, wl.name)
 
 
