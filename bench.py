@@ -27,9 +27,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "WTConv fwd+bwd Gelem/s and achieved HBM GB/s as % of GB300 peak (1 GPU)"
-NUM_SMS = 152
-FP32_LANES_PER_SM = 128
-SM_MAX_MHZ = 2070.0
+FP32_LANES_PER_SM = 128  # FP32 multiply-add lanes per SM (Blackwell: 4 partitions x 32)
 NOMINAL_HBM_GBS = 7900.0
 HBM_FALLBACK_GBS = 6800.0
 PROFILES = os.path.join(ROOT, "profiles")
@@ -50,9 +48,52 @@ def measured_peaks() -> dict:
         return {"hbm_gbs": HBM_FALLBACK_GBS, "source": "fallback"}
 
 
-def fp32_peak_tflops(mhz: float = SM_MAX_MHZ) -> float:
-    """FP32 FMA peak from unit counts: 152 SMs x 128 FP32 lanes x 2 FLOP x SM clock."""
-    return NUM_SMS * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+def sm_max_mhz(gpu_index: int):
+    """The GPU's maximum SM clock as nvidia-smi reports it (None if unavailable)."""
+    try:
+        out = subprocess.run(["nvidia-smi", f"--id={gpu_index}", "--query-gpu=clocks.max.sm",
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                             timeout=20).stdout.strip()
+        return float(out.splitlines()[0])
+    except Exception:
+        return None
+
+
+def derived_fp32_peak_tflops(num_sms: int, mhz: float) -> float:
+    """FP32 multiply-add peak from unit counts: SMs x 128 lanes x 2 FLOP x SM clock."""
+    return num_sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+
+
+def measure_fp32_peak(dev, repeats: int = 3) -> dict:
+    """Measured FP32 multiply-add throughput: the library's probe kernel (packed f32x2
+    multiply-adds on 8 independent chains per thread, 8 CTAs of 256 threads per SM), timed
+    with CUDA events on its stream; best of `repeats` runs of ~2 ms each. The scalar form is
+    measured beside it."""
+    import torch
+
+    from depthwise_receptive_field_gb300 import binding as B
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks, iters = sms * 8, 20000
+    out = torch.empty(blocks * 256, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for packed in (1, 0):
+        best = None
+        for _ in range(1 + repeats):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            B.wtconv_fma_probe(blocks, iters, packed, out, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)  # first run is a warm-up too
+        fmas = blocks * 256 * iters * 8 * (2 if packed else 1)
+        res["packed" if packed else "scalar"] = 2 * fmas / (best * 1e-3) / 1e12
+    mhz = sm_max_mhz(dev.index or 0)
+    return {"tflops": res["packed"], "scalar_tflops": res["scalar"], "num_sms": sms,
+            "sm_max_mhz": mhz,
+            "derived_tflops": derived_fp32_peak_tflops(sms, mhz) if mhz else None}
 
 
 def source_sha256() -> str:
@@ -191,7 +232,8 @@ def oracle_sample(wl, images: int, channels: int):
     from depthwise_receptive_field_gb300.inputs import make_inputs
     inp = make_inputs(wl, n=images)
     sl = slice(0, channels)
-    return {"x": inp["x"][:, sl], "dy": inp["dy"][:, sl], "w0": inp["w0"][sl],
+    dy = inp["dy"][:, sl] if inp["dy"] is not None else None
+    return {"x": inp["x"][:, sl], "dy": dy, "w0": inp["w0"][sl],
             "b0": inp["b0"][sl], "s0": inp["s0"][sl], "wl": inp["wl"][:, sl],
             "sl": inp["sl"][:, sl]}
 
@@ -200,7 +242,8 @@ def time_oracle_step(s: dict, levels: int) -> float:
     import oracle
     t0 = time.perf_counter()
     oracle.forward(s["x"], s["w0"], s["b0"], s["s0"], s["wl"], s["sl"], levels)
-    oracle.backward(s["x"], s["dy"], s["w0"], s["b0"], s["s0"], s["wl"], s["sl"], levels)
+    if s["dy"] is not None:
+        oracle.backward(s["x"], s["dy"], s["w0"], s["b0"], s["s0"], s["wl"], s["sl"], levels)
     return time.perf_counter() - t0
 
 
@@ -225,7 +268,7 @@ def host_cpu() -> dict:
     return {"cpu_model": model, "os_cpu_count": os.cpu_count()}
 
 
-def cpu_baseline(wl, target_s: float = 10.0, single_s: float = 3.0) -> dict:
+def cpu_baseline(wl, target_s: float = 10.0, single_s: float = 3.0, brief: bool = False) -> dict:
     """The oracle, as it stands, on a bounded sample of the workload: up to 8 images of
     all channels on all host cores, passes repeated until about `target_s` seconds of CPU
     work; then one image of up to 64 channels on one thread for about `single_s` seconds
@@ -251,6 +294,12 @@ def cpu_baseline(wl, target_s: float = 10.0, single_s: float = 3.0) -> dict:
             passes1 += 1
     finally:
         oracle.set_num_threads(cores)
+    if brief:
+        return {"all_cores_gelem_s": elems * passes / total / 1e9, "cores": cores,
+                "one_thread_gelem_s": elems1 * passes1 / total1 / 1e9,
+                "sample": f"{images} images x {wl.c} channels on {cores} threads "
+                          f"({passes} passes); 1 image x {chans} channels on 1 thread "
+                          f"({passes1} passes)"}
     return {"value": elems * passes / total / 1e9, "unit": "Gelem/s", "cores": cores,
             "kind": "oracle",
             "sample": f"{images} of {wl.n} images x all {wl.c} channels ({elems} elements), "
@@ -300,12 +349,174 @@ def run_reference(args, wl):
 # the CUDA path
 # ----------------------------------------------------------------------------------
 
+class Case:
+    """One workload's inputs, parameters, outputs and workspace on the device, and its
+    training step (fold -> forward -> backward-data -> backward-weight) through the C ABI;
+    forward-only workloads stop after the forward."""
+
+    def __init__(self, wl, dev):
+        import torch
+
+        from depthwise_receptive_field_gb300 import binding as B
+        from depthwise_receptive_field_gb300 import layer
+        from depthwise_receptive_field_gb300.inputs import make_inputs
+
+        self.wl = wl
+        self.inp = make_inputs(wl)
+        self.p = layer.Params.from_inputs(self.inp, dev)
+        self.x = self.inp["x"].to(dev)
+        self.dy = self.inp["dy"].to(dev) if wl.backward else None
+        self.desc = B.desc_like(self.x, self.p.k, wl.levels)
+        self.ws = layer.Workspace(dev)
+        _, nbd, nbw = B.wtconv_workspace_size(self.desc)
+        self.buf, self.bufn = self.ws.get(max(nbd, nbw))
+        self.f = layer.fold(self.p, self.desc)
+        self.y = torch.empty_like(self.x)
+        p = self.p
+        self.g = {"dx": torch.empty_like(self.x), "dw0": torch.empty_like(p.w0),
+                  "db0": torch.empty_like(p.s0), "ds0": torch.empty_like(p.s0),
+                  "dwl": torch.empty_like(p.wl), "dsl": torch.empty_like(p.sl)}
+        self.launches = 0
+
+    def step(self, stream, ev=None):
+        from depthwise_receptive_field_gb300 import binding as B
+
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+
+        p, f, g, d = self.p, self.f, self.g, self.desc
+        lv = self.wl.levels > 0
+        mark(0)
+        B.wtconv_fold_scales(d, p.w0, p.b0, p.s0, p.wl if lv else None, p.sl if lv else None,
+                             f.w0f, f.b0f, f.wlf if lv else None, stream)
+        self.launches += B.wtconv_last_launch_count()
+        mark(1)
+        B.wtconv_forward(d, self.x, f.w0f, f.b0f, f.wlf if lv else None, self.y, self.buf,
+                         self.bufn, stream)
+        self.launches += B.wtconv_last_launch_count()
+        mark(2)
+        if self.wl.backward:
+            B.wtconv_backward_data(d, self.dy, f.w0f, f.wlf if lv else None, g["dx"], self.buf,
+                                   self.bufn, stream)
+            self.launches += B.wtconv_last_launch_count()
+        mark(3)
+        if self.wl.backward:
+            B.wtconv_backward_weight(d, self.x, self.dy, p.w0, p.b0, p.s0,
+                                     p.wl if lv else None, p.sl if lv else None, g["dw0"],
+                                     g["db0"], g["ds0"], g["dwl"] if lv else None,
+                                     g["dsl"] if lv else None, self.buf, self.bufn, stream)
+            self.launches += B.wtconv_last_launch_count()
+        mark(4)
+
+
+def segments(evs) -> dict:
+    """Mean per-pass milliseconds from the per-step event quintuples."""
+    seg = {"fold": 0.0, "forward": 0.0, "backward_data": 0.0, "backward_weight": 0.0}
+    for ev in evs:
+        seg["fold"] += ev[0].elapsed_time(ev[1])
+        seg["forward"] += ev[1].elapsed_time(ev[2])
+        seg["backward_data"] += ev[2].elapsed_time(ev[3])
+        seg["backward_weight"] += ev[3].elapsed_time(ev[4])
+    return {k: v / len(evs) for k, v in seg.items()}
+
+
+def roofs(wl, seg_ms: dict, step_ms: float, peak_tf: float, hbm_gbs: float) -> dict:
+    """FP32-ALU fraction of the dominant plane kernel and HBM fraction of the step's ideal
+    bytes, from per-pass times."""
+    from depthwise_receptive_field_gb300 import iomodel
+    alg = iomodel.algorithmic(wl.k, wl.levels, 4 if wl.dtype == "f32" else 2)
+    if wl.backward:
+        fwd_ms = (seg_ms["forward"] + seg_ms["backward_data"]) / 2
+        dw_ms = seg_ms["backward_weight"]
+        if 2 * fwd_ms >= dw_ms:
+            dom, dom_ms, dom_alg = "wt_fwd_plane_kernel", fwd_ms, alg["forward"]
+        else:
+            dom, dom_ms, dom_alg = "wt_dw_plane_kernel", dw_ms, alg["backward_weight"]
+        step_bytes = wl.elements * sum(a["bytes"] for a in alg.values())
+    else:
+        dom, dom_ms, dom_alg = "wt_fwd_plane_kernel", seg_ms["forward"], alg["forward"]
+        step_bytes = wl.elements * alg["forward"]["bytes"]
+    tflops = wl.elements * dom_alg["flops"] / (dom_ms * 1e-3) / 1e12
+    gbs = step_bytes / (step_ms * 1e-3) / 1e9
+    return {"kernel": dom, "kernel_ms": dom_ms, "achieved_tflops": tflops,
+            "alu_frac": tflops / peak_tf, "flops_per_element": dom_alg["flops"],
+            "step_bytes": step_bytes, "hbm_gbs": gbs, "hbm_frac": gbs / hbm_gbs}
+
+
+def run_per_config(args, dev, stream, peak_tf: float, hbm_gbs: float, with_oracle: bool):
+    """Every other synthetic workload (the small forward-only case, the fp32 and stage-1
+    training cases, the 128x128 level sweep at L = 0..4), timed as the pages' layer
+    benchmark does (20 warm-up and 50 timed steps, WTConv-IO §5.1) with L2 flushed before
+    every timed step (these inputs are near or below the L2 size), each with the oracle
+    timed on a bounded sample on all host cores and on one thread."""
+    import torch
+
+    from depthwise_receptive_field_gb300.inputs import WORKLOADS
+    wls = [WORKLOADS["c1_small_fwd"], WORKLOADS["c2_fp32_train"], WORKLOADS["c3_stage1_bf16"]]
+    wls += [WORKLOADS["c4_sweep_bf16"].with_levels(L) for L in range(5)]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = []
+    for wl in wls:
+        case = Case(wl, dev)
+        for _ in range(20):
+            case.step(stream)
+        torch.cuda.synchronize()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(50)]
+        for ev in evs:
+            flush.fill_(1)
+            case.step(stream, ev)
+        torch.cuda.synchronize()
+        seg = segments(evs)
+        step_ms = sum(seg.values())
+        passes = 3 if wl.backward else 1
+        entry = {"workload": workload_config(wl)["workload"],
+                 "gelem_s": wl.elements / (step_ms * 1e-3) / 1e9,
+                 "ms_per_step": step_ms, "segments_ms": seg,
+                 "passes": "fold + forward + backward_data + backward_weight" if passes == 3
+                 else "fold + forward", "steps": 50, "warmup": 20,
+                 "l2": "flushed (256 MB write) before every timed step"}
+        entry.update(roofs(wl, seg, step_ms, peak_tf, hbm_gbs))
+        if with_oracle:
+            entry["oracle"] = cpu_baseline(wl, target_s=1.5, single_s=0.7, brief=True)
+        out.append(entry)
+        del case
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_noalloc(case, stream, steps: int = 5) -> dict:
+    """The backward-weight entry point without a workspace on the same workload (its
+    fixed 4 MiB scratch bounds its grid on large planes), timed beside the workspace path."""
+    import torch
+
+    from depthwise_receptive_field_gb300 import binding as B
+    p, g, lv = case.p, case.g, case.wl.levels > 0
+
+    def call():
+        B.wtconv_backward_weight_noalloc(case.desc, case.x, case.dy, p.w0, p.b0, p.s0,
+                                         p.wl if lv else None, p.sl if lv else None, g["dw0"],
+                                         g["db0"], g["ds0"], g["dwl"] if lv else None,
+                                         g["dsl"] if lv else None, stream)
+    try:
+        call()
+    except Exception as e:  # e.g. a shape beyond the 4 MiB scratch
+        return {"unavailable": str(e)}
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return {"ms": e0.elapsed_time(e1) / steps, "steps": steps}
+
+
 def run_ours(args, wl):
     import torch
 
     from depthwise_receptive_field_gb300 import binding as B
-    from depthwise_receptive_field_gb300 import iomodel, layer
-    from depthwise_receptive_field_gb300.inputs import make_inputs
 
     world, rank, local = dist_env()
     if not torch.cuda.is_available():
@@ -316,50 +527,14 @@ def run_ours(args, wl):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     B.load_library()
-
-    inp = make_inputs(wl)
-    p = layer.Params.from_inputs(inp, dev)
-    x = inp["x"].to(dev)
-    dy = inp["dy"].to(dev)
-    desc = B.desc_like(x, p.k, wl.levels)
-    ws = layer.Workspace(dev)
-    _, nbd, nbw = B.wtconv_workspace_size(desc)
-    buf, bufn = ws.get(max(nbd, nbw))
-    f = layer.fold(p, desc)
-    y = torch.empty_like(x)
-    g = {"dx": torch.empty_like(dy), "dw0": torch.empty_like(p.w0),
-         "db0": torch.empty_like(p.s0), "ds0": torch.empty_like(p.s0),
-         "dwl": torch.empty_like(p.wl), "dsl": torch.empty_like(p.sl)}
     stream = torch.cuda.current_stream(dev)
-    lv = wl.levels > 0
+    fp32 = measure_fp32_peak(dev)
+    peak_tf = fp32["tflops"]
+    peaks = measured_peaks()
 
-    launches = {"n": 0}
-
-    def step(ev=None):
-        def mark(i):
-            if ev is not None:
-                ev[i].record(stream)
-        mark(0)
-        B.wtconv_fold_scales(desc, p.w0, p.b0, p.s0, p.wl if lv else None,
-                             p.sl if lv else None, f.w0f, f.b0f, f.wlf if lv else None, stream)
-        launches["n"] += B.wtconv_last_launch_count()
-        mark(1)
-        B.wtconv_forward(desc, x, f.w0f, f.b0f, f.wlf if lv else None, y, buf, bufn, stream)
-        launches["n"] += B.wtconv_last_launch_count()
-        mark(2)
-        B.wtconv_backward_data(desc, dy, f.w0f, f.wlf if lv else None, g["dx"], buf, bufn,
-                               stream)
-        launches["n"] += B.wtconv_last_launch_count()
-        mark(3)
-        B.wtconv_backward_weight(desc, x, dy, p.w0, p.b0, p.s0, p.wl if lv else None,
-                                 p.sl if lv else None, g["dw0"], g["db0"], g["ds0"],
-                                 g["dwl"] if lv else None, g["dsl"] if lv else None, buf,
-                                 bufn, stream)
-        launches["n"] += B.wtconv_last_launch_count()
-        mark(4)
-
+    case = Case(wl, dev)
     for _ in range(max(3, args.warmup)):
-        step()
+        case.step(stream)
     torch.cuda.synchronize()
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
@@ -368,43 +543,24 @@ def run_ours(args, wl):
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
-    launches["n"] = 0
+    case.launches = 0
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
-        step(evs[i])
+        case.step(stream, evs[i])
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
     total_ms = max_over_ranks(total_ms, world, dev)
-
-    seg = {"fold": 0.0, "forward": 0.0, "backward_data": 0.0, "backward_weight": 0.0}
-    for ev in evs:
-        seg["fold"] += ev[0].elapsed_time(ev[1])
-        seg["forward"] += ev[1].elapsed_time(ev[2])
-        seg["backward_data"] += ev[2].elapsed_time(ev[3])
-        seg["backward_weight"] += ev[3].elapsed_time(ev[4])
-    seg_ms = {k: v / args.steps for k, v in seg.items()}
+    seg_ms = segments(evs)
 
     elems = wl.elements
     value = world * elems * args.steps / (total_ms * 1e-3) / 1e9
-    peaks = measured_peaks()
-    alg = iomodel.algorithmic(wl.k, wl.levels, 4 if wl.dtype == "f32" else 2)
-    # dominant kernel: the plane kernel shared by forward and backward-data, or dW
-    fwd_kernel_ms = (seg_ms["forward"] + seg_ms["backward_data"]) / 2
-    dw_ms = seg_ms["backward_weight"]
-    if 2 * fwd_kernel_ms >= dw_ms:
-        dom, dom_ms, dom_alg = "wt_fwd_plane_kernel", fwd_kernel_ms, alg["forward"]
-    else:
-        dom, dom_ms, dom_alg = "wt_dw_plane_kernel", dw_ms, alg["backward_weight"]
-    tflops = elems * dom_alg["flops"] / (dom_ms * 1e-3) / 1e12
-    peak_tf = fp32_peak_tflops()
-    traffic = committed_traffic(dom, wl.name)
-    step_bytes = elems * sum(a["bytes"] for a in alg.values())
-    hbm_gbs = step_bytes * args.steps / (total_ms * 1e-3) / 1e9
+    rf = roofs(wl, seg_ms, total_ms / args.steps, peak_tf, peaks["hbm_gbs"])
+    traffic = committed_traffic(rf["kernel"], wl.name)
 
     result = {
         "metric": METRIC, "value": value, "unit": "Gelem/s", "n_gpus": world,
@@ -413,29 +569,48 @@ def run_ours(args, wl):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": workload_config(wl),
         "roofline": {
-            "bound": "alu", "kernel": dom, "achieved": tflops, "peak": peak_tf,
-            "unit": "TFLOP/s", "frac": tflops / peak_tf, "traffic": traffic,
-            "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x 2070 MHz",
-            "algorithmic_flops_per_element": dom_alg["flops"],
+            "bound": "alu", "kernel": rf["kernel"], "achieved": rf["achieved_tflops"],
+            "peak": peak_tf, "unit": "TFLOP/s", "frac": rf["achieved_tflops"] / peak_tf,
+            "traffic": traffic,
+            "peak_source": "measured: FP32 multiply-add probe (packed f32x2, "
+                           f"{fp32['num_sms']} SMs x 8 CTAs x 256 threads, best of 3)",
+            "derived_peak": fp32["derived_tflops"],
+            "derived_peak_source": f"{fp32['num_sms']} SMs (queried) x {FP32_LANES_PER_SM} "
+                                   f"FP32 lanes x 2 FLOP x {fp32['sm_max_mhz']} MHz "
+                                   "(nvidia-smi clocks.max.sm)",
+            "scalar_fma_tflops": fp32["scalar_tflops"],
+            "algorithmic_flops_per_element": rf["flops_per_element"],
+            "kernel_ms": rf["kernel_ms"],
         },
         "hbm": {
-            "achieved_gbs": hbm_gbs, "peak_gbs": peaks["hbm_gbs"],
-            "frac": hbm_gbs / peaks["hbm_gbs"], "peak_source": peaks["source"],
-            "nominal_gbs": NOMINAL_HBM_GBS, "frac_of_nominal": hbm_gbs / NOMINAL_HBM_GBS,
+            "achieved_gbs": rf["hbm_gbs"], "peak_gbs": peaks["hbm_gbs"],
+            "frac": rf["hbm_frac"], "peak_source": peaks["source"],
+            "nominal_gbs": NOMINAL_HBM_GBS, "frac_of_nominal": rf["hbm_gbs"] / NOMINAL_HBM_GBS,
             "nominal_source": "nominal HBM3e bandwidth of one GB300 GPU (7.9 TB/s)",
-            "algorithmic_bytes_per_step": step_bytes,
+            "algorithmic_bytes_per_step": rf["step_bytes"],
         },
         "segments_ms": seg_ms,
         "clocks": clk,
-        "gpu_launches": launches["n"],
+        "gpu_launches": case.launches,
     }
 
     if wl.levels > 0 and not args.no_depthwise:
-        result["depthwise_context"] = run_depthwise_context(args, wl, p, x, dy, g, stream, dev)
+        result["depthwise_context"] = run_depthwise_context(args, wl, case.p, case.x, case.dy,
+                                                            case.g, stream, dev, peak_tf)
     if not args.no_e2e:
-        result["e2e"] = run_e2e(args, wl, inp, p, f, desc, buf, bufn, stream, world, dev)
+        result["e2e"] = run_e2e(args, wl, case.inp, case.p, case.f, case.desc, case.buf,
+                                case.bufn, stream, world, dev)
+    if not args.no_noalloc:
+        result["noalloc_backward_weight"] = dict(
+            run_noalloc(case, stream), workspace_path_ms=seg_ms["backward_weight"])
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl)
+    if not args.no_per_config:
+        del case
+        torch.cuda.empty_cache()
+        result["per_config"] = run_per_config(args, dev, stream, peak_tf, peaks["hbm_gbs"],
+                                              with_oracle=(rank == 0 and world == 1
+                                                           and not args.no_cpu_baseline))
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -444,7 +619,7 @@ def run_ours(args, wl):
     return 0
 
 
-def run_depthwise_context(args, wl, p, x, dy, g, stream, dev) -> dict:
+def run_depthwise_context(args, wl, p, x, dy, g, stream, dev, peak_tf) -> dict:
     """The same-shape plain depthwise k x k conv (this layer at L = 0: base conv + bias and
     scale, no wavelet levels), forward + backward-data + backward-weight through the same
     C ABI, timed like the main step. Context for what the wavelet levels cost on top."""
@@ -484,7 +659,8 @@ def run_depthwise_context(args, wl, p, x, dy, g, stream, dev) -> dict:
     flops = wl.elements * sum(a["flops"] for a in alg.values())
     return {"op": f"plain depthwise {wl.k}x{wl.k} conv, same shape (this library at L=0)",
             "value": wl.elements / (ms * 1e-3) / 1e9, "unit": "Gelem/s", "ms_per_step": ms,
-            "steps": steps, "alu_tflops": flops / (ms * 1e-3) / 1e12}
+            "steps": steps, "alu_tflops": flops / (ms * 1e-3) / 1e12,
+            "alu_frac": flops / (ms * 1e-3) / 1e12 / peak_tf}
 
 
 def run_ablation(args) -> int:
@@ -740,6 +916,10 @@ def main(argv=None):
                     help="with --ablation: one extra call per variant inside an NVTX range")
     ap.add_argument("--no-depthwise", action="store_true",
                     help="skip the same-shape plain depthwise conv context line")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other workloads' per-config figures")
+    ap.add_argument("--no-noalloc", action="store_true",
+                    help="skip timing the no-workspace backward-weight entry point")
     args = ap.parse_args(argv)
     if args.ablation:
         return run_ablation(args)

@@ -18,7 +18,7 @@ import threading
 
 from . import build as _build
 
-WT_OK, WT_ERR_INVALID_ARG, WT_ERR_UNSUPPORTED, WT_ERR_WORKSPACE, WT_ERR_CUDA = range(5)
+WT_OK, WT_ERR_INVALID_ARG, WT_ERR_UNSUPPORTED, WT_ERR_WORKSPACE, WT_ERR_CUDA, WT_ERR_TIMEOUT = range(6)
 WT_F32, WT_BF16, WT_F16 = 0, 1, 2
 (WT_VARIANT_REFERENCE, WT_VARIANT_FUSED_ANALYSIS, WT_VARIANT_COLLAPSED_SYNTHESIS,
  WT_VARIANT_FOLDED) = range(4)
@@ -27,7 +27,9 @@ VARIANT_NAMES = {WT_VARIANT_REFERENCE: "reference", WT_VARIANT_FUSED_ANALYSIS: "
                  WT_VARIANT_FOLDED: "folded"}
 
 HEADER = os.path.join(_build.INCLUDE, "wtconv.h")
-HEADERS = [HEADER, os.path.join(_build.INCLUDE, "wtconv_ablation.h")]
+HEADERS = [HEADER, os.path.join(_build.INCLUDE, "wtconv_ablation.h"),
+           os.path.join(_build.INCLUDE, "wtconv_probe.h"),
+           os.path.join(_build.INCLUDE, "wtconv_testing.h")]
 
 
 class wt_desc(ctypes.Structure):
@@ -62,6 +64,9 @@ _SIGNATURES = {
     "wtconv_backward_weight_noalloc": [_DESC_P] + [_vp] * 12 + [_vp],
     "wtconv_variant_workspace_size": [_DESC_P, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)],
     "wtconv_forward_variant": [_DESC_P, ctypes.c_int] + [_vp] * 8 + [ctypes.c_size_t, _vp],
+    "wtconv_fma_probe": [ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp],
+    "wtconv_workspace_status": [_vp, _vp, ctypes.POINTER(ctypes.c_int)],
+    "wtconv_testing_set_wait_limit_ns": [ctypes.c_ulonglong],
 }
 
 
@@ -204,6 +209,28 @@ def wtconv_forward_variant(desc, variant, x, w0, b0, s0, wl, sl, y, ws, ws_bytes
     _check(load_library().wtconv_forward_variant(
         ctypes.byref(desc), int(variant), _ptr(x), _ptr(w0), _ptr(b0), _ptr(s0), _ptr(wl),
         _ptr(sl), _ptr(y), _ptr(ws), int(ws_bytes), _stream(stream)), "wtconv_forward_variant")
+
+
+def wtconv_workspace_status(ws, stream=None) -> int:
+    """Bit flags of the calls whose kernels timed out on this workspace (0 = none); see
+    include/wtconv.h. Synchronizes the stream."""
+    flags = ctypes.c_int(0)
+    st = load_library().wtconv_workspace_status(_ptr(ws), _stream(stream), ctypes.byref(flags))
+    if st not in (WT_OK, WT_ERR_TIMEOUT):
+        _check(st, "wtconv_workspace_status")
+    return flags.value
+
+
+def wtconv_testing_set_wait_limit_ns(ns: int):
+    """Test hook (include/wtconv_testing.h): limit of the kernels' bounded waits; 0 = 1 s."""
+    _check(load_library().wtconv_testing_set_wait_limit_ns(int(ns)),
+           "wtconv_testing_set_wait_limit_ns")
+
+
+def wtconv_fma_probe(blocks: int, iters: int, packed: bool, out, stream=None):
+    """Launch the FP32 multiply-add throughput probe (include/wtconv_probe.h)."""
+    _check(load_library().wtconv_fma_probe(int(blocks), int(iters), 1 if packed else 0,
+                                           _ptr(out), _stream(stream)), "wtconv_fma_probe")
 
 
 def wtconv_status_string(status: int) -> str:

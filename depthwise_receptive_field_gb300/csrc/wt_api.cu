@@ -3,8 +3,12 @@
 // Reformulation") and dispatch to the forward / backward kernels.
 #include <stdint.h>
 
+#include <atomic>
+
 #include "wt_common.cuh"
 #include "wt_internal.h"
+#include "wt_tma.cuh"
+#include "wtconv_testing.h"
 
 namespace wt {
 
@@ -38,6 +42,15 @@ wt_status check_param(const void* p) {
 }  // namespace
 
 void set_last_launch_count(int launches) { g_last_launches = launches; }
+
+namespace {
+std::atomic<unsigned long long> g_wait_limit_ns{0};  // 0: the default
+}  // namespace
+
+unsigned long long wait_limit_ns() {
+    const unsigned long long v = g_wait_limit_ns.load(std::memory_order_relaxed);
+    return v == 0 ? kWaitLimitNs : v;
+}
 
 // §4.3 Eq. 8: one thread per folded weight (plus the bias fold).
 __global__ void wt_fold_kernel(int C, int KK, int L, const float* w0, const float* b0,
@@ -188,6 +201,25 @@ wt_status wtconv_backward(const wt_desc* desc, const void* x, const void* dy,
     return st;
 }
 
+wt_status wtconv_workspace_status(const void* ws, wt_stream_t stream, int* flags) {
+    if (flags) *flags = 0;
+    if (ws == nullptr) return WT_ERR_INVALID_ARG;
+    int words[6] = {0, 0, 0, 0, 0, 0};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(words, ws, sizeof(words), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return WT_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return WT_ERR_CUDA;
+    const int f = (words[kStatusForward] ? 1 : 0) | (words[kStatusBackwardData] ? 2 : 0) |
+                  (words[kStatusBackwardWeight] ? 4 : 0);
+    if (flags) *flags = f;
+    return f ? WT_ERR_TIMEOUT : WT_OK;
+}
+
+wt_status wtconv_testing_set_wait_limit_ns(unsigned long long ns) {
+    g_wait_limit_ns.store(ns, std::memory_order_relaxed);
+    return WT_OK;
+}
+
 const char* wtconv_status_string(wt_status status) {
     switch (status) {
         case WT_OK: return "WT_OK";
@@ -195,6 +227,7 @@ const char* wtconv_status_string(wt_status status) {
         case WT_ERR_UNSUPPORTED: return "WT_ERR_UNSUPPORTED: shape or kernel size not built";
         case WT_ERR_WORKSPACE: return "WT_ERR_WORKSPACE: workspace missing or too small";
         case WT_ERR_CUDA: return "WT_ERR_CUDA: a CUDA launch or runtime call failed";
+        case WT_ERR_TIMEOUT: return "WT_ERR_TIMEOUT: a kernel's bounded wait timed out";
         default: return "unknown wt_status";
     }
 }

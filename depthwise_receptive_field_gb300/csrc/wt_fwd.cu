@@ -44,8 +44,9 @@ struct FwdArgs {
     const float* b0f;
     const float* wimg;  // per channel, the shared-memory image of its folded weights
     float* zd;         // scratch: per CTA the deep sums, then the level-2 subbands
-    int* err;          // first word of the workspace: set on a stuck TMA wait
-    int* next;         // second word: the next plane to hand out (zeroed before the launch)
+    int* err;          // this call's status word in the workspace: set on a stuck TMA wait
+    int* next;         // the word after it: the next plane to hand out (zeroed before launch)
+    unsigned long long wait_ns;  // limit of every bounded wait
     long long zd_slot;  // floats of each of the two arrays of a CTA's slot
     long long slot;     // floats between consecutive CTAs' slots (2 * zd_slot + deep state)
     long long planes;
@@ -142,11 +143,11 @@ __device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, floa
             if (tid == 0 && t >= 1) {
                 const int nt = t - 1 + NB, nb = (t - 1) % NB;
                 if (nt < nbox && ok && *s_abort == 0) {
-                    ok = mbar_wait_bounded(bar_e + nb, (ph_e >> nb) & 1u);
+                    ok = mbar_wait_bounded(bar_e + nb, (ph_e >> nb) & 1u, a.wait_ns);
                     if (ok) {
                         const int ny = nt / bxn, nx = nt - ny * bxn;
                         fence_proxy_async_smem();
-                        mbar_arrive_expect_tx(bar_s + nb, SweepBox<T>::BYTES);
+                        mbar_expect_tx_noted(bar_s + nb, SweepBox<T>::BYTES);
                         tma_load_3d(buf + nb * (BW * BH), &a.tms, nx * BW, ny * BH, (int)plane,
                                     bar_s + nb);
                     } else {
@@ -156,7 +157,7 @@ __device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, floa
                 ph_e ^= 1u << nb;
             }
             if (ok && *s_abort == 0) {
-                ok = mbar_wait_bounded(bar_s + b, (ph_s >> b) & 1u);
+                ok = mbar_wait_bounded(bar_s + b, (ph_s >> b) & 1u, a.wait_ns);
                 if (!ok) *s_abort = 1;
             }
             ph_s ^= 1u << b;
@@ -414,7 +415,7 @@ __device__ __forceinline__ bool deep_levels(const FwdArgs& a, float* sm, float* 
     constexpr bool tma2 = STAGED && !DG;
     float* ubuf = sm + (tma2 ? a.o_u : 0);
     auto issue2 = [&](int ti0, int tj0) {
-        mbar_arrive_expect_tx(bar_u, 16u * FG<K>::BT * FG<K>::BT);
+        mbar_expect_tx_noted(bar_u, 16u * FG<K>::BT * FG<K>::BT);
         tma_load_3d(ubuf, &a.tmu, 4 * (tj0 - R), ti0 - R, (int)blockIdx.x, bar_u);
     };
     bool ok = true;
@@ -442,7 +443,7 @@ __device__ __forceinline__ bool deep_levels(const FwdArgs& a, float* sm, float* 
             for (int tj0 = 0; tj0 < Wl; tj0 += kCT) {
                 if (l == 2 && tma2) {
                     // a timed-out wait repacks stale data; the vote below ends the kernel
-                    ok = mbar_wait_bounded(bar_u, ph_u) && ok;
+                    ok = mbar_wait_bounded(bar_u, ph_u, a.wait_ns) && ok;
                     ph_u ^= 1;
                     repack_level2<K>(ubuf, bs);
                 } else {
@@ -579,6 +580,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
         mbar_init(bar_u, 1);
         fence_mbar_init();
     }
+    if (leader) mbar_track_init();
     volatile int* s_abort = reinterpret_cast<volatile int*>(sm + a.o_bar + 26);
     if (leader) *s_abort = 0;
     __syncthreads();
@@ -588,7 +590,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
     auto weights_ready = [&]() -> bool {
         bool ok = true;
         if (use_tma) {
-            ok = mbar_wait_bounded(bar_w, ph_w);
+            ok = mbar_wait_bounded(bar_w, ph_w, a.wait_ns);
             ph_w ^= 1;
         }
         return !__syncthreads_or(!ok);
@@ -612,9 +614,9 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
         if (leader) {
             if (use_tma) {  // this channel's weights and the first tile of this plane
                 fence_proxy_async_smem();
-                mbar_arrive_expect_tx(bar_w, (uint32_t)a.img * 4u);
+                mbar_expect_tx_noted(bar_w, (uint32_t)a.img * 4u);
                 bulk_load(wsm, wimg, (uint32_t)a.img * 4u, bar_w);
-                mbar_arrive_expect_tx(bar_x, XBox<K, T>::BYTES);
+                mbar_expect_tx_noted(bar_x, XBox<K, T>::BYTES);
                 tma_load_3d(sm + a.o_raw, &a.tmx, -XBox<K, T>::XOFF, -2 * R, (int)plane, bar_x);
             }
             if (use_tma && a.L >= 2) {  // first boxes of the level-2 sweep
@@ -623,7 +625,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                 T* buf = reinterpret_cast<T*>(sm + a.o_b);
                 for (int t = 0; t < SweepBox<T>::NBUF && t < nbox; ++t) {
                     const int ny = t / bxn, nx = t - ny * bxn;
-                    mbar_arrive_expect_tx(bar_s + t, SweepBox<T>::BYTES);
+                    mbar_expect_tx_noted(bar_s + t, SweepBox<T>::BYTES);
                     tma_load_3d(buf + t * (BW * BH), &a.tms, nx * BW, ny * BH, (int)plane,
                                 bar_s + t);
                 }
@@ -662,7 +664,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
         }
         if (a.L >= 2 && use_tma && leader) {  // deep sums of the first tile
             fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar_d, kDBytes);
+            mbar_expect_tx_noted(bar_d, kDBytes);
             tma_load_3d(dblk, &a.tmd, 0, 0, (int)blockIdx.x, bar_d);
         }
         // Tiles: raw X tiles and band-pair tiles are double-buffered, so one barrier per
@@ -682,7 +684,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
             bool ok_x = true;
             if (use_tma) {
                 // a timed-out wait converts stale data; the vote below ends the kernel
-                ok_x = mbar_wait_bounded(bar_x + rb, (ph_x >> rb) & 1u);
+                ok_x = mbar_wait_bounded(bar_x + rb, (ph_x >> rb) & 1u, a.wait_ns);
                 ph_x ^= 1u << rb;
             } else {
                 stage_raw<K, T>(xp, a.H, a.W, raw, y0, x0);
@@ -705,11 +707,11 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
             }
             if (use_tma && leader && t + 1 < ntiles) {  // tile t + 1: X and its deep sums
                 const int ny = (t + 1) / tiles_x, nx = (t + 1) - ny * tiles_x, nb = rb ^ 1;
-                mbar_arrive_expect_tx(bar_x + nb, XBox<K, T>::BYTES);
+                mbar_expect_tx_noted(bar_x + nb, XBox<K, T>::BYTES);
                 tma_load_3d(sm + a.o_raw + nb * a.raw_f, &a.tmx, nx * kTile - XBox<K, T>::XOFF,
                             ny * kTile - 2 * R, (int)plane, bar_x + nb);
                 if (a.L >= 2) {
-                    mbar_arrive_expect_tx(bar_d + nb, kDBytes);
+                    mbar_expect_tx_noted(bar_d + nb, kDBytes);
                     tma_load_3d(dblk + nb * (kDBytes / 4), &a.tmd, nx * kTile,
                                 (ny * kTile) >> 2, (int)blockIdx.x, bar_d + nb);
                 }
@@ -751,7 +753,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                 if (a.L >= 1) {
                     float4 d = f4_zero();
                     if (a.L >= 2) {
-                        if (use_tma) ok_d = mbar_wait_bounded(bar_d + rb, (ph_d >> rb) & 1u);
+                        if (use_tma) ok_d = mbar_wait_bounded(bar_d + rb, (ph_d >> rb) & 1u, a.wait_ns);
                         d = reinterpret_cast<const float4*>(dcur)[tid];
                     }
                     const float dv[2][2] = {{d.x, d.y}, {d.z, d.w}};
@@ -810,7 +812,10 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
         __syncthreads();
         plane = (a.next != nullptr) ? (long long)*s_next : plane + gridDim.x;
     }
-    if (failed && leader && a.err != nullptr) atomicExch(a.err, kErrTmaTimeout);
+    if (failed && leader) {
+        if (a.err != nullptr) atomicExch(a.err, kErrTmaTimeout);
+        mbar_drain_issued(kWaitLimitNs);  // copies still in flight land before the CTA leaves
+    }
 }
 
 // ---------------------------------------------------------------------------------
@@ -871,7 +876,7 @@ struct FwdPlan {
     size_t ws_bytes = 0;
 };
 
-constexpr size_t kErrWordBytes = 256;  // the workspace starts with the error word
+constexpr size_t kErrWordBytes = kStatusBytes;  // the workspace starts with the status words
 // shared memory per CTA that still lets two CTAs share an SM
 constexpr size_t kTwoCtaSmem = 228 * 1024 / 2 - 1024;
 
@@ -884,8 +889,8 @@ template <int K, typename T>
 void fwd_layout(FwdArgs& a, int L, int hp, int wp, int nbs, int car2, int stage_u, int& xend,
                 int& local_end, int& deep) {
     int off = 0;
-    a.o_bar = off;
-    off += 32;  // seven mbarriers and the next-plane word, padded to 128 bytes
+    a.o_bar = off;  // 0: the mbarrier region starts dynamic shared memory (wt_tma.cuh)
+    off += 32;  // ten mbarriers, the next-plane and abort words and the issue bookkeeping
     a.o_raw = off;
     a.raw_f = round32((XBox<K, T>::BYTES + 3) / 4);
     off += 2 * a.raw_f;
@@ -1042,8 +1047,9 @@ wt_status launch_fwd_k(const wt_desc& d, const void* x, const float* w0f, const 
     a.x = x;
     a.y = y;
     a.b0f = flip ? nullptr : b0f;
-    a.err = reinterpret_cast<int*>(ws);
+    a.err = reinterpret_cast<int*>(ws) + (flip ? kStatusBackwardData : kStatusForward);
     a.next = a.err + 1;
+    a.wait_ns = wait_limit_ns();
     float* wimg = reinterpret_cast<float*>(static_cast<char*>(ws) + kErrWordBytes);
     a.wimg = wimg;
     a.zd = reinterpret_cast<float*>(static_cast<char*>(ws) + kErrWordBytes + p.img_bytes);

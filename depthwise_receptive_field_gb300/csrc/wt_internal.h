@@ -43,6 +43,19 @@ inline int padded_side(int n, int levels) {
 // Bytes per element of an I/O dtype.
 inline size_t io_bytes(wt_dtype io) { return io == WT_F32 ? 4 : 2; }
 
+// The first 256 bytes of every workspace: one status word per kind of call (set by the
+// plane kernel when one of its bounded waits timed out), each followed by that call's plane
+// counter; a launch clears only its own pair, so wtconv_workspace_status can report the
+// most recent call of each kind.
+constexpr int kStatusForward = 0;         // words 0, 1
+constexpr int kStatusBackwardData = 2;    // words 2, 3
+constexpr int kStatusBackwardWeight = 4;  // words 4, 5
+constexpr size_t kStatusBytes = 256;
+
+// Limit of every bounded wait inside the kernels, in nanoseconds of %globaltimer (1 s
+// unless a test shortened it with wtconv_testing_set_wait_limit_ns).
+unsigned long long wait_limit_ns();
+
 // sm_103a: 227 KB of shared memory per block (opt-in), 152 SMs.
 constexpr size_t kMaxSmemPerBlock = 227 * 1024;
 constexpr int kNumSMs = 152;
@@ -63,16 +76,18 @@ wt_status launch_backward_weight(const wt_desc& d, const void* x, const void* dy
 size_t backward_weight_ws_bytes(const wt_desc& d);
 // pieces of the backward-weight path: the per-plane partial kernel alone (partials
 // [C][d.n][KP] to `part`; its CTAs' level-2 scratch slots, backward_weight_slot_bytes each,
-// in [slots, slots + slots_bytes), the grid shrinking to the slots that fit) and the
-// reduce + unfold kernel alone over [C][groups][KP]
+// in [slots, slots + slots_bytes), the grid shrinking to the slots that fit; err[0] is
+// set on a timed-out wait and err[1] is the plane counter, zero before the launch; err may
+// be null) and the reduce + unfold kernel alone over [C][groups][KP] (NaN gradients when
+// err is non-null and *err != 0)
 wt_status launch_dw_partials(const wt_desc& d, const void* x, const void* dy, float* part,
-                             float* slots, size_t slots_bytes, cudaStream_t stream,
+                             float* slots, size_t slots_bytes, int* err, cudaStream_t stream,
                              int* launches);
 size_t backward_weight_slot_bytes(const wt_desc& d);
 wt_status launch_dw_reduce(const wt_desc& d, const float* part, int groups, const float* w0,
                            const float* b0, const float* s0, const float* wl, const float* sl,
                            float* dw0, float* db0, float* ds0, float* dwl, float* dsl,
-                           cudaStream_t stream, int* launches);
+                           const int* err, cudaStream_t stream, int* launches);
 size_t dw_partial_floats(const wt_desc& d);
 size_t backward_weight_smem_bytes(const wt_desc& d);
 

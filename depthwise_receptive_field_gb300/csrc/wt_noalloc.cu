@@ -7,13 +7,21 @@
 // the library (kNoAllocScratchBytes, 4 MiB). Every GPU that loads the library holds that
 // array until the process exits.
 //
-// The scratch holds the per-channel running totals [C][KP], the per-plane partial vectors
-// of one chunk of images [C][nc][KP] (KP = k*k + 1 + 4 k*k L), and the level-2 scratch
-// slots of the plane kernel's CTAs (when L >= 2; the kernel runs as many CTAs as slots
-// fit). The batch is processed in chunks of nc images; each chunk runs the ordinary
+// The scratch holds a 256-byte header (a status word that the plane kernel sets when one
+// of its bounded waits times out, and the counter that hands planes to its CTAs; both are
+// cleared with cudaMemsetAsync, which allocates nothing), the per-channel running totals
+// [C][KP], the per-plane partial vectors of one chunk of images [C][nc][KP]
+// (KP = k*k + 1 + 4 k*k L), and the level-2 scratch slots of the plane kernel's CTAs (when
+// L >= 2). The batch is processed in chunks of nc images; each chunk runs the ordinary
 // per-plane partial kernel, then a small kernel folds the chunk into the totals (the
 // first chunk overwrites them, so nothing needs clearing beforehand), and finally the
-// ordinary reduce + unfold kernel turns the totals into gradients.
+// ordinary reduce + unfold kernel turns the totals into gradients; it writes NaN gradients
+// if the status word was set, so that a failed call cannot pass for a result.
+//
+// Grid: the plane kernel runs one CTA per level-2 slot that fits in what the header,
+// totals and partials leave of the 4 MiB, at most two per SM. On large planes that is far
+// fewer than the workspace path's 304 CTAs (16 x 256 x 256 x 256 at k = 5, L = 5: 23 CTAs
+// of 128 KB slots), so this call is correspondingly slower there.
 //
 // Every call shares the one array and leaves its last contents behind: two calls whose
 // kernels overlap on the GPU (different streams, or different host threads on the same
@@ -29,6 +37,7 @@ namespace wt {
 namespace {
 
 constexpr size_t kNoAllocScratchFloats = size_t(1) << 20;
+constexpr size_t kHeaderFloats = 64;  // status word and plane counter, padded to 256 bytes
 constexpr size_t kNoAllocScratchBytes = kNoAllocScratchFloats * sizeof(float);  // 4 MiB
 constexpr int kMaxDevices = 64;
 
@@ -95,33 +104,40 @@ extern "C" wt_status wtconv_backward_weight_noalloc(const wt_desc* desc, const v
                              !aligned4(dwl) || !aligned4(dsl)))
         return WT_ERR_INVALID_ARG;
 
-    // sizes: totals [C][KP], then one chunk of partial vectors [C][nc][KP], then the
-    // plane kernel's level-2 scratch slots (as many CTAs' as fit, up to one per plane of
-    // the chunk or two per SM, whichever is fewer; at least one)
+    // sizes: a 256-byte header (status word, plane counter), totals [C][KP], then one chunk
+    // of partial vectors [C][nc][KP], then the plane kernel's level-2 scratch slots (as many
+    // CTAs' as fit, up to one per plane of the chunk or two per SM, whichever is fewer; at
+    // least one)
     const size_t KP = dw_partial_floats(*desc);
     const size_t per_image = (size_t)desc->c * KP;
     const size_t totals_floats = (per_image + 63) & ~size_t(63);
     const size_t slot_floats = backward_weight_slot_bytes(*desc) / sizeof(float);
-    if (totals_floats + per_image + slot_floats > kNoAllocScratchFloats) return WT_ERR_WORKSPACE;
-    size_t want_slots = (size_t)desc->c * desc->n < 304 ? (size_t)desc->c * desc->n : 304;
+    if (kHeaderFloats + totals_floats + per_image + slot_floats > kNoAllocScratchFloats)
+        return WT_ERR_WORKSPACE;
+    const size_t room = kNoAllocScratchFloats - kHeaderFloats - totals_floats;
+    size_t want_slots = (size_t)desc->c * desc->n < 2 * (size_t)kNumSMs
+                            ? (size_t)desc->c * desc->n
+                            : 2 * (size_t)kNumSMs;
     if (slot_floats == 0) want_slots = 0;
     size_t nc_max = 1;
-    if (kNoAllocScratchFloats > totals_floats + want_slots * slot_floats + per_image)
-        nc_max = (kNoAllocScratchFloats - totals_floats - want_slots * slot_floats) / per_image;
+    if (room > want_slots * slot_floats + per_image)
+        nc_max = (room - want_slots * slot_floats) / per_image;
     if (nc_max > (size_t)desc->n) nc_max = (size_t)desc->n;
     const size_t part_floats = (nc_max * per_image + 63) & ~size_t(63);
 
     float* scratch = nullptr;
     st = scratch_on_current_device(&scratch);
     if (st != WT_OK) return st;
-    float* totals = scratch;
-    float* part = scratch + totals_floats;
+    int* status = reinterpret_cast<int*>(scratch);  // [0] timed-out wait, [1] plane counter
+    float* totals = scratch + kHeaderFloats;
+    float* part = totals + totals_floats;
     float* slots = part + part_floats;
+    const size_t used = kHeaderFloats + totals_floats + part_floats;
     const size_t slots_bytes =
-        (kNoAllocScratchFloats > totals_floats + part_floats)
-            ? (kNoAllocScratchFloats - totals_floats - part_floats) * sizeof(float)
-            : 0;
+        (kNoAllocScratchFloats > used) ? (kNoAllocScratchFloats - used) * sizeof(float) : 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // cudaMemsetAsync allocates nothing; the status word starts at zero for this call
+    if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return WT_ERR_CUDA;
 
     const size_t esize = io_bytes(desc->io);
     const size_t image_bytes = (size_t)desc->c * desc->h * desc->w * esize;
@@ -132,7 +148,8 @@ extern "C" wt_status wtconv_backward_weight_noalloc(const wt_desc* desc, const v
         sub.n = nc;
         const char* xb = static_cast<const char*>(x) + (size_t)n0 * image_bytes;
         const char* gb = static_cast<const char*>(dy) + (size_t)n0 * image_bytes;
-        st = launch_dw_partials(sub, xb, gb, part, slots, slots_bytes, s, &launches);
+        if (cudaMemsetAsync(status + 1, 0, sizeof(int), s) != cudaSuccess) return WT_ERR_CUDA;
+        st = launch_dw_partials(sub, xb, gb, part, slots, slots_bytes, status, s, &launches);
         if (st != WT_OK) return st;
         const size_t n_tot = per_image;
         const unsigned blocks = (unsigned)((n_tot + 255) / 256 < 1024 ? (n_tot + 255) / 256 : 1024);
@@ -141,9 +158,10 @@ extern "C" wt_status wtconv_backward_weight_noalloc(const wt_desc* desc, const v
         if (cudaGetLastError() != cudaSuccess) return WT_ERR_CUDA;
         ++launches;
     }
-    st = launch_dw_reduce(*desc, totals, 1, w0, b0, s0, wl, sl, dw0, db0, ds0, dwl, dsl, s,
-                          &launches);
+    st = launch_dw_reduce(*desc, totals, 1, w0, b0, s0, wl, sl, dw0, db0, ds0, dwl, dsl, status,
+                          s, &launches);
     (void)fws;
     (void)bws;
+    if (st == WT_OK) set_last_launch_count(launches);
     return st;
 }

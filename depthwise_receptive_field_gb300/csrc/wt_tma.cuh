@@ -8,7 +8,7 @@
 
 namespace wt {
 
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s, the default limit
 constexpr int kErrTmaTimeout = 1;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -42,6 +42,44 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
+// Every kernel keeps its mbarriers at the start of dynamic shared memory (a region of 32
+// words: at most 14 barriers, then bookkeeping words). Word kTrackParity holds, for each
+// barrier b, the parity of the number of phases issued on it (bit b flips with each
+// arrive.expect_tx); word kTrackUsed marks the barriers that ever had a phase issued.
+constexpr int kTrackParity = 28;
+constexpr int kTrackUsed = 29;
+
+__device__ __forceinline__ uint64_t* mbar_region() {
+    extern __shared__ __align__(128) float4 smem_f4[];
+    return reinterpret_cast<uint64_t*>(smem_f4);
+}
+
+// Clears the issue bookkeeping (one thread, before the CTA's first barrier).
+__device__ __forceinline__ void mbar_track_init() {
+    volatile uint32_t* w = reinterpret_cast<volatile uint32_t*>(mbar_region());
+    w[kTrackParity] = 0;
+    w[kTrackUsed] = 0;
+}
+
+// arrive.expect_tx on `bar` (one of the region's barriers) that also records the phase it
+// opens, for the drain below. Only the thread that issues a CTA's copies calls it.
+__device__ __forceinline__ void mbar_expect_tx_noted(uint64_t* bar, uint32_t bytes) {
+    uint64_t* base = mbar_region();
+    volatile uint32_t* w = reinterpret_cast<volatile uint32_t*>(base);
+    const int idx = (int)(bar - base);
+    w[kTrackParity] ^= 1u << idx;
+    w[kTrackUsed] |= 1u << idx;
+    mbar_arrive_expect_tx(bar, bytes);
+}
+
+// After a timed-out wait, before the CTA leaves: wait, at most `limit_ns` in all, until
+// the last phase issued on every used barrier has completed, so that no copy lands in
+// shared memory after the CTA is gone. Each barrier has at most one phase outstanding
+// (a copy is issued on it only after its previous phase was waited for), and the last
+// issued phase's parity is the opposite of the issue-count parity. Returns false if the
+// limit ran out.
+__device__ __forceinline__ bool mbar_drain_issued(unsigned long long limit_ns);
+
 // 3-D tiled TMA load of one box into shared memory, completing on `bar`.
 // Coordinates are in elements; c0 * element size must be a multiple of 16 bytes.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1,
@@ -65,20 +103,62 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probe of the same phase (mbarrier.test_wait returns at once).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
 
-// Wait for the phase of `bar` with the given parity to complete; false after ~1 s.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// The same wait with non-blocking probes (a limit shorter than the default: only a test
+// sets one; try_wait may suspend the thread for a while before it reports an incomplete
+// phase, which would hide a short limit). Kept out of line, off the kernels' hot path.
+static __device__ __noinline__ bool mbar_wait_probing(uint64_t* bar, uint32_t parity,
+                                               unsigned long long limit_ns) {
+    const unsigned long long t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// Wait for the phase of `bar` with the given parity to complete; false once `limit_ns`
+// nanoseconds have passed without it.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  unsigned long long limit_ns) {
+    if (limit_ns < kWaitLimitNs) return mbar_wait_probing(bar, parity, limit_ns);
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
+}
+
+__device__ __forceinline__ bool mbar_drain_issued(unsigned long long limit_ns) {
+    uint64_t* base = mbar_region();
+    const volatile uint32_t* w = reinterpret_cast<const volatile uint32_t*>(base);
+    const uint32_t par = w[kTrackParity], used = w[kTrackUsed];
+    const unsigned long long t0 = globaltimer_ns();
+    for (int b = 0; b < kTrackParity / 2; ++b) {
+        if (((used >> b) & 1u) == 0) continue;
+        const uint32_t last = ((par >> b) & 1u) ^ 1u;
+        while (!mbar_try_wait(base + b, last))
+            if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+    return true;
 }
 
 // One arrival on `bar` (release semantics: this thread's earlier shared-memory accesses are

@@ -48,6 +48,7 @@ struct DwArgs {
     float* part;      // [C][N][KP]
     int* err;         // set when a TMA wait times out (may be null)
     int* next;        // the next plane to hand out (zeroed before the launch; may be null)
+    unsigned long long wait_ns;  // limit of every bounded wait
     float* slots;     // per CTA: level-2 subbands of X, of dY (u2 floats each), carriers
     long long slot_floats, u2_floats;
     long long planes;
@@ -276,7 +277,7 @@ __device__ __forceinline__ bool dw_sweep(const DwArgs& a, const T* xp, const T* 
         };
         auto refill = [&](int nt, int nb) {  // pair nt into buffers nb
             const int ny = nt / bxn, nx = nt - ny * bxn;
-            mbar_arrive_expect_tx(bar_s + nb, 2 * S::BYTES);
+            mbar_expect_tx_noted(bar_s + nb, 2 * S::BYTES);
             tma_load_3d(buf + nb * (BW * BH), &a.tsx, nx * BW, ny * BH, (int)plane, bar_s + nb);
             tma_load_3d(buf + (NB + nb) * (BW * BH), &a.tsg, nx * BW, ny * BH, (int)plane,
                         bar_s + nb);
@@ -285,7 +286,7 @@ __device__ __forceinline__ bool dw_sweep(const DwArgs& a, const T* xp, const T* 
             // three or more pairs in flight: one CTA barrier per pair (measured faster here
             // than the per-warp releases below, which win with two pairs)
             for (int t = 0, b = 0, nb = NB - 1; t < nbox; ++t) {
-                const bool okb = mbar_wait_bounded(bar_s + b, (ph_s >> b) & 1u);
+                const bool okb = mbar_wait_bounded(bar_s + b, (ph_s >> b) & 1u, a.wait_ns);
                 ph_s ^= 1u << b;
                 if (__syncthreads_or(!okb)) return false;
                 // every thread is past pair t - 1: refill its buffers with pair t - 1 + NB
@@ -302,7 +303,7 @@ __device__ __forceinline__ bool dw_sweep(const DwArgs& a, const T* xp, const T* 
                 // pair t - 1 + NB into the buffers of pair t - 1 once every warp released them
                 const int nt = t - 1 + NB;
                 if (nt < nbox && ok && *s_abort == 0) {
-                    ok = mbar_wait_bounded(bar_e + nb, (ph_e >> nb) & 1u);
+                    ok = mbar_wait_bounded(bar_e + nb, (ph_e >> nb) & 1u, a.wait_ns);
                     if (ok)
                         refill(nt, nb);
                     else
@@ -311,7 +312,7 @@ __device__ __forceinline__ bool dw_sweep(const DwArgs& a, const T* xp, const T* 
                 ph_e ^= 1u << nb;  // the release of pair t - 1 (waited for or not)
             }
             if (ok && *s_abort == 0) {
-                ok = mbar_wait_bounded(bar_s + b, (ph_s >> b) & 1u);
+                ok = mbar_wait_bounded(bar_s + b, (ph_s >> b) & 1u, a.wait_ns);
                 if (!ok) *s_abort = 1;
             }
             ph_s ^= 1u << b;
@@ -456,6 +457,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
         }
         fence_mbar_init();
     }
+    if (leader) mbar_track_init();
     volatile int* s_abort = reinterpret_cast<volatile int*>(sm + a.o_bar + 26);  // a wait timed out
     if (leader) *s_abort = 0;
     __syncthreads();
@@ -478,7 +480,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
             // the first full-resolution tile pair, in flight during the deep levels, and the
             // first box pairs of the level-2 sweep
             fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar, BYTES);
+            mbar_expect_tx_noted(bar, BYTES);
             tma_load_3d(sm + a.o_rawx, &a.tmx, -XBox<K, T>::XOFF, -2 * R, (int)plane, bar);
             tma_load_3d(sm + a.o_rawg, &a.tmg, 0, 0, (int)plane, bar);
             if (a.L >= 2) {
@@ -487,7 +489,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
                 T* buf = reinterpret_cast<T*>(sm + a.o_xb);
                 for (int t = 0; t < a.nsw && t < nbox; ++t) {
                     const int ny = t / bxn, nx = t - ny * bxn;
-                    mbar_arrive_expect_tx(bar_s + t, 2 * S::BYTES);
+                    mbar_expect_tx_noted(bar_s + t, 2 * S::BYTES);
                     tma_load_3d(buf + t * (BW * BH), &a.tsx, nx * BW, ny * BH, (int)plane,
                                 bar_s + t);
                     tma_load_3d(buf + (a.nsw + t) * (BW * BH), &a.tsg, nx * BW, ny * BH,
@@ -650,7 +652,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
             bool ok = true;
             if (use_tma) {
                 // a timed-out wait converts stale data; the vote below ends the kernel
-                ok = mbar_wait_bounded(bar + rb, (ph >> rb) & 1u);
+                ok = mbar_wait_bounded(bar + rb, (ph >> rb) & 1u, a.wait_ns);
                 ph ^= 1u << rb;
             } else {
                 stage_raw<K, T>(xp, a.H, a.W, const_cast<T*>(rawx), y0, x0);
@@ -665,7 +667,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
             }
             if (use_tma && leader && t + 1 < ntiles) {
                 const int ny = (t + 1) / tiles_x, nx = (t + 1) - ny * tiles_x, nb = rb ^ 1;
-                mbar_arrive_expect_tx(bar + nb, BYTES);
+                mbar_expect_tx_noted(bar + nb, BYTES);
                 tma_load_3d(sm + a.o_rawx + nb * a.rawx_f, &a.tmx, nx * kTile - XBox<K, T>::XOFF,
                             ny * kTile - 2 * R, (int)plane, bar + nb);
                 tma_load_3d(sm + a.o_rawg + nb * a.rawg_f, &a.tmg, nx * kTile, ny * kTile,
@@ -737,22 +739,28 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
         __syncthreads();
         plane = (a.next != nullptr) ? (long long)*s_next : plane + gridDim.x;
     }
-    if (failed && leader && a.err != nullptr) atomicExch(a.err, kErrTmaTimeout);
+    if (failed && leader) {
+        if (a.err != nullptr) atomicExch(a.err, kErrTmaTimeout);
+        mbar_drain_issued(kWaitLimitNs);  // copies still in flight land before the CTA leaves
+    }
 }
 
-// Per channel: fixed-order sum of the N partial vectors, then §4.3 Eq. 9.
+// Per channel: fixed-order sum of the N partial vectors, then §4.3 Eq. 9. When the plane
+// kernel recorded a timed-out wait (*err != 0), every gradient is written as NaN instead,
+// so that the failure cannot pass for a result.
 __global__ void wt_dw_reduce_kernel(const float* part, int C, int G, int KP, int K, int L,
                                     const float* w0, const float* b0, const float* s0,
                                     const float* wl, const float* sl, float* dw0, float* db0,
-                                    float* ds0, float* dwl, float* dsl) {
+                                    float* ds0, float* dwl, float* dsl, const int* err) {
     extern __shared__ float tot[];
     const int c = blockIdx.x;
     const int KK = K * K;
+    const bool bad = err != nullptr && *reinterpret_cast<const volatile int*>(err) != 0;
     for (int e = threadIdx.x; e < KP; e += blockDim.x) {
         float s = 0.f;
         for (int gi = 0; gi < G; ++gi) s += part[((size_t)c * G + gi) * KP + e];
         // level entries were accumulated from unnormalized subbands on both sides (4x)
-        tot[e] = (e > KK) ? 0.25f * s : s;
+        tot[e] = bad ? __int_as_float(0x7fc00000) : (e > KK) ? 0.25f * s : s;
     }
     __syncthreads();
     const float s0c = s0[c];
@@ -788,7 +796,7 @@ namespace {
 int round4(int v) { return (v + 3) & ~3; }
 int round32(int v) { return (v + 31) & ~31; }
 
-constexpr size_t kDwErrBytes = 256;  // the workspace starts with a status word
+constexpr size_t kDwErrBytes = kStatusBytes;  // the workspace starts with the status words
 constexpr size_t kTwoCtaSmem = 228 * 1024 / 2 - 1024;  // two CTAs per SM still fit
 
 size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -810,8 +818,8 @@ DwPlan dw_layout(const wt_desc& d) {
     const int hp = padded_side(d.h, L), wp = padded_side(d.w, L);
     a.KP = KK + 1 + 4 * KK * L;
     int off = 0;
-    a.o_bar = off;
-    off += 32;  // mbarriers and the next-plane word, padded to 128 bytes
+    a.o_bar = off;  // 0: the mbarrier region starts dynamic shared memory (wt_tma.cuh)
+    off += 32;  // mbarriers, the next-plane and abort words and the issue bookkeeping
     a.o_rawx = off;
     a.rawx_f = round32((XBox<K, T>::BYTES + 3) / 4);
     off += 2 * a.rawx_f;
@@ -919,6 +927,7 @@ bool dw_prepare(const wt_desc& d, const void* x, const void* dy, float* part, fl
     a.part = part;
     a.err = err;
     a.next = (err != nullptr) ? err + 1 : nullptr;
+    a.wait_ns = wait_limit_ns();
     a.planes = (long long)d.n * d.c;
     a.N = d.n;
     a.C = d.c;
@@ -972,7 +981,7 @@ wt_status launch_dw_k(const wt_desc& d, const void* x, const void* dy, const flo
     DwPlan p = dw_layout<K, T>(d);
     const size_t need = kDwErrBytes + part_bytes + (size_t)p.grid * p.slot_bytes;
     if (ws == nullptr || ws_bytes < need) return WT_ERR_WORKSPACE;
-    int* err = reinterpret_cast<int*>(ws);
+    int* err = reinterpret_cast<int*>(ws) + kStatusBackwardWeight;
     float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + kDwErrBytes);
     float* slots = reinterpret_cast<float*>(static_cast<char*>(ws) + kDwErrBytes + part_bytes);
     if (!dw_prepare<K, T>(d, x, dy, part, slots, err, p)) return WT_ERR_UNSUPPORTED;
@@ -980,7 +989,7 @@ wt_status launch_dw_k(const wt_desc& d, const void* x, const void* dy, const flo
     wt_status st = launch_dw_plane<K, T>(p, stream, launches);
     if (st != WT_OK) return st;
     wt_dw_reduce_kernel<<<(unsigned)d.c, 128, (size_t)p.a.KP * sizeof(float), stream>>>(
-        part, d.c, d.n, p.a.KP, K, d.levels, w0, b0, s0, wl, sl, dw0, db0, ds0, dwl, dsl);
+        part, d.c, d.n, p.a.KP, K, d.levels, w0, b0, s0, wl, sl, dw0, db0, ds0, dwl, dsl, err);
     if (cudaGetLastError() != cudaSuccess) return WT_ERR_CUDA;
     ++*launches;
     return WT_OK;
@@ -990,7 +999,7 @@ wt_status launch_dw_k(const wt_desc& d, const void* x, const void* dy, const flo
 // the grid shrinks to the slots that fit.
 template <int K, typename T>
 wt_status launch_dw_partials_k(const wt_desc& d, const void* x, const void* dy, float* part,
-                               float* slots, size_t slots_bytes, cudaStream_t stream,
+                               float* slots, size_t slots_bytes, int* err, cudaStream_t stream,
                                int* launches) {
     DwPlan p = dw_layout<K, T>(d);
     if (p.slot_bytes > 0) {
@@ -998,21 +1007,21 @@ wt_status launch_dw_partials_k(const wt_desc& d, const void* x, const void* dy, 
         if (fit == 0) return WT_ERR_WORKSPACE;
         if ((size_t)p.grid > fit) p.grid = (int)fit;
     }
-    if (!dw_prepare<K, T>(d, x, dy, part, slots, nullptr, p)) return WT_ERR_UNSUPPORTED;
+    if (!dw_prepare<K, T>(d, x, dy, part, slots, err, p)) return WT_ERR_UNSUPPORTED;
     return launch_dw_plane<K, T>(p, stream, launches);
 }
 
 }  // namespace
 
 wt_status launch_dw_partials(const wt_desc& d, const void* x, const void* dy, float* part,
-                             float* slots, size_t slots_bytes, cudaStream_t stream,
+                             float* slots, size_t slots_bytes, int* err, cudaStream_t stream,
                              int* launches) {
     switch (d.k) {
 #define WT_CASE(KV)                                                                           \
     case KV:                                                                                  \
         return with_io_type(d.io, [&](auto t) {                                               \
             return launch_dw_partials_k<KV, decltype(t)>(d, x, dy, part, slots, slots_bytes,  \
-                                                         stream, launches);                   \
+                                                         err, stream, launches);              \
         });
         WT_CASE(1)
         WT_CASE(3)
@@ -1027,10 +1036,10 @@ wt_status launch_dw_partials(const wt_desc& d, const void* x, const void* dy, fl
 wt_status launch_dw_reduce(const wt_desc& d, const float* part, int groups, const float* w0,
                            const float* b0, const float* s0, const float* wl, const float* sl,
                            float* dw0, float* db0, float* ds0, float* dwl, float* dsl,
-                           cudaStream_t stream, int* launches) {
+                           const int* err, cudaStream_t stream, int* launches) {
     const int KP = (int)dw_partial_floats(d);
     wt_dw_reduce_kernel<<<(unsigned)d.c, 128, (size_t)KP * sizeof(float), stream>>>(
-        part, d.c, groups, KP, d.k, d.levels, w0, b0, s0, wl, sl, dw0, db0, ds0, dwl, dsl);
+        part, d.c, groups, KP, d.k, d.levels, w0, b0, s0, wl, sl, dw0, db0, ds0, dwl, dsl, err);
     if (cudaGetLastError() != cudaSuccess) return WT_ERR_CUDA;
     ++*launches;
     return WT_OK;

@@ -18,11 +18,14 @@
  *      sl, dsl                 [L][C][4]          float32
  *    "f" marks scale-folded parameters (§4.3 Eq. 8): w0f = s0*w0, b0f = s0*b0, wlf = sl*wl.
  *  - Depthwise convolution is cross-correlation with zero padding R = (k-1)/2.
- *  - The library allocates no device memory and keeps no state that affects results
- *    (only a per-host-thread launch counter, see wtconv_last_launch_count). Scratch
- *    comes from the caller's workspace (ws, ws_bytes); query its size with
- *    wtconv_workspace_size. A workspace may be reused by consecutive calls on one stream;
- *    calls that run concurrently on different streams need separate workspaces.
+ *  - The library allocates no device memory. Scratch comes from the caller's workspace
+ *    (ws, ws_bytes); query its size with wtconv_workspace_size. A workspace may be reused
+ *    by consecutive calls on one stream; calls that run concurrently on different streams
+ *    need separate workspaces. State kept between calls: a per-host-thread launch counter
+ *    (wtconv_last_launch_count), and the fixed 4 MiB device array of
+ *    wtconv_backward_weight_noalloc, whose contents one call leaves to the next (that call
+ *    clears what must start at zero, so results do not depend on it; concurrent calls of
+ *    that entry point race on it).
  *  - Every call is asynchronous on `stream` (0 = legacy default stream). Argument errors
  *    are reported synchronously and nothing is launched. Launch failures are read with
  *    cudaGetLastError right after each launch and reported as WT_ERR_CUDA; faults that
@@ -59,7 +62,8 @@ typedef enum {
     WT_ERR_INVALID_ARG = 1, /* bad shape, null or misaligned pointer */
     WT_ERR_UNSUPPORTED = 2, /* valid by the definition but not built (e.g. k = 9) */
     WT_ERR_WORKSPACE = 3,   /* ws too small (or NULL with ws_bytes > 0 needed) */
-    WT_ERR_CUDA = 4         /* a CUDA launch or runtime call failed */
+    WT_ERR_CUDA = 4,        /* a CUDA launch or runtime call failed */
+    WT_ERR_TIMEOUT = 5      /* a kernel's bounded wait timed out (wtconv_workspace_status) */
 } wt_status;
 
 typedef enum { WT_F32 = 0, WT_BF16 = 1, WT_F16 = 2 } wt_dtype;
@@ -140,7 +144,9 @@ wt_status wtconv_backward(const wt_desc* desc, const void* x, const void* dy,
 /*
  * wtconv_backward_weight without a workspace (the paper has no counterpart: this entry
  * point exists for callers of this library that cannot provide device memory).
- * Same arguments, results and determinism as wtconv_backward_weight, minus ws/ws_bytes.
+ * Same arguments and gradients as wtconv_backward_weight, minus ws/ws_bytes. Results are
+ * deterministic and agree with wtconv_backward_weight to fp32 rounding, not bitwise: the
+ * batch is summed chunk by chunk into running totals, a different fixed order.
  *
  * Who needs it: callers that cannot hand the library a workspace, e.g. a runtime that
  * owns all device memory through its own pool and forbids raw cudaMalloc, or a
@@ -149,9 +155,21 @@ wt_status wtconv_backward(const wt_desc* desc, const void* x, const void* dy,
  * (held by every GPU that loads the library until the process exits); this call makes
  * no cudaMalloc/cudaFree and calls no allocating library routine.
  *
- * Limit: the per-channel totals plus one image's partial vectors must fit in 4 MiB:
- * 2 * C * (k*k + 1 + 4*k*k*L) * 4 bytes <= 4 MiB (e.g. C <= 996 at k = 5, L = 5);
- * larger shapes return WT_ERR_WORKSPACE. The batch is processed in chunks of images.
+ * Limit, in floats (4 bytes), with KP = k*k + 1 + 4*k*k*L:
+ *     64 + round64(C*KP) + C*KP + S  <=  1048576 (4 MiB)
+ * where S is the level-2 scratch of one CTA (0 when L < 2, else
+ * 2 * round64(4 * ceil(H/2^L) * ceil(W/2^L) * 4^(L-2)) plus, for planes whose deep levels
+ * do not fit in shared memory, their carriers). Examples at k = 5, L = 5: C <= 994 for
+ * 64 x 64 planes, C <= 965 for 256 x 256; at C = 1, k = 5, L = 2 square planes up to
+ * 1444 x 1444.
+ * Larger shapes return WT_ERR_WORKSPACE before anything is launched. The batch is
+ * processed in chunks of images, and the plane kernel runs one CTA per level-2 slot that
+ * fits in what is left of the 4 MiB (at most two per SM): on large planes far fewer CTAs
+ * than the workspace path (16 x 256 x 256 x 256 at k = 5, L = 5: 23 instead of 304), so
+ * the call is correspondingly slower there.
+ *
+ * Failure: if a bounded wait inside the plane kernel times out, every gradient is written
+ * as NaN (the status is also WT_OK at return, since the call is asynchronous).
  *
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture.
@@ -163,6 +181,22 @@ wt_status wtconv_backward_weight_noalloc(const wt_desc* desc, const void* x, con
                                          const float* wl, const float* sl, float* dw0,
                                          float* db0, float* ds0, float* dwl, float* dsl,
                                          wt_stream_t stream);
+
+/*
+ * Device-side status of the most recent forward, backward-data and backward-weight call
+ * that used this workspace (ws as passed to those calls). Every data load inside the plane
+ * kernels completes on an mbarrier whose wait is bounded (1 s); a CTA whose wait runs out
+ * records it in its call's status word in the workspace, waits (again bounded) for its
+ * copies still in flight and leaves, so that call's outputs are incomplete.
+ * This call synchronizes `stream` (the stream those calls ran on) and reads the words.
+ * flags (may be NULL) receives bit 0 = forward, bit 1 = backward-data, bit 2 =
+ * backward-weight timed out. Returns WT_ERR_TIMEOUT if any bit is set, WT_OK if none,
+ * WT_ERR_INVALID_ARG for a NULL ws, WT_ERR_CUDA if the copy fails. Each call clears its
+ * own word when it starts, so the words describe the latest call of each kind; the fused
+ * wtconv_backward sets the backward-data and backward-weight words. backward-weight also
+ * turns a timeout into NaN gradients, so that it cannot pass for a result.
+ */
+wt_status wtconv_workspace_status(const void* ws, wt_stream_t stream, int* flags);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* wtconv_status_string(wt_status status);

@@ -29,7 +29,7 @@ def test_header_declares_the_method_entry_points():
 
 
 def test_status_strings(lib):
-    for s in range(5):
+    for s in range(6):
         assert B.status_string(s).startswith("WT_")
     assert "unknown" in B.status_string(99)
 
@@ -166,3 +166,18 @@ def test_variant_validation(lib):
     with pytest.raises(B.WTConvError) as e:
         B.wtconv_forward_variant(d, 0, None, 16, None, 16, 16, 16, 16, 256, sizes[0], stream=0)
     assert e.value.status == B.WT_ERR_INVALID_ARG
+
+
+def test_status_query_and_probe_validate_before_any_device_call(lib):
+    """wtconv_workspace_status rejects a NULL workspace, the probe rejects bad sizes and a
+    NULL output, and the wait-limit test hook accepts any value; none touches the device."""
+    flags = ctypes.c_int(5)
+    assert lib.wtconv_workspace_status(None, None, ctypes.byref(flags)) == B.WT_ERR_INVALID_ARG
+    assert flags.value == 0
+    assert lib.wtconv_fma_probe(0, 10, 1, 256, None) == B.WT_ERR_INVALID_ARG
+    assert lib.wtconv_fma_probe(4, 0, 1, 256, None) == B.WT_ERR_INVALID_ARG
+    assert lib.wtconv_fma_probe(4, 10, 1, None, None) == B.WT_ERR_INVALID_ARG
+    assert lib.wtconv_fma_probe(4, 10, 1, 258, None) == B.WT_ERR_INVALID_ARG  # misaligned
+    assert lib.wtconv_testing_set_wait_limit_ns(1000) == B.WT_OK
+    assert lib.wtconv_testing_set_wait_limit_ns(0) == B.WT_OK
+    assert B.status_string(B.WT_ERR_TIMEOUT).startswith("WT_ERR_TIMEOUT")

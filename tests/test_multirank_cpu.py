@@ -66,7 +66,17 @@ def test_single_rank_is_identity():
 
 def test_fp32_peak_from_unit_counts():
     import bench
-    assert bench.fp32_peak_tflops(2070.0) == pytest.approx(152 * 128 * 2 * 2.07e9 / 1e12)
+    assert bench.derived_fp32_peak_tflops(152, 2070.0) == pytest.approx(
+        152 * 128 * 2 * 2.07e9 / 1e12)
+
+
+def test_cpu_baseline_brief_leg_for_forward_only_workloads():
+    """The per-config oracle figures: a brief all-cores and one-thread timing, also for the
+    forward-only workload (no dY)."""
+    import bench
+    from depthwise_receptive_field_gb300.inputs import WORKLOADS
+    r = bench.cpu_baseline(WORKLOADS["c1_small_fwd"], target_s=0.02, single_s=0.02, brief=True)
+    assert r["all_cores_gelem_s"] > 0 and r["one_thread_gelem_s"] > 0 and r["cores"] >= 1
 
 
 def test_cpu_baseline_legs():
