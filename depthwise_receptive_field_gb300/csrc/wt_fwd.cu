@@ -124,7 +124,8 @@ template <typename T, bool FAST>
 __device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, float* sm, float* deep,
                                              float* u2, uint64_t* bar_s, uint64_t* bar_e,
                                              uint32_t& ph_s, uint32_t& ph_e,
-                                             volatile int* s_abort, long long plane) {
+                                             volatile int* s_abort, long long plane,
+                                             Issued& iss) {
     constexpr int BW = SweepBox<T>::BW, BH = SweepBox<T>::BH, NB = SweepBox<T>::NBUF;
     constexpr int PR = BH / 4;  // rows of level-2 positions per box
     const int H2 = a.Hp >> 2, W2 = a.Wp >> 2;
@@ -147,7 +148,7 @@ __device__ __forceinline__ bool level2_sweep(const FwdArgs& a, const T* xp, floa
                     if (ok) {
                         const int ny = nt / bxn, nx = nt - ny * bxn;
                         fence_proxy_async_smem();
-                        mbar_expect_tx_noted(bar_s + nb, SweepBox<T>::BYTES);
+                        mbar_expect_tx_noted(bar_s + nb, SweepBox<T>::BYTES, iss);
                         tma_load_3d(buf + nb * (BW * BH), &a.tms, nx * BW, ny * BH, (int)plane,
                                     bar_s + nb);
                     } else {
@@ -401,7 +402,7 @@ __device__ __forceinline__ void repack_level2(const float* ubuf, float* bs) {
 template <int K, bool DG, bool STAGED>
 __device__ __forceinline__ bool deep_levels(const FwdArgs& a, float* sm, float* deep_g,
                                             const float* u2, float* zslot, uint64_t* bar_u,
-                                            uint32_t& ph_u) {
+                                            uint32_t& ph_u, Issued& iss) {
     constexpr int R = FG<K>::R;
     constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, WS = PG<K>::WS;
     constexpr int ZROW = PG<K>::ZROW, ZTILE = PG<K>::ZTILE;
@@ -415,7 +416,7 @@ __device__ __forceinline__ bool deep_levels(const FwdArgs& a, float* sm, float* 
     constexpr bool tma2 = STAGED && !DG;
     float* ubuf = sm + (tma2 ? a.o_u : 0);
     auto issue2 = [&](int ti0, int tj0) {
-        mbar_expect_tx_noted(bar_u, 16u * FG<K>::BT * FG<K>::BT);
+        mbar_expect_tx_noted(bar_u, 16u * FG<K>::BT * FG<K>::BT, iss);
         tma_load_3d(ubuf, &a.tmu, 4 * (tj0 - R), ti0 - R, (int)blockIdx.x, bar_u);
     };
     bool ok = true;
@@ -580,7 +581,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
         mbar_init(bar_u, 1);
         fence_mbar_init();
     }
-    if (leader) mbar_track_init();
+    Issued iss;  // phases the leader opened (for the drain after a timeout)
     volatile int* s_abort = reinterpret_cast<volatile int*>(sm + a.o_bar + 26);
     if (leader) *s_abort = 0;
     __syncthreads();
@@ -614,9 +615,9 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
         if (leader) {
             if (use_tma) {  // this channel's weights and the first tile of this plane
                 fence_proxy_async_smem();
-                mbar_expect_tx_noted(bar_w, (uint32_t)a.img * 4u);
+                mbar_expect_tx_noted(bar_w, (uint32_t)a.img * 4u, iss);
                 bulk_load(wsm, wimg, (uint32_t)a.img * 4u, bar_w);
-                mbar_expect_tx_noted(bar_x, XBox<K, T>::BYTES);
+                mbar_expect_tx_noted(bar_x, XBox<K, T>::BYTES, iss);
                 tma_load_3d(sm + a.o_raw, &a.tmx, -XBox<K, T>::XOFF, -2 * R, (int)plane, bar_x);
             }
             if (use_tma && a.L >= 2) {  // first boxes of the level-2 sweep
@@ -625,7 +626,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                 T* buf = reinterpret_cast<T*>(sm + a.o_b);
                 for (int t = 0; t < SweepBox<T>::NBUF && t < nbox; ++t) {
                     const int ny = t / bxn, nx = t - ny * bxn;
-                    mbar_expect_tx_noted(bar_s + t, SweepBox<T>::BYTES);
+                    mbar_expect_tx_noted(bar_s + t, SweepBox<T>::BYTES, iss);
                     tma_load_3d(buf + t * (BW * BH), &a.tms, nx * BW, ny * BH, (int)plane,
                                 bar_s + t);
                 }
@@ -640,14 +641,15 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
         // (i2, j2) holds the sums for level-1 positions (2i2 + a, 2j2 + b) as
         // (a, b) = (0,0), (0,1), (1,0), (1,1).
         if (a.L >= 2) {
-            if (!level2_sweep<T, FAST>(a, xp, sm, deep, u2, bar_s, bar_e, ph_s, ph_e, s_abort, plane) || !weights_ready()) {
+            if (!level2_sweep<T, FAST>(a, xp, sm, deep, u2, bar_s, bar_e, ph_s, ph_e, s_abort, plane, iss) || !weights_ready()) {
                 failed = true;
                 break;
             }
             const bool dok =
                 deep_global ? deep_levels<K, true, false>(a, sm, zslot + 2 * a.zd_slot, u2, zslot,
-                                                          bar_u, ph_u)
-                            : deep_levels<K, false, MODE == 2>(a, sm, sm, u2, zslot, bar_u, ph_u);
+                                                          bar_u, ph_u, iss)
+                            : deep_levels<K, false, MODE == 2>(a, sm, sm, u2, zslot, bar_u, ph_u,
+                                                               iss);
             if (!dok) {
                 failed = true;
                 break;
@@ -664,7 +666,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
         }
         if (a.L >= 2 && use_tma && leader) {  // deep sums of the first tile
             fence_proxy_async_smem();
-            mbar_expect_tx_noted(bar_d, kDBytes);
+            mbar_expect_tx_noted(bar_d, kDBytes, iss);
             tma_load_3d(dblk, &a.tmd, 0, 0, (int)blockIdx.x, bar_d);
         }
         // Tiles: raw X tiles and band-pair tiles are double-buffered, so one barrier per
@@ -707,11 +709,11 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
             }
             if (use_tma && leader && t + 1 < ntiles) {  // tile t + 1: X and its deep sums
                 const int ny = (t + 1) / tiles_x, nx = (t + 1) - ny * tiles_x, nb = rb ^ 1;
-                mbar_expect_tx_noted(bar_x + nb, XBox<K, T>::BYTES);
+                mbar_expect_tx_noted(bar_x + nb, XBox<K, T>::BYTES, iss);
                 tma_load_3d(sm + a.o_raw + nb * a.raw_f, &a.tmx, nx * kTile - XBox<K, T>::XOFF,
                             ny * kTile - 2 * R, (int)plane, bar_x + nb);
                 if (a.L >= 2) {
-                    mbar_expect_tx_noted(bar_d + nb, kDBytes);
+                    mbar_expect_tx_noted(bar_d + nb, kDBytes, iss);
                     tma_load_3d(dblk + nb * (kDBytes / 4), &a.tmd, nx * kTile,
                                 (ny * kTile) >> 2, (int)blockIdx.x, bar_d + nb);
                 }
@@ -814,7 +816,9 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
     }
     if (failed && leader) {
         if (a.err != nullptr) atomicExch(a.err, kErrTmaTimeout);
-        mbar_drain_issued(kWaitLimitNs);  // copies still in flight land before the CTA leaves
+        // copies in flight land before the CTA leaves: X tiles, deep-sum blocks, weights,
+        // sweep boxes and level-2 tiles (the release barriers take no copies)
+        if (use_tma) mbar_drain_issued(iss, 0x7fu | (1u << 9), kWaitLimitNs);
     }
 }
 

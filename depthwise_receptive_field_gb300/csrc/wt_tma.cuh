@@ -42,43 +42,35 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
-// Every kernel keeps its mbarriers at the start of dynamic shared memory (a region of 32
-// words: at most 14 barriers, then bookkeeping words). Word kTrackParity holds, for each
-// barrier b, the parity of the number of phases issued on it (bit b flips with each
-// arrive.expect_tx); word kTrackUsed marks the barriers that ever had a phase issued.
-constexpr int kTrackParity = 28;
-constexpr int kTrackUsed = 29;
+// Every kernel keeps its mbarriers at the start of dynamic shared memory (at most 32 of
+// them). The thread that issues a CTA's copies keeps one mask in a register for the drain
+// below: bit b flips with every phase it opens on barrier b, so it holds the parity of the
+// number of phases issued there.
+struct Issued {
+    uint32_t par = 0;
+};
 
 __device__ __forceinline__ uint64_t* mbar_region() {
     extern __shared__ __align__(128) float4 smem_f4[];
     return reinterpret_cast<uint64_t*>(smem_f4);
 }
 
-// Clears the issue bookkeeping (one thread, before the CTA's first barrier).
-__device__ __forceinline__ void mbar_track_init() {
-    volatile uint32_t* w = reinterpret_cast<volatile uint32_t*>(mbar_region());
-    w[kTrackParity] = 0;
-    w[kTrackUsed] = 0;
-}
-
 // arrive.expect_tx on `bar` (one of the region's barriers) that also records the phase it
-// opens, for the drain below. Only the thread that issues a CTA's copies calls it.
-__device__ __forceinline__ void mbar_expect_tx_noted(uint64_t* bar, uint32_t bytes) {
-    uint64_t* base = mbar_region();
-    volatile uint32_t* w = reinterpret_cast<volatile uint32_t*>(base);
-    const int idx = (int)(bar - base);
-    w[kTrackParity] ^= 1u << idx;
-    w[kTrackUsed] |= 1u << idx;
+// opens in `iss`. Only the thread that issues a CTA's copies calls it.
+__device__ __forceinline__ void mbar_expect_tx_noted(uint64_t* bar, uint32_t bytes, Issued& iss) {
+    iss.par ^= 1u << (uint32_t)(bar - mbar_region());
     mbar_arrive_expect_tx(bar, bytes);
 }
 
 // After a timed-out wait, before the CTA leaves: wait, at most `limit_ns` in all, until
-// the last phase issued on every used barrier has completed, so that no copy lands in
-// shared memory after the CTA is gone. Each barrier has at most one phase outstanding
-// (a copy is issued on it only after its previous phase was waited for), and the last
-// issued phase's parity is the opposite of the issue-count parity. Returns false if the
-// limit ran out.
-__device__ __forceinline__ bool mbar_drain_issued(unsigned long long limit_ns);
+// the last phase issued on every barrier of `mask` (the initialized barriers that copies
+// complete on) has completed, so that no copy lands in shared memory after the CTA is
+// gone. Each barrier has at most one phase outstanding (a copy is issued on it only after
+// its previous phase was waited for), and the last issued phase's parity is the opposite
+// of the issue-count parity; on a barrier that never had a phase issued that test passes
+// at once. Returns false if the limit ran out.
+__device__ __forceinline__ bool mbar_drain_issued(const Issued& iss, uint32_t mask,
+                                                  unsigned long long limit_ns);
 
 // 3-D tiled TMA load of one box into shared memory, completing on `bar`.
 // Coordinates are in elements; c0 * element size must be a multiple of 16 bytes.
@@ -103,7 +95,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Non-blocking probe of the same phase (mbarrier.test_wait returns at once).
+// Non-blocking probe of the same phase (test_wait returns at once; try_wait may first
+// suspend the thread for a while).
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -122,39 +115,28 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
     return t;
 }
 
-// The same wait with non-blocking probes (a limit shorter than the default: only a test
-// sets one; try_wait may suspend the thread for a while before it reports an incomplete
-// phase, which would hide a short limit). Kept out of line, off the kernels' hot path.
-static __device__ __noinline__ bool mbar_wait_probing(uint64_t* bar, uint32_t parity,
-                                               unsigned long long limit_ns) {
-    const unsigned long long t0 = globaltimer_ns();
-    while (true) {
-        if (mbar_test_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > limit_ns) return false;
-    }
-}
-
 // Wait for the phase of `bar` with the given parity to complete; false once `limit_ns`
-// nanoseconds have passed without it.
+// nanoseconds have passed without it. With a limit shorter than the default (only a test
+// sets one) the wait probes without suspending, since try_wait's own suspension could
+// outlast a short limit and hide it.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   unsigned long long limit_ns) {
-    if (limit_ns < kWaitLimitNs) return mbar_wait_probing(bar, parity, limit_ns);
-    if (mbar_try_wait(bar, parity)) return true;
+    const bool probe = limit_ns < kWaitLimitNs;
+    if (!probe && mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (probe ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 
-__device__ __forceinline__ bool mbar_drain_issued(unsigned long long limit_ns) {
+__device__ __forceinline__ bool mbar_drain_issued(const Issued& iss, uint32_t mask,
+                                                  unsigned long long limit_ns) {
     uint64_t* base = mbar_region();
-    const volatile uint32_t* w = reinterpret_cast<const volatile uint32_t*>(base);
-    const uint32_t par = w[kTrackParity], used = w[kTrackUsed];
     const unsigned long long t0 = globaltimer_ns();
-    for (int b = 0; b < kTrackParity / 2; ++b) {
-        if (((used >> b) & 1u) == 0) continue;
-        const uint32_t last = ((par >> b) & 1u) ^ 1u;
+    for (int b = 0; b < 32; ++b) {
+        if (((mask >> b) & 1u) == 0) continue;
+        const uint32_t last = ((iss.par >> b) & 1u) ^ 1u;
         while (!mbar_try_wait(base + b, last))
             if (globaltimer_ns() - t0 > limit_ns) return false;
     }

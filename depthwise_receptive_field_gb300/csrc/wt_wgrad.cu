@@ -246,7 +246,7 @@ template <typename T, bool FAST>
 __device__ __forceinline__ bool dw_sweep(const DwArgs& a, const T* xp, const T* gp, float* sm,
                                          float* u2x, float* u2g, uint64_t* bar_s,
                                          uint64_t* bar_e, uint32_t& ph_s, uint32_t& ph_e,
-                                         volatile int* s_abort, long long plane) {
+                                         volatile int* s_abort, long long plane, Issued& iss) {
     using S = DwSweep<T>;
     constexpr int BW = S::BW, BH = S::BH, PR = BH / 4, PC = BW / 4;
     const int NB = a.nsw;
@@ -277,7 +277,7 @@ __device__ __forceinline__ bool dw_sweep(const DwArgs& a, const T* xp, const T* 
         };
         auto refill = [&](int nt, int nb) {  // pair nt into buffers nb
             const int ny = nt / bxn, nx = nt - ny * bxn;
-            mbar_expect_tx_noted(bar_s + nb, 2 * S::BYTES);
+            mbar_expect_tx_noted(bar_s + nb, 2 * S::BYTES, iss);
             tma_load_3d(buf + nb * (BW * BH), &a.tsx, nx * BW, ny * BH, (int)plane, bar_s + nb);
             tma_load_3d(buf + (NB + nb) * (BW * BH), &a.tsg, nx * BW, ny * BH, (int)plane,
                         bar_s + nb);
@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
         }
         fence_mbar_init();
     }
-    if (leader) mbar_track_init();
+    Issued iss;  // phases the leader opened (for the drain after a timeout)
     volatile int* s_abort = reinterpret_cast<volatile int*>(sm + a.o_bar + 26);  // a wait timed out
     if (leader) *s_abort = 0;
     __syncthreads();
@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
             // the first full-resolution tile pair, in flight during the deep levels, and the
             // first box pairs of the level-2 sweep
             fence_proxy_async_smem();
-            mbar_expect_tx_noted(bar, BYTES);
+            mbar_expect_tx_noted(bar, BYTES, iss);
             tma_load_3d(sm + a.o_rawx, &a.tmx, -XBox<K, T>::XOFF, -2 * R, (int)plane, bar);
             tma_load_3d(sm + a.o_rawg, &a.tmg, 0, 0, (int)plane, bar);
             if (a.L >= 2) {
@@ -489,7 +489,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
                 T* buf = reinterpret_cast<T*>(sm + a.o_xb);
                 for (int t = 0; t < a.nsw && t < nbox; ++t) {
                     const int ny = t / bxn, nx = t - ny * bxn;
-                    mbar_expect_tx_noted(bar_s + t, 2 * S::BYTES);
+                    mbar_expect_tx_noted(bar_s + t, 2 * S::BYTES, iss);
                     tma_load_3d(buf + t * (BW * BH), &a.tsx, nx * BW, ny * BH, (int)plane,
                                 bar_s + t);
                     tma_load_3d(buf + (a.nsw + t) * (BW * BH), &a.tsg, nx * BW, ny * BH,
@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
         // ---- deep levels l = 2..L: band pair pp = tid / 128, 2x4 block per thread ----
         if (a.L >= 2) {
             if (!dw_sweep<T, FAST>(a, xp, gp, sm, u2x, u2g, bar_s, bar_e, ph_s, ph_e, s_abort,
-                                   plane)) {
+                                   plane, iss)) {
                 failed = true;
                 break;
             }
@@ -667,7 +667,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
             }
             if (use_tma && leader && t + 1 < ntiles) {
                 const int ny = (t + 1) / tiles_x, nx = (t + 1) - ny * tiles_x, nb = rb ^ 1;
-                mbar_expect_tx_noted(bar + nb, BYTES);
+                mbar_expect_tx_noted(bar + nb, BYTES, iss);
                 tma_load_3d(sm + a.o_rawx + nb * a.rawx_f, &a.tmx, nx * kTile - XBox<K, T>::XOFF,
                             ny * kTile - 2 * R, (int)plane, bar + nb);
                 tma_load_3d(sm + a.o_rawg + nb * a.rawg_f, &a.tmg, nx * kTile, ny * kTile,
@@ -741,7 +741,9 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
     }
     if (failed && leader) {
         if (a.err != nullptr) atomicExch(a.err, kErrTmaTimeout);
-        mbar_drain_issued(kWaitLimitNs);  // copies still in flight land before the CTA leaves
+        // copies in flight land before the CTA leaves: the tile pairs and the sweep pairs
+        // (the release barriers take no copies)
+        if (use_tma) mbar_drain_issued(iss, 0x3u | (((1u << a.nsw) - 1u) << 2), kWaitLimitNs);
     }
 }
 
