@@ -376,6 +376,27 @@ __device__ __forceinline__ void deep_group_filter(const FwdArgs& a, const float*
     }
 }
 
+// Levels 3..L summed once at level-3 resolution, in place over Z^(3): quadruple (i3, j3)
+// becomes Eq. 7's sum over levels 3..L at its four level-2 children (a, b) = (0,0), (0,1),
+// (1,0), (1,1), so that a level-2 position reads one value instead of L - 2 quadruples.
+__device__ __forceinline__ void deep_cascade(const FwdArgs& a, float* deep) {
+    const int H3 = a.Hp >> 3, W3 = a.Wp >> 3;
+    float4* z3 = reinterpret_cast<float4*>(deep + a.o_zl[3]);
+    for (int p = threadIdx.x; p < H3 * W3; p += kFT) {
+        const int i3 = p / W3, j3 = p - i3 * W3;
+        float v = 0.f;
+        for (int m = 4; m <= a.L; ++m) {
+            const int sh = m - 3, Wm = a.Wp >> m;
+            const float4 zm =
+                reinterpret_cast<const float4*>(deep + a.o_zl[m])[(i3 >> sh) * Wm + (j3 >> sh)];
+            v += synth_rt(zm, (i3 >> (m - 4)) & 1, (j3 >> (m - 4)) & 1);
+        }
+        const float4 z = z3[p];
+        z3[p] = make_float4(synth<0, 0>(z) + v, synth<0, 1>(z) + v, synth<1, 0>(z) + v,
+                            synth<1, 1>(z) + v);
+    }
+}
+
 // A TMA-staged level-2 tile ([BT][BT] quadruples (LL, LH, HL, HH), zero outside the level
 // grid) into the two band-pair tiles.
 template <int K>
@@ -450,6 +471,7 @@ __device__ __forceinline__ bool deep_levels(const FwdArgs& a, float* sm, float* 
                 } else {
                     deep_stage<K>(a, u2, sm, deep, l, ti0, tj0);
                 }
+                if (l == 2 && ti0 == 0 && tj0 == 0 && a.L >= 3) deep_cascade(a, deep);
                 if (l == 2 && tma2) {
                     if (__syncthreads_or(!ok)) return false;
                 } else {
@@ -514,13 +536,10 @@ __device__ __forceinline__ bool deep_levels(const FwdArgs& a, float* sm, float* 
                         const float2 za = *reinterpret_cast<const float2*>(zc);
                         const float2 zb = *reinterpret_cast<const float2*>(zc + ZTILE);
                         const float4 z = make_float4(za.x, za.y, zb.x, zb.y);
-                        float v = 0.f;
-                        for (int m = 3; m <= a.L; ++m) {
-                            const int sh = m - 2, Wm = a.Wp >> m;
-                            const float4 zm = reinterpret_cast<const float4*>(deep + a.o_zl[m])
-                                [(i2 >> sh) * Wm + (j2 >> sh)];
-                            v += synth_rt(zm, (i2 >> (m - 3)) & 1, (j2 >> (m - 3)) & 1);
-                        }
+                        const float v = (a.L >= 3)
+                            ? deep[a.o_zl[3] + 4 * ((i2 >> 1) * (a.Wp >> 3) + (j2 >> 1)) +
+                                   2 * (i2 & 1) + (j2 & 1)]
+                            : 0.f;
                         dsum[(size_t)i2 * Wl + j2] =
                             make_float4(synth<0, 0>(z) + v, synth<0, 1>(z) + v,
                                         synth<1, 0>(z) + v, synth<1, 1>(z) + v);
