@@ -62,6 +62,7 @@ struct FwdArgs {
     int o_dz;        // the deep levels' filtered level-2 pairs (floats)
     int car2;        // the carrier X^(2) is kept in the deep state (else re-read from u2)
     int o_u;         // level-2 tiles are TMA-staged here (over the carriers), or -1
+    int small2;      // levels L..2 all fit one stacked round (small planes; L >= 3)
     // deep-level state, in shared memory or (deep_global) in the CTA's workspace slot:
     int deep_global;
     int o_car[kMaxLevels + 1];                    // carriers X^(l), l = 2..L-1
@@ -280,16 +281,16 @@ __device__ __forceinline__ void deep_stage(const FwdArgs& a, const float* u2, fl
 }
 
 // Small deep levels share one stage/filter round. A group is the levels l, l-1, ..., lo >= 3
-// whose grids fit one output tile, stacked in the band-pair tiles: level m takes
-// 2 ceil(Hm/2) + 2R rows from row offset off_m and 4 ceil(Wm/4) + 2R columns, exactly the
-// cells its 2x4-block filter reads; the stack fits the tile's BT rows and the blocks of all
-// its levels fit one pass of the CTA's threads. Returns lo (lo = l + 1: no group, level l
-// is filtered tile by tile).
-template <int K>
+// (>= 2 with L2: small planes, below) whose grids fit one output tile, stacked in the
+// band-pair tiles: level m takes 2 ceil(Hm/2) + 2R rows from row offset off_m and
+// 4 ceil(Wm/4) + 2R columns, exactly the cells its 2x4-block filter reads; the stack fits
+// the tile's BT rows and the blocks of all its levels fit one pass of the CTA's threads.
+// Returns lo (lo = l + 1: no group, level l is filtered tile by tile).
+template <int K, bool L2 = false>
 __device__ __forceinline__ int deep_group(const FwdArgs& a, int l) {
     constexpr int R = FG<K>::R, BT = FG<K>::BT;
     int lo = l + 1, rows = 0, blocks = 0;
-    for (int m = l; m >= 3; --m) {
+    for (int m = l; m >= (L2 ? 2 : 3); --m) {
         const int Hm = a.Hp >> m, Wm = a.Wp >> m;
         if (Hm > kCT || Wm > kCT) break;
         const int nbi = (Hm + 1) >> 1, nbj = (Wm + 3) >> 2;
@@ -304,8 +305,9 @@ __device__ __forceinline__ int deep_group(const FwdArgs& a, int l) {
 }
 
 // Stage a group (levels l..lo): every level's subbands, transformed from its carrier
-// X^(m-1) by Eq. 5, with an R halo and zeros outside its grid.
-template <int K>
+// X^(m-1) by Eq. 5 (with L2, level 2 read from the sweep's stored subbands), with an R halo
+// and zeros outside its grid.
+template <int K, bool L2 = false>
 __device__ __forceinline__ void deep_group_stage(const FwdArgs& a, const float* u2,
                                                  const float* deep, float* bs, int l, int lo) {
     constexpr int R = FG<K>::R;
@@ -320,8 +322,12 @@ __device__ __forceinline__ void deep_group_stage(const FwdArgs& a, const float* 
             const int gi = si - R, gj = sj - R;
             float4 u = f4_zero();
             if (gi >= 0 && gi < Hm && gj >= 0 && gj < Wm) {
-                const float4 q = carrier_block(u2, cp, gi, gj, Wp);
-                u = haar_u(q.x, q.y, q.z, q.w);
+                if (L2 && m == 2) {
+                    u = __ldcg(reinterpret_cast<const float4*>(u2) + (size_t)gi * Wm + gj);
+                } else {
+                    const float4 q = carrier_block(u2, cp, gi, gj, Wp);
+                    u = haar_u(q.x, q.y, q.z, q.w);
+                }
             }
             float* q = bs + (off + si) * PROW + 4 * pchunk(sj >> 1, PHALF) + 2 * (sj & 1);
             *reinterpret_cast<float2*>(q) = make_float2(u.x, u.y);
@@ -332,11 +338,12 @@ __device__ __forceinline__ void deep_group_stage(const FwdArgs& a, const float* 
 }
 
 // Filter a staged group: thread t takes one 2x4 block of one band pair of one level (the
-// levels' blocks numbered one after another), and writes its Z^(m) quadruples.
-template <int K>
+// levels' blocks numbered one after another), and writes its Z^(m) quadruples (with L2,
+// level 2's into the filtered level-2 pair tiles zs, which the deep sums read).
+template <int K, bool L2 = false>
 __device__ __forceinline__ void deep_group_filter(const FwdArgs& a, const float* bs,
                                                   const float* wsm, float* deep, int l,
-                                                  int lo) {
+                                                  int lo, float* zs = nullptr) {
     constexpr int R = FG<K>::R;
     constexpr int PROW = PG<K>::PROW, PTILE = PG<K>::PTILE, WS = PG<K>::WS;
     int t = threadIdx.x, off = 0, lev = 0, Hm = 0, Wm = 0, nbj = 1, nb = 1;
@@ -363,8 +370,26 @@ __device__ __forceinline__ void deep_group_filter(const FwdArgs& a, const float*
     f2x acc[2][4];
     conv_pair_2x4<K>(bs + pp * PTILE + (off + 2 * bi) * PROW, bj,
                      wsm + (1 + 2 * (lev - 1) + pp) * WS, acc);
-    float* zl = deep + a.o_zl[lev];
     const int gi0 = 2 * bi, gj0 = 4 * bj;
+    if constexpr (L2) {
+        if (lev == 2) {
+            constexpr int ZROW = PG<K>::ZROW, ZTILE = PG<K>::ZTILE;
+#pragma unroll
+            for (int o = 0; o < 2; ++o) {
+                if (gi0 + o >= Hm) continue;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int j = gj0 + q;
+                    if (j < Wm)
+                        *reinterpret_cast<float2*>(zs + pp * ZTILE + (gi0 + o) * ZROW +
+                                                   4 * zunit(j >> 1) + 2 * (j & 1)) =
+                            upk2(acc[o][q]);
+                }
+            }
+            return;
+        }
+    }
+    float* zl = deep + a.o_zl[lev];
 #pragma unroll
     for (int o = 0; o < 2; ++o) {
         if (gi0 + o >= Hm) continue;
@@ -394,6 +419,38 @@ __device__ __forceinline__ void deep_cascade(const FwdArgs& a, float* deep) {
         const float4 z = z3[p];
         z3[p] = make_float4(synth<0, 0>(z) + v, synth<0, 1>(z) + v, synth<1, 0>(z) + v,
                             synth<1, 1>(z) + v);
+    }
+}
+
+// Small planes (the host sets small2 when levels L..2, L >= 3, all fit one stacked round):
+// the whole deep phase in one stage/filter round, level 2 included, then Eq. 7's sum over
+// levels 2..L at level-1 resolution into the scratch slot: levels 3..L cascaded into Z^(3),
+// then every level-2 position, as in the tiled level-2 pass below. Out of line, so that the
+// kernel's other paths keep their own code.
+template <int K>
+__device__ __noinline__ void small_deep_round(const FwdArgs& a, const float* u2, float* deep,
+                                              float* sm, float* zslot) {
+    constexpr int ZROW = PG<K>::ZROW, ZTILE = PG<K>::ZTILE;
+    float* bs = sm + a.o_b;
+    float* zs = sm + a.o_dz;
+    deep_group_stage<K, true>(a, u2, deep, bs, a.L, 2);
+    __syncthreads();
+    deep_group_filter<K, true>(a, bs, sm + a.o_w, deep, a.L, 2, zs);
+    __syncthreads();
+    deep_cascade(a, deep);
+    __syncthreads();
+    float4* dsum = reinterpret_cast<float4*>(zslot);
+    const int H2 = a.Hp >> 2, W2 = a.Wp >> 2;
+    for (int p = threadIdx.x; p < H2 * W2; p += kFT) {
+        const int i2 = p / W2, j2 = p - i2 * W2;
+        const float* zc = zs + i2 * ZROW + 4 * zunit(j2 >> 1) + 2 * (j2 & 1);
+        const float2 za = *reinterpret_cast<const float2*>(zc);
+        const float2 zb = *reinterpret_cast<const float2*>(zc + ZTILE);
+        const float4 z = make_float4(za.x, za.y, zb.x, zb.y);
+        const float v = deep[a.o_zl[3] + 4 * ((i2 >> 1) * (a.Wp >> 3) + (j2 >> 1)) +
+                             2 * (i2 & 1) + (j2 & 1)];
+        dsum[p] = make_float4(synth<0, 0>(z) + v, synth<0, 1>(z) + v, synth<1, 0>(z) + v,
+                              synth<1, 1>(z) + v);
     }
 }
 
@@ -442,6 +499,10 @@ __device__ __forceinline__ bool deep_levels(const FwdArgs& a, float* sm, float* 
     };
     bool ok = true;
     deep_carriers(a, u2, deep);
+    if (a.small2) {
+        small_deep_round<K>(a, u2, deep, sm, zslot);
+        return true;
+    }
     for (int l = a.L; l >= 2; --l) {
         const int Hl = a.Hp >> l, Wl = a.Wp >> l;
         if (l >= 3) {
@@ -988,6 +1049,25 @@ void fwd_layout(FwdArgs& a, int L, int hp, int wp, int nbs, int car2, int stage_
     }
 }
 
+// Whether levels L..2 (L >= 3) all fit one stacked round (the kernel's small_deep_round):
+// every grid within one output tile, the stack within its BT rows and one 2x4 block of every
+// level and band pair per thread.
+template <int K>
+bool small2_fits(int L, int hp, int wp) {
+    if (L < 3) return false;
+    constexpr int R = FG<K>::R, BT = FG<K>::BT;
+    int rows = 0, blocks = 0;
+    for (int m = L; m >= 2; --m) {
+        const int Hm = hp >> m, Wm = wp >> m;
+        if (Hm > kCT || Wm > kCT) return false;
+        const int nbi = (Hm + 1) >> 1, nbj = (Wm + 3) >> 2;
+        rows += 2 * nbi + 2 * R;
+        blocks += 2 * nbi * nbj;
+        if (rows > BT || blocks > kFT) return false;
+    }
+    return true;
+}
+
 template <int K, typename T>
 FwdPlan fwd_plan(const wt_desc& d) {
     FwdPlan p;
@@ -1042,6 +1122,7 @@ FwdPlan fwd_plan(const wt_desc& d) {
         }
     }
     if (deep == 0) a.deep_global = 0;
+    a.small2 = small2_fits<K>(L, hp, wp) ? 1 : 0;
     p.smem = (size_t)total * sizeof(float);
     // per CTA: deep sums and level-2 subbands, each [H/4][W/4][4] fp32 (+ the deep state)
     a.zd_slot = (L >= 2) ? ((4LL * (hp >> 2) * (wp >> 2) + 63) & ~63LL) : 0;

@@ -119,6 +119,9 @@ GROUP = [  # small deep levels sharing one stage/filter round (stacked in the ti
     (1, 2, 128, 128, 7, 5, "bf16"),   # k = 7: larger halos, fewer levels per round
     (1, 2, 128, 128, 1, 6, "f32"),    # k = 1: no halo
     (2, 3, 112, 80, 3, 6, "bf16"),    # padded plane (general kernels)
+    (1, 2, 128, 96, 5, 4, "f32"),     # forward: level 2 (32x24) alone in a compact round
+    (2, 3, 56, 56, 5, 3, "f32"),      # forward: levels 3 and 2 in one round (fp32 gate)
+    (2, 2, 40, 72, 3, 4, "f32"),      # forward: levels 4..2 in one round, non-square
 ]
 
 
