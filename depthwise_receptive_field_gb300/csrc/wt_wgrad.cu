@@ -467,6 +467,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
     // planes: first blockIdx.x, then whichever is next in the shared counter (planes are
     // independent, so the order does not change any result), else a fixed stride
     int* s_next = reinterpret_cast<int*>(sm + a.o_bar + 24);
+    int ticket = 0;  // the leader's reservation of the plane after the current one
     for (long long plane = blockIdx.x; plane < a.planes;) {
         const int n = (int)(plane / a.C), c = (int)(plane - (long long)n * a.C);
         const T* xp = reinterpret_cast<const T*>(a.x) + plane * plane_elems;
@@ -475,6 +476,9 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
         // ordered before the TMA writes issued below and during this plane
         fence_proxy_async_smem();
         __syncthreads();
+        // the plane after this one is reserved now; the atomic's latency hides behind the
+        // plane's work (its result is read only at the end of the plane)
+        if (leader && a.next != nullptr) ticket = atomicAdd(a.next, 1);
         for (int e = tid; e < a.KP; e += kDT) acc_sm[e] = 0.f;
         if (use_tma && leader) {
             // the first full-resolution tile pair, in flight during the deep levels, and the
@@ -735,7 +739,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
         float* out = a.part + ((size_t)c * a.N + n) * a.KP;
         for (int e = tid; e < a.KP; e += kDT) out[e] = acc_sm[e];
         if (leader)
-            *s_next = (a.next != nullptr) ? (int)gridDim.x + atomicAdd(a.next, 1) : -1;
+            *s_next = (a.next != nullptr) ? (int)gridDim.x + ticket : -1;
         __syncthreads();
         plane = (a.next != nullptr) ? (long long)*s_next : plane + gridDim.x;
     }
