@@ -532,8 +532,9 @@ def run_ours(args, wl):
 
     case = Case(wl, dev)
     # the end-to-end figure first, before any other GPU work of this process: taken after
-    # the device-resident timing it came out at twice its copy bound on this pool's boxes,
-    # alone it runs at the bound (the step's copies are the bottleneck, not the kernels)
+    # the device-resident timing it came out at about twice its copy bound on the GB300
+    # machines measured, taken first it runs at the bound (the step's copies are the
+    # bottleneck, not the kernels)
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, wl, case.inp, case.p, case.f, case.desc, case.buf, case.bufn,

@@ -116,16 +116,25 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 }
 
 // Wait for the phase of `bar` with the given parity to complete; false once `limit_ns`
-// nanoseconds have passed without it. With a limit shorter than the default (only a test
-// sets one) the wait probes without suspending, since try_wait's own suspension could
-// outlast a short limit and hide it.
+// nanoseconds have passed without it. A limit shorter than the default (only a test sets
+// one) is counted in SM clock cycles, checked before every non-suspending probe:
+// %globaltimer advances in steps of up to a microsecond and try_wait may suspend the
+// thread for a while, either of which could outlast a short limit and hide it. At SM clocks
+// of 1 GHz or more, that many cycles last no longer than that many nanoseconds; a limit
+// shorter than one clock64 read gives up before the first probe, whether or not the copy
+// has landed.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   unsigned long long limit_ns) {
-    const bool probe = limit_ns < kWaitLimitNs;
-    if (!probe && mbar_try_wait(bar, parity)) return true;
+    if (limit_ns < kWaitLimitNs) {
+        const long long c0 = clock64();
+        while ((unsigned long long)(clock64() - c0) < limit_ns)
+            if (mbar_test_wait(bar, parity)) return true;
+        return false;
+    }
+    if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     while (true) {
-        if (probe ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }

@@ -19,6 +19,11 @@ extern "C" {
 /*
  * Sets the limit of every bounded wait of the kernels launched afterwards by any host
  * thread, in nanoseconds; 0 restores the default (1 s). Process-wide; meant for tests only.
+ * A limit below the default is counted in SM clock cycles (the device's nanosecond timer
+ * advances in steps of up to a microsecond, too coarse for a short limit), which at SM
+ * clocks of 1 GHz or more last no longer than the nanoseconds asked for, and is checked
+ * before each probe of the barrier: with a limit of 1, every wait runs out at once, whether
+ * or not its copy has landed, so the first wait of every CTA reports a timeout.
  * The bounded wait for in-flight copies that a CTA performs before it leaves after a
  * timeout always keeps the default limit. Returns WT_OK.
  */

@@ -1,12 +1,13 @@
 """The kernels' bounded waits: a wait that runs out is reported, not hidden.
 
 Every data load of the plane kernels completes on an mbarrier whose wait is bounded. Here
-the test hook shortens that bound to 1 ns, so that waits run out while their copies are
-still in flight (nothing faults or hangs: every CTA that gives up first waits, with the
-normal bound, for the copies it issued, then leaves). The test checks that each kind of
-call reports its timeout through wtconv_workspace_status, that backward-weight turns it
-into NaN gradients, and that the next ordinary calls on the same workspace are bit-identical
-to a clean run and report no timeout.
+the test hook shortens that bound to 1 (a short limit counts SM cycles and is checked
+before each probe), so that every wait runs out at once, its copies possibly still in
+flight (nothing faults or hangs: every CTA that gives up first waits, with the normal
+bound, for the copies it issued, then leaves). The test checks that each kind of call
+reports its timeout through wtconv_workspace_status, that backward-weight turns it into NaN
+gradients, and that the next ordinary calls on the same workspace are bit-identical to a
+clean run and report no timeout.
 """
 import numpy as np
 import pytest

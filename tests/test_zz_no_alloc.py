@@ -6,9 +6,9 @@ must not call cudaMalloc because it may synchronize the device. Its scratch is a
 4 MiB array inside the library, shared by every call. These tests call it through the C ABI
 twice in a row (the second call finds the first call's leftovers in the array) and check
 each result against the ordinary workspace entry point on the same inputs, within the
-parameter-gradient tolerance used by the parity tests, and once against the oracle. This
-file sorts last so that a run stopping at the first failure has already run every other
-test.
+parameter-gradient tolerance used by the parity tests, and once against the oracle; a
+forced timeout inside its plane kernel must come back as NaN gradients. This file sorts
+last so that a run stopping at the first failure has already run every other test.
 """
 import numpy as np
 import pytest
@@ -104,3 +104,29 @@ def test_noalloc_rejects_shapes_beyond_its_scratch(n, c, h, w, k, L, dtype):
                                          g["dsl"])
     assert ei.value.status == B.WT_ERR_WORKSPACE
     torch.cuda.synchronize()
+
+
+def test_noalloc_reports_a_timed_out_wait_as_nan_gradients():
+    """With the kernels' bounded waits shortened to 1 (the test hook; a short limit counts SM
+    cycles and is checked before each probe), the plane kernel's waits run out at once; the status word in the fixed array turns
+    every gradient into NaN, and the next ordinary call (which clears the word) agrees with
+    the workspace path again."""
+    wl = shape_workload(8, 32, 128, 128, 5, 4, "bf16", seed=123)
+    inp = make_inputs(wl, bias_and_scale=True)
+    dev = torch.device("cuda", 0)
+    p = layer.Params.from_inputs(inp, dev)
+    x = inp["x"].to(dev)
+    dy = inp["dy"].to(dev)
+    ref = layer.backward_weight(x, dy, p)
+    desc = B.desc_like(x, p.k, wl.levels)
+    B.wtconv_testing_set_wait_limit_ns(1)
+    try:
+        bad = _noalloc(desc, x, dy, p, ref)
+    finally:
+        B.wtconv_testing_set_wait_limit_ns(0)
+    for name in ("dw0", "db0", "ds0", "dwl", "dsl"):
+        assert torch.isnan(bad[name]).all(), name
+    good = _noalloc(desc, x, dy, p, ref)
+    for name in ("dw0", "db0", "ds0", "dwl", "dsl"):
+        err = rel_err(good[name].double().cpu().numpy(), ref[name].double().cpu().numpy())
+        assert err <= TOL_PARAM["bf16"], (name, err)
