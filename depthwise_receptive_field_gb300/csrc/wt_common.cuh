@@ -126,7 +126,9 @@ namespace wt {
 
 // ---------------------------------------------------------------------------------
 // Packed fp32 pairs (sm_100+ f32x2 arithmetic): two independent lanes of work per
-// instruction, halving the issue slots of the FMA-bound loops.
+// instruction on an aligned register pair. Where the operands of a loop are not pairs
+// already (a window read at odd pixel offsets), building them costs moves that scalar
+// FMAs do not need; the base loops measured faster scalar for k >= 5.
 // ---------------------------------------------------------------------------------
 typedef unsigned long long f2x;
 
@@ -154,6 +156,15 @@ __device__ __forceinline__ f2x sub2(f2x a, f2x b) {
     f2x d;
     asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
+}
+// Scalar acc.lo += a * b on the low lane of a packed accumulator (the high lane is kept).
+__device__ __forceinline__ void fma_lo(f2x& acc, float a, float b) {
+    asm("{\n\t.reg .f32 lo, hi;\n\t"
+        "mov.b64 {lo, hi}, %0;\n\t"
+        "fma.rn.f32 lo, %1, %2, lo;\n\t"
+        "mov.b64 %0, {lo, hi};\n\t}"
+        : "+l"(acc)
+        : "f"(a), "f"(b));
 }
 
 }  // namespace wt

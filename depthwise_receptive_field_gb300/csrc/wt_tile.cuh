@@ -271,94 +271,159 @@ __device__ __forceinline__ void load_raw_vec(const T* p, float (&v)[N]) {
     for (int i = 0; i < N; ++i) v[i] = e[S - A0 + i];
 }
 
-// Packed base k x k filter of the 4x4 pixel block (by, bx) of a tile, read from the raw tile
+// Base k x k filter of the 4x4 pixel block (by, bx) of a tile, read from the raw tile
 // (widened in registers), accumulating onto acc[o][p] = (pixel (o, 2p), pixel (o, 2p+1)).
 // Window row r is raw row 4by + R + r; window column j is raw column 4bx + XOFF - R + j.
-// wdup = KK taps as (w, w) pairs.
+// wdup = KK taps as (w, w) pairs. Scalar FMAs for k >= 5 (the packed form would pair the
+// window at odd offsets with moves: measured 14% slower at k = 5, 11% at k = 7), packed
+// for k <= 3 (4% faster there).
 template <int K, typename T>
 __device__ __forceinline__ void conv_base_4x4_raw(const T* raw, int by, int bx,
                                                   const float* wdup, f2x (&acc)[4][2]) {
     constexpr int R = FG<K>::R, KK = FG<K>::KK;
     constexpr int RW = XBox<K, T>::XBW, S = XBox<K, T>::XOFF - R;
     constexpr int NV = 4 + 2 * R;
-    f2x w[KK];
-#pragma unroll
-    for (int q = 0; q + 1 < KK; q += 2) {
-        const float4 t = *reinterpret_cast<const float4*>(wdup + 2 * q);
-        w[q] = pk2(t.x, t.y);
-        w[q + 1] = pk2(t.z, t.w);
-    }
-    if constexpr (KK & 1) {
-        const float2 t = *reinterpret_cast<const float2*>(wdup + 2 * (KK - 1));
-        w[KK - 1] = pk2(t.x, t.y);
-    }
     const T* base = raw + (4 * by + R) * RW + 4 * bx;
+    if constexpr (K >= 5) {
+        float w[KK];
 #pragma unroll
-    for (int r = 0; r < 4 + 2 * R; ++r) {
-        float v[NV];
-        load_raw_vec<T, NV, S>(base + r * RW, v);
-        f2x A[NV / 2], B[NV / 2 - 1];
+        for (int q = 0; q + 1 < KK; q += 2) {
+            const float4 t = *reinterpret_cast<const float4*>(wdup + 2 * q);
+            w[q] = t.x;
+            w[q + 1] = t.z;
+        }
+        if constexpr (KK & 1) w[KK - 1] = wdup[2 * (KK - 1)];
+        float a[4][4];
 #pragma unroll
-        for (int m = 0; m < NV / 2; ++m) A[m] = pk2(v[2 * m], v[2 * m + 1]);
+        for (int o = 0; o < 4; ++o) {
+            const float2 lo = upk2(acc[o][0]), hi = upk2(acc[o][1]);
+            a[o][0] = lo.x; a[o][1] = lo.y; a[o][2] = hi.x; a[o][3] = hi.y;
+        }
 #pragma unroll
-        for (int m = 0; m < NV / 2 - 1; ++m) B[m] = pk2(v[2 * m + 1], v[2 * m + 2]);
-        // taps outermost: consecutive packed FMAs update different accumulators
+        for (int r = 0; r < 4 + 2 * R; ++r) {
+            float v[NV];
+            load_raw_vec<T, NV, S>(base + r * RW, v);
+            // taps outermost: consecutive FMAs update different accumulators
 #pragma unroll
-        for (int vv = 0; vv < K; ++vv)
+            for (int vv = 0; vv < K; ++vv)
 #pragma unroll
-            for (int o = 0; o < 4; ++o) {
-                const int u = r - o;
-                if (u < 0 || u >= K) continue;
+                for (int o = 0; o < 4; ++o) {
+                    const int u = r - o;
+                    if (u < 0 || u >= K) continue;
 #pragma unroll
-                for (int pp = 0; pp < 2; ++pp) {
-                    const int idx = 2 * pp + vv;
-                    const f2x in = (idx & 1) ? B[(idx - 1) >> 1] : A[idx >> 1];
-                    acc[o][pp] = fma2(w[u * K + vv], in, acc[o][pp]);
+                    for (int q = 0; q < 4; ++q) a[o][q] = fmaf(w[u * K + vv], v[q + vv], a[o][q]);
                 }
-            }
+        }
+#pragma unroll
+        for (int o = 0; o < 4; ++o) {
+            acc[o][0] = pk2(a[o][0], a[o][1]);
+            acc[o][1] = pk2(a[o][2], a[o][3]);
+        }
+    } else {
+        f2x w[KK];
+#pragma unroll
+        for (int q = 0; q + 1 < KK; q += 2) {
+            const float4 t = *reinterpret_cast<const float4*>(wdup + 2 * q);
+            w[q] = pk2(t.x, t.y);
+            w[q + 1] = pk2(t.z, t.w);
+        }
+        if constexpr (KK & 1) {
+            const float2 t = *reinterpret_cast<const float2*>(wdup + 2 * (KK - 1));
+            w[KK - 1] = pk2(t.x, t.y);
+        }
+#pragma unroll
+        for (int r = 0; r < 4 + 2 * R; ++r) {
+            float v[NV];
+            load_raw_vec<T, NV, S>(base + r * RW, v);
+            f2x A[NV / 2], B[NV / 2 - 1];
+#pragma unroll
+            for (int m = 0; m < NV / 2; ++m) A[m] = pk2(v[2 * m], v[2 * m + 1]);
+#pragma unroll
+            for (int m = 0; m < NV / 2 - 1; ++m) B[m] = pk2(v[2 * m + 1], v[2 * m + 2]);
+#pragma unroll
+            for (int vv = 0; vv < K; ++vv)
+#pragma unroll
+                for (int o = 0; o < 4; ++o) {
+                    const int u = r - o;
+                    if (u < 0 || u >= K) continue;
+#pragma unroll
+                    for (int pp = 0; pp < 2; ++pp) {
+                        const int idx = 2 * pp + vv;
+                        const f2x in = (idx & 1) ? B[(idx - 1) >> 1] : A[idx >> 1];
+                        acc[o][pp] = fma2(w[u * K + vv], in, acc[o][pp]);
+                    }
+                }
+        }
     }
 }
 
-// Packed base weight-gradient correlation of the 4x4 pixel block (by, bx), read from the raw
-// tiles and widened in registers: X in the layout above (window row r is raw row
-// 4by + R + r, window column j raw column 4bx + XOFF - R + j) and the 64x64 dY tile.
-// With g[o][p] = (dY[o][2p], dY[o][2p+1]), acc[u*K+v] accumulates the even- and odd-column
-// partial sums of sum_{o,q} dY[o][q] X[o+u][q+v] (add the two halves at the end).
+// Base weight-gradient correlation of the 4x4 pixel block (by, bx), read from the raw tiles
+// and widened in registers: X in the layout above (window row r is raw row 4by + R + r,
+// window column j raw column 4bx + XOFF - R + j) and the 64x64 dY tile. acc[u*K+v]
+// accumulates sum_{o,q} dY[o][q] X[o+u][q+v] over its two lanes (add them at the end):
+// with 16-bit I/O and k = 5 all of it in the low lane by scalar FMAs (the packed form pairs
+// the window at odd offsets with moves: measured 9% slower in isolation, 2.7% on the whole
+// 16x256x256x256 backward-weight), else the even and odd columns packed,
+// g[o][p] = (dY[o][2p], dY[o][2p+1]) (at k = 7, whose kernel runs one CTA per SM with
+// twice the accumulators, the scalar form measured 6% slower; fp32 and k = 3 gain nothing).
 template <int K, typename T>
 __device__ __forceinline__ void corr_base_4x4_raw(const T* rawx, const T* rawg, int by, int bx,
                                                   f2x (&acc)[K * K]) {
     constexpr int R = FG<K>::R;
     constexpr int RW = XBox<K, T>::XBW, S = XBox<K, T>::XOFF - R;
     constexpr int NV = 4 + 2 * R;
-    f2x g[4][2];
-#pragma unroll
-    for (int o = 0; o < 4; ++o) {
-        const float4 t = ld4_smem<T>(rawg + (4 * by + o) * kTile + 4 * bx);
-        g[o][0] = pk2(t.x, t.y);
-        g[o][1] = pk2(t.z, t.w);
-    }
     const T* base = rawx + (4 * by + R) * RW + 4 * bx;
-#pragma unroll
-    for (int r = 0; r < 4 + 2 * R; ++r) {
-        float v[NV];
-        load_raw_vec<T, NV, S>(base + r * RW, v);
-        f2x A[NV / 2], B[NV / 2 - 1];
-#pragma unroll
-        for (int m = 0; m < NV / 2; ++m) A[m] = pk2(v[2 * m], v[2 * m + 1]);
-#pragma unroll
-        for (int m = 0; m < NV / 2 - 1; ++m) B[m] = pk2(v[2 * m + 1], v[2 * m + 2]);
+    if constexpr (K == 5 && sizeof(T) == 2) {
+        float g[4][4];
 #pragma unroll
         for (int o = 0; o < 4; ++o) {
-            const int u = r - o;
-            if (u < 0 || u >= K) continue;
+            const float4 t = ld4_smem<T>(rawg + (4 * by + o) * kTile + 4 * bx);
+            g[o][0] = t.x; g[o][1] = t.y; g[o][2] = t.z; g[o][3] = t.w;
+        }
 #pragma unroll
-            for (int vv = 0; vv < K; ++vv)
+        for (int r = 0; r < 4 + 2 * R; ++r) {
+            float v[NV];
+            load_raw_vec<T, NV, S>(base + r * RW, v);
 #pragma unroll
-                for (int pp = 0; pp < 2; ++pp) {
-                    const int idx = 2 * pp + vv;
-                    const f2x in = (idx & 1) ? B[(idx - 1) >> 1] : A[idx >> 1];
-                    acc[u * K + vv] = fma2(g[o][pp], in, acc[u * K + vv]);
-                }
+            for (int o = 0; o < 4; ++o) {
+                const int u = r - o;
+                if (u < 0 || u >= K) continue;
+#pragma unroll
+                for (int vv = 0; vv < K; ++vv)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) fma_lo(acc[u * K + vv], g[o][q], v[q + vv]);
+            }
+        }
+    } else {
+        f2x g[4][2];
+#pragma unroll
+        for (int o = 0; o < 4; ++o) {
+            const float4 t = ld4_smem<T>(rawg + (4 * by + o) * kTile + 4 * bx);
+            g[o][0] = pk2(t.x, t.y);
+            g[o][1] = pk2(t.z, t.w);
+        }
+#pragma unroll
+        for (int r = 0; r < 4 + 2 * R; ++r) {
+            float v[NV];
+            load_raw_vec<T, NV, S>(base + r * RW, v);
+            f2x A[NV / 2], B[NV / 2 - 1];
+#pragma unroll
+            for (int m = 0; m < NV / 2; ++m) A[m] = pk2(v[2 * m], v[2 * m + 1]);
+#pragma unroll
+            for (int m = 0; m < NV / 2 - 1; ++m) B[m] = pk2(v[2 * m + 1], v[2 * m + 2]);
+#pragma unroll
+            for (int o = 0; o < 4; ++o) {
+                const int u = r - o;
+                if (u < 0 || u >= K) continue;
+#pragma unroll
+                for (int vv = 0; vv < K; ++vv)
+#pragma unroll
+                    for (int pp = 0; pp < 2; ++pp) {
+                        const int idx = 2 * pp + vv;
+                        const f2x in = (idx & 1) ? B[(idx - 1) >> 1] : A[idx >> 1];
+                        acc[u * K + vv] = fma2(g[o][pp], in, acc[u * K + vv]);
+                    }
+            }
         }
     }
 }

@@ -717,7 +717,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
         __syncthreads();
         const int nbase = (a.L == 0) ? 8 : 4;
         for (int e = tid; e <= KK; e += kDT) {
-            // base taps: even + odd column halves of each base warp; e == KK: the sum of dY,
+            // base taps: both lanes of each base warp's accumulators; e == KK: the sum of dY,
             // which every warp holds a share of (it is taken while converting the dY tiles)
             float s = 0.f;
             if (e < KK) {
