@@ -214,12 +214,44 @@ __device__ __forceinline__ float4 carrier_block(const float* u2, const float* cp
     if (cp == nullptr)
         return make_float4(0.5f * __ldcg(u2 + 4 * o), 0.5f * __ldcg(u2 + 4 * (o + 1)),
                            0.5f * __ldcg(u2 + 4 * (o + Wp)), 0.5f * __ldcg(u2 + 4 * (o + Wp + 1)));
-    return make_float4(cp[o], cp[o + 1], cp[o + Wp], cp[o + Wp + 1]);
+    // o and Wp are even and the carriers 16-byte aligned: two 8-byte loads
+    const float2 r0 = *reinterpret_cast<const float2*>(cp + o);
+    const float2 r1 = *reinterpret_cast<const float2*>(cp + o + Wp);
+    return make_float4(r0.x, r0.y, r1.x, r1.y);
 }
 
 // Carriers X^(l) = LL of X^(l-1) (normalized, Eq. 5) for l = 3..L-1, in the deep state.
+// With L >= 5 and X^(2) in the deep state, X^(3) and X^(4) are formed in one pass (an X^(4)
+// value recomputes its four X^(3) parents, with the same operations in the same order),
+// saving a barrier; re-reading X^(2) as LL / 2 of the stored subbands instead would cost
+// more than the barrier.
 __device__ __forceinline__ void deep_carriers(const FwdArgs& a, const float* u2, float* deep) {
-    for (int l = 3; l < a.L; ++l) {
+    int l0 = 3;
+    if (a.L >= 5 && a.car2) {
+        const float* c2 = deep + a.o_car[2];
+        const int W2 = a.Wp >> 2, H3 = a.Hp >> 3, W3 = a.Wp >> 3, H4 = a.Hp >> 4, W4 = a.Wp >> 4;
+        float* c3 = deep + a.o_car[3];
+        float* c4 = deep + a.o_car[4];
+        for (int p = threadIdx.x; p < H3 * W3 + H4 * W4; p += kFT) {
+            if (p < H3 * W3) {
+                const int i = p / W3, j = p - i * W3;
+                const float4 q = carrier_block(u2, c2, i, j, W2);
+                c3[p] = 0.5f * (q.x + q.y + q.z + q.w);
+            } else {
+                const int r = p - H3 * W3, i = r / W4, j = r - i * W4;
+                float x3[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float4 q = carrier_block(u2, c2, 2 * i + (k >> 1), 2 * j + (k & 1), W2);
+                    x3[k] = 0.5f * (q.x + q.y + q.z + q.w);
+                }
+                c4[r] = 0.5f * (x3[0] + x3[1] + x3[2] + x3[3]);
+            }
+        }
+        __syncthreads();
+        l0 = 5;
+    }
+    for (int l = l0; l < a.L; ++l) {
         const int Hl = a.Hp >> l, Wl = a.Wp >> l, Wp = a.Wp >> (l - 1);
         const float* cp = (l >= 4 || a.car2) ? deep + a.o_car[l - 1] : nullptr;
         float* cl = deep + a.o_car[l];
@@ -404,7 +436,33 @@ __device__ __forceinline__ void deep_group_filter(const FwdArgs& a, const float*
 // Levels 3..L summed once at level-3 resolution, in place over Z^(3): quadruple (i3, j3)
 // becomes Eq. 7's sum over levels 3..L at its four level-2 children (a, b) = (0,0), (0,1),
 // (1,0), (1,1), so that a level-2 position reads one value instead of L - 2 quadruples.
+// Levels 4 and 5 are read through pointers set up once (their offsets are compile-time
+// indices into the argument block); deeper levels, rare, in a loop.
 __device__ __forceinline__ void deep_cascade(const FwdArgs& a, float* deep) {
+    const int H3 = a.Hp >> 3, W3 = a.Wp >> 3, W4 = a.Wp >> 4, W5 = a.Wp >> 5;
+    float4* z3 = reinterpret_cast<float4*>(deep + a.o_zl[3]);
+    const float4* z4 = reinterpret_cast<const float4*>(deep + a.o_zl[4]);
+    const float4* z5 = reinterpret_cast<const float4*>(deep + a.o_zl[5]);
+#pragma unroll 2
+    for (int p = threadIdx.x; p < H3 * W3; p += kFT) {
+        const int i3 = p / W3, j3 = p - i3 * W3;
+        float v = 0.f;
+        if (a.L >= 4) v += synth_rt(z4[(i3 >> 1) * W4 + (j3 >> 1)], i3 & 1, j3 & 1);
+        if (a.L >= 5) v += synth_rt(z5[(i3 >> 2) * W5 + (j3 >> 2)], (i3 >> 1) & 1, (j3 >> 1) & 1);
+        for (int m = 6; m <= a.L; ++m) {
+            const int sh = m - 3, Wm = a.Wp >> m;
+            const float4 zm =
+                reinterpret_cast<const float4*>(deep + a.o_zl[m])[(i3 >> sh) * Wm + (j3 >> sh)];
+            v += synth_rt(zm, (i3 >> (m - 4)) & 1, (j3 >> (m - 4)) & 1);
+        }
+        const float4 z = z3[p];
+        z3[p] = make_float4(synth<0, 0>(z) + v, synth<0, 1>(z) + v, synth<1, 0>(z) + v,
+                            synth<1, 1>(z) + v);
+    }
+}
+
+// The same sum with one loop over the levels (small planes: a few positions, compact code).
+__device__ __forceinline__ void deep_cascade_loop(const FwdArgs& a, float* deep) {
     const int H3 = a.Hp >> 3, W3 = a.Wp >> 3;
     float4* z3 = reinterpret_cast<float4*>(deep + a.o_zl[3]);
     for (int p = threadIdx.x; p < H3 * W3; p += kFT) {
@@ -437,7 +495,7 @@ __device__ __noinline__ void small_deep_round(const FwdArgs& a, const float* u2,
     __syncthreads();
     deep_group_filter<K, true>(a, bs, sm + a.o_w, deep, a.L, 2, zs);
     __syncthreads();
-    deep_cascade(a, deep);
+    deep_cascade_loop(a, deep);
     __syncthreads();
     float4* dsum = reinterpret_cast<float4*>(zslot);
     const int H2 = a.Hp >> 2, W2 = a.Wp >> 2;
