@@ -8,8 +8,9 @@
 //     (several in flight) and turns every 4x4 pixel block into the four subbands of level
 //     2 (§4.1 Eq. 5 twice: the level-1 carrier X^(1), then its Haar transform), stored in
 //     the CTA's scratch slot; LL / 2 of them is the carrier X^(2). Levels l = 3..L then run
-//     from the carriers at their own resolution, and level 2 from the stored subbands: 32x32 output tiles of the subbands are staged with an R-coefficient halo
-//     and filtered by the four folded k x k kernels (§4.3 Eq. 8). A last pass sums Eq. 7's
+//     from the carriers at their own resolution, and level 2 from the stored subbands:
+//     32x32 output tiles of the subbands are staged with an R-coefficient halo and
+//     filtered by the four folded k x k kernels (§4.3 Eq. 8). A last pass sums Eq. 7's
 //     terms of levels 2..L at level-1 resolution (§4.2 Prop. 2: coefficient address by
 //     coordinate shifts, signs by coordinate bits) into the scratch slot.
 //   full-resolution phase -- 64x64-pixel tiles: a TMA load brings the tile of X with a

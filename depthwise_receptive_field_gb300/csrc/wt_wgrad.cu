@@ -13,7 +13,8 @@
 //   level-2 sweep (L >= 2): X and dY stream through shared memory in TMA boxes (2 to 4
 //     box pairs in flight, as shared memory allows); every 4x4 pixel block becomes its
 //     four level-2 subbands (Eq. 5 twice), stored for both tensors in the CTA's
-//     workspace slot (L2-resident); LL / 2 of it is the carrier X^(2), dY^(2) of level 3.
+//     workspace slot (L2-resident while the slots fit in L2); LL / 2 of it is the carrier
+//     X^(2), dY^(2) of level 3.
 //   deep levels (l >= 2): 32x32 tiles of the level's subbands of X (R halo) and dY are
 //     staged as band-pair tiles, (LL, LH) and (HL, HH) (level 2 from the slot, deeper
 //     levels from the carriers); threads 0-127 correlate pair 0 and 128-255 pair 1 with
