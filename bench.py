@@ -885,25 +885,34 @@ def run_e2e(args, wl, inp, p, f, desc, buf, bufn, stream, world, dev) -> dict:
                 h[k].copy_(d[k], non_blocking=True)
         ev["d2h"][j].record(s_d2h)
 
+    # Five blocks of up to 20 steps each, the median block reported and every block listed:
+    # on the shared GB300 hosts single blocks intermittently take up to twice the copy
+    # bound (the two copy directions then stop overlapping) while the link probe right
+    # after is unchanged, so one block alone is a noisy figure.
     steps = max(2, min(args.steps, 20))
     for i in range(3):
         step(i)
     torch.cuda.synchronize()
-    barrier(world)
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(s_h2d)
-    for i in range(steps):
-        step(i)
-    b.record(s_d2h)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(a.elapsed_time(b), world, dev)
+    blocks = []
+    for _ in range(5):
+        barrier(world)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(s_h2d)
+        for i in range(steps):
+            step(i)
+        b.record(s_d2h)
+        torch.cuda.synchronize()
+        blocks.append(max_over_ranks(a.elapsed_time(b), world, dev) / steps)
+    ms_step = sorted(blocks)[len(blocks) // 2]
     link = host_link(xh, sets[0]["x"], hosts[0]["y"], sets[0]["y"], s_h2d, s_d2h)
     bound_ms = max(h2d / (link["h2d_gbs"] * 1e9), d2h / (link["d2h_gbs"] * 1e9),
                    (h2d + d2h) / (link["both_gbs"] * 1e9)) * 1e3
-    return {"value": world * wl.elements * steps / (ms * 1e-3) / 1e9, "unit": "Gelem/s",
+    return {"value": world * wl.elements / (ms_step * 1e-3) / 1e9, "unit": "Gelem/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "ms_per_step": ms / steps,
+            "ms_per_step": ms_step,
+            "blocks_ms_per_step": blocks,
+            "timing": f"median of {len(blocks)} blocks of {steps} steps",
             "pipeline": "H2D, compute and D2H on separate streams; two device buffer sets",
             "host_link": link, "copy_bound_ms_per_step": bound_ms}
 
