@@ -125,7 +125,14 @@ GROUP = [  # small deep levels sharing one stage/filter round (stacked in the ti
 ]
 
 
-@pytest.mark.parametrize("n,c,h,w,k,L,dtype", EDGE + F16 + ODD + LARGE + LAYOUT + GROUP)
+DEEP = [  # the deepest cascades the boundary accepts (L <= 12)
+    (1, 1, 16, 16, 3, 12, "bf16"),    # L = 12: the kernels run on the plane padded to 4096^2
+    (1, 2, 40, 24, 5, 10, "f32"),     # L = 10 on a small non-square plane (padded to 1024^2)
+    (1, 1, 1024, 1024, 3, 10, "bf16"),  # L = 10 on a whole 1024x1024 plane, down to 1x1
+]
+
+
+@pytest.mark.parametrize("n,c,h,w,k,L,dtype", EDGE + F16 + ODD + LARGE + LAYOUT + GROUP + DEEP)
 def test_edge_shapes(n, c, h, w, k, L, dtype):
     wl = shape_workload(n, c, h, w, k, L, dtype, seed=1000 + h + w + k + L)
     errs, _ = run_and_compare(wl, bias_and_scale=True)
