@@ -756,6 +756,78 @@ def run_ablation(args) -> int:
     return 0
 
 
+PHASES_FWD = {0: "plane setup", 1: "level-2 sweep and weights", 2: "carriers",
+              3: "grouped small levels", 4: "level >= 3 stage", 5: "level >= 3 filter, barriers",
+              6: "level-2 tile wait and repack (or stage)", 7: "cascade of levels >= 4 into Z^(3)",
+              8: "level-2 barrier", 9: "level-2 filter", 10: "level-2 deep sums, barrier",
+              11: "end of deep phase", 12: "full-resolution remainder", 13: "plane end",
+              14: "tile wait", 15: "band conversion", 16: "barrier A, next tile issued",
+              17: "level-1 filter", 18: "base filter, synthesis, store"}
+PHASES_DW = {0: "plane setup", 1: "level-2 sweep", 3: "tile pair wait",
+             4: "band conversions, dY sum", 5: "barrier B1, next pair issued",
+             6: "correlations (base | level 1)", 7: "barrier B2", 8: "flush, partial vector",
+             9: "plane end", 10: "grouped small levels", 11: "tiled level stage",
+             12: "tiled level barrier 1", 13: "tiled level correlations",
+             14: "tiled level barrier 2", 15: "tiled level flush"}
+
+
+def run_phase_clocks(args, wl) -> int:
+    """Per-phase clocks of the two plane kernels on one workload: builds the library with the
+    clocks compiled in (a separate build; the ordinary library has none of that code), runs
+    `warmup` + `steps` forward and backward-weight calls, and prints, per kernel, the cycles
+    thread 0 of a CTA spends in each phase per plane and their shares. With two CTAs per SM
+    each CTA is timed while the other runs: the shares say where a CTA's time goes, not what
+    a phase would cost alone. The clocks add a little time; no bench figure comes from this
+    mode."""
+    import torch
+
+    from depthwise_receptive_field_gb300 import binding as B
+    from depthwise_receptive_field_gb300 import build as _build
+    from depthwise_receptive_field_gb300 import layer
+    from depthwise_receptive_field_gb300.inputs import make_inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    B.use_library(_build.build_phase_clocks())
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    inp = make_inputs(wl)
+    x = inp["x"].to(dev)
+    dy = inp["dy"].to(dev)
+    p = layer.Params.from_inputs(inp, dev)
+    desc = B.desc_like(x, p.k, wl.levels)
+    f = layer.fold(p, desc)
+    ws = layer.Workspace(dev)
+    y = torch.empty_like(x)
+    steps = max(1, min(args.steps, 20))
+    for _ in range(max(1, args.warmup)):
+        layer.forward(x, p, f, ws, y)
+        layer.backward_weight(x, dy, p, ws)
+    torch.cuda.synchronize()
+    B.wtconv_debug_phase_clocks(0, reset=True)
+    B.wtconv_debug_phase_clocks(1, reset=True)
+    for _ in range(steps):
+        layer.forward(x, p, f, ws, y)
+        layer.backward_weight(x, dy, p, ws)
+    torch.cuda.synchronize()
+    out = {"mode": "phase_clocks", "workload": wl.name, "steps": steps, "kernels": {}}
+    for kern, names in ((0, PHASES_FWD), (1, PHASES_DW)):
+        v = B.wtconv_debug_phase_clocks(kern)
+        planes = v[31]
+        total = sum(v[:31])
+        rows = {names.get(i, f"phase {i}"): {"cycles_per_plane": v[i] / max(planes, 1),
+                                             "share": v[i] / max(total, 1)}
+                for i in range(31) if v[i]}
+        name = "wt_fwd_plane_kernel" if kern == 0 else "wt_dw_plane_kernel"
+        out["kernels"][name] = {"planes": planes, "cycles_per_plane": total / max(planes, 1),
+                                "phases": rows}
+        print(f"{name}: {planes} planes, {total / max(planes, 1):.0f} cycles per plane (thread 0)")
+        for k, r in rows.items():
+            print(f"  {k:40s} {r['cycles_per_plane']:9.0f}  {100 * r['share']:5.1f}%")
+    print(json.dumps(out))
+    return 0
+
+
 def run_memory(args, wl) -> int:
     """Peak device memory of one training step (fold + forward + backward-data +
     backward-weight through the C ABI), from a clean allocator state: the input X, the
@@ -978,6 +1050,8 @@ def main(argv=None):
                     help="skip the other workloads' per-config figures")
     ap.add_argument("--no-noalloc", action="store_true",
                     help="skip timing the no-workspace backward-weight entry point")
+    ap.add_argument("--phase-clocks", action="store_true",
+                    help="print the plane kernels' per-phase clocks instead (separate build)")
     args = ap.parse_args(argv)
     if args.ablation:
         return run_ablation(args)
@@ -992,6 +1066,8 @@ def main(argv=None):
         raise SystemExit(f"{wl.name} is forward-only; the benchmarked step needs dY")
     if args.memory:
         return run_memory(args, wl)
+    if args.phase_clocks:
+        return run_phase_clocks(args, wl)
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)

@@ -29,7 +29,8 @@ VARIANT_NAMES = {WT_VARIANT_REFERENCE: "reference", WT_VARIANT_FUSED_ANALYSIS: "
 HEADER = os.path.join(_build.INCLUDE, "wtconv.h")
 HEADERS = [HEADER, os.path.join(_build.INCLUDE, "wtconv_ablation.h"),
            os.path.join(_build.INCLUDE, "wtconv_probe.h"),
-           os.path.join(_build.INCLUDE, "wtconv_testing.h")]
+           os.path.join(_build.INCLUDE, "wtconv_testing.h"),
+           os.path.join(_build.INCLUDE, "wtconv_debug.h")]
 
 
 class wt_desc(ctypes.Structure):
@@ -50,6 +51,7 @@ class WTConvError(RuntimeError):
 
 _LOCK = threading.Lock()
 _LIB = None
+_LIB_PATH = None  # None: the ordinary library (build.LIB)
 _vp = ctypes.c_void_p
 _DESC_P = ctypes.POINTER(wt_desc)
 
@@ -67,6 +69,7 @@ _SIGNATURES = {
     "wtconv_fma_probe": [ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp],
     "wtconv_workspace_status": [_vp, _vp, ctypes.POINTER(ctypes.c_int)],
     "wtconv_testing_set_wait_limit_ns": [ctypes.c_ulonglong],
+    "wtconv_debug_phase_clocks": [ctypes.c_int, ctypes.c_int, _vp, ctypes.c_int],
 }
 
 
@@ -74,16 +77,27 @@ def library_path() -> str:
     return _build.LIB
 
 
+def use_library(path: str):
+    """Load the calls from the library at `path` from now on (for the separately built
+    phase-clock library, build.build_phase_clocks()); must precede the first call."""
+    global _LIB_PATH
+    with _LOCK:
+        if _LIB is not None:
+            raise RuntimeError("use_library must precede the first call into the library")
+        _LIB_PATH = path
+
+
 def load_library(rebuild_if_stale: bool = True):
     """Load (building first if needed) libwtconv.so and declare its signatures."""
     global _LIB
     with _LOCK:
         if _LIB is None:
-            if rebuild_if_stale and _build.stale():
+            path = _LIB_PATH or _build.LIB
+            if _LIB_PATH is None and rebuild_if_stale and _build.stale():
                 _build.build()
-            if not os.path.exists(_build.LIB):
-                raise RuntimeError(f"libwtconv.so not found at {_build.LIB}; run build() first")
-            lib = ctypes.CDLL(_build.LIB)
+            if not os.path.exists(path):
+                raise RuntimeError(f"libwtconv.so not found at {path}; run build() first")
+            lib = ctypes.CDLL(path)
             for name, argtypes in _SIGNATURES.items():
                 fn = getattr(lib, name)
                 fn.argtypes = argtypes
@@ -225,6 +239,17 @@ def wtconv_testing_set_wait_limit_ns(ns: int):
     """Test hook (include/wtconv_testing.h): limit of the kernels' bounded waits; 0 = 1 s."""
     _check(load_library().wtconv_testing_set_wait_limit_ns(int(ns)),
            "wtconv_testing_set_wait_limit_ns")
+
+
+def wtconv_debug_phase_clocks(kernel: int, reset: bool = False) -> list:
+    """The 32 phase counters of a plane kernel (include/wtconv_debug.h): 0 forward /
+    backward-data, 1 backward-weight. Raises WTConvError (WT_ERR_UNSUPPORTED) unless the
+    library was built with the clocks."""
+    buf = (ctypes.c_ulonglong * 32)()
+    _check(load_library().wtconv_debug_phase_clocks(int(kernel), 1 if reset else 0,
+                                                    ctypes.cast(buf, _vp), 32),
+           "wtconv_debug_phase_clocks")
+    return list(buf)
 
 
 def wtconv_fma_probe(blocks: int, iters: int, packed: bool, out, stream=None):

@@ -18,6 +18,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libwtconv.so")
+# the same library with the plane kernels' per-phase clocks compiled in (analysis only)
+PHASE_BUILD = os.path.join(BUILD, "phase")
+PHASE_LIB = os.path.join(PHASE_BUILD, "libwtconv.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -40,23 +43,25 @@ def _deps():
         os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h")) + [__file__]
 
 
-def stale() -> bool:
-    if not os.path.exists(LIB):
+def stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(p) > t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    """Compile and link; returns the library path. Rebuilds only when sources changed."""
-    if not force and not stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=None, out_dir: str = BUILD) -> str:
+    """Compile and link into out_dir/libwtconv.so; returns the library path. Rebuilds only
+    when sources changed."""
+    lib_path = os.path.join(out_dir, "libwtconv.so")
+    if not force and not stale(lib_path):
+        return lib_path
+    os.makedirs(out_dir, exist_ok=True)
     extra = list(extra_flags or [])
     cc = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
+        obj = os.path.join(out_dir, os.path.basename(src).replace(".cu", ".o"))
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
@@ -70,13 +75,19 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     if verbose:
         for _, log in results:
             sys.stderr.write(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", *[o for o, _ in results], "-o", tmp]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
+
+
+def build_phase_clocks(force: bool = False) -> str:
+    """The library with the plane kernels' per-phase clocks (-DWT_PHASE_CLOCKS), built apart
+    from the ordinary one; returns its path."""
+    return build(force=force, extra_flags=["-DWT_PHASE_CLOCKS"], out_dir=PHASE_BUILD)
 
 
 if __name__ == "__main__":

@@ -8,6 +8,7 @@
 #include "wt_common.cuh"
 #include "wt_internal.h"
 #include "wt_tma.cuh"
+#include "wtconv_debug.h"
 #include "wtconv_testing.h"
 
 namespace wt {
@@ -213,6 +214,12 @@ wt_status wtconv_workspace_status(const void* ws, wt_stream_t stream, int* flags
                   (words[kStatusBackwardWeight] ? 4 : 0);
     if (flags) *flags = f;
     return f ? WT_ERR_TIMEOUT : WT_OK;
+}
+
+wt_status wtconv_debug_phase_clocks(int kernel, int reset, unsigned long long* out, int n) {
+    if (out == nullptr || n < 32 || (kernel != 0 && kernel != 1)) return WT_ERR_INVALID_ARG;
+    return kernel == 0 ? wt::phase_clocks_forward(reset, out)
+                       : wt::phase_clocks_backward_weight(reset, out);
 }
 
 wt_status wtconv_testing_set_wait_limit_ns(unsigned long long ns) {

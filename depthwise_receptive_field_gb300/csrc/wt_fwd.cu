@@ -28,12 +28,23 @@
 #include <mutex>
 
 #include "wt_internal.h"
+#include "wt_phase.cuh"
 #include "wt_tile.cuh"
 #include "wt_tma.cuh"
 
 namespace wt {
 
 constexpr int kFT = 256;  // threads per CTA
+#ifdef WT_PHASE_CLOCKS
+// per-phase cycle sums of the plane kernel's thread 0, all CTAs (wt_phase.cuh). Phases:
+// 0 plane setup, 1 level-2 sweep and weights, 2 carriers, 3 grouped rounds, 4 level >= 3
+// stage, 5 level >= 3 filter and barriers, 6 level-2 tile wait and repack (or stage),
+// 7 cascade of levels >= 4 into Z^(3), 8 level-2 barrier, 9 level-2 filter, 10 level-2 deep
+// sums and barrier, 11 end of the deep phase, 12 full-resolution remainder, 13 plane end,
+// 14 tile wait, 15 band conversion, 16 barrier A and the next tile's issue, 17 level-1
+// filter, 18 base filter, synthesis and store; 31 planes.
+__device__ unsigned long long g_phase_fwd[32];
+#endif
 
 struct FwdArgs {
     CUtensorMap tmx;  // X: dims {W, H, planes}, box {XBW, XBH, 1}
@@ -558,6 +569,7 @@ __device__ __forceinline__ bool deep_levels(const FwdArgs& a, float* sm, float* 
     };
     bool ok = true;
     deep_carriers(a, u2, deep);
+    WT_PHASE(2);
     if (a.small2) {
         small_deep_round<K>(a, u2, deep, sm, zslot);
         return true;
@@ -571,6 +583,7 @@ __device__ __forceinline__ bool deep_levels(const FwdArgs& a, float* sm, float* 
                 __syncthreads();
                 deep_group_filter<K>(a, bs, wsm, deep, l, lo);
                 __syncthreads();  // the band-pair tiles are free for the next stage
+                WT_PHASE(3);
                 l = lo;
                 continue;
             }
@@ -591,12 +604,15 @@ __device__ __forceinline__ bool deep_levels(const FwdArgs& a, float* sm, float* 
                 } else {
                     deep_stage<K>(a, u2, sm, deep, l, ti0, tj0);
                 }
+                WT_PHASE(l == 2 ? 6 : 4);
                 if (l == 2 && ti0 == 0 && tj0 == 0 && a.L >= 3) deep_cascade(a, deep);
+                WT_PHASE(l == 2 ? 7 : 4);
                 if (l == 2 && tma2) {
                     if (__syncthreads_or(!ok)) return false;
                 } else {
                     __syncthreads();
                 }
+                WT_PHASE(l == 2 ? 8 : 5);
                 if (l == 2 && tma2 && tid == 0) {  // the next level-2 tile
                     const int nj = tj0 + kCT < Wl ? tj0 + kCT : 0;
                     const int ni = tj0 + kCT < Wl ? ti0 : ti0 + kCT;
@@ -643,6 +659,7 @@ __device__ __forceinline__ bool deep_levels(const FwdArgs& a, float* sm, float* 
                         }
                     }
                 }
+                WT_PHASE(l == 2 ? 9 : 5);
                 if (l == 2) {
                     // deep sums of this level-2 tile's positions: warp w, rows 4w..4w+3
                     __syncwarp();
@@ -666,6 +683,7 @@ __device__ __forceinline__ bool deep_levels(const FwdArgs& a, float* sm, float* 
                     }
                 }
                 __syncthreads();  // the band-pair tiles are free for the next stage
+                WT_PHASE(l == 2 ? 10 : 5);
             }
         }
     }
@@ -721,6 +739,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
         fence_mbar_init();
     }
     Issued iss;  // phases the leader opened (for the drain after a timeout)
+    WT_PHASE_BEGIN();
     volatile int* s_abort = reinterpret_cast<volatile int*>(sm + a.o_bar + 26);
     if (leader) *s_abort = 0;
     __syncthreads();
@@ -772,6 +791,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
             }
         }
         __syncthreads();
+        WT_PHASE(0);
 
         // ---- deep phase (L >= 2) ----
         // carriers top-down; levels L..3 filtered into shared memory; level 2 last, its
@@ -784,6 +804,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                 failed = true;
                 break;
             }
+            WT_PHASE(1);
             const bool dok =
                 deep_global ? deep_levels<K, true, false>(a, sm, zslot + 2 * a.zd_slot, u2, zslot,
                                                           bar_u, ph_u, iss)
@@ -796,6 +817,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
             fence_proxy_async_global();
             fence_proxy_async_smem();  // the deep state's space is reused by TMA (deep sums)
             __syncthreads();
+            WT_PHASE(11);
         }
 
         // ---- full-resolution phase ----
@@ -841,7 +863,9 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                 }
                 __syncthreads();
             }
+            WT_PHASE(14);
             if (a.L >= 1) convert_bands<K, T>(raw, bs);
+            WT_PHASE(15);
             if (__syncthreads_or(!(ok_x && ok_prev))) {  // barrier A(t)
                 failed = true;
                 break;
@@ -857,6 +881,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                                 (ny * kTile) >> 2, (int)blockIdx.x, bar_d + nb);
                 }
             }
+            WT_PHASE(16);
             if (a.L >= 1) {
                 // level-1 filters: 2 band pairs x 128 blocks of 2x4 coefficients, one per
                 // thread. Warp w filters coefficient rows 4w..4w+3 of both pairs, exactly the
@@ -881,6 +906,7 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
                 }
                 __syncwarp();
             }
+            WT_PHASE(17);
             // the deep sums are waited for just before their use; the wait is voted on at the
             // next barrier
             bool ok_d = true;
@@ -944,7 +970,9 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
             }
             if (a.L >= 2 && use_tma) ph_d ^= 1u << rb;
             ok_prev = ok_d;
+            WT_PHASE(18);
         }
+        WT_PHASE(12);
         // the last tile's deep-sum wait, and every thread done with this plane's tiles
         if (!failed && __syncthreads_or(!ok_prev)) failed = true;
         if (failed) break;
@@ -952,7 +980,12 @@ __global__ void __launch_bounds__(kFT, 2) wt_fwd_plane_kernel(const __grid_const
             *s_next = (a.next != nullptr) ? (int)gridDim.x + atomicAdd(a.next, 1) : -1;
         __syncthreads();
         plane = (a.next != nullptr) ? (long long)*s_next : plane + gridDim.x;
+        WT_PHASE(13);
+        WT_PHASE_PLANE();
     }
+#ifdef WT_PHASE_CLOCKS
+    WT_PHASE_END(g_phase_fwd);
+#endif
     if (failed && leader) {
         if (a.err != nullptr) atomicExch(a.err, kErrTmaTimeout);
         // copies in flight land before the CTA leaves: X tiles, deep-sum blocks, weights,
@@ -1307,6 +1340,22 @@ wt_status launch_forward(const wt_desc& d, const void* x, const float* w0f, cons
         default:
             return WT_ERR_UNSUPPORTED;
     }
+}
+
+wt_status phase_clocks_forward(int reset, unsigned long long* out) {
+#ifdef WT_PHASE_CLOCKS
+    if (cudaMemcpyFromSymbol(out, g_phase_fwd, sizeof(g_phase_fwd)) != cudaSuccess)
+        return WT_ERR_CUDA;
+    if (reset) {
+        static const unsigned long long zero[32] = {0};
+        if (cudaMemcpyToSymbol(g_phase_fwd, zero, sizeof(zero)) != cudaSuccess) return WT_ERR_CUDA;
+    }
+    return WT_OK;
+#else
+    (void)reset;
+    (void)out;
+    return WT_ERR_UNSUPPORTED;
+#endif
 }
 
 bool forward_sizes(const wt_desc& d, size_t* smem, size_t* ws) {

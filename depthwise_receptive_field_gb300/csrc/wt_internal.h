@@ -67,6 +67,11 @@ wt_status launch_forward(const wt_desc& d, const void* x, const float* w0f, cons
                          cudaStream_t stream, int* launches);
 bool forward_sizes(const wt_desc& d, size_t* smem, size_t* ws);
 
+// per-phase clocks of the two plane kernels (32 counters each; only in a library built with
+// -DWT_PHASE_CLOCKS, else WT_ERR_UNSUPPORTED)
+wt_status phase_clocks_forward(int reset, unsigned long long* out);
+wt_status phase_clocks_backward_weight(int reset, unsigned long long* out);
+
 // backward-weight: plane kernel + reduce/unfold kernel
 wt_status launch_backward_weight(const wt_desc& d, const void* x, const void* dy,
                                  const float* w0, const float* b0, const float* s0,

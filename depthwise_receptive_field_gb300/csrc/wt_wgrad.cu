@@ -32,12 +32,21 @@
 // No atomics on data (only the counter that hands out planes): results are bitwise
 // reproducible.
 #include "wt_internal.h"
+#include "wt_phase.cuh"
 #include "wt_tile.cuh"
 #include "wt_tma.cuh"
 
 namespace wt {
 
 constexpr int kDT = 256;  // threads per CTA
+#ifdef WT_PHASE_CLOCKS
+// per-phase cycle sums of the plane kernel's thread 0, all CTAs (wt_phase.cuh). Phases:
+// 0 plane setup, 1 level-2 sweep, 3 tile pair wait, 4 band conversions and dY sum, 5 barrier
+// B1 and the next pair's issue, 6 correlations, 7 barrier B2, 8 flush and partial vector,
+// 9 plane end, 10 grouped small levels, 11 tiled level stage, 12 its first barrier, 13 its
+// correlations, 14 its second barrier, 15 its flush; 31 planes.
+__device__ unsigned long long g_phase_dw[32];
+#endif
 
 struct DwArgs {
     CUtensorMap tmx;  // X: dims {W, H, planes}, box {XBW, XBH, 1} (2R halo)
@@ -459,6 +468,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
         fence_mbar_init();
     }
     Issued iss;  // phases the leader opened (for the drain after a timeout)
+    WT_PHASE_BEGIN();
     volatile int* s_abort = reinterpret_cast<volatile int*>(sm + a.o_bar + 26);  // a wait timed out
     if (leader) *s_abort = 0;
     __syncthreads();
@@ -503,6 +513,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
             }
         }
         __syncthreads();
+        WT_PHASE(0);
 
         // ---- deep levels l = 2..L: band pair pp = tid / 128, 2x4 block per thread ----
         if (a.L >= 2) {
@@ -513,6 +524,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
             }
             __syncthreads();
         }
+        WT_PHASE(1);
         for (int l = 2; l <= a.L; ++l) {
             const int Hl = a.Hp >> l, Wl = a.Wp >> l;
             const int hi = dw_group<K>(a, l);
@@ -593,6 +605,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
                     }
                 }
                 __syncthreads();
+                WT_PHASE(10);
                 l = hi;
                 continue;
             }
@@ -603,7 +616,9 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
             for (int ti0 = 0; ti0 < Hl; ti0 += kCT) {
                 for (int tj0 = 0; tj0 < Wl; tj0 += kCT) {
                     dw_deep_stage<K>(a, u2x, u2g, sm, cbase, l, ti0, tj0);
+                    WT_PHASE(11);
                     __syncthreads();
+                    WT_PHASE(12);
                     if (ti0 + 2 * bi < Hl && tj0 + 4 * bj < Wl) {
                         f2x g[2][4];
 #pragma unroll
@@ -618,7 +633,9 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
                         }
                         corr_pair<K, 2>(xb + pp * PTILE + (2 * bi) * PROW, bj, g, accd);
                     }
+                    WT_PHASE(13);
                     __syncthreads();
+                    WT_PHASE(14);
                 }
             }
             // flush: warps 4pp..4pp+3 hold band pair pp; fixed-order sum into acc_sm
@@ -631,6 +648,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
                 acc_sm[KK + 1 + (l - 1) * 4 * KK + (2 * p2 + (k & 1)) * KK + (k >> 1)] += s;
             }
             __syncthreads();
+            WT_PHASE(15);
         }
         fence_proxy_async_smem();  // warp totals may sit in raw X buffer 1, refilled by TMA
 
@@ -664,8 +682,10 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
                 stage_raw_tile<T>(gp, a.H, a.W, const_cast<T*>(rawg), y0, x0);
                 __syncthreads();
             }
+            WT_PHASE(3);
             if (a.L >= 1) convert_bands<K, T>(rawx, xb);
             dpart += convert_raw_dy<T>(rawg, gb, a.L >= 1);
+            WT_PHASE(4);
             if (__syncthreads_or(!ok)) {  // B1(t)
                 failed = true;
                 break;
@@ -678,6 +698,7 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
                 tma_load_3d(sm + a.o_rawg + nb * a.rawg_f, &a.tmg, nx * kTile, ny * kTile,
                             (int)plane, bar + nb);
             }
+            WT_PHASE(5);
             if ((t & 15) == 15 || t + 1 == ntiles) {
                 kahan_add(kah, dpart);
                 dpart = 0.f;
@@ -707,7 +728,9 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
                     corr_pair<K, 4>(xb + pp * PTILE + (4 * bi) * PROW, bj, g, acc);
                 }
             }
+            WT_PHASE(6);
             __syncthreads();  // B2(t): the band-pair tiles and raw buffer rb are free
+            WT_PHASE(7);
         }
         if (failed) break;
 
@@ -739,11 +762,17 @@ __global__ void __launch_bounds__(kDT, (K >= 7) ? 1 : 2) wt_dw_plane_kernel(cons
         __syncthreads();
         float* out = a.part + ((size_t)c * a.N + n) * a.KP;
         for (int e = tid; e < a.KP; e += kDT) out[e] = acc_sm[e];
+        WT_PHASE(8);
         if (leader)
             *s_next = (a.next != nullptr) ? (int)gridDim.x + ticket : -1;
         __syncthreads();
         plane = (a.next != nullptr) ? (long long)*s_next : plane + gridDim.x;
+        WT_PHASE(9);
+        WT_PHASE_PLANE();
     }
+#ifdef WT_PHASE_CLOCKS
+    WT_PHASE_END(g_phase_dw);
+#endif
     if (failed && leader) {
         if (a.err != nullptr) atomicExch(a.err, kErrTmaTimeout);
         // copies in flight land before the CTA leaves: the tile pairs and the sweep pairs
@@ -1050,6 +1079,22 @@ wt_status launch_dw_reduce(const wt_desc& d, const float* part, int groups, cons
     if (cudaGetLastError() != cudaSuccess) return WT_ERR_CUDA;
     ++*launches;
     return WT_OK;
+}
+
+wt_status phase_clocks_backward_weight(int reset, unsigned long long* out) {
+#ifdef WT_PHASE_CLOCKS
+    if (cudaMemcpyFromSymbol(out, g_phase_dw, sizeof(g_phase_dw)) != cudaSuccess)
+        return WT_ERR_CUDA;
+    if (reset) {
+        static const unsigned long long zero[32] = {0};
+        if (cudaMemcpyToSymbol(g_phase_dw, zero, sizeof(zero)) != cudaSuccess) return WT_ERR_CUDA;
+    }
+    return WT_OK;
+#else
+    (void)reset;
+    (void)out;
+    return WT_ERR_UNSUPPORTED;
+#endif
 }
 
 size_t dw_partial_floats(const wt_desc& d) {

@@ -181,3 +181,15 @@ def test_status_query_and_probe_validate_before_any_device_call(lib):
     assert lib.wtconv_testing_set_wait_limit_ns(1000) == B.WT_OK
     assert lib.wtconv_testing_set_wait_limit_ns(0) == B.WT_OK
     assert B.status_string(B.WT_ERR_TIMEOUT).startswith("WT_ERR_TIMEOUT")
+
+
+def test_phase_clocks_are_absent_from_the_ordinary_library(lib):
+    """wtconv_debug_phase_clocks validates its arguments, then reports WT_ERR_UNSUPPORTED:
+    the ordinary build has no clock code (only the separate -DWT_PHASE_CLOCKS build does)."""
+    buf = (ctypes.c_ulonglong * 32)()
+    ptr = ctypes.cast(buf, ctypes.c_void_p)
+    assert lib.wtconv_debug_phase_clocks(0, 0, None, 32) == B.WT_ERR_INVALID_ARG
+    assert lib.wtconv_debug_phase_clocks(0, 0, ptr, 31) == B.WT_ERR_INVALID_ARG
+    assert lib.wtconv_debug_phase_clocks(2, 0, ptr, 32) == B.WT_ERR_INVALID_ARG
+    assert lib.wtconv_debug_phase_clocks(0, 0, ptr, 32) == B.WT_ERR_UNSUPPORTED
+    assert lib.wtconv_debug_phase_clocks(1, 1, ptr, 32) == B.WT_ERR_UNSUPPORTED
