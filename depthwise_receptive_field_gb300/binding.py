@@ -128,6 +128,44 @@ def _ptr(t):
     return t.data_ptr()
 
 
+def _dev(t, what: str, dtype=None, numel=None):
+    """Device pointer of a tensor argument, after the checks the C ABI cannot make from a
+    raw pointer: contiguous, of the expected dtype and size, on a CUDA device. None and
+    raw integer addresses pass through unchecked (the ABI's own tests of null and
+    misaligned pointers use them)."""
+    if t is None or isinstance(t, int):
+        return t
+    if not t.is_contiguous():
+        raise ValueError(f"{what}: the tensor must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{what}: dtype {t.dtype}, expected {dtype}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{what}: {t.numel()} elements, expected {numel}")
+    if not t.is_cuda:
+        raise ValueError(f"{what}: a CUDA tensor is required")
+    return t.data_ptr()
+
+
+def _io_dtype(desc):
+    import torch
+    return {WT_F32: torch.float32, WT_BF16: torch.bfloat16, WT_F16: torch.float16}[desc.io]
+
+
+def _sizes(desc):
+    """Element counts of a plane tensor and of the parameter arrays of desc."""
+    kk, c, L = desc.k * desc.k, desc.c, desc.levels
+    return {"x": desc.n * c * desc.h * desc.w, "w0": c * kk, "c": c, "wl": L * c * 4 * kk,
+            "sl": L * c * 4}
+
+
+def _ws(ws, ws_bytes, what: str):
+    if ws is not None and not isinstance(ws, int) and \
+            ws.numel() * ws.element_size() < int(ws_bytes):
+        raise ValueError(f"{what}: workspace of {ws.numel() * ws.element_size()} bytes, "
+                         f"ws_bytes says {int(ws_bytes)}")
+    return _dev(ws, what + " (workspace)")
+
+
 def _stream(s):
     if s is None:
         import torch
@@ -167,47 +205,78 @@ def wtconv_workspace_size(desc: wt_desc):
     return a.value, b.value, c.value
 
 
+def _params(desc, where, **named):
+    """Device pointers of fp32 parameter-shaped arguments, by name: w0-like [C,k,k],
+    c-like [C], wl-like [L,C,4,k,k], sl-like [L,C,4]."""
+    import torch
+    n = _sizes(desc)
+    kind = {"w0": "w0", "w0f": "w0", "dw0": "w0", "b0": "c", "s0": "c", "b0f": "c",
+            "db0": "c", "ds0": "c", "wl": "wl", "wlf": "wl", "dwl": "wl", "sl": "sl",
+            "dsl": "sl"}
+    return {k: _dev(v, f"{where}: {k}", torch.float32, n[kind[k]]) for k, v in named.items()}
+
+
+def _plane(desc, where, name, t):
+    return _dev(t, f"{where}: {name}", _io_dtype(desc), _sizes(desc)["x"])
+
+
 def wtconv_fold_scales(desc, w0, b0, s0, wl, sl, w0f, b0f, wlf, stream=None):
+    w = "wtconv_fold_scales"
+    p = _params(desc, w, w0=w0, b0=b0, s0=s0, wl=wl, sl=sl, w0f=w0f, b0f=b0f, wlf=wlf)
     _check(load_library().wtconv_fold_scales(
-        ctypes.byref(desc), _ptr(w0), _ptr(b0), _ptr(s0), _ptr(wl), _ptr(sl), _ptr(w0f),
-        _ptr(b0f), _ptr(wlf), _stream(stream)), "wtconv_fold_scales")
+        ctypes.byref(desc), p["w0"], p["b0"], p["s0"], p["wl"], p["sl"], p["w0f"], p["b0f"],
+        p["wlf"], _stream(stream)), w)
 
 
 def wtconv_forward(desc, x, w0f, b0f, wlf, y, ws=None, ws_bytes=0, stream=None):
+    w = "wtconv_forward"
+    p = _params(desc, w, w0f=w0f, b0f=b0f, wlf=wlf)
     _check(load_library().wtconv_forward(
-        ctypes.byref(desc), _ptr(x), _ptr(w0f), _ptr(b0f), _ptr(wlf), _ptr(y), _ptr(ws),
-        int(ws_bytes), _stream(stream)), "wtconv_forward")
+        ctypes.byref(desc), _plane(desc, w, "x", x), p["w0f"], p["b0f"], p["wlf"],
+        _plane(desc, w, "y", y), _ws(ws, ws_bytes, w), int(ws_bytes), _stream(stream)), w)
 
 
 def wtconv_backward_data(desc, dy, w0f, wlf, dx, ws=None, ws_bytes=0, stream=None):
+    w = "wtconv_backward_data"
+    p = _params(desc, w, w0f=w0f, wlf=wlf)
     _check(load_library().wtconv_backward_data(
-        ctypes.byref(desc), _ptr(dy), _ptr(w0f), _ptr(wlf), _ptr(dx), _ptr(ws), int(ws_bytes),
-        _stream(stream)), "wtconv_backward_data")
+        ctypes.byref(desc), _plane(desc, w, "dy", dy), p["w0f"], p["wlf"],
+        _plane(desc, w, "dx", dx), _ws(ws, ws_bytes, w), int(ws_bytes), _stream(stream)), w)
 
 
 def wtconv_backward_weight(desc, x, dy, w0, b0, s0, wl, sl, dw0, db0, ds0, dwl, dsl, ws,
                            ws_bytes, stream=None):
+    w = "wtconv_backward_weight"
+    p = _params(desc, w, w0=w0, b0=b0, s0=s0, wl=wl, sl=sl, dw0=dw0, db0=db0, ds0=ds0,
+                dwl=dwl, dsl=dsl)
     _check(load_library().wtconv_backward_weight(
-        ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(w0), _ptr(b0), _ptr(s0), _ptr(wl),
-        _ptr(sl), _ptr(dw0), _ptr(db0), _ptr(ds0), _ptr(dwl), _ptr(dsl), _ptr(ws),
-        int(ws_bytes), _stream(stream)), "wtconv_backward_weight")
+        ctypes.byref(desc), _plane(desc, w, "x", x), _plane(desc, w, "dy", dy), p["w0"],
+        p["b0"], p["s0"], p["wl"], p["sl"], p["dw0"], p["db0"], p["ds0"], p["dwl"], p["dsl"],
+        _ws(ws, ws_bytes, w), int(ws_bytes), _stream(stream)), w)
 
 
 def wtconv_backward(desc, x, dy, w0f, wlf, w0, b0, s0, wl, sl, dx, dw0, db0, ds0, dwl, dsl,
                     ws, ws_bytes, stream=None):
+    w = "wtconv_backward"
+    p = _params(desc, w, w0f=w0f, wlf=wlf, w0=w0, b0=b0, s0=s0, wl=wl, sl=sl, dw0=dw0,
+                db0=db0, ds0=ds0, dwl=dwl, dsl=dsl)
     _check(load_library().wtconv_backward(
-        ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(w0f), _ptr(wlf), _ptr(w0), _ptr(b0),
-        _ptr(s0), _ptr(wl), _ptr(sl), _ptr(dx), _ptr(dw0), _ptr(db0), _ptr(ds0), _ptr(dwl),
-        _ptr(dsl), _ptr(ws), int(ws_bytes), _stream(stream)), "wtconv_backward")
+        ctypes.byref(desc), _plane(desc, w, "x", x), _plane(desc, w, "dy", dy), p["w0f"],
+        p["wlf"], p["w0"], p["b0"], p["s0"], p["wl"], p["sl"], _plane(desc, w, "dx", dx),
+        p["dw0"], p["db0"], p["ds0"], p["dwl"], p["dsl"], _ws(ws, ws_bytes, w), int(ws_bytes),
+        _stream(stream)), w)
 
 
 def wtconv_backward_weight_noalloc(desc, x, dy, w0, b0, s0, wl, sl, dw0, db0, ds0, dwl, dsl,
                                    stream=None):
     """Backward-weight with the library's built-in 4 MiB scratch (no workspace)."""
+    w = "wtconv_backward_weight_noalloc"
+    p = _params(desc, w, w0=w0, b0=b0, s0=s0, wl=wl, sl=sl, dw0=dw0, db0=db0, ds0=ds0,
+                dwl=dwl, dsl=dsl)
     _check(load_library().wtconv_backward_weight_noalloc(
-        ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(w0), _ptr(b0), _ptr(s0), _ptr(wl),
-        _ptr(sl), _ptr(dw0), _ptr(db0), _ptr(ds0), _ptr(dwl), _ptr(dsl), _stream(stream)),
-        "wtconv_backward_weight_noalloc")
+        ctypes.byref(desc), _plane(desc, w, "x", x), _plane(desc, w, "dy", dy), p["w0"],
+        p["b0"], p["s0"], p["wl"], p["sl"], p["dw0"], p["db0"], p["ds0"], p["dwl"], p["dsl"],
+        _stream(stream)), w)
 
 
 def wtconv_variant_workspace_size(desc: wt_desc, variant: int) -> int:

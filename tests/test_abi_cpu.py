@@ -193,3 +193,23 @@ def test_phase_clocks_are_absent_from_the_ordinary_library(lib):
     assert lib.wtconv_debug_phase_clocks(2, 0, ptr, 32) == B.WT_ERR_INVALID_ARG
     assert lib.wtconv_debug_phase_clocks(0, 0, ptr, 32) == B.WT_ERR_UNSUPPORTED
     assert lib.wtconv_debug_phase_clocks(1, 1, ptr, 32) == B.WT_ERR_UNSUPPORTED
+
+
+def test_binding_rejects_tensors_the_abi_cannot_check():
+    """The C ABI sees raw pointers only; the binding rejects what a pointer cannot tell:
+    a non-contiguous tensor, a wrong dtype or size, a host tensor, a workspace smaller than
+    ws_bytes. Raw integer addresses pass through (the ABI's own pointer tests use them)."""
+    import torch
+    desc = B.make_desc(1, 2, 8, 8, 3, 1, B.WT_F32)
+    x = torch.zeros(1, 2, 8, 8)
+    for bad, msg in ((x.transpose(2, 3), "contiguous"), (x.double(), "dtype"),
+                     (x[:, :1], "elements"), (x, "CUDA")):
+        with pytest.raises(ValueError, match=msg):
+            B.wtconv_forward(desc, bad, 256, 256, 256, 256)
+    with pytest.raises(ValueError, match="dtype"):
+        B.wtconv_forward(desc, 256, torch.zeros(2, 3, 3, dtype=torch.float64), 256, 256, 256)
+    with pytest.raises(ValueError, match="elements"):
+        B.wtconv_backward_weight(desc, 256, 256, torch.zeros(2, 3, 2), 256, 256, 256, 256, 256,
+                                 256, 256, 256, 256, None, 0)
+    with pytest.raises(ValueError, match="workspace"):
+        B.wtconv_forward(desc, 256, 256, 256, 256, 256, torch.zeros(8, dtype=torch.uint8), 64)
