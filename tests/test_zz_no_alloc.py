@@ -30,6 +30,9 @@ CASES = [
     # 128 KB level-2 slots: only 29 fit, fewer than the 64 CTAs the plane kernel would
     # otherwise run, so the grid shrinks and the CTAs take planes from the shared counter
     (2, 64, 256, 256, 5, 5, "bf16"),
+    # k = 7 (the one-CTA-per-SM backward-weight kernel) and k = 3 at fp16 I/O
+    (4, 24, 96, 96, 7, 3, "bf16"),
+    (3, 20, 72, 64, 3, 3, "f16"),
 ]
 
 
